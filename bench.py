@@ -1,0 +1,413 @@
+"""Benchmark of the fused linear + cross-entropy forward+backward on GB300.
+
+Default: the bf16 LLM-head workload (N=8192 tokens, D=4096, C=128256, Zipf
+targets, 5% ignored, mean), one step = one lce_forward_backward call (loss,
+dX, dW) on inputs resident in HBM. Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl reference]
+
+--impl reference times the float64 CPU oracle on the host cores on a
+bounded sample of the same workload (the method has no other reference
+implementation). With torchrun (N > 1) every rank runs an independent
+replica (the step does not shard); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_cross_entropy_lce_gb300.workloads import WORKLOADS, make_workload  # noqa: E402
+
+METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor peak"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    return ws, rank
+
+
+def _oracle_sample_seconds(name, rows, device_inputs=None, seed=0):
+    """Time the float64 oracle on `rows` rows of the workload (host cores)."""
+    from oracle import lce_oracle as O
+
+    w = WORKLOADS[name]
+    inp = device_inputs if device_inputs is not None else make_workload(name, "cpu")
+    if w.kind == "logits":
+        z = inp["logits"][:rows].float().cpu().numpy()
+        t = inp["target"][:rows].cpu().numpy()
+        t0 = time.perf_counter()
+        O.ce_from_logits(z, t, w.reduction, -100)
+        return time.perf_counter() - t0
+    X = inp["X"][:rows].float().cpu().numpy()
+    W = inp["W"].float().cpu().numpy()
+    b = None if inp["b"] is None else inp["b"].double().cpu().numpy()
+    t = inp["target"][:rows].cpu().numpy()
+    g = None if inp["grad_out"] is None else inp["grad_out"][:rows].double().cpu().numpy()
+    t0 = time.perf_counter()
+    O.lce_forward_backward(X, W, b, t, w.reduction, -100, g)
+    return time.perf_counter() - t0
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    ws, rank = _dist()
+    if rank != 0:
+        return 0
+    name = args.workload
+    w = WORKLOADS[name]
+    rows = args.ref_rows
+    inp = make_workload(name, "cuda" if torch.cuda.is_available() else "cpu")
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        _oracle_sample_seconds(name, rows, inp)
+    times = [_oracle_sample_seconds(name, rows, inp) for _ in range(args.steps)]
+    sec = float(np.mean(times))
+    value = rows / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "N": w.N, "D": w.D, "C": w.C, "reduction": w.reduction},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+                         "sample": f"{rows} of {w.N} rows per step, full method (loss and all gradients "
+                                   f"for those rows) in float64 numpy"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_gpu(args):
+    import linear_cross_entropy_lce_gb300 as lce
+
+    ws, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist_mod
+
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    lce.load_library()
+    name = args.workload
+    w = WORKLOADS[name]
+    inp = make_workload(name, "cuda")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks = _peaks()
+
+    if w.kind == "logits":
+        logits, t = inp["logits"], inp["target"]
+        N, V = logits.shape
+        nbytes = lce.lce_workspace_size(lce.LCE_OP_CE_FROM_LOGITS, N, 1, V, lce.LCE_F32, lce.LCE_RED_MEAN,
+                                        lce.LCE_F32, 0)
+        wsbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+        def step():
+            return lce.lce_cross_entropy_from_logits(logits, t, w.reduction, -100, workspace=wsbuf)
+
+        flops = 0.0
+        dominant = "ce_resident"
+        algo_bytes = 2.0 * N * V * logits.element_size()
+    else:
+        X, W, b, t, g = inp["X"], inp["W"], inp["b"], inp["target"], inp["grad_out"]
+        N, D = X.shape
+        C = W.shape[0]
+        dt = lce.LCE_BF16 if X.dtype == torch.bfloat16 else lce.LCE_F32
+        red = {"none": 0, "sum": 1, "mean": 2}[w.reduction]
+        nbytes = lce.lce_workspace_size(lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, red, dt, 0)
+        wsbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        dX = torch.empty_like(X)
+        dW = torch.empty_like(W)
+        db = torch.empty_like(b) if b is not None else None
+        loss = torch.empty(N if red == 0 else 1, dtype=torch.float32, device=dev)
+        lib = lce.load_library()
+        import ctypes
+
+        P = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())
+
+        def step():
+            if red == 0:  # reduction none: forward, then forward+backward with the upstream vector
+                lce._check(lib.lce_forward(P(X), P(W), P(b), P(t), N, D, C, dt, 0, red, -100, P(loss), None,
+                                           P(wsbuf), nbytes, ctypes.c_void_p(stream.cuda_stream)), "fwd")
+            lce._check(lib.lce_forward_backward(P(X), P(W), P(b), P(t), N, D, C, dt, 0, red, -100, P(g), P(loss),
+                                                P(dX), P(dW), P(db), dt, P(wsbuf), nbytes,
+                                                ctypes.c_void_p(stream.cuda_stream)), "fwd+bwd")
+            return loss
+
+        flops = w.flops_fwd_bwd
+        dominant = None
+        algo_bytes = None
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+
+    # ---- device-timed region
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    lce.profile_reset()
+    lce.profile_enable(True)
+    launches0 = lce.launch_count()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    lce.profile_enable(False)
+    launches = lce.launch_count() - launches0
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    prof = lce.profile_summary()
+    lce.profile_reset()
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if w.kind != "logits":
+        hX = X.cpu().pin_memory()
+        hW = W.cpu().pin_memory()
+        ht = t.cpu().pin_memory()
+        hb = b.cpu().pin_memory() if b is not None else None
+        hg = g.cpu().pin_memory() if g is not None else None
+        hloss = torch.empty_like(loss, device="cpu").pin_memory()
+        h2d = hX.numel() * hX.element_size() + hW.numel() * hW.element_size() + ht.numel() * 8
+        h2d += (hb.numel() * hb.element_size() if hb is not None else 0) + (hg.numel() * 4 if hg is not None else 0)
+        d2h = hloss.numel() * 4
+
+        def e2e_step():
+            X.copy_(hX, non_blocking=True)
+            W.copy_(hW, non_blocking=True)
+            t.copy_(ht, non_blocking=True)
+            if hb is not None:
+                b.copy_(hb, non_blocking=True)
+            if hg is not None:
+                g.copy_(hg, non_blocking=True)
+            step()
+            hloss.copy_(loss, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        barrier()
+        ems = f0.elapsed_time(f1) / args.steps
+        if dist is not None:
+            tt = torch.tensor([ems], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ems = float(tt.item())
+        e2e = {"value": ws * N / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": ems}
+    else:
+        hl = inp["logits"].cpu().pin_memory()
+        ht = t.cpu().pin_memory()
+        hloss = torch.empty(1, dtype=torch.float32).pin_memory()
+        h2d = hl.numel() * hl.element_size() + ht.numel() * 8
+
+        def e2e_step():
+            logits.copy_(hl, non_blocking=True)
+            t.copy_(ht, non_blocking=True)
+            l = step()
+            hloss.copy_(l.reshape(1), non_blocking=True)
+
+        e2e_step()
+        barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        barrier()
+        ems = f0.elapsed_time(f1) / args.steps
+        e2e = {"value": ws * N / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": 4, "ms_per_step": ems}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel
+    if dominant is None:
+        dominant = max(prof, key=lambda k: prof[k][1]) if prof else None
+    roofline = None
+    if dominant in prof:
+        n_l, tot_ms = prof[dominant]
+        avg_s = tot_ms / n_l / 1e3
+        if w.kind == "logits":
+            achieved = algo_bytes / avg_s / 1e9
+            roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": dominant,
+                        "peak_source": peaks["source"] + " hbm_gbs (copy)",
+                        "algorithmic_bytes_per_launch": algo_bytes}
+        else:
+            per_launch_flops = 2.0 * w.N * w.D * w.C  # each of the three GEMMs is 2NDC per call
+            achieved = per_launch_flops / avg_s / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak, "traffic": None, "kernel": dominant,
+                        "peak_source": peaks["source"] + " bf16_tflops_sustained (kernel timed inside a "
+                                                         "long run of back-to-back steps)",
+                        "algorithmic_flops_per_launch": per_launch_flops}
+
+    # ---- CPU baseline: the oracle on a bounded sample, rank 0, N=1 only
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        rows = args.ref_rows
+        sec = _oracle_sample_seconds(name, rows, inp)
+        cpu = {"value": rows / sec, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+               "sample": f"{rows} of {w.N} rows, full method (loss and all gradients for those rows) in "
+                         f"float64 numpy, {sec:.1f} s"}
+
+    tokens_per_s = ws * w.N / (ms / 1e3)
+    line = {
+        "metric": METRIC,
+        "value": tokens_per_s,
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic",
+        "config": {"workload": name, "N": w.N, "D": w.D, "C": w.C, "reduction": w.reduction,
+                   "bias": w.bias, "targets": w.target_dist, "parallelism": "replicas" if ws > 1 else "single",
+                   "l2": "inputs larger than L2 (W is %.2f GB)" % (w.C * max(w.D, 1) * 2 / 1e9)},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "kernels_ms_per_step": {k: v[1] / args.steps for k, v in sorted(prof.items(), key=lambda kv: -kv[1][1])},
+    }
+    if flops:
+        line["tflops"] = flops * ws / (ms / 1e3) / 1e12
+        line["pct_bf16_peak"] = 100.0 * line["tflops"] / ws / peaks["bf16_tflops"]
+        line["pct_bf16_peak_sustained"] = 100.0 * line["tflops"] / ws / peaks["bf16_tflops_sustained"]
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="bf16_llm_head", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,197 @@
+/*
+ * lce.h -- C ABI of liblce.so: fused linear + cross-entropy loss on GB300.
+ *
+ * The operation (PyTorch source torch/nn/modules/linear_cross_entropy.py,
+ * the batch-chunked implementation; PyTorch commit ddfa80bd "Fix NJT
+ * linear_backward() memory usage" for the gradient formulas):
+ *
+ *   z[n, j]  = sum_d X[n, d] W[j, d] + b[j]          n < N, j < C, d < D
+ *   lse_n    = log sum_j exp z[n, j]
+ *   loss_n   = lse_n - z[n, t_n]   (0 when t_n == ignore_index)
+ *   loss     = none: loss_n | sum: sum_n loss_n | mean: sum_n loss_n / n_valid
+ *   G[n, j]  = w_n (softmax(z_n)_j - [j == t_n]),
+ *              w_n = 0 on ignored rows, else g / n_valid (mean), g (sum),
+ *                    g_n (none), with g the upstream gradient
+ *   dX = G W,  dW = G^T X,  db = sum_n G[n, :]
+ *
+ * and cross entropy on logits the caller already holds, whose gradient
+ * replaces the logits in place (Liger-Kernel issue #343, "cross entropy
+ * kernel: inplace modification of input").
+ *
+ * Conventions shared by every entry point
+ *  - Every pointer named X, W, b, target, logits, dX, dW, db, grad_out,
+ *    loss_out, lse_out and workspace is a DEVICE pointer on the current
+ *    CUDA device; stream is a cudaStream_t (NULL = legacy default stream).
+ *    All work is enqueued asynchronously on that stream; the call returns
+ *    before the GPU finishes.
+ *  - Matrices are dense row-major: X [N, D], W [C, D], dX [N, D],
+ *    dW [C, D], logits [N, V]; vectors b, db [C]; target [N] int64;
+ *    loss_out [1] (sum, mean) or [N] (none); lse_out [N] fp32.
+ *  - The caller owns and allocates every buffer, including the workspace
+ *    (size from lce_workspace_size). The library allocates no device
+ *    memory and keeps no state between calls (except the optional
+ *    profiling records below). Inputs are never written, except
+ *    logits_inout of lce_cross_entropy_from_logits.
+ *  - Gradients are the full result, WRITTEN into the caller's buffers
+ *    (not accumulated into them).
+ *  - Host-side argument errors return a nonzero status synchronously and
+ *    enqueue nothing. Errors found by the kernels (a target that is neither
+ *    ignore_index nor in [0, C), an internal wait that timed out) are
+ *    recorded in the workspace and read back with lce_read_device_status;
+ *    rows with such a target get loss 0 and gradient 0 and do not count
+ *    toward n_valid.
+ *  - Types: dtype LCE_F32 or LCE_BF16 for X, W, b (or for logits);
+ *    acc_dtype must be LCE_F32 (accumulation is always fp32);
+ *    grad_dtype (dX, dW, db) LCE_F32 or LCE_BF16. Loss and lse are fp32.
+ *  - LCE_BF16 inputs run on the tcgen05 tensor cores and need D % 8 == 0
+ *    and 16-byte aligned X, W, dX, dW (else LCE_ERR_ALIGN). LCE_F32
+ *    inputs run exact fp32 FMA on the CUDA cores and accept any shape.
+ *  - Device: compute capability 10.3 (GB300, sm_103a); else LCE_ERR_DEVICE.
+ */
+#ifndef LCE_H_
+#define LCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifndef LCE_API
+#if defined(__GNUC__)
+#define LCE_API __attribute__((visibility("default")))
+#else
+#define LCE_API
+#endif
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types (linear_cross_entropy.py supports fp32 accumulation for
+ * fp16/bf16 inputs, and accumulation in the input type otherwise). */
+enum lce_dtype_e { LCE_F32 = 0, LCE_BF16 = 1 };
+
+/* Reductions accepted by linear_cross_entropy.py: "none", "sum", "mean". */
+enum lce_reduction_e { LCE_RED_NONE = 0, LCE_RED_SUM = 1, LCE_RED_MEAN = 2 };
+
+/* Operations, for lce_workspace_size. */
+enum lce_op_e { LCE_OP_FORWARD = 0, LCE_OP_FORWARD_BACKWARD = 1, LCE_OP_CE_FROM_LOGITS = 2 };
+
+/* Status codes. */
+enum lce_status_e {
+  LCE_OK = 0,
+  LCE_ERR_NULL = 1,         /* a required pointer is NULL */
+  LCE_ERR_SHAPE = 2,        /* N < 0, D < 1, C < 1 or V < 1, or a size too large */
+  LCE_ERR_DTYPE = 3,        /* unknown dtype, or acc_dtype != LCE_F32 */
+  LCE_ERR_REDUCTION = 4,    /* reduction not one of none / sum / mean */
+  LCE_ERR_GRAD_OUT = 5,     /* reduction none without a per-row upstream gradient */
+  LCE_ERR_WORKSPACE = 6,    /* workspace NULL or smaller than needed for 128-row chunks */
+  LCE_ERR_CUDA = 7,         /* a CUDA runtime call or kernel launch failed */
+  LCE_ERR_TARGET_RANGE = 8, /* device: a target neither ignore_index nor in [0, C) */
+  LCE_ERR_ALIGN = 9,        /* bf16 path: D % 8 != 0 or a pointer not 16-byte aligned */
+  LCE_ERR_TIMEOUT = 10,     /* device: an internal pipeline wait gave up */
+  LCE_ERR_DEVICE = 11       /* current device is not compute capability 10.3 */
+};
+
+/*
+ * Workspace bytes needed by one call.
+ *   op          LCE_OP_FORWARD, LCE_OP_FORWARD_BACKWARD or LCE_OP_CE_FROM_LOGITS
+ *   N, D, C     problem sizes (for CE_FROM_LOGITS pass D = 1 and C = V)
+ *   dtype       input type; grad_dtype: gradient type (ignored for FORWARD)
+ *   chunk_rows  rows per batch chunk of the backward; 0 picks the default:
+ *               as many rows as keep the [chunk_rows, C] gradient buffer
+ *               within 4 GiB. Fewer rows need less memory: the backward
+ *               keeps one [chunk_rows, ceil(C/256)*256] buffer of the input
+ *               type (the batch-chunked buffer of linear_cross_entropy.py)
+ *               and, when there is more than one chunk and dW is bf16, an
+ *               fp32 [C, D] accumulator for dW.
+ * The size depends only on these arguments. A call given ws_bytes >= this
+ * size uses the largest chunk (a multiple of 128 rows, or all rows) that
+ * fits in ws_bytes. Returns 0 on invalid arguments.
+ */
+LCE_API size_t lce_workspace_size(int op, int64_t N, int64_t D, int64_t C, int dtype,
+                          int reduction, int grad_dtype, int64_t chunk_rows);
+
+/*
+ * Loss only (linear_cross_entropy.py: the chunked forward and the
+ * reduction="none" loss-only branch).
+ *   X [N, D], W [C, D] of dtype; b [C] of dtype or NULL; target [N] int64.
+ *   loss_out: [1] for sum / mean, [N] for none. mean with no valid row
+ *   (N == 0 or every row ignored) gives NaN; sum over no row gives 0.
+ *   lse_out: NULL or [N] fp32, receives log sum_j exp z[n, j].
+ */
+LCE_API int lce_forward(const void* X, const void* W, const void* b, const int64_t* target,
+                int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype,
+                int reduction, int64_t ignore_index,
+                float* loss_out, float* lse_out,
+                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Loss and gradients in one call.
+ *   grad_out: sum / mean: NULL (= 1.0) or a device fp32 scalar g; the
+ *             gradients are those of the loss times g (the scalar-reduction
+ *             ops of linear_cross_entropy.py precompute the gradients and
+ *             scale them by grad_output in the backward).
+ *             none: required, [N] fp32 per-row upstream gradient; the
+ *             gradients are the vector-Jacobian product (grad_output folded
+ *             into neg_weight_target).
+ *   loss_out: as lce_forward (the forward loss, not multiplied by g).
+ *   dX [N, D], dW [C, D], db [C] of grad_dtype; a NULL pointer skips that
+ *   gradient (like compute_input_grad / compute_linear_weight_grad /
+ *   compute_linear_bias_grad). db is only computed when b is given.
+ *   mean with every row ignored gives NaN loss and NaN gradients
+ *   (neg_weight_target divides by NaN when the valid count is 0).
+ */
+LCE_API int lce_forward_backward(const void* X, const void* W, const void* b, const int64_t* target,
+                         int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype,
+                         int reduction, int64_t ignore_index, const float* grad_out,
+                         float* loss_out, void* dX, void* dW, void* db, int grad_dtype,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Cross entropy on given logits [N, V] (dtype LCE_F32 or LCE_BF16); the
+ * gradient w_n (softmax - onehot) REPLACES the logits in place, in the
+ * logits' own type (a PyTorch wrapper must declare the tensor dirty).
+ *   grad_out: as lce_forward_backward (NULL = 1.0 for sum / mean: no extra
+ *   scaling; required [N] for none). loss_out: [1] or [N].
+ * Liger-Kernel issue #343: loss and gradient in one pass, gradient written
+ * into the input buffer, so no separate gradient pass or accumulation runs.
+ */
+LCE_API int lce_cross_entropy_from_logits(void* logits_inout, const int64_t* target,
+                                  int64_t N, int64_t V, int dtype, int reduction,
+                                  int64_t ignore_index, const float* grad_out,
+                                  float* loss_out, void* workspace, size_t ws_bytes,
+                                  void* stream);
+
+/* Human-readable text of a status code (static storage). */
+LCE_API const char* lce_status_string(int status);
+
+/*
+ * Device-side status of the last call that used this workspace: waits for
+ * the stream, then returns LCE_OK, LCE_ERR_TARGET_RANGE or LCE_ERR_TIMEOUT
+ * (LCE_ERR_CUDA if the read itself fails). workspace is the device pointer
+ * given to that call.
+ */
+LCE_API int lce_read_device_status(const void* workspace, void* stream);
+
+/*
+ * Kernel accounting (used by the benchmark; not needed for the math).
+ * lce_launch_count: kernels this library has launched since it was loaded.
+ * lce_profile_enable(1): from now on, bracket every launch with CUDA events
+ * on the launching stream; lce_profile_enable(0) stops, and
+ * lce_profile_reset clears the records. lce_profile_query waits for the
+ * recorded events and returns, for one kernel id, the number of launches
+ * and their summed duration in ms. lce_kernel_name gives the id's name;
+ * ids run from 0 to lce_num_kernel_ids() - 1. Not thread-safe.
+ */
+LCE_API int64_t lce_launch_count(void);
+LCE_API int lce_profile_enable(int on);
+LCE_API int lce_profile_reset(void);
+LCE_API int lce_profile_query(int kernel_id, int64_t* launches, double* total_ms);
+LCE_API const char* lce_kernel_name(int kernel_id);
+LCE_API int lce_num_kernel_ids(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCE_H_ */

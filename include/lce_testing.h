@@ -1,0 +1,53 @@
+/*
+ * lce_testing.h -- building-block entry points of liblce.so for tests.
+ *
+ * These expose the two GEMM engines that the fused loss is built from, so a
+ * test can check a contraction on its own. They are not part of the loss
+ * computation's interface. The source pages define the contractions used
+ * (PyTorch commit ddfa80bd "Fix NJT linear_backward() memory usage":
+ * dX = G W and dW = G^T X; linear_cross_entropy.py: logits = X W^T); the
+ * operand layouts below are the three that those products need.
+ *
+ * out[m, n] = sum_k A(m, k) B(n, k), fp32 [M, N] row-major, written.
+ *   A(m, k) = A[m * K + k] when a_mn_major == 0 (A stored [M, K]),
+ *             A[k * M + m] when a_mn_major == 1 (A stored [K, M]).
+ *   B(n, k) = B[n * K + k] when b_mn_major == 0 (B stored [N, K]),
+ *             B[k * N + n] when b_mn_major == 1 (B stored [K, N]).
+ * All pointers are device pointers; stream is a cudaStream_t. dev_status
+ * is NULL or a device int that receives LCE status bits (2 = a pipeline
+ * wait timed out); it is OR-ed, not cleared.
+ *
+ * lce_test_gemm_bf16: bf16 A, B on the tcgen05 tensor cores (TMA-fed,
+ *   fp32 accumulation in tensor memory). Needs the contiguous dimension of
+ *   each operand to be a multiple of 8 and 16-byte aligned pointers.
+ * lce_test_gemm_f32: fp32 A, B with fp32 FMA on the CUDA cores; any shape.
+ * Return an lce_status_e code.
+ */
+#ifndef LCE_TESTING_H_
+#define LCE_TESTING_H_
+
+#include <stdint.h>
+
+#ifndef LCE_API
+#if defined(__GNUC__)
+#define LCE_API __attribute__((visibility("default")))
+#else
+#define LCE_API
+#endif
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+LCE_API int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t M, int64_t N,
+                       int64_t K, int a_mn_major, int b_mn_major, int* dev_status, void* stream);
+
+LCE_API int lce_test_gemm_f32(const float* A, const float* B, float* out, int64_t M, int64_t N,
+                      int64_t K, int a_mn_major, int b_mn_major, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCE_TESTING_H_ */

@@ -1,0 +1,278 @@
+"""Fused linear + cross-entropy loss for GB300 (sm_103a).
+
+A thin ctypes binding over liblce.so (see include/lce.h). Every step of the
+computation runs in the library's CUDA kernels; this module only marshals
+arguments: it allocates outputs and the workspace with torch, takes the data
+pointers and the current CUDA stream, and raises ``LceError`` on a nonzero
+status. There is no CPU fallback: without the built library every call
+raises.
+
+Functions (same names as the C ABI):
+  lce_workspace_size(op, N, D, C, dtype, reduction, grad_dtype, chunk_rows=0)
+  lce_forward(X, W, b, target, reduction="mean", ignore_index=-100, ...)
+  lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=-100,
+                       grad_out=None, ...)
+  lce_cross_entropy_from_logits(logits, target, reduction="mean",
+                                ignore_index=-100, grad_out=None, ...)
+  lce_status_string(code), lce_read_device_status(workspace)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblce.so")
+
+LCE_F32, LCE_BF16 = 0, 1
+LCE_RED_NONE, LCE_RED_SUM, LCE_RED_MEAN = 0, 1, 2
+LCE_OP_FORWARD, LCE_OP_FORWARD_BACKWARD, LCE_OP_CE_FROM_LOGITS = 0, 1, 2
+STATUS = {
+    0: "LCE_OK", 1: "LCE_ERR_NULL", 2: "LCE_ERR_SHAPE", 3: "LCE_ERR_DTYPE", 4: "LCE_ERR_REDUCTION",
+    5: "LCE_ERR_GRAD_OUT", 6: "LCE_ERR_WORKSPACE", 7: "LCE_ERR_CUDA", 8: "LCE_ERR_TARGET_RANGE",
+    9: "LCE_ERR_ALIGN", 10: "LCE_ERR_TIMEOUT", 11: "LCE_ERR_DEVICE",
+}
+_REDUCTION = {"none": LCE_RED_NONE, "sum": LCE_RED_SUM, "mean": LCE_RED_MEAN}
+_DTYPE = {torch.float32: LCE_F32, torch.bfloat16: LCE_BF16}
+_TORCH_DTYPE = {LCE_F32: torch.float32, LCE_BF16: torch.bfloat16}
+
+_lib = None
+
+c_void_p, c_int, c_int64, c_size_t, c_double = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                                 ctypes.c_size_t, ctypes.c_double)
+
+_SIGNATURES = {
+    "lce_workspace_size": (c_size_t, [c_int, c_int64, c_int64, c_int64, c_int, c_int, c_int, c_int64]),
+    "lce_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int,
+                            c_int, c_int64, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "lce_forward_backward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int,
+                                     c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_int, c_void_p, c_size_t, c_void_p]),
+    "lce_cross_entropy_from_logits": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_int64,
+                                              c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "lce_status_string": (ctypes.c_char_p, [c_int]),
+    "lce_read_device_status": (c_int, [c_void_p, c_void_p]),
+    "lce_launch_count": (c_int64, []),
+    "lce_profile_enable": (c_int, [c_int]),
+    "lce_profile_reset": (c_int, []),
+    "lce_profile_query": (c_int, [c_int, ctypes.POINTER(c_int64), ctypes.POINTER(c_double)]),
+    "lce_kernel_name": (ctypes.c_char_p, [c_int]),
+    "lce_num_kernel_ids": (c_int, []),
+    "lce_test_gemm_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int,
+                                   c_void_p, c_void_p]),
+    "lce_test_gemm_f32": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int,
+                                  c_void_p]),
+}
+
+
+class LceError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({status_string(code)})")
+
+
+def load_library(path: Optional[str] = None):
+    """Load liblce.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build the CUDA library first "
+            "(python -m linear_cross_entropy_lce_gb300._build)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    if _lib is None:
+        return STATUS.get(code, "unknown")
+    return _lib.lce_status_string(code).decode()
+
+
+lce_status_string = status_string
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise LceError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPE:
+        raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+    return _DTYPE[t.dtype]
+
+
+def lce_workspace_size(op: int, N: int, D: int, C: int, dtype: int, reduction: int, grad_dtype: int,
+                       chunk_rows: int = 0) -> int:
+    lib = load_library()
+    return int(lib.lce_workspace_size(op, N, D, C, dtype, reduction, grad_dtype, chunk_rows))
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
+    if workspace is not None:
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _check_inputs(X, W, b, target):
+    if X.dim() != 2 or W.dim() != 2 or X.shape[1] != W.shape[1]:
+        raise ValueError("expected X [N, D] and W [C, D]")
+    if X.dtype != W.dtype or (b is not None and b.dtype != X.dtype):
+        raise TypeError("X, W and b must share one dtype")
+    if target.dtype != torch.int64:
+        raise TypeError("target must be int64")
+    if b is not None and b.shape != (W.shape[0],):
+        raise ValueError(f"expected bias shape ({W.shape[0]},), got {tuple(b.shape)}")
+    for t in (X, W, b, target):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("inputs must be contiguous")
+
+
+def lce_forward(X, W, b, target, reduction="mean", ignore_index=-100, want_lse=False,
+                workspace=None, stream=None):
+    """Loss (fp32 scalar, or [N] for 'none') and optionally lse [N]."""
+    lib = load_library()
+    _check_inputs(X, W, b, target)
+    N, D = X.shape
+    C = W.shape[0]
+    red = _REDUCTION[reduction]
+    dt = _dtype_code(X)
+    dev = X.device
+    loss = torch.empty(N if red == LCE_RED_NONE else 1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if want_lse else None
+    nbytes = lib.lce_workspace_size(LCE_OP_FORWARD, N, D, C, dt, red, LCE_F32, 0)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib.lce_forward(_ptr(X), _ptr(W), _ptr(b), _ptr(target), N, D, C, dt, LCE_F32, red, ignore_index,
+                           _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), "lce_forward")
+    loss = loss if red == LCE_RED_NONE else loss[0]
+    return (loss, lse) if want_lse else loss
+
+
+def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=-100, grad_out=None,
+                         want_dx=True, want_dw=True, want_db=True, grad_dtype=None, chunk_rows=0,
+                         workspace=None, stream=None):
+    """Loss and (dX, dW, db); a gradient not wanted (or db without bias) is None.
+
+    grad_out: None (= 1) or a scalar / 1-element tensor for sum and mean; a
+    float32 [N] tensor for 'none'.
+    """
+    lib = load_library()
+    _check_inputs(X, W, b, target)
+    N, D = X.shape
+    C = W.shape[0]
+    red = _REDUCTION[reduction]
+    dt = _dtype_code(X)
+    gdt = dt if grad_dtype is None else _DTYPE[grad_dtype]
+    gtype = _TORCH_DTYPE[gdt]
+    dev = X.device
+    g = None
+    if grad_out is not None:
+        g = torch.as_tensor(grad_out, dtype=torch.float32, device=dev).reshape(-1).contiguous()
+        if red != LCE_RED_NONE and g.numel() != 1:
+            raise ValueError("grad_out must be a scalar for sum / mean")
+    loss = torch.empty(N if red == LCE_RED_NONE else 1, dtype=torch.float32, device=dev)
+    dX = torch.empty(N, D, dtype=gtype, device=dev) if want_dx else None
+    dW = torch.empty(C, D, dtype=gtype, device=dev) if want_dw else None
+    db = torch.empty(C, dtype=gtype, device=dev) if (want_db and b is not None) else None
+    nbytes = lib.lce_workspace_size(LCE_OP_FORWARD_BACKWARD, N, D, C, dt, red, gdt, chunk_rows)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib.lce_forward_backward(_ptr(X), _ptr(W), _ptr(b), _ptr(target), N, D, C, dt, LCE_F32, red,
+                                    ignore_index, _ptr(g), _ptr(loss), _ptr(dX), _ptr(dW), _ptr(db), gdt,
+                                    _ptr(ws), ws.numel(), _stream(stream)), "lce_forward_backward")
+    return (loss if red == LCE_RED_NONE else loss[0]), dX, dW, db
+
+
+def lce_cross_entropy_from_logits(logits, target, reduction="mean", ignore_index=-100, grad_out=None,
+                                  workspace=None, stream=None):
+    """Loss; the gradient overwrites ``logits`` in place."""
+    lib = load_library()
+    if logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("expected contiguous logits [N, V]")
+    if target.dtype != torch.int64:
+        raise TypeError("target must be int64")
+    N, V = logits.shape
+    red = _REDUCTION[reduction]
+    dt = _dtype_code(logits)
+    dev = logits.device
+    g = None
+    if grad_out is not None:
+        g = torch.as_tensor(grad_out, dtype=torch.float32, device=dev).reshape(-1).contiguous()
+    loss = torch.empty(N if red == LCE_RED_NONE else 1, dtype=torch.float32, device=dev)
+    nbytes = lib.lce_workspace_size(LCE_OP_CE_FROM_LOGITS, N, 1, V, dt, red, dt, 0)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(lib.lce_cross_entropy_from_logits(_ptr(logits), _ptr(target), N, V, dt, red, ignore_index, _ptr(g),
+                                             _ptr(loss), _ptr(ws), ws.numel(), _stream(stream)),
+           "lce_cross_entropy_from_logits")
+    return loss if red == LCE_RED_NONE else loss[0]
+
+
+def lce_read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    lib = load_library()
+    return int(lib.lce_read_device_status(_ptr(workspace), _stream(stream)))
+
+
+# ---- kernel accounting (benchmark support)
+
+def launch_count() -> int:
+    return int(load_library().lce_launch_count())
+
+
+def profile_enable(on: bool = True):
+    load_library().lce_profile_enable(1 if on else 0)
+
+
+def profile_reset():
+    load_library().lce_profile_reset()
+
+
+def profile_summary() -> dict:
+    """{kernel name: (launches, total ms)} for the recorded launches."""
+    lib = load_library()
+    out = {}
+    for k in range(lib.lce_num_kernel_ids()):
+        n = c_int64(0)
+        ms = c_double(0.0)
+        _check(lib.lce_profile_query(k, ctypes.byref(n), ctypes.byref(ms)), "lce_profile_query")
+        if n.value:
+            out[lib.lce_kernel_name(k).decode()] = (int(n.value), float(ms.value))
+    return out
+
+
+# ---- building-block checks (include/lce_testing.h)
+
+def test_gemm_bf16(A, B, M, N, K, a_mn_major, b_mn_major, status=None, stream=None):
+    lib = load_library()
+    out = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    _check(lib.lce_test_gemm_bf16(_ptr(A), _ptr(B), _ptr(out), M, N, K, int(a_mn_major), int(b_mn_major),
+                                  _ptr(status), _stream(stream)), "lce_test_gemm_bf16")
+    return out
+
+
+def test_gemm_f32(A, B, M, N, K, a_mn_major, b_mn_major, stream=None):
+    lib = load_library()
+    out = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    _check(lib.lce_test_gemm_f32(_ptr(A), _ptr(B), _ptr(out), M, N, K, int(a_mn_major), int(b_mn_major),
+                                 _stream(stream)), "lce_test_gemm_f32")
+    return out

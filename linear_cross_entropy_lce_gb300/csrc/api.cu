@@ -1,0 +1,583 @@
+// api.cu -- the C ABI of liblce.so: argument checks, workspace plan, and the
+// launch sequence of the fused linear + cross-entropy loss.
+//
+// Launch sequence of lce_forward_backward for one call (all on `stream`):
+//   prep            valid-target count n_valid, target-range check
+//   per batch chunk of Bc rows (the page's batch chunking, with Bc chosen
+//   from the workspace so that a single chunk is the common case on GB300):
+//     logits GEMM   z = X_c W^T (+ b) with the per-segment (max, sum-exp)
+//                   epilogue; stores P~ = exp(z - m_seg) in the chunk buffer
+//     combine       row lse, loss_n, scales w_n exp(m_seg - lse), G at target
+//     grad          chunk buffer P~ -> G in place (+ bias-gradient column sums)
+//     dX GEMM       dX_c = G W
+//     dW GEMM       dW (+)= G^T X_c
+//   loss finalize, bias-gradient finalize
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "../../include/lce.h"
+#include "../../include/lce_testing.h"
+#include "internal.h"
+
+namespace lce {
+
+// ------------------------------------------------------------ device facts
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {0};
+int g_cc_ok[kMaxDevices] = {0};  // 0 unknown, 1 ok, -1 not sm_103
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+}  // namespace
+
+int num_sms() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 148;
+  if (g_sms[d] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    g_sms[d] = n > 0 ? n : 148;
+  }
+  return g_sms[d];
+}
+
+static int check_device() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return LCE_ERR_CUDA;
+  if (g_cc_ok[d] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess)
+      return LCE_ERR_CUDA;
+    g_cc_ok[d] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return g_cc_ok[d] == 1 ? LCE_OK : LCE_ERR_DEVICE;
+}
+
+// ------------------------------------------------------------ profiler
+namespace {
+struct ProfRec {
+  int id;
+  cudaEvent_t a, b;
+};
+std::vector<ProfRec> g_recs;
+bool g_prof = false;
+std::atomic<int64_t> g_launches{0};
+const char* kNames[K_NUM_IDS] = {
+    "prep",          "gemm_logits_tc", "gemm_dx_tc",  "gemm_dw_tc",      "gemm_logits_simt",
+    "gemm_dx_simt",  "gemm_dw_simt",   "lse_combine", "grad_logits",     "loss_finalize",
+    "db_finalize",   "ce_resident",    "ce_stream",   "gemm_test"};
+}  // namespace
+
+const char* kernel_id_name(int id) { return (id >= 0 && id < K_NUM_IDS) ? kNames[id] : "?"; }
+
+void prof_before(int id, cudaStream_t s) {
+  g_launches.fetch_add(1);
+  if (!g_prof) return;
+  ProfRec r{id, nullptr, nullptr};
+  cudaEventCreate(&r.a);
+  cudaEventCreate(&r.b);
+  cudaEventRecord(r.a, s);
+  g_recs.push_back(r);
+}
+void prof_after(int id, cudaStream_t s) {
+  if (!g_prof || g_recs.empty() || g_recs.back().id != id) return;
+  cudaEventRecord(g_recs.back().b, s);
+}
+
+// ------------------------------------------------------------ workspace plan
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int64_t kDefaultChunkBytes = int64_t(4) << 30;  // chunk buffer budget of the default plan
+
+inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int esize(int dt) { return dt == LCE_BF16 ? 2 : 4; }
+
+struct Plan {
+  bool tc;          // tensor-core (bf16) path
+  int segw;         // columns per (max, sum-exp) segment
+  int nseg;
+  int64_t C_pad;    // chunk buffer row pitch (elements)
+  int64_t Bc;       // rows per chunk
+  int64_t nchunks;
+  bool dw_acc;      // fp32 dW accumulator in the workspace
+  size_t off_loss, off_zt, off_tcol, off_gt, off_partial, off_L, off_dw, off_db, total;
+};
+
+// Bytes for chunk size Bc. backward: chunk buffer and gradient scratch;
+// need_dw_acc_if_multi: a bf16 dW needs an fp32 accumulator once Bc < N.
+bool make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, bool want_dw, bool want_db,
+               int64_t Bc, Plan* p) {
+  const bool backward = op == LCE_OP_FORWARD_BACKWARD;
+  p->tc = dtype == LCE_BF16;
+  p->segw = p->tc ? 256 : 64;
+  p->nseg = static_cast<int>(ceil_div(C, p->segw));
+  p->C_pad = p->tc ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
+  if (N == 0) Bc = 0;
+  p->Bc = Bc;
+  p->nchunks = Bc > 0 ? ceil_div(N, Bc) : 0;
+  p->dw_acc = backward && want_dw && p->nchunks > 1 && grad_dtype == LCE_BF16;
+  size_t off = align_up(sizeof(WsHeader));
+  p->off_loss = off;
+  off = align_up(off + static_cast<size_t>(N) * 4);
+  p->off_zt = off;
+  off = align_up(off + static_cast<size_t>(Bc) * 4);
+  p->off_tcol = off;
+  off = align_up(off + static_cast<size_t>(Bc) * 4);
+  p->off_gt = off;
+  off = align_up(off + static_cast<size_t>(Bc) * 4);
+  p->off_partial = off;
+  off = align_up(off + static_cast<size_t>(p->nseg) * static_cast<size_t>(Bc) * 8);
+  p->off_L = off;
+  if (backward) off = align_up(off + static_cast<size_t>(Bc) * static_cast<size_t>(p->C_pad) * esize(dtype));
+  p->off_dw = off;
+  if (p->dw_acc) off = align_up(off + static_cast<size_t>(C) * static_cast<size_t>(D) * 4);
+  p->off_db = off;
+  if (backward && want_db) off = align_up(off + static_cast<size_t>(C) * 4);
+  p->total = off;
+  return true;
+}
+
+int64_t default_chunk(int op, int64_t N, int64_t C, int dtype) {
+  if (N == 0) return 0;
+  const int64_t C_pad = dtype == LCE_BF16 ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
+  const int64_t per_row = (op == LCE_OP_FORWARD_BACKWARD ? C_pad * esize(dtype) : 0) + ceil_div(C, 64) * 8;
+  if (N * per_row <= kDefaultChunkBytes) return N;
+  int64_t bc = 128;
+  while (bc * 2 * per_row <= kDefaultChunkBytes && bc * 2 < N) bc *= 2;
+  return bc;
+}
+
+// Largest chunk (N itself, else 128 * 2^k < N) whose plan fits ws_bytes.
+bool choose_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, bool want_dw, bool want_db,
+                 size_t ws_bytes, Plan* p) {
+  if (N == 0) {
+    make_plan(op, 0, D, C, dtype, grad_dtype, want_dw, want_db, 0, p);
+    return p->total <= ws_bytes;
+  }
+  std::vector<int64_t> cands;
+  cands.push_back(N);
+  int64_t bc = 128;
+  while (bc * 2 < N) bc *= 2;
+  for (; bc >= 128; bc /= 2)
+    if (bc < N) cands.push_back(bc);
+  for (int64_t c : cands) {
+    make_plan(op, N, D, C, dtype, grad_dtype, want_dw, want_db, c, p);
+    if (p->total <= ws_bytes) return true;
+  }
+  return false;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? LCE_OK : LCE_ERR_CUDA; }
+
+int check_common(int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype, int reduction) {
+  if (dtype != LCE_F32 && dtype != LCE_BF16) return LCE_ERR_DTYPE;
+  if (acc_dtype != LCE_F32) return LCE_ERR_DTYPE;
+  if (reduction != LCE_RED_NONE && reduction != LCE_RED_SUM && reduction != LCE_RED_MEAN) return LCE_ERR_REDUCTION;
+  if (N < 0 || D < 1 || C < 1) return LCE_ERR_SHAPE;
+  if (N > (int64_t(1) << 40) || D > (int64_t(1) << 30) || C > (int64_t(1) << 30)) return LCE_ERR_SHAPE;
+  return LCE_OK;
+}
+
+#define LCE_TRY(expr)                        \
+  do {                                       \
+    cudaError_t _e = (expr);                 \
+    if (_e != cudaSuccess) return LCE_ERR_CUDA; \
+  } while (0)
+
+// The shared body of lce_forward and lce_forward_backward.
+int run_lce(bool backward, const void* X, const void* W, const void* b, const int64_t* target, int64_t N,
+            int64_t D, int64_t C, int dtype, int acc_dtype, int reduction, int64_t ignore_index,
+            const float* grad_out, float* loss_out, float* lse_out, void* dX, void* dW, void* db, int grad_dtype,
+            void* workspace, size_t ws_bytes, void* stream) {
+  int st = check_common(N, D, C, dtype, acc_dtype, reduction);
+  if (st != LCE_OK) return st;
+  if (backward && grad_dtype != LCE_F32 && grad_dtype != LCE_BF16) return LCE_ERR_DTYPE;
+  if (N > 0 && (X == nullptr || W == nullptr || target == nullptr || loss_out == nullptr)) return LCE_ERR_NULL;
+  if (reduction != LCE_RED_NONE && loss_out == nullptr) return LCE_ERR_NULL;
+  if (backward && reduction == LCE_RED_NONE && N > 0 && grad_out == nullptr) return LCE_ERR_GRAD_OUT;
+  if (workspace == nullptr) return LCE_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return LCE_ERR_ALIGN;
+  const bool want_dx = backward && dX != nullptr;
+  const bool want_dw = backward && dW != nullptr;
+  const bool want_db = backward && db != nullptr && b != nullptr;
+  if (dtype == LCE_BF16) {
+    if (D % 8 != 0) return LCE_ERR_ALIGN;
+    if (N > 0 && (!aligned16(X) || !aligned16(W))) return LCE_ERR_ALIGN;
+    if ((want_dx && !aligned16(dX)) || (want_dw && !aligned16(dW))) return LCE_ERR_ALIGN;
+  }
+  Plan p;
+  if (!choose_plan(backward ? LCE_OP_FORWARD_BACKWARD : LCE_OP_FORWARD, N, D, C, dtype, grad_dtype, want_dw,
+                   want_db, ws_bytes, &p))
+    return LCE_ERR_WORKSPACE;
+  if (p.Bc > 2147483647LL) return LCE_ERR_SHAPE;
+  st = check_device();
+  if (st != LCE_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  float* loss_rows = reinterpret_cast<float*>(ws + p.off_loss);
+  float* zt = reinterpret_cast<float*>(ws + p.off_zt);
+  int* tcol = reinterpret_cast<int*>(ws + p.off_tcol);
+  float* gt = reinterpret_cast<float*>(ws + p.off_gt);
+  float2* partial = reinterpret_cast<float2*>(ws + p.off_partial);
+  void* Lbuf = ws + p.off_L;
+  float* dw_acc = reinterpret_cast<float*>(ws + p.off_dw);
+  float* db_acc = reinterpret_cast<float*>(ws + p.off_db);
+  const int gsz = grad_dtype == LCE_BF16 ? 2 : 4;
+
+  LCE_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
+  if (N == 0) {
+    if (reduction != LCE_RED_NONE) LCE_TRY(launch_loss_finalize(loss_rows, 0, reduction, hdr, loss_out, s));
+    if (want_dw) LCE_TRY(cudaMemsetAsync(dW, 0, static_cast<size_t>(C) * D * gsz, s));
+    if (want_db) LCE_TRY(cudaMemsetAsync(db, 0, static_cast<size_t>(C) * gsz, s));
+    return LCE_OK;
+  }
+  LCE_TRY(launch_prep(target, N, C, ignore_index, hdr, s));
+  if (want_db) LCE_TRY(cudaMemsetAsync(db_acc, 0, static_cast<size_t>(C) * 4, s));
+  float* rows_out = reduction == LCE_RED_NONE ? loss_out : loss_rows;
+
+  RowWeight rw;
+  rw.grad_out = grad_out;
+  rw.reduction = reduction;
+  rw.grad_is_vector = reduction == LCE_RED_NONE ? 1 : 0;
+
+  CUtensorMap tmW_k, tmW_n;
+  if (p.tc) {
+    if (!encode_tmap_bf16(&tmW_k, W, D, C, D, TC_BN)) return LCE_ERR_CUDA;
+    if (want_dx && !encode_tmap_bf16(&tmW_n, W, D, C, D, 64)) return LCE_ERR_CUDA;
+  }
+
+  for (int64_t ci = 0; ci < p.nchunks; ++ci) {
+    const int64_t row0 = ci * p.Bc;
+    const int64_t rows = std::min(p.Bc, N - row0);
+    // ---- logits GEMM with the (max, sum-exp) epilogue
+    EpiLse::Params el;
+    el.bias = b;
+    el.bias_bf16 = dtype == LCE_BF16;
+    el.target = target + row0;
+    el.C = C;
+    el.rows = static_cast<int>(rows);
+    el.partial = partial;
+    el.partial_ld = p.Bc;
+    el.zt = zt;
+    el.ptilde = backward ? Lbuf : nullptr;
+    el.ld_p = p.C_pad;
+    el.ptilde_bf16 = dtype == LCE_BF16;
+    if (p.tc) {
+      const void* Xc = static_cast<const __nv_bfloat16*>(X) + row0 * D;
+      CUtensorMap tmX_k;
+      if (!encode_tmap_bf16(&tmX_k, Xc, D, rows, D, TC_BM)) return LCE_ERR_CUDA;
+      LCE_TRY(launch_tc_logits(tmX_k, tmW_k, static_cast<int>(rows), static_cast<int>(C), static_cast<int>(D),
+                               &hdr->status, el, s));
+    } else {
+      const float* Xc = static_cast<const float*>(X) + row0 * D;
+      LCE_TRY(launch_simt_logits(Xc, static_cast<const float*>(W), D, D, rows, C, D, el, s));
+    }
+    // ---- row lse, loss, scales
+    CombineArgs ca;
+    ca.partial = partial;
+    ca.ld = p.Bc;
+    ca.nseg = p.nseg;
+    ca.rows = rows;
+    ca.row0 = row0;
+    ca.zt = zt;
+    ca.tcol = tcol;
+    ca.gt = gt;
+    ca.target = target;
+    ca.ignore_index = ignore_index;
+    ca.C = C;
+    ca.rw = rw;
+    ca.hdr = hdr;
+    ca.loss_rows = rows_out;
+    ca.lse_out = lse_out;
+    ca.backward = backward ? 1 : 0;
+    LCE_TRY(launch_combine(ca, s));
+    if (!backward) continue;
+    // ---- G in place
+    GradArgs ga;
+    ga.L = Lbuf;
+    ga.ld = p.C_pad;
+    ga.rows = rows;
+    ga.C = C;
+    ga.segw = p.segw;
+    ga.nseg = p.nseg;
+    ga.scale = partial;
+    ga.sld = p.Bc;
+    ga.tcol = tcol;
+    ga.gt = gt;
+    ga.db_acc = want_db ? db_acc : nullptr;
+    LCE_TRY(launch_grad_logits(ga, dtype == LCE_BF16, s));
+    // ---- dX = G W
+    if (want_dx) {
+      EpiStore::Params es;
+      es.out = static_cast<uint8_t*>(dX) + static_cast<size_t>(row0) * D * gsz;
+      es.out_bf16 = grad_dtype == LCE_BF16;
+      es.ldo = D;
+      es.acc32 = nullptr;
+      es.mode = 0;
+      es.rows = rows;
+      es.cols = D;
+      es.vec_ok = aligned16(dX) && ((D * gsz) % 16 == 0);
+      if (p.tc) {
+        CUtensorMap tmG_k;
+        if (!encode_tmap_bf16(&tmG_k, Lbuf, C, rows, p.C_pad, TC_BM)) return LCE_ERR_CUDA;
+        LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmW_n, static_cast<int>(rows), static_cast<int>(D),
+                                static_cast<int>(C), &hdr->status, es, s));
+      } else {
+        LCE_TRY(launch_simt_store(TC_DX, static_cast<const float*>(Lbuf), static_cast<const float*>(W), p.C_pad, D,
+                                  rows, D, C, es, s));
+      }
+    }
+    // ---- dW (+)= G^T X_c
+    if (want_dw) {
+      EpiStore::Params es;
+      es.out = dW;
+      es.out_bf16 = grad_dtype == LCE_BF16;
+      es.ldo = D;
+      es.rows = C;
+      es.cols = D;
+      es.vec_ok = aligned16(dW) && ((D * gsz) % 16 == 0);
+      if (p.nchunks == 1) {
+        es.mode = 0;
+        es.acc32 = nullptr;
+      } else if (grad_dtype == LCE_F32) {
+        es.mode = ci == 0 ? 0 : 2;
+        es.acc32 = static_cast<float*>(dW);
+      } else {
+        es.mode = ci == 0 ? 1 : (ci == p.nchunks - 1 ? 3 : 2);
+        es.acc32 = dw_acc;
+      }
+      if (p.tc) {
+        const void* Xc = static_cast<const __nv_bfloat16*>(X) + row0 * D;
+        CUtensorMap tmG_m, tmX_n;
+        if (!encode_tmap_bf16(&tmG_m, Lbuf, C, rows, p.C_pad, 64)) return LCE_ERR_CUDA;
+        if (!encode_tmap_bf16(&tmX_n, Xc, D, rows, D, 64)) return LCE_ERR_CUDA;
+        LCE_TRY(launch_tc_store(TC_DW, tmG_m, tmX_n, static_cast<int>(C), static_cast<int>(D),
+                                static_cast<int>(rows), &hdr->status, es, s));
+      } else {
+        const float* Xc = static_cast<const float*>(X) + row0 * D;
+        LCE_TRY(launch_simt_store(TC_DW, static_cast<const float*>(Lbuf), Xc, p.C_pad, D, C, D, rows, es, s));
+      }
+    }
+  }
+  if (reduction != LCE_RED_NONE) LCE_TRY(launch_loss_finalize(loss_rows, N, reduction, hdr, loss_out, s));
+  if (want_db) LCE_TRY(launch_db_finalize(db_acc, db, C, grad_dtype == LCE_BF16, s));
+  return LCE_OK;
+}
+
+}  // namespace
+}  // namespace lce
+
+using namespace lce;
+
+extern "C" {
+
+size_t lce_workspace_size(int op, int64_t N, int64_t D, int64_t C, int dtype, int reduction, int grad_dtype,
+                          int64_t chunk_rows) {
+  if (op == LCE_OP_CE_FROM_LOGITS) {
+    if (N < 0 || C < 1) return 0;
+    return align_up(sizeof(WsHeader)) + align_up(static_cast<size_t>(N) * 4);
+  }
+  if (op != LCE_OP_FORWARD && op != LCE_OP_FORWARD_BACKWARD) return 0;
+  if (check_common(N, D, C, dtype, LCE_F32, reduction) != LCE_OK) return 0;
+  if (op == LCE_OP_FORWARD_BACKWARD && grad_dtype != LCE_F32 && grad_dtype != LCE_BF16) return 0;
+  if (chunk_rows < 0) return 0;
+  int64_t bc;
+  if (chunk_rows == 0) {
+    bc = default_chunk(op, N, C, dtype);
+  } else if (chunk_rows >= N) {
+    bc = N;
+  } else {
+    // the calls use N or a power of two times 128 rows
+    bc = 128;
+    while (bc * 2 <= chunk_rows) bc *= 2;
+    if (bc >= N) bc = N;
+  }
+  Plan p;
+  make_plan(op, N, D, C, dtype, grad_dtype, true, true, bc, &p);
+  return p.total;
+}
+
+int lce_forward(const void* X, const void* W, const void* b, const int64_t* target, int64_t N, int64_t D, int64_t C,
+                int dtype, int acc_dtype, int reduction, int64_t ignore_index, float* loss_out, float* lse_out,
+                void* workspace, size_t ws_bytes, void* stream) {
+  return run_lce(false, X, W, b, target, N, D, C, dtype, acc_dtype, reduction, ignore_index, nullptr, loss_out,
+                 lse_out, nullptr, nullptr, nullptr, LCE_F32, workspace, ws_bytes, stream);
+}
+
+int lce_forward_backward(const void* X, const void* W, const void* b, const int64_t* target, int64_t N, int64_t D,
+                         int64_t C, int dtype, int acc_dtype, int reduction, int64_t ignore_index,
+                         const float* grad_out, float* loss_out, void* dX, void* dW, void* db, int grad_dtype,
+                         void* workspace, size_t ws_bytes, void* stream) {
+  return run_lce(true, X, W, b, target, N, D, C, dtype, acc_dtype, reduction, ignore_index, grad_out, loss_out,
+                 nullptr, dX, dW, db, grad_dtype, workspace, ws_bytes, stream);
+}
+
+int lce_cross_entropy_from_logits(void* logits_inout, const int64_t* target, int64_t N, int64_t V, int dtype,
+                                  int reduction, int64_t ignore_index, const float* grad_out, float* loss_out,
+                                  void* workspace, size_t ws_bytes, void* stream) {
+  if (dtype != LCE_F32 && dtype != LCE_BF16) return LCE_ERR_DTYPE;
+  if (reduction != LCE_RED_NONE && reduction != LCE_RED_SUM && reduction != LCE_RED_MEAN) return LCE_ERR_REDUCTION;
+  if (N < 0 || V < 1 || N > (int64_t(1) << 40) || V > (int64_t(1) << 40)) return LCE_ERR_SHAPE;
+  if (N > 0 && (logits_inout == nullptr || target == nullptr || loss_out == nullptr)) return LCE_ERR_NULL;
+  if (reduction != LCE_RED_NONE && loss_out == nullptr) return LCE_ERR_NULL;
+  if (reduction == LCE_RED_NONE && N > 0 && grad_out == nullptr) return LCE_ERR_GRAD_OUT;
+  if (workspace == nullptr) return LCE_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return LCE_ERR_ALIGN;
+  if (ws_bytes < lce_workspace_size(LCE_OP_CE_FROM_LOGITS, N, 1, V, dtype, reduction, dtype, 0))
+    return LCE_ERR_WORKSPACE;
+  int st = check_device();
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  float* loss_rows = reinterpret_cast<float*>(ws + align_up(sizeof(WsHeader)));
+  LCE_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
+  if (N > 0) {
+    LCE_TRY(launch_prep(target, N, V, ignore_index, hdr, s));
+    CeArgs a;
+    a.logits = logits_inout;
+    a.N = N;
+    a.V = V;
+    a.target = target;
+    a.ignore_index = ignore_index;
+    a.rw.grad_out = grad_out;
+    a.rw.reduction = reduction;
+    a.rw.grad_is_vector = reduction == LCE_RED_NONE ? 1 : 0;
+    a.hdr = hdr;
+    a.loss_rows = reduction == LCE_RED_NONE ? loss_out : loss_rows;
+    a.status = &hdr->status;
+    LCE_TRY(launch_ce_logits(a, dtype == LCE_BF16, s));
+  }
+  if (reduction != LCE_RED_NONE) LCE_TRY(launch_loss_finalize(loss_rows, N, reduction, hdr, loss_out, s));
+  return LCE_OK;
+}
+
+const char* lce_status_string(int status) {
+  switch (status) {
+    case LCE_OK: return "ok";
+    case LCE_ERR_NULL: return "a required pointer is NULL";
+    case LCE_ERR_SHAPE: return "invalid problem size";
+    case LCE_ERR_DTYPE: return "unsupported dtype (inputs fp32/bf16, accumulation fp32)";
+    case LCE_ERR_REDUCTION: return "reduction must be none, sum or mean";
+    case LCE_ERR_GRAD_OUT: return "reduction none needs a per-row upstream gradient";
+    case LCE_ERR_WORKSPACE: return "workspace missing or too small";
+    case LCE_ERR_CUDA: return "CUDA runtime error or kernel launch failure";
+    case LCE_ERR_TARGET_RANGE: return "a target is neither ignore_index nor a class index";
+    case LCE_ERR_ALIGN: return "bf16 path needs D % 8 == 0 and 16-byte aligned buffers";
+    case LCE_ERR_TIMEOUT: return "a device pipeline wait timed out";
+    case LCE_ERR_DEVICE: return "device is not compute capability 10.3 (GB300)";
+    default: return "unknown status";
+  }
+}
+
+int lce_read_device_status(const void* workspace, void* stream) {
+  if (workspace == nullptr) return LCE_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LCE_ERR_CUDA;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LCE_ERR_CUDA;
+  if (v & kStatusTimeout) return LCE_ERR_TIMEOUT;
+  if (v & kStatusTargetRange) return LCE_ERR_TARGET_RANGE;
+  return LCE_OK;
+}
+
+int64_t lce_launch_count(void) { return g_launches.load(); }
+
+int lce_profile_enable(int on) {
+  g_prof = on != 0;
+  return LCE_OK;
+}
+
+int lce_profile_reset(void) {
+  for (auto& r : g_recs) {
+    if (r.a) cudaEventDestroy(r.a);
+    if (r.b) cudaEventDestroy(r.b);
+  }
+  g_recs.clear();
+  return LCE_OK;
+}
+
+int lce_profile_query(int kernel_id, int64_t* launches, double* total_ms) {
+  if (launches == nullptr || total_ms == nullptr) return LCE_ERR_NULL;
+  int64_t n = 0;
+  double tot = 0.0;
+  for (auto& r : g_recs) {
+    if (r.id != kernel_id || r.b == nullptr) continue;
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return LCE_ERR_CUDA;
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return LCE_ERR_CUDA;
+    ++n;
+    tot += ms;
+  }
+  *launches = n;
+  *total_ms = tot;
+  return LCE_OK;
+}
+
+const char* lce_kernel_name(int kernel_id) { return kernel_id_name(kernel_id); }
+int lce_num_kernel_ids(void) { return K_NUM_IDS; }
+
+int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t M, int64_t N, int64_t K, int a_mn_major,
+                       int b_mn_major, int* dev_status, void* stream) {
+  if (A == nullptr || B == nullptr || out == nullptr) return LCE_ERR_NULL;
+  if (M < 1 || N < 1 || K < 1 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return LCE_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return LCE_ERR_ALIGN;
+  if ((a_mn_major ? M : K) % 8 != 0 || (b_mn_major ? N : K) % 8 != 0) return LCE_ERR_ALIGN;
+  int st = check_device();
+  if (st != LCE_OK) return st;
+  CUtensorMap ta, tb;
+  bool ok = a_mn_major ? encode_tmap_bf16(&ta, A, M, K, M, 64) : encode_tmap_bf16(&ta, A, K, M, K, TC_BM);
+  ok = ok && (b_mn_major ? encode_tmap_bf16(&tb, B, N, K, N, 64) : encode_tmap_bf16(&tb, B, K, N, K, TC_BN));
+  if (!ok) return LCE_ERR_CUDA;
+  EpiStore::Params es;
+  es.out = out;
+  es.out_bf16 = 0;
+  es.ldo = N;
+  es.acc32 = nullptr;
+  es.mode = 0;
+  es.rows = M;
+  es.cols = N;
+  es.vec_ok = (N % 4) == 0;
+  const int op = a_mn_major ? (b_mn_major ? TC_TEST_MM : TC_TEST_MK) : (b_mn_major ? TC_TEST_KM : TC_TEST_KK);
+  return from_cuda(launch_tc_store(op, ta, tb, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                                   dev_status, es, static_cast<cudaStream_t>(stream)));
+}
+
+int lce_test_gemm_f32(const float* A, const float* B, float* out, int64_t M, int64_t N, int64_t K, int a_mn_major,
+                      int b_mn_major, void* stream) {
+  if (A == nullptr || B == nullptr || out == nullptr) return LCE_ERR_NULL;
+  if (M < 1 || N < 1 || K < 1) return LCE_ERR_SHAPE;
+  int st = check_device();
+  if (st != LCE_OK) return st;
+  EpiStore::Params es;
+  es.out = out;
+  es.out_bf16 = 0;
+  es.ldo = N;
+  es.acc32 = nullptr;
+  es.mode = 0;
+  es.rows = M;
+  es.cols = N;
+  es.vec_ok = aligned16(out) && (N % 4) == 0;
+  const int op = a_mn_major ? (b_mn_major ? TC_TEST_MM : TC_TEST_MK) : (b_mn_major ? TC_TEST_KM : TC_TEST_KK);
+  return from_cuda(launch_simt_store(op, A, B, a_mn_major ? M : K, b_mn_major ? N : K, M, N, K, es,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,259 @@
+// ce_logits.cu -- cross entropy on given logits, gradient written in place.
+//
+// Liger-Kernel issue #343 ("cross entropy kernel: inplace modification of
+// input") describes one kernel that produces the loss and overwrites the
+// logits with dLoss/dlogits during the forward. Here the whole row is read
+// from HBM once and written once:
+//
+//  * resident kernel: a thread-block cluster of CS CTAs (CS = 1..8) owns a
+//    row; each CTA holds a 16384-element slice in registers (512 threads x
+//    32 elements, 16-byte vector loads), reduces its slice to (max, sum-exp),
+//    exchanges the pairs through distributed shared memory, and writes
+//    g * w_n * (softmax - onehot) back from registers. Clusters walk the
+//    rows persistently. Needs V <= 8 * 16384 and 16-byte aligned rows.
+//  * streaming kernel (any V, any alignment): one CTA per row, online
+//    (max, sum-exp) in a first pass, gradient in a second pass that reads
+//    the row again (largely from L2).
+#include <cfloat>
+
+#include "internal.h"
+
+namespace lce {
+
+namespace {
+
+constexpr int CE_THREADS = 512;
+constexpr int CE_EPT = 32;
+constexpr int64_t CE_SLICE = static_cast<int64_t>(CE_THREADS) * CE_EPT;  // 16384
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+// Block-wide reductions over CE_THREADS threads; every thread gets the result.
+__device__ __forceinline__ float block_max(float v, float* scratch) {
+  v = warp_max(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  v = (lane < (int)(blockDim.x >> 5)) ? scratch[lane] : -INFINITY;
+  return warp_max(v);
+}
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  v = (lane < (int)(blockDim.x >> 5)) ? scratch[lane] : 0.0f;
+  return warp_sum(v);
+}
+
+template <class T>
+__device__ __forceinline__ void load_vec(const T* p, float* x);
+template <>
+__device__ __forceinline__ void load_vec<float>(const float* p, float* x) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  x[0] = v.x;
+  x[1] = v.y;
+  x[2] = v.z;
+  x[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void load_vec<__nv_bfloat16>(const __nv_bfloat16* p, float* x) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+template <class T>
+__device__ __forceinline__ void store_vec(T* p, const float* x);
+template <>
+__device__ __forceinline__ void store_vec<float>(float* p, const float* x) {
+  *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+}
+template <>
+__device__ __forceinline__ void store_vec<__nv_bfloat16>(__nv_bfloat16* p, const float* x) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+template <class T>
+__global__ void __launch_bounds__(CE_THREADS, 2) ce_resident_kernel(const CeArgs a, int cs) {
+  constexpr int VE = 16 / static_cast<int>(sizeof(T));
+  constexpr int NV = CE_EPT / VE;
+  __shared__ float scratch[32];
+  __shared__ float xch[2][2];
+  __shared__ float bc[2];
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t cid = cluster_id_x();
+  const uint32_t ncl = nclusters_x();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t V = a.V;
+  const int64_t sbeg = static_cast<int64_t>(rank) * CE_SLICE;
+  int iter = 0;
+  for (int64_t row = cid; row < a.N; row += ncl, ++iter) {
+    T* rowp = static_cast<T*>(a.logits) + row * V;
+    float x[CE_EPT];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t col = sbeg + static_cast<int64_t>(tid + k * CE_THREADS) * VE;
+      if (col + VE <= V) {
+        load_vec<T>(rowp + col, &x[k * VE]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < VE; ++i) x[k * VE + i] = (col + i < V) ? to_f32(rowp[col + i]) : -INFINITY;
+      }
+    }
+    const int64_t t = a.target[row];
+    const bool valid = target_valid(t, a.ignore_index, V);
+    float zt = 0.0f;
+    if (rank == 0 && tid == 0 && valid) zt = to_f32(rowp[t]);  // read before any CTA writes the row
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < CE_EPT; ++i) m = fmaxf(m, x[i]);
+    const float cm = block_max(m, scratch);
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < CE_EPT; ++i) s += fast_exp2((x[i] - cm) * kLog2e);
+    const float csum = block_sum(s, scratch);
+    if (tid == 0) {
+      xch[iter & 1][0] = cm;
+      xch[iter & 1][1] = csum;
+    }
+    cluster_sync();
+    if (warp == 0) {
+      float pm = -INFINITY, ps = 0.0f;
+      if (lane < cs) {
+        pm = dsmem_ld_f32(&xch[iter & 1][0], lane);
+        ps = dsmem_ld_f32(&xch[iter & 1][1], lane);
+      }
+      const float M = warp_max(pm);
+      const float S = warp_sum(lane < cs ? ps * expf(pm - M) : 0.0f);
+      if (lane == 0) {
+        bc[0] = M + logf(S);
+        bc[1] = row_weight(a.rw, &a.hdr->n_valid, row, valid);
+      }
+    }
+    __syncthreads();
+    const float lse = bc[0], w = bc[1];
+    const float lse2 = lse * kLog2e;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t col = sbeg + static_cast<int64_t>(tid + k * CE_THREADS) * VE;
+      float gv[VE];
+#pragma unroll
+      for (int i = 0; i < VE; ++i) {
+        const float p = fast_exp2(fmaf(x[k * VE + i], kLog2e, -lse2));
+        gv[i] = w * ((valid && col + i == t) ? p - 1.0f : p);
+      }
+      if (col + VE <= V) {
+        store_vec<T>(rowp + col, gv);
+      } else {
+#pragma unroll
+        for (int i = 0; i < VE; ++i)
+          if (col + i < V) rowp[col + i] = from_f32<T>(gv[i]);
+      }
+    }
+    if (rank == 0 && tid == 0) a.loss_rows[row] = valid ? lse - zt : 0.0f;
+  }
+  cluster_sync();  // no CTA leaves while a peer may still read its xch
+}
+
+template <class T>
+__global__ void __launch_bounds__(CE_THREADS) ce_stream_kernel(const CeArgs a) {
+  __shared__ float scratch[32];
+  __shared__ float s_zt;
+  const int tid = threadIdx.x;
+  const int64_t V = a.V;
+  for (int64_t row = blockIdx.x; row < a.N; row += gridDim.x) {
+    T* rowp = static_cast<T*>(a.logits) + row * V;
+    const int64_t t = a.target[row];
+    const bool valid = target_valid(t, a.ignore_index, V);
+    if (tid == 0) s_zt = valid ? to_f32(rowp[t]) : 0.0f;
+    float m = -INFINITY, s = 0.0f;
+    for (int64_t j = tid; j < V; j += CE_THREADS) {
+      const float x = to_f32(rowp[j]);
+      if (x > m) {
+        s = s * fast_exp2((m - x) * kLog2e) + 1.0f;
+        m = x;
+      } else {
+        s += fast_exp2((x - m) * kLog2e);
+      }
+    }
+    const float M = block_max(m, scratch);
+    const float S = block_sum(m == -INFINITY ? 0.0f : s * fast_exp2((m - M) * kLog2e), scratch);
+    const float lse = M + logf(S);
+    const float w = row_weight(a.rw, &a.hdr->n_valid, row, valid);
+    const float zt = s_zt;
+    for (int64_t j = tid; j < V; j += CE_THREADS) {
+      const float p = fast_exp2((to_f32(rowp[j]) - lse) * kLog2e);
+      rowp[j] = from_f32<T>(w * ((valid && j == t) ? p - 1.0f : p));
+    }
+    if (tid == 0) a.loss_rows[row] = valid ? lse - zt : 0.0f;
+    __syncthreads();  // s_zt is rewritten for the next row
+  }
+}
+
+template <class T>
+cudaError_t launch_ce_t(const CeArgs& a, cudaStream_t s) {
+  const size_t esz = sizeof(T);
+  const bool aligned = (reinterpret_cast<uintptr_t>(a.logits) % 16 == 0) && ((a.V * esz) % 16 == 0);
+  int cs = 1;
+  while (static_cast<int64_t>(cs) * CE_SLICE < a.V && cs < 8) cs *= 2;
+  if (aligned && static_cast<int64_t>(cs) * CE_SLICE >= a.V) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(CE_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(cs);
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, ce_resident_kernel<T>, &cfg) == cudaSuccess &&
+        max_clusters > 0) {
+      int64_t ncl = max_clusters;
+      if (ncl > a.N) ncl = a.N;
+      cfg.gridDim = dim3(static_cast<unsigned>(ncl * cs));
+      prof_before(K_CE_RESIDENT, s);
+      cudaError_t e = cudaLaunchKernelEx(&cfg, ce_resident_kernel<T>, a, cs);
+      prof_after(K_CE_RESIDENT, s);
+      return e;
+    }
+    cudaGetLastError();  // clear a failed occupancy query and stream the rows instead
+  }
+  int64_t grid = a.N < 4 * num_sms() ? a.N : 4 * num_sms();
+  prof_before(K_CE_STREAM, s);
+  ce_stream_kernel<T><<<static_cast<unsigned>(grid), CE_THREADS, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  prof_after(K_CE_STREAM, s);
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_ce_logits(const CeArgs& a, bool bf16, cudaStream_t s) {
+  if (a.N == 0) return cudaSuccess;
+  return bf16 ? launch_ce_t<__nv_bfloat16>(a, s) : launch_ce_t<float>(a, s);
+}
+
+}  // namespace lce

@@ -1,0 +1,75 @@
+// common.cuh -- types shared by the kernels and the host side of liblce.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/lce.h"
+
+namespace lce {
+
+// Output tile of the tcgen05 GEMM (rows x columns); TC_BN is also the
+// segment width of the per-row (max, sum-exp) partials on the bf16 path.
+constexpr int TC_BM = 128;
+constexpr int TC_BN = 256;
+
+// Bits of the device status word (workspace header).
+constexpr int kStatusTargetRange = 1;
+constexpr int kStatusTimeout = 2;
+
+// Workspace header, at offset 0 of every workspace.
+struct WsHeader {
+  int status;       // kStatus* bits, OR-ed by kernels
+  int n_valid;      // rows whose target is a class index (not ignored, in range)
+  double loss_sum;  // unused padding for alignment / future use
+  int pad[60];
+};
+static_assert(sizeof(WsHeader) <= 256, "header must fit 256 bytes");
+
+// Per-row weight parameters: w_n = valid ? base * (vec ? g[n] : g0) : 0,
+// with base = 1 (sum, none) or 1 / n_valid (mean; NaN when n_valid == 0).
+struct RowWeight {
+  const float* grad_out;  // device scalar (sum/mean) or [N] (none); may be NULL
+  int reduction;
+  int grad_is_vector;
+};
+
+// Element load / store helpers.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <class T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float row_weight(const RowWeight& rw, const int* n_valid_ptr, int64_t n, bool valid) {
+  if (!valid) {
+    // an ignored row still sees NaN under mean with no valid row
+    if (rw.reduction == LCE_RED_MEAN && *n_valid_ptr == 0) return __int_as_float(0x7fc00000);
+    return 0.0f;
+  }
+  float g = 1.0f;
+  if (rw.grad_out != nullptr) g = rw.grad_is_vector ? rw.grad_out[n] : rw.grad_out[0];
+  if (rw.reduction == LCE_RED_MEAN) {
+    const int nv = *n_valid_ptr;
+    const float base = nv == 0 ? __int_as_float(0x7fc00000) : 1.0f / static_cast<float>(nv);
+    return base * g;
+  }
+  return g;
+}
+
+// A row's target is valid iff it is not ignore_index; a target outside
+// [0, C) that is not ignore_index is an error (status bit) and the row is
+// treated as ignored.
+__device__ __forceinline__ bool target_valid(int64_t t, int64_t ignore_index, int64_t C) {
+  return t != ignore_index && t >= 0 && t < C;
+}
+
+}  // namespace lce

@@ -1,0 +1,57 @@
+// gemm_simt.cu -- instantiations and host launchers of the fp32 SIMT GEMM.
+#include "internal.h"
+#include "simt_gemm.cuh"
+
+namespace lce {
+
+namespace {
+
+template <bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_sg(const float* A, const float* B, int64_t lda, int64_t ldb, int64_t M, int64_t N, int64_t K,
+                      const typename Epi::Params& ep, int kid, cudaStream_t s) {
+  auto kern = simt_gemm_kernel<A_MN, B_MN, Epi>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SG_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (M == 0 || N == 0) return cudaSuccess;
+  const int64_t gx = (N + SG_BN - 1) / SG_BN, gy = (M + SG_BM - 1) / SG_BM;
+  if (gy > 65535 || gx > 2147483647LL) return cudaErrorInvalidValue;
+  prof_before(kid, s);
+  kern<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), SG_THREADS, SG_SMEM_BYTES, s>>>(
+      A, B, lda, ldb, M, N, K, ep);
+  cudaError_t e = cudaGetLastError();
+  prof_after(kid, s);
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_simt_logits(const float* A, const float* B, int64_t lda, int64_t ldb, int64_t M, int64_t N,
+                               int64_t K, const EpiLse::Params& ep, cudaStream_t s) {
+  return launch_sg<false, false, EpiLse>(A, B, lda, ldb, M, N, K, ep, K_GEMM_LOGITS_SIMT, s);
+}
+
+cudaError_t launch_simt_store(int op, const float* A, const float* B, int64_t lda, int64_t ldb, int64_t M,
+                              int64_t N, int64_t K, const EpiStore::Params& ep, cudaStream_t s) {
+  switch (op) {
+    case TC_DX:
+      return launch_sg<false, true, EpiStore>(A, B, lda, ldb, M, N, K, ep, K_GEMM_DX_SIMT, s);
+    case TC_DW:
+      return launch_sg<true, true, EpiStore>(A, B, lda, ldb, M, N, K, ep, K_GEMM_DW_SIMT, s);
+    case TC_TEST_KK:
+      return launch_sg<false, false, EpiStore>(A, B, lda, ldb, M, N, K, ep, K_GEMM_TEST, s);
+    case TC_TEST_KM:
+      return launch_sg<false, true, EpiStore>(A, B, lda, ldb, M, N, K, ep, K_GEMM_TEST, s);
+    case TC_TEST_MK:
+      return launch_sg<true, false, EpiStore>(A, B, lda, ldb, M, N, K, ep, K_GEMM_TEST, s);
+    case TC_TEST_MM:
+      return launch_sg<true, true, EpiStore>(A, B, lda, ldb, M, N, K, ep, K_GEMM_TEST, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace lce

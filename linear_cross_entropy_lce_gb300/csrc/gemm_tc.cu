@@ -1,0 +1,100 @@
+// gemm_tc.cu -- instantiations and host launchers of the tcgen05 GEMM.
+#include <mutex>
+
+#include "internal.h"
+#include "tc_gemm.cuh"
+
+namespace lce {
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+template <bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, int m_inner,
+                      int* status, const typename Epi::Params& ep, int kid, cudaStream_t s) {
+  auto kern = tc_gemm_kernel<A_MN, B_MN, Epi>;
+  static bool attr_set = false;  // one device per process is assumed for the attribute cache
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  TcGemmArgs g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.num_m_blocks = (M + TC_BM - 1) / TC_BM;
+  g.num_n_blocks = (N + TC_BN - 1) / TC_BN;
+  g.num_tiles = g.num_m_blocks * g.num_n_blocks;
+  g.m_inner = m_inner;
+  g.status = status;
+  if (g.num_tiles == 0) return cudaSuccess;
+  const int grid = g.num_tiles < num_sms() ? g.num_tiles : num_sms();
+  prof_before(kid, s);
+  kern<<<grid, TC_THREADS, TC_SMEM_BYTES, s>>>(tmA, tmB, g, ep);
+  cudaError_t e = cudaGetLastError();
+  prof_after(kid, s);
+  return e;
+}
+
+}  // namespace
+
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
+                      uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// logits: A = X [M rows, K] K-major, B = W [N rows, K] K-major; consecutive
+// tiles walk down the rows so the CTAs in flight share one W panel.
+cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, int M, int N, int K, int* status,
+                             const EpiLse::Params& ep, cudaStream_t s) {
+  return launch_tc<false, false, EpiLse>(tmX, tmW, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s);
+}
+
+cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
+                            int* status, const EpiStore::Params& ep, cudaStream_t s) {
+  switch (op) {
+    case TC_DX:  // A = G [rows, C] K-major, B = W [C, D] N-major
+      return launch_tc<false, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_DX_TC, s);
+    case TC_DW:  // A = G^T from G [rows, C] (M-major), B = X [rows, D] N-major
+      return launch_tc<true, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_DW_TC, s);
+    case TC_TEST_KK:
+      return launch_tc<false, false, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+    case TC_TEST_KM:
+      return launch_tc<false, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+    case TC_TEST_MK:
+      return launch_tc<true, false, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+    case TC_TEST_MM:
+      return launch_tc<true, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace lce

@@ -1,0 +1,113 @@
+// internal.h -- host-side launchers shared between the translation units of
+// liblce.so. Every launcher enqueues on `stream` and returns cudaSuccess or
+// the launch error.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "common.cuh"
+#include "epilogues.cuh"
+
+namespace lce {
+
+// Kernel ids for the launch accounting / profiler.
+enum KernelId {
+  K_PREP = 0,
+  K_GEMM_LOGITS_TC,
+  K_GEMM_DX_TC,
+  K_GEMM_DW_TC,
+  K_GEMM_LOGITS_SIMT,
+  K_GEMM_DX_SIMT,
+  K_GEMM_DW_SIMT,
+  K_LSE_COMBINE,
+  K_GRAD_LOGITS,
+  K_LOSS_FINALIZE,
+  K_DB_FINALIZE,
+  K_CE_RESIDENT,
+  K_CE_STREAM,
+  K_GEMM_TEST,
+  K_NUM_IDS
+};
+const char* kernel_id_name(int id);
+
+// Launch accounting: called around every launch.
+void prof_before(int id, cudaStream_t s);
+void prof_after(int id, cudaStream_t s);
+
+int num_sms();
+
+// ---- tcgen05 GEMM (gemm_tc.cu)
+enum TcOp { TC_LOGITS = 0, TC_DX = 1, TC_DW = 2, TC_TEST_KK = 3, TC_TEST_KM = 4, TC_TEST_MK = 5, TC_TEST_MM = 6 };
+// Encodes a 2-D bf16 tensor map over a row-major matrix with `rows` rows of
+// `inner` elements, row pitch `ld` elements, box {64, box_rows}, 128B swizzle.
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
+                      uint32_t box_rows);
+cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, int M, int N, int K, int* status,
+                             const EpiLse::Params& ep, cudaStream_t s);
+cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
+                            int* status, const EpiStore::Params& ep, cudaStream_t s);
+
+// ---- SIMT fp32 GEMM (gemm_simt.cu); op as TcOp (LOGITS: A K-major, B
+// K-major; DX: A K-major, B N-major; DW: A M-major, B N-major).
+cudaError_t launch_simt_logits(const float* A, const float* B, int64_t lda, int64_t ldb, int64_t M, int64_t N,
+                               int64_t K, const EpiLse::Params& ep, cudaStream_t s);
+cudaError_t launch_simt_store(int op, const float* A, const float* B, int64_t lda, int64_t ldb, int64_t M,
+                              int64_t N, int64_t K, const EpiStore::Params& ep, cudaStream_t s);
+
+// ---- row kernels (rowops.cu)
+cudaError_t launch_prep(const int64_t* target, int64_t N, int64_t C, int64_t ignore_index, WsHeader* hdr,
+                        cudaStream_t s);
+struct CombineArgs {
+  float2* partial;  // [nseg][ld]; overwritten: .x = w_n exp(m - lse) when backward
+  int64_t ld;
+  int nseg;
+  int64_t rows;
+  int64_t row0;              // global index of chunk row 0
+  const float* zt;           // [rows]
+  int* tcol;                 // [rows] out: target column or -1
+  float* gt;                 // [rows] out: G at the target column
+  const int64_t* target;     // global
+  int64_t ignore_index;
+  int64_t C;
+  RowWeight rw;
+  const WsHeader* hdr;
+  float* loss_rows;          // global [N]
+  float* lse_out;            // global [N] or NULL
+  int backward;
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+struct GradArgs {
+  void* L;  // [rows][ld] P~ in, G out
+  int64_t ld;
+  int64_t rows;
+  int64_t C;
+  int segw;
+  int nseg;
+  const float2* scale;  // [nseg][sld] (.x)
+  int64_t sld;
+  const int* tcol;
+  const float* gt;
+  float* db_acc;  // [C] or NULL
+};
+cudaError_t launch_grad_logits(const GradArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_loss_finalize(const float* loss_rows, int64_t N, int reduction, const WsHeader* hdr,
+                                 float* loss_out, cudaStream_t s);
+cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, bool bf16, cudaStream_t s);
+
+// ---- cross entropy on given logits (ce_logits.cu)
+struct CeArgs {
+  void* logits;
+  int64_t N, V;
+  const int64_t* target;
+  int64_t ignore_index;
+  RowWeight rw;
+  const WsHeader* hdr;
+  float* loss_rows;  // [N]
+  int* status;
+};
+cudaError_t launch_ce_logits(const CeArgs& a, bool bf16, cudaStream_t s);
+
+}  // namespace lce

@@ -1,0 +1,239 @@
+// rowops.cu -- the per-row and elementwise steps around the GEMMs:
+// valid-target count, merge of the per-segment (max, sum-exp) pairs into
+// the row log-sum-exp and loss, formation of the gradient tile G, and the
+// final loss / bias-gradient reductions.
+#include "internal.h"
+
+namespace lce {
+
+namespace {
+
+// n_valid = #rows whose target is a class index; a target that is neither
+// ignore_index nor in [0, C) sets the target-range status bit
+// (linear_cross_entropy.py: the _mask / corrected_target / neg_weight_target
+// d = sum of unmasked weights).
+__global__ void prep_kernel(const int64_t* __restrict__ target, int64_t N, int64_t C, int64_t ign, WsHeader* hdr) {
+  __shared__ int s_cnt[32];
+  __shared__ int s_bad[32];
+  int cnt = 0, bad = 0;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < N;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = target[i];
+    if (t != ign) {
+      if (t >= 0 && t < C)
+        ++cnt;
+      else
+        bad = 1;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    s_cnt[warp] = cnt;
+    s_bad[warp] = bad;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    cnt = lane < nw ? s_cnt[lane] : 0;
+    bad = lane < nw ? s_bad[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    if (lane == 0) {
+      if (cnt) atomicAdd(&hdr->n_valid, cnt);
+      if (bad) atomicOr(&hdr->status, kStatusTargetRange);
+    }
+  }
+}
+
+// One thread per chunk row: lse = M + log sum_s s_s exp(m_s - M) over the
+// row's segments, loss_n = lse - z_t (0 on ignored rows). For the backward
+// it turns each pair into the scale w_n exp(m_s - lse) that maps the stored
+// P~ to G, and computes G at the target column, w_n (softmax_t - 1), from
+// the fp32 target logit (expm1 keeps it accurate when softmax_t ~ 1).
+__global__ void combine_kernel(const CombineArgs a) {
+  const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (r >= a.rows) return;
+  float M = -INFINITY, S = 0.0f;
+  for (int s = 0; s < a.nseg; ++s) {
+    const float2 p = a.partial[s * a.ld + r];
+    if (p.x > M) {
+      S = S * expf(M - p.x) + p.y;
+      M = p.x;
+    } else {
+      S += p.y * expf(p.x - M);
+    }
+  }
+  const float lse = M + logf(S);
+  const int64_t g = a.row0 + r;
+  const int64_t t = a.target[g];
+  const bool valid = target_valid(t, a.ignore_index, a.C);
+  const float zt = valid ? a.zt[r] : 0.0f;
+  a.loss_rows[g] = valid ? lse - zt : 0.0f;
+  if (a.lse_out != nullptr) a.lse_out[g] = lse;
+  if (a.backward) {
+    const float w = row_weight(a.rw, &a.hdr->n_valid, g, valid);
+    for (int s = 0; s < a.nseg; ++s) {
+      float2* p = &a.partial[s * a.ld + r];
+      p->x = w * expf(p->x - lse);
+    }
+    a.tcol[r] = valid ? static_cast<int>(t) : -1;
+    a.gt[r] = valid ? w * expm1f(zt - lse) : 0.0f;
+  }
+}
+
+// G[r, j] = P~[r, j] * scale[seg(j), r], replaced by gt[r] at the target
+// column, written in place over P~ (linear_cross_entropy.py: logits scaled
+// by w / denominator, then the one-hot corrections). Optionally adds the
+// column sums of G over the block's rows into db_acc (fp32 atomics, one per
+// column per block).
+template <class T, int SEGW>
+__global__ void __launch_bounds__(256) grad_logits_kernel(const GradArgs a) {
+  constexpr int VE = 16 / static_cast<int>(sizeof(T));
+  constexpr int TPR = SEGW / VE;
+  constexpr int RPP = 256 / TPR;
+  constexpr int RB = 64;
+  __shared__ float red[RPP][TPR * VE];
+  const int seg = blockIdx.x;
+  const int64_t r_begin = static_cast<int64_t>(blockIdx.y) * RB;
+  const int64_t r_end = (r_begin + RB < a.rows) ? r_begin + RB : a.rows;
+  const int lt = threadIdx.x % TPR;
+  const int rsub = threadIdx.x / TPR;
+  const int64_t col = static_cast<int64_t>(seg) * SEGW + lt * VE;
+  float colsum[VE];
+#pragma unroll
+  for (int i = 0; i < VE; ++i) colsum[i] = 0.0f;
+  for (int64_t r = r_begin + rsub; r < r_end; r += RPP) {
+    const float sc = a.scale[seg * a.sld + r].x;
+    const int tc = a.tcol[r];
+    T* p = static_cast<T*>(a.L) + r * a.ld + col;
+    uint4 raw = *reinterpret_cast<const uint4*>(p);
+    T* e = reinterpret_cast<T*>(&raw);
+#pragma unroll
+    for (int i = 0; i < VE; ++i) {
+      float gv = to_f32(e[i]) * sc;
+      if (col + i == tc) gv = a.gt[r];
+      e[i] = from_f32<T>(gv);
+      colsum[i] += to_f32(e[i]);
+    }
+    *reinterpret_cast<uint4*>(p) = raw;
+  }
+  if (a.db_acc == nullptr) return;
+#pragma unroll
+  for (int i = 0; i < VE; ++i) red[rsub][lt * VE + i] = colsum[i];
+  __syncthreads();
+  for (int c = threadIdx.x; c < TPR * VE; c += 256) {
+    float acc = 0.0f;
+#pragma unroll 4
+    for (int q = 0; q < RPP; ++q) acc += red[q][c];
+    const int64_t gc = static_cast<int64_t>(seg) * SEGW + c;
+    if (gc < a.C) atomicAdd(&a.db_acc[gc], acc);
+  }
+}
+
+// Deterministic single-block sum of the per-row losses in fp64; mean
+// divides by n_valid (NaN when it is 0).
+__global__ void loss_finalize_kernel(const float* __restrict__ loss_rows, int64_t N, int reduction,
+                                     const WsHeader* hdr, float* loss_out) {
+  __shared__ double s[32];
+  double acc = 0.0;
+  for (int64_t i = threadIdx.x; i < N; i += blockDim.x) acc += loss_rows[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) s[warp] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    acc = lane < nw ? s[lane] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      if (reduction == LCE_RED_SUM) {
+        loss_out[0] = static_cast<float>(acc);
+      } else {
+        const int nv = hdr->n_valid;
+        loss_out[0] = nv == 0 ? __int_as_float(0x7fc00000) : static_cast<float>(acc / nv);
+      }
+    }
+  }
+}
+
+template <class T>
+__global__ void db_finalize_kernel(const float* __restrict__ db_acc, T* db, int64_t C) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < C;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    db[i] = from_f32<T>(db_acc[i]);
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const int64_t* target, int64_t N, int64_t C, int64_t ignore_index, WsHeader* hdr,
+                        cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  int64_t blocks = (N + 1023) / 1024;
+  if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
+  prof_before(K_PREP, s);
+  prep_kernel<<<static_cast<unsigned>(blocks), 1024, 0, s>>>(target, N, C, ignore_index, hdr);
+  cudaError_t e = cudaGetLastError();
+  prof_after(K_PREP, s);
+  return e;
+}
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
+  if (a.rows == 0) return cudaSuccess;
+  const int64_t blocks = (a.rows + 63) / 64;
+  prof_before(K_LSE_COMBINE, s);
+  combine_kernel<<<static_cast<unsigned>(blocks), 64, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  prof_after(K_LSE_COMBINE, s);
+  return e;
+}
+
+cudaError_t launch_grad_logits(const GradArgs& a, bool bf16, cudaStream_t s) {
+  if (a.rows == 0) return cudaSuccess;
+  const int64_t gy = (a.rows + 63) / 64;
+  if (gy > 65535) return cudaErrorInvalidValue;
+  if (a.segw != (bf16 ? 256 : 64)) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(a.nseg), static_cast<unsigned>(gy));
+  prof_before(K_GRAD_LOGITS, s);
+  if (bf16)
+    grad_logits_kernel<__nv_bfloat16, 256><<<grid, 256, 0, s>>>(a);
+  else
+    grad_logits_kernel<float, 64><<<grid, 256, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  prof_after(K_GRAD_LOGITS, s);
+  return e;
+}
+
+cudaError_t launch_loss_finalize(const float* loss_rows, int64_t N, int reduction, const WsHeader* hdr,
+                                 float* loss_out, cudaStream_t s) {
+  prof_before(K_LOSS_FINALIZE, s);
+  loss_finalize_kernel<<<1, 1024, 0, s>>>(loss_rows, N, reduction, hdr, loss_out);
+  cudaError_t e = cudaGetLastError();
+  prof_after(K_LOSS_FINALIZE, s);
+  return e;
+}
+
+cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, bool bf16, cudaStream_t s) {
+  int64_t blocks = (C + 255) / 256;
+  if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
+  prof_before(K_DB_FINALIZE, s);
+  if (bf16)
+    db_finalize_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        db_acc, static_cast<__nv_bfloat16*>(db), C);
+  else
+    db_finalize_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, s>>>(db_acc, static_cast<float*>(db), C);
+  cudaError_t e = cudaGetLastError();
+  prof_after(K_DB_FINALIZE, s);
+  return e;
+}
+
+}  // namespace lce
