@@ -128,8 +128,10 @@ __global__ void __launch_bounds__(CE_THREADS, 2) ce_resident_kernel(const CeArgs
     for (int i = 0; i < CE_EPT; ++i) m = fmaxf(m, x[i]);
     const float cm = block_max(m, scratch);
     float s = 0.0f;
+    if (cm != -INFINITY) {  // a slice wholly past V holds only padding
 #pragma unroll
-    for (int i = 0; i < CE_EPT; ++i) s += fast_exp2((x[i] - cm) * kLog2e);
+      for (int i = 0; i < CE_EPT; ++i) s += fast_exp2((x[i] - cm) * kLog2e);
+    }
     const float csum = block_sum(s, scratch);
     if (tid == 0) {
       xch[iter & 1][0] = cm;
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(CE_THREADS, 2) ce_resident_kernel(const CeArgs
         ps = dsmem_ld_f32(&xch[iter & 1][1], lane);
       }
       const float M = warp_max(pm);
-      const float S = warp_sum(lane < cs ? ps * expf(pm - M) : 0.0f);
+      const float S = warp_sum((lane < cs && pm != -INFINITY) ? ps * expf(pm - M) : 0.0f);
       if (lane == 0) {
         bc[0] = M + logf(S);
         bc[1] = row_weight(a.rw, &a.hdr->n_valid, row, valid);
