@@ -162,6 +162,37 @@ LCE_API int lce_cross_entropy_from_logits(void* logits_inout, const int64_t* tar
                                   float* loss_out, void* workspace, size_t ws_bytes,
                                   void* stream);
 
+/*
+ * Allocation-free variant of lce_cross_entropy_from_logits. The source pages
+ * have no counterpart; it exists for callers that cannot allocate device
+ * memory when they need the loss (code running inside a caching allocator's
+ * own hooks, where allocating would re-enter the allocator, or an embedded
+ * runtime that reserves a fixed memory budget up front and passes only the
+ * buffers it owns). Same arguments and results as
+ * lce_cross_entropy_from_logits, except:
+ *  - no workspace: the call uses a fixed scratch array inside the library's
+ *    device image (256 B + 4 B per row for at most LCE_NOALLOC_MAX_ROWS
+ *    rows, i.e. 4 MiB + 256 B), reserved on every GPU that loads the library
+ *    until the process exits. N > LCE_NOALLOC_MAX_ROWS returns LCE_ERR_SHAPE.
+ *  - device_status: NULL or a device int; after the kernels it receives the
+ *    device status bits of this call (1 = a target out of range, 2 = a wait
+ *    timed out), copied on the stream.
+ *  - every call shares that one array, which keeps the last call's contents
+ *    (the call clears the part that must start at zero itself): calls that
+ *    overlap on the GPU, on different streams or from different threads,
+ *    race and give wrong results. Serialise them on one stream.
+ *  - the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture on the device.
+ * The call allocates nothing (no cudaMalloc / cudaFree, no allocating
+ * library routine).
+ */
+#define LCE_NOALLOC_MAX_ROWS (1 << 20)
+LCE_API int lce_cross_entropy_from_logits_noalloc(void* logits_inout, const int64_t* target,
+                                                  int64_t N, int64_t V, int dtype, int reduction,
+                                                  int64_t ignore_index, const float* grad_out,
+                                                  float* loss_out, int* device_status, void* stream);
+
 /* Human-readable text of a status code (static storage). */
 LCE_API const char* lce_status_string(int status);
 

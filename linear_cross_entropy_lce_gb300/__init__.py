@@ -31,6 +31,7 @@ LIB_PATH = os.path.join(_PKG, "liblce.so")
 LCE_F32, LCE_BF16 = 0, 1
 LCE_RED_NONE, LCE_RED_SUM, LCE_RED_MEAN = 0, 1, 2
 LCE_OP_FORWARD, LCE_OP_FORWARD_BACKWARD, LCE_OP_CE_FROM_LOGITS = 0, 1, 2
+LCE_NOALLOC_MAX_ROWS = 1 << 20
 STATUS = {
     0: "LCE_OK", 1: "LCE_ERR_NULL", 2: "LCE_ERR_SHAPE", 3: "LCE_ERR_DTYPE", 4: "LCE_ERR_REDUCTION",
     5: "LCE_ERR_GRAD_OUT", 6: "LCE_ERR_WORKSPACE", 7: "LCE_ERR_CUDA", 8: "LCE_ERR_TARGET_RANGE",
@@ -54,6 +55,8 @@ _SIGNATURES = {
                                      c_int, c_void_p, c_size_t, c_void_p]),
     "lce_cross_entropy_from_logits": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_int64,
                                               c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "lce_cross_entropy_from_logits_noalloc": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int,
+                                                      c_int64, c_void_p, c_void_p, c_void_p, c_void_p]),
     "lce_status_string": (ctypes.c_char_p, [c_int]),
     "lce_read_device_status": (c_int, [c_void_p, c_void_p]),
     "lce_launch_count": (c_int64, []),
