@@ -35,6 +35,12 @@ from linear_cross_entropy_lce_gb300.workloads import WORKLOADS, make_workload  #
 METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor peak"
 
 
+# DRAM bytes (read + write) per launch of a kernel, from an ncu capture of
+# the same command: {(workload, kernel): bytes}. An entry is removed when the
+# kernel changes after its capture.
+MEASURED_TRAFFIC = {}
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -42,8 +48,9 @@ def _peaks():
             d = json.load(f)
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
-                "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
 
 
 class ClockSampler:
@@ -126,6 +133,30 @@ def _oracle_sample_seconds(name, rows, device_inputs=None, seed=0):
     return time.perf_counter() - t0
 
 
+def _workload(args):
+    """The named workload, or a copy resized by --rows / --dim / --classes
+    (smaller cases of the same kernels, e.g. for profiler captures)."""
+    import dataclasses
+
+    w = WORKLOADS[args.workload]
+    if not (args.rows or args.dim or args.classes):
+        return w
+    N = args.rows or w.N
+    D = args.dim or w.D
+    C = args.classes or w.C
+    n_ign = int(round(w.n_ignored * N / w.N))
+    return dataclasses.replace(w, name=f"{w.name}[N={N},D={D},C={C}]", N=N, D=D, C=C, n_ignored=n_ign)
+
+
+def _make_resized(w):
+    from linear_cross_entropy_lce_gb300.workloads import make_linear_inputs, make_logits_inputs
+
+    if w.kind == "logits":
+        return make_logits_inputs(w.N, w.C, w.dtype, "cuda", w.seed, w.x_std, w.target_dist, w.n_ignored)
+    return make_linear_inputs(w.N, w.D, w.C, w.dtype, "cuda", w.seed, w.bias, w.x_std, w.w_std, w.b_std,
+                              w.scale_by_sqrt_d, w.target_dist, w.zipf_s, w.n_ignored, w.grad_out_std)
+
+
 def _cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -174,8 +205,10 @@ def run_gpu(args):
         dist = dist_mod
     lce.load_library()
     name = args.workload
-    w = WORKLOADS[name]
-    inp = make_workload(name, "cuda")
+    w = _workload(args)
+    inp = make_workload(name, "cuda") if w is WORKLOADS[name] else _make_resized(w)
+    if w is not WORKLOADS[name]:
+        name = w.name
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     peaks = _peaks()
@@ -191,8 +224,6 @@ def run_gpu(args):
             return lce.lce_cross_entropy_from_logits(logits, t, w.reduction, -100, workspace=wsbuf)
 
         flops = 0.0
-        dominant = "ce_resident"
-        algo_bytes = 2.0 * N * V * logits.element_size()
     else:
         X, W, b, t, g = inp["X"], inp["W"], inp["b"], inp["target"], inp["grad_out"]
         N, D = X.shape
@@ -220,8 +251,6 @@ def run_gpu(args):
             return loss
 
         flops = w.flops_fwd_bwd
-        dominant = None
-        algo_bytes = None
 
     def barrier():
         if dist is not None:
@@ -328,34 +357,44 @@ def run_gpu(args):
             dist.destroy_process_group()
         return 0
 
-    # ---- roofline of the dominant kernel
-    if dominant is None:
-        dominant = max(prof, key=lambda k: prof[k][1]) if prof else None
+    # ---- roofline of the dominant kernel (the one with the most device time)
     roofline = None
-    if dominant in prof:
-        n_l, tot_ms = prof[dominant]
+    if prof:
+        dominant = max(prof, key=lambda k: prof[k][1])
+        n_l, tot_ms, work = prof[dominant]
         avg_s = tot_ms / n_l / 1e3
-        if w.kind == "logits":
-            achieved = algo_bytes / avg_s / 1e9
-            roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": dominant,
-                        "peak_source": peaks["source"] + " hbm_gbs (copy)",
-                        "algorithmic_bytes_per_launch": algo_bytes}
-        else:
-            per_launch_flops = 2.0 * w.N * w.D * w.C  # each of the three GEMMs is 2NDC per call
-            achieved = per_launch_flops / avg_s / 1e12
+        per_launch = work / n_l
+        traffic = MEASURED_TRAFFIC.get((name, dominant))
+        if dominant.startswith("gemm_") and dominant.endswith("_tc"):
+            achieved = per_launch / avg_s / 1e12
             peak = peaks["bf16_tflops_sustained"]
             roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                        "frac": achieved / peak, "traffic": None, "kernel": dominant,
-                        "peak_source": peaks["source"] + " bf16_tflops_sustained (kernel timed inside a "
-                                                         "long run of back-to-back steps)",
-                        "algorithmic_flops_per_launch": per_launch_flops}
+                        "frac": achieved / peak, "traffic": traffic, "kernel": dominant,
+                        "peak_source": peaks["source"] + " bf16_tflops_sustained (the kernel runs inside a "
+                                                         "long sequence of back-to-back steps)",
+                        "algorithmic_flops_per_launch": per_launch}
+        elif dominant.startswith("gemm_"):
+            # exact fp32 FMA on the CUDA cores: SMs x 128 FP32 lanes x 2 flop x max SM clock
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            peak = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+            achieved = per_launch / avg_s / 1e12
+            roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak, "traffic": traffic, "kernel": dominant,
+                        "peak_source": f"derived: {sms} SMs x 128 FP32 FMA lanes x 2 flop x "
+                                       f"{peaks['sm_max_mhz']:.0f} MHz",
+                        "algorithmic_flops_per_launch": per_launch}
+        else:
+            achieved = per_launch / avg_s / 1e9
+            roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": dominant,
+                        "peak_source": peaks["source"] + " hbm_gbs (copy)",
+                        "algorithmic_bytes_per_launch": per_launch}
 
     # ---- CPU baseline: the oracle on a bounded sample, rank 0, N=1 only
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
         rows = args.ref_rows
-        sec = _oracle_sample_seconds(name, rows, inp)
+        sec = _oracle_sample_seconds(args.workload, rows, inp)
         cpu = {"value": rows / sec, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
                "sample": f"{rows} of {w.N} rows, full method (loss and all gradients for those rows) in "
                          f"float64 numpy, {sec:.1f} s"}
@@ -383,6 +422,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in sorted(prof.items(), key=lambda kv: -kv[1][1])},
+        "kernels_launches_per_step": {k: v[0] / args.steps for k, v in prof.items()},
     }
     if flops:
         line["tflops"] = flops * ws / (ms / 1e3) / 1e12
@@ -403,6 +443,9 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=0, help="override N (profiling a smaller case)")
+    ap.add_argument("--dim", type=int, default=0, help="override D")
+    ap.add_argument("--classes", type=int, default=0, help="override C (or V)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

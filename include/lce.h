@@ -99,7 +99,7 @@ enum lce_status_e {
  *   dtype       input type; grad_dtype: gradient type (ignored for FORWARD)
  *   chunk_rows  rows per batch chunk of the backward; 0 picks the default:
  *               as many rows as keep the [chunk_rows, C] gradient buffer
- *               within 4 GiB. Fewer rows need less memory: the backward
+ *               within 8 GiB. Fewer rows need less memory: the backward
  *               keeps one [chunk_rows, ceil(C/256)*256] buffer of the input
  *               type (the batch-chunked buffer of linear_cross_entropy.py)
  *               and, when there is more than one chunk and dW is bf16, an
@@ -210,14 +210,16 @@ LCE_API int lce_read_device_status(const void* workspace, void* stream);
  * lce_profile_enable(1): from now on, bracket every launch with CUDA events
  * on the launching stream; lce_profile_enable(0) stops, and
  * lce_profile_reset clears the records. lce_profile_query waits for the
- * recorded events and returns, for one kernel id, the number of launches
- * and their summed duration in ms. lce_kernel_name gives the id's name;
+ * recorded events and returns, for one kernel id, the number of launches,
+ * their summed duration in ms and (if total_work is not NULL) their summed
+ * algorithmic work: flop for the gemm_* kernels (2 M N K per launch), bytes
+ * that must cross HBM for the others. lce_kernel_name gives the id's name;
  * ids run from 0 to lce_num_kernel_ids() - 1. Not thread-safe.
  */
 LCE_API int64_t lce_launch_count(void);
 LCE_API int lce_profile_enable(int on);
 LCE_API int lce_profile_reset(void);
-LCE_API int lce_profile_query(int kernel_id, int64_t* launches, double* total_ms);
+LCE_API int lce_profile_query(int kernel_id, int64_t* launches, double* total_ms, double* total_work);
 LCE_API const char* lce_kernel_name(int kernel_id);
 LCE_API int lce_num_kernel_ids(void);
 

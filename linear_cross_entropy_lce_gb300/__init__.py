@@ -62,7 +62,8 @@ _SIGNATURES = {
     "lce_launch_count": (c_int64, []),
     "lce_profile_enable": (c_int, [c_int]),
     "lce_profile_reset": (c_int, []),
-    "lce_profile_query": (c_int, [c_int, ctypes.POINTER(c_int64), ctypes.POINTER(c_double)]),
+    "lce_profile_query": (c_int, [c_int, ctypes.POINTER(c_int64), ctypes.POINTER(c_double),
+                                  ctypes.POINTER(c_double)]),
     "lce_kernel_name": (ctypes.c_char_p, [c_int]),
     "lce_num_kernel_ids": (c_int, []),
     "lce_test_gemm_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int,
@@ -251,15 +252,18 @@ def profile_reset():
 
 
 def profile_summary() -> dict:
-    """{kernel name: (launches, total ms)} for the recorded launches."""
+    """{kernel name: (launches, total ms, total algorithmic work)} for the
+    recorded launches; work is flop for gemm_* kernels, HBM bytes otherwise."""
     lib = load_library()
     out = {}
     for k in range(lib.lce_num_kernel_ids()):
         n = c_int64(0)
         ms = c_double(0.0)
-        _check(lib.lce_profile_query(k, ctypes.byref(n), ctypes.byref(ms)), "lce_profile_query")
+        work = c_double(0.0)
+        _check(lib.lce_profile_query(k, ctypes.byref(n), ctypes.byref(ms), ctypes.byref(work)),
+               "lce_profile_query")
         if n.value:
-            out[lib.lce_kernel_name(k).decode()] = (int(n.value), float(ms.value))
+            out[lib.lce_kernel_name(k).decode()] = (int(n.value), float(ms.value), float(work.value))
     return out
 
 

@@ -69,6 +69,7 @@ namespace {
 struct ProfRec {
   int id;
   cudaEvent_t a, b;
+  double work;
 };
 std::vector<ProfRec> g_recs;
 bool g_prof = false;
@@ -81,10 +82,10 @@ const char* kNames[K_NUM_IDS] = {
 
 const char* kernel_id_name(int id) { return (id >= 0 && id < K_NUM_IDS) ? kNames[id] : "?"; }
 
-void prof_before(int id, cudaStream_t s) {
+void prof_before(int id, cudaStream_t s, double work) {
   g_launches.fetch_add(1);
   if (!g_prof) return;
-  ProfRec r{id, nullptr, nullptr};
+  ProfRec r{id, nullptr, nullptr, work};
   cudaEventCreate(&r.a);
   cudaEventCreate(&r.b);
   cudaEventRecord(r.a, s);
@@ -99,7 +100,7 @@ void prof_after(int id, cudaStream_t s) {
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int64_t kDefaultChunkBytes = int64_t(4) << 30;  // chunk buffer budget of the default plan
+constexpr int64_t kDefaultChunkBytes = int64_t(8) << 30;  // chunk buffer budget of the default plan
 
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -514,10 +515,10 @@ int lce_profile_reset(void) {
   return LCE_OK;
 }
 
-int lce_profile_query(int kernel_id, int64_t* launches, double* total_ms) {
+int lce_profile_query(int kernel_id, int64_t* launches, double* total_ms, double* total_work) {
   if (launches == nullptr || total_ms == nullptr) return LCE_ERR_NULL;
   int64_t n = 0;
-  double tot = 0.0;
+  double tot = 0.0, work = 0.0;
   for (auto& r : g_recs) {
     if (r.id != kernel_id || r.b == nullptr) continue;
     if (cudaEventSynchronize(r.b) != cudaSuccess) return LCE_ERR_CUDA;
@@ -525,9 +526,11 @@ int lce_profile_query(int kernel_id, int64_t* launches, double* total_ms) {
     if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return LCE_ERR_CUDA;
     ++n;
     tot += ms;
+    work += r.work;
   }
   *launches = n;
   *total_ms = tot;
+  if (total_work != nullptr) *total_work = work;
   return LCE_OK;
 }
 

@@ -236,7 +236,7 @@ cudaError_t launch_ce_t(const CeArgs& a, cudaStream_t s) {
       int64_t ncl = max_clusters;
       if (ncl > a.N) ncl = a.N;
       cfg.gridDim = dim3(static_cast<unsigned>(ncl * cs));
-      prof_before(K_CE_RESIDENT, s);
+      prof_before(K_CE_RESIDENT, s, 2.0 * sizeof(T) * a.N * static_cast<double>(a.V));
       cudaError_t e = cudaLaunchKernelEx(&cfg, ce_resident_kernel<T>, a, cs);
       prof_after(K_CE_RESIDENT, s);
       return e;
@@ -244,7 +244,7 @@ cudaError_t launch_ce_t(const CeArgs& a, cudaStream_t s) {
     cudaGetLastError();  // clear a failed occupancy query and stream the rows instead
   }
   int64_t grid = a.N < 4 * num_sms() ? a.N : 4 * num_sms();
-  prof_before(K_CE_STREAM, s);
+  prof_before(K_CE_STREAM, s, 2.0 * sizeof(T) * a.N * static_cast<double>(a.V));
   ce_stream_kernel<T><<<static_cast<unsigned>(grid), CE_THREADS, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   prof_after(K_CE_STREAM, s);

@@ -19,7 +19,7 @@ cudaError_t launch_sg(const float* A, const float* B, int64_t lda, int64_t ldb, 
   if (M == 0 || N == 0) return cudaSuccess;
   const int64_t gx = (N + SG_BN - 1) / SG_BN, gy = (M + SG_BM - 1) / SG_BM;
   if (gy > 65535 || gx > 2147483647LL) return cudaErrorInvalidValue;
-  prof_before(kid, s);
+  prof_before(kid, s, 2.0 * M * N * static_cast<double>(K));
   kern<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), SG_THREADS, SG_SMEM_BYTES, s>>>(
       A, B, lda, ldb, M, N, K, ep);
   cudaError_t e = cudaGetLastError();

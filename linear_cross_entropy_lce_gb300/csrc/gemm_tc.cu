@@ -47,7 +47,7 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int
   g.status = status;
   if (g.num_tiles == 0) return cudaSuccess;
   const int grid = g.num_tiles < num_sms() ? g.num_tiles : num_sms();
-  prof_before(kid, s);
+  prof_before(kid, s, 2.0 * M * N * static_cast<double>(K));
   kern<<<grid, TC_THREADS, TC_SMEM_BYTES, s>>>(tmA, tmB, g, ep);
   cudaError_t e = cudaGetLastError();
   prof_after(kid, s);

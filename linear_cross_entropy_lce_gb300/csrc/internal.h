@@ -33,8 +33,9 @@ enum KernelId {
 };
 const char* kernel_id_name(int id);
 
-// Launch accounting: called around every launch.
-void prof_before(int id, cudaStream_t s);
+// Launch accounting: called around every launch. work = the launch's
+// algorithmic flop (GEMM kernels) or bytes (every other kernel).
+void prof_before(int id, cudaStream_t s, double work = 0.0);
 void prof_after(int id, cudaStream_t s);
 
 int num_sms();

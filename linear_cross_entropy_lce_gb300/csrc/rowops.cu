@@ -53,39 +53,54 @@ __global__ void prep_kernel(const int64_t* __restrict__ target, int64_t N, int64
   }
 }
 
-// One thread per chunk row: lse = M + log sum_s s_s exp(m_s - M) over the
-// row's segments, loss_n = lse - z_t (0 on ignored rows). For the backward
-// it turns each pair into the scale w_n exp(m_s - lse) that maps the stored
-// P~ to G, and computes G at the target column, w_n (softmax_t - 1), from
-// the fp32 target logit (expm1 keeps it accurate when softmax_t ~ 1).
+// One warp per chunk row: the lanes merge the row's per-segment (max,
+// sum-exp) pairs into lse = M + log sum_s s_s exp(m_s - M), then
+// loss_n = lse - z_t (0 on ignored rows). For the backward each pair becomes
+// the scale w_n exp(m_s - lse) that maps the stored P~ to G, and G at the
+// target column is w_n (softmax_t - 1) from the fp32 target logit (expm1
+// keeps it accurate when softmax_t ~ 1).
+__device__ __forceinline__ void merge_pair(float& M, float& S, float m2, float s2) {
+  const float Mn = fmaxf(M, m2);
+  const float a = (M == -INFINITY) ? 0.0f : S * expf(M - Mn);
+  const float b = (m2 == -INFINITY) ? 0.0f : s2 * expf(m2 - Mn);
+  M = Mn;
+  S = a + b;
+}
+
 __global__ void combine_kernel(const CombineArgs a) {
-  const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-  if (r >= a.rows) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  if (r >= a.rows) return;  // warp-uniform
   float M = -INFINITY, S = 0.0f;
-  for (int s = 0; s < a.nseg; ++s) {
+  for (int s = lane; s < a.nseg; s += 32) {
     const float2 p = a.partial[s * a.ld + r];
-    if (p.x > M) {
-      S = S * expf(M - p.x) + p.y;
-      M = p.x;
-    } else {
-      S += p.y * expf(p.x - M);
-    }
+    merge_pair(M, S, p.x, p.y);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+    merge_pair(M, S, m2, s2);
   }
   const float lse = M + logf(S);
   const int64_t g = a.row0 + r;
   const int64_t t = a.target[g];
   const bool valid = target_valid(t, a.ignore_index, a.C);
   const float zt = valid ? a.zt[r] : 0.0f;
-  a.loss_rows[g] = valid ? lse - zt : 0.0f;
-  if (a.lse_out != nullptr) a.lse_out[g] = lse;
+  if (lane == 0) {
+    a.loss_rows[g] = valid ? lse - zt : 0.0f;
+    if (a.lse_out != nullptr) a.lse_out[g] = lse;
+  }
   if (a.backward) {
     const float w = row_weight(a.rw, &a.hdr->n_valid, g, valid);
-    for (int s = 0; s < a.nseg; ++s) {
+    for (int s = lane; s < a.nseg; s += 32) {
       float2* p = &a.partial[s * a.ld + r];
       p->x = w * expf(p->x - lse);
     }
-    a.tcol[r] = valid ? static_cast<int>(t) : -1;
-    a.gt[r] = valid ? w * expm1f(zt - lse) : 0.0f;
+    if (lane == 0) {
+      a.tcol[r] = valid ? static_cast<int>(t) : -1;
+      a.gt[r] = valid ? w * expm1f(zt - lse) : 0.0f;
+    }
   }
 }
 
@@ -107,23 +122,35 @@ __global__ void __launch_bounds__(256) grad_logits_kernel(const GradArgs a) {
   const int lt = threadIdx.x % TPR;
   const int rsub = threadIdx.x / TPR;
   const int64_t col = static_cast<int64_t>(seg) * SEGW + lt * VE;
+  constexpr int NR = RB / RPP;  // rows per thread, all loaded before any store
   float colsum[VE];
 #pragma unroll
   for (int i = 0; i < VE; ++i) colsum[i] = 0.0f;
-  for (int64_t r = r_begin + rsub; r < r_end; r += RPP) {
-    const float sc = a.scale[seg * a.sld + r].x;
-    const int tc = a.tcol[r];
-    T* p = static_cast<T*>(a.L) + r * a.ld + col;
-    uint4 raw = *reinterpret_cast<const uint4*>(p);
-    T* e = reinterpret_cast<T*>(&raw);
+  uint4 raw[NR];
+  float sc[NR];
+  int tc[NR];
+#pragma unroll
+  for (int k = 0; k < NR; ++k) {
+    const int64_t r = r_begin + rsub + k * RPP;
+    if (r < r_end) {
+      raw[k] = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.L) + r * a.ld + col);
+      sc[k] = a.scale[seg * a.sld + r].x;
+      tc[k] = a.tcol[r];
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < NR; ++k) {
+    const int64_t r = r_begin + rsub + k * RPP;
+    if (r >= r_end) continue;
+    T* e = reinterpret_cast<T*>(&raw[k]);
 #pragma unroll
     for (int i = 0; i < VE; ++i) {
-      float gv = to_f32(e[i]) * sc;
-      if (col + i == tc) gv = a.gt[r];
+      float gv = to_f32(e[i]) * sc[k];
+      if (col + i == tc[k]) gv = a.gt[r];
       e[i] = from_f32<T>(gv);
       colsum[i] += to_f32(e[i]);
     }
-    *reinterpret_cast<uint4*>(p) = raw;
+    *reinterpret_cast<uint4*>(static_cast<T*>(a.L) + r * a.ld + col) = raw[k];
   }
   if (a.db_acc == nullptr) return;
 #pragma unroll
@@ -180,7 +207,7 @@ cudaError_t launch_prep(const int64_t* target, int64_t N, int64_t C, int64_t ign
   if (N == 0) return cudaSuccess;
   int64_t blocks = (N + 1023) / 1024;
   if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
-  prof_before(K_PREP, s);
+  prof_before(K_PREP, s, 8.0 * N);
   prep_kernel<<<static_cast<unsigned>(blocks), 1024, 0, s>>>(target, N, C, ignore_index, hdr);
   cudaError_t e = cudaGetLastError();
   prof_after(K_PREP, s);
@@ -189,9 +216,9 @@ cudaError_t launch_prep(const int64_t* target, int64_t N, int64_t C, int64_t ign
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;
-  const int64_t blocks = (a.rows + 63) / 64;
-  prof_before(K_LSE_COMBINE, s);
-  combine_kernel<<<static_cast<unsigned>(blocks), 64, 0, s>>>(a);
+  const int64_t blocks = (a.rows + 7) / 8;  // 8 warps, one row each
+  prof_before(K_LSE_COMBINE, s, 8.0 * a.rows * a.nseg * (a.backward ? 2 : 1));
+  combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   prof_after(K_LSE_COMBINE, s);
   return e;
@@ -203,7 +230,7 @@ cudaError_t launch_grad_logits(const GradArgs& a, bool bf16, cudaStream_t s) {
   if (gy > 65535) return cudaErrorInvalidValue;
   if (a.segw != (bf16 ? 256 : 64)) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(a.nseg), static_cast<unsigned>(gy));
-  prof_before(K_GRAD_LOGITS, s);
+  prof_before(K_GRAD_LOGITS, s, 2.0 * (bf16 ? 2 : 4) * a.rows * static_cast<double>(a.ld));
   if (bf16)
     grad_logits_kernel<__nv_bfloat16, 256><<<grid, 256, 0, s>>>(a);
   else
@@ -215,7 +242,7 @@ cudaError_t launch_grad_logits(const GradArgs& a, bool bf16, cudaStream_t s) {
 
 cudaError_t launch_loss_finalize(const float* loss_rows, int64_t N, int reduction, const WsHeader* hdr,
                                  float* loss_out, cudaStream_t s) {
-  prof_before(K_LOSS_FINALIZE, s);
+  prof_before(K_LOSS_FINALIZE, s, 4.0 * N);
   loss_finalize_kernel<<<1, 1024, 0, s>>>(loss_rows, N, reduction, hdr, loss_out);
   cudaError_t e = cudaGetLastError();
   prof_after(K_LOSS_FINALIZE, s);
@@ -225,7 +252,7 @@ cudaError_t launch_loss_finalize(const float* loss_rows, int64_t N, int reductio
 cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, bool bf16, cudaStream_t s) {
   int64_t blocks = (C + 255) / 256;
   if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
-  prof_before(K_DB_FINALIZE, s);
+  prof_before(K_DB_FINALIZE, s, (bf16 ? 6.0 : 8.0) * C);
   if (bf16)
     db_finalize_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         db_acc, static_cast<__nv_bfloat16*>(db), C);
