@@ -18,8 +18,10 @@
  * wait timed out); it is OR-ed, not cleared.
  *
  * lce_test_gemm_bf16: bf16 A, B on the tcgen05 tensor cores (TMA-fed,
- *   fp32 accumulation in tensor memory). Needs the contiguous dimension of
- *   each operand to be a multiple of 8 and 16-byte aligned pointers.
+ *   fp32 accumulation in tensor memory). cta_pair = 0: one CTA per 128x256
+ *   tile; 1: a pair of CTAs on two SMs per 256x256 tile (cta_group::2).
+ *   Needs the contiguous dimension of each operand to be a multiple of 8 and
+ *   16-byte aligned pointers.
  * lce_test_gemm_f32: fp32 A, B with fp32 FMA on the CUDA cores; any shape.
  * Return an lce_status_e code.
  */
@@ -41,7 +43,8 @@ extern "C" {
 #endif
 
 LCE_API int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t M, int64_t N,
-                       int64_t K, int a_mn_major, int b_mn_major, int* dev_status, void* stream);
+                       int64_t K, int a_mn_major, int b_mn_major, int cta_pair, int* dev_status,
+                       void* stream);
 
 LCE_API int lce_test_gemm_f32(const float* A, const float* B, float* out, int64_t M, int64_t N,
                       int64_t K, int a_mn_major, int b_mn_major, void* stream);

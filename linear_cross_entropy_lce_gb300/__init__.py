@@ -67,7 +67,7 @@ _SIGNATURES = {
     "lce_kernel_name": (ctypes.c_char_p, [c_int]),
     "lce_num_kernel_ids": (c_int, []),
     "lce_test_gemm_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int,
-                                   c_void_p, c_void_p]),
+                                   c_int, c_void_p, c_void_p]),
     "lce_test_gemm_f32": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int,
                                   c_void_p]),
 }
@@ -269,11 +269,11 @@ def profile_summary() -> dict:
 
 # ---- building-block checks (include/lce_testing.h)
 
-def test_gemm_bf16(A, B, M, N, K, a_mn_major, b_mn_major, status=None, stream=None):
+def test_gemm_bf16(A, B, M, N, K, a_mn_major, b_mn_major, status=None, cta_pair=False, stream=None):
     lib = load_library()
     out = torch.empty(M, N, dtype=torch.float32, device=A.device)
     _check(lib.lce_test_gemm_bf16(_ptr(A), _ptr(B), _ptr(out), M, N, K, int(a_mn_major), int(b_mn_major),
-                                  _ptr(status), _stream(stream)), "lce_test_gemm_bf16")
+                                  int(cta_pair), _ptr(status), _stream(stream)), "lce_test_gemm_bf16")
     return out
 
 

@@ -259,8 +259,9 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
   rw.grad_is_vector = reduction == LCE_RED_NONE ? 1 : 0;
 
   CUtensorMap tmW_k, tmW_n;
+  const bool pair = tc_pair_default();
   if (p.tc) {
-    if (!encode_tmap_bf16(&tmW_k, W, D, C, D, TC_BN)) return LCE_ERR_CUDA;
+    if (!encode_tmap_bf16(&tmW_k, W, D, C, D, pair ? 128 : TC_BN)) return LCE_ERR_CUDA;
     if (want_dx && !encode_tmap_bf16(&tmW_n, W, D, C, D, 64)) return LCE_ERR_CUDA;
   }
 
@@ -285,7 +286,7 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       CUtensorMap tmX_k;
       if (!encode_tmap_bf16(&tmX_k, Xc, D, rows, D, TC_BM)) return LCE_ERR_CUDA;
       LCE_TRY(launch_tc_logits(tmX_k, tmW_k, static_cast<int>(rows), static_cast<int>(C), static_cast<int>(D),
-                               &hdr->status, el, s));
+                               &hdr->status, el, pair, s));
     } else {
       const float* Xc = static_cast<const float*>(X) + row0 * D;
       LCE_TRY(launch_simt_logits(Xc, static_cast<const float*>(W), D, D, rows, C, D, el, s));
@@ -339,7 +340,7 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
         CUtensorMap tmG_k;
         if (!encode_tmap_bf16(&tmG_k, Lbuf, C, rows, p.C_pad, TC_BM)) return LCE_ERR_CUDA;
         LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmW_n, static_cast<int>(rows), static_cast<int>(D),
-                                static_cast<int>(C), &hdr->status, es, s));
+                                static_cast<int>(C), &hdr->status, es, pair, s));
       } else {
         LCE_TRY(launch_simt_store(TC_DX, static_cast<const float*>(Lbuf), static_cast<const float*>(W), p.C_pad, D,
                                   rows, D, C, es, s));
@@ -370,7 +371,7 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
         if (!encode_tmap_bf16(&tmG_m, Lbuf, C, rows, p.C_pad, 64)) return LCE_ERR_CUDA;
         if (!encode_tmap_bf16(&tmX_n, Xc, D, rows, D, 64)) return LCE_ERR_CUDA;
         LCE_TRY(launch_tc_store(TC_DW, tmG_m, tmX_n, static_cast<int>(C), static_cast<int>(D),
-                                static_cast<int>(rows), &hdr->status, es, s));
+                                static_cast<int>(rows), &hdr->status, es, pair, s));
       } else {
         const float* Xc = static_cast<const float*>(X) + row0 * D;
         LCE_TRY(launch_simt_store(TC_DW, static_cast<const float*>(Lbuf), Xc, p.C_pad, D, C, D, rows, es, s));
@@ -538,7 +539,7 @@ const char* lce_kernel_name(int kernel_id) { return kernel_id_name(kernel_id); }
 int lce_num_kernel_ids(void) { return K_NUM_IDS; }
 
 int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t M, int64_t N, int64_t K, int a_mn_major,
-                       int b_mn_major, int* dev_status, void* stream) {
+                       int b_mn_major, int cta_pair, int* dev_status, void* stream) {
   if (A == nullptr || B == nullptr || out == nullptr) return LCE_ERR_NULL;
   if (M < 1 || N < 1 || K < 1 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return LCE_ERR_SHAPE;
   if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return LCE_ERR_ALIGN;
@@ -547,7 +548,8 @@ int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t M, int6
   if (st != LCE_OK) return st;
   CUtensorMap ta, tb;
   bool ok = a_mn_major ? encode_tmap_bf16(&ta, A, M, K, M, 64) : encode_tmap_bf16(&ta, A, K, M, K, TC_BM);
-  ok = ok && (b_mn_major ? encode_tmap_bf16(&tb, B, N, K, N, 64) : encode_tmap_bf16(&tb, B, K, N, K, TC_BN));
+  ok = ok && (b_mn_major ? encode_tmap_bf16(&tb, B, N, K, N, 64)
+                         : encode_tmap_bf16(&tb, B, K, N, K, cta_pair ? 128 : TC_BN));
   if (!ok) return LCE_ERR_CUDA;
   EpiStore::Params es;
   es.out = out;
@@ -560,7 +562,7 @@ int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t M, int6
   es.vec_ok = (N % 4) == 0;
   const int op = a_mn_major ? (b_mn_major ? TC_TEST_MM : TC_TEST_MK) : (b_mn_major ? TC_TEST_KM : TC_TEST_KK);
   return from_cuda(launch_tc_store(op, ta, tb, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                   dev_status, es, static_cast<cudaStream_t>(stream)));
+                                   dev_status, es, cta_pair != 0, static_cast<cudaStream_t>(stream)));
 }
 
 int lce_test_gemm_f32(const float* A, const float* B, float* out, int64_t M, int64_t N, int64_t K, int a_mn_major,

@@ -1,8 +1,10 @@
 // gemm_tc.cu -- instantiations and host launchers of the tcgen05 GEMM.
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
 #include "tc_gemm.cuh"
+#include "tc2_gemm.cuh"
 
 namespace lce {
 
@@ -54,7 +56,56 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int
   return e;
 }
 
+template <bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, int m_inner,
+                       int* status, const typename Epi::Params& ep, int kid, cudaStream_t s) {
+  auto kern = tc2_gemm_kernel<A_MN, B_MN, Epi>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TC2_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  TcGemmArgs g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.num_m_blocks = (M + TC2_TILE_M - 1) / TC2_TILE_M;
+  g.num_n_blocks = (N + TC2_TILE_N - 1) / TC2_TILE_N;
+  g.num_tiles = g.num_m_blocks * g.num_n_blocks;
+  g.m_inner = m_inner;
+  g.status = status;
+  if (g.num_tiles == 0) return cudaSuccess;
+  const int max_pairs = num_sms() / 2;
+  const int pairs = g.num_tiles < max_pairs ? g.num_tiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(TC2_THREADS);
+  cfg.dynamicSmemBytes = TC2_SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  prof_before(kid, s, 2.0 * M * N * static_cast<double>(K));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, g, ep);
+  prof_after(kid, s);
+  return e;
+}
+
 }  // namespace
+
+bool tc_pair_default() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("LCE_TC_PAIR");
+    v = (e != nullptr && e[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
+}
 
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
                       uint32_t box_rows) {
@@ -73,12 +124,31 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
 // logits: A = X [M rows, K] K-major, B = W [N rows, K] K-major; consecutive
 // tiles walk down the rows so the CTAs in flight share one W panel.
 cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, int M, int N, int K, int* status,
-                             const EpiLse::Params& ep, cudaStream_t s) {
+                             const EpiLse::Params& ep, bool pair, cudaStream_t s) {
+  if (pair) return launch_tc2<false, false, EpiLse>(tmX, tmW, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s);
   return launch_tc<false, false, EpiLse>(tmX, tmW, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s);
 }
 
 cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
-                            int* status, const EpiStore::Params& ep, cudaStream_t s) {
+                            int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s) {
+  if (pair) {
+    switch (op) {
+      case TC_DX:
+        return launch_tc2<false, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_DX_TC, s);
+      case TC_DW:
+        return launch_tc2<true, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_DW_TC, s);
+      case TC_TEST_KK:
+        return launch_tc2<false, false, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+      case TC_TEST_KM:
+        return launch_tc2<false, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+      case TC_TEST_MK:
+        return launch_tc2<true, false, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+      case TC_TEST_MM:
+        return launch_tc2<true, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
   switch (op) {
     case TC_DX:  // A = G [rows, C] K-major, B = W [C, D] N-major
       return launch_tc<false, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_DX_TC, s);

@@ -46,10 +46,14 @@ enum TcOp { TC_LOGITS = 0, TC_DX = 1, TC_DW = 2, TC_TEST_KK = 3, TC_TEST_KM = 4,
 // `inner` elements, row pitch `ld` elements, box {64, box_rows}, 128B swizzle.
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
                       uint32_t box_rows);
+// pair: run the CTA-pair kernel (256 x 256 tiles, cta_group::2); its B
+// operand maps use boxes of 128 rows (K-major) instead of 256.
 cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, int M, int N, int K, int* status,
-                             const EpiLse::Params& ep, cudaStream_t s);
+                             const EpiLse::Params& ep, bool pair, cudaStream_t s);
 cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
-                            int* status, const EpiStore::Params& ep, cudaStream_t s);
+                            int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s);
+// Whether the fused path uses the CTA-pair GEMM (default yes; LCE_TC_PAIR=0 selects the one-CTA kernel).
+bool tc_pair_default();
 
 // ---- SIMT fp32 GEMM (gemm_simt.cu); op as TcOp (LOGITS: A K-major, B
 // K-major; DX: A K-major, B N-major; DW: A M-major, B N-major).

@@ -1,0 +1,201 @@
+// tc2_gemm.cuh -- persistent bf16 GEMM on CTA pairs (tcgen05 cta_group::2).
+//
+// Same contraction and epilogues as tc_gemm.cuh, but each cluster of two
+// CTAs (on two SMs) owns a 256 x 256 output tile:
+//   * CTA r of the pair loads rows [128r, 128r+128) of the A tile and rows
+//     [128r, 128r+128) of the 256-row B tile into its own shared memory; the
+//     even CTA issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16), which
+//     reads both CTAs' halves and leaves rows 128r.. of the accumulator in
+//     CTA r's tensor memory. Each SM thus streams 32 KB per 64-wide K step
+//     instead of 48 KB for the same flops, and the 192 KB of shared memory
+//     hold 6 stages instead of 4.
+//   * both CTAs' TMA loads complete on the even CTA's "full" barrier
+//     (cta_group::2 form of the tensor load); the MMA completion is
+//     multicast to the "empty" / "accumulator full" barriers of both CTAs;
+//     both CTAs' epilogue warps release an accumulator on the even CTA's
+//     "accumulator empty" barrier (8 arrivals).
+// Every wait is bounded as in tc_gemm.cuh.
+#pragma once
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace lce {
+
+constexpr int TC2_BK = 64;
+constexpr int TC2_STAGES = 6;
+constexpr int TC2_A_BYTES = 128 * TC2_BK * 2;  // this CTA's 128 rows of A
+constexpr int TC2_B_BYTES = 128 * TC2_BK * 2;  // this CTA's 128 rows of the 256-row B tile
+constexpr int TC2_STAGE_BYTES = TC2_A_BYTES + TC2_B_BYTES;
+constexpr int TC2_SMEM_BYTES = TC2_STAGES * TC2_STAGE_BYTES + 1024 + 512;
+constexpr int TC2_THREADS = 256;
+constexpr int TC2_TMEM_COLS = 512;
+constexpr int TC2_TILE_M = 256;  // rows per pair tile (128 per CTA)
+constexpr int TC2_TILE_N = 256;
+
+template <bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(TC2_THREADS, 1)
+    tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const TcGemmArgs g, const typename Epi::Params ep) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TC2_STAGES * TC2_STAGE_BYTES);
+  uint64_t* empty = full + TC2_STAGES;
+  uint64_t* tfull = empty + TC2_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 = the CTA that issues the MMAs
+  const int pair = static_cast<int>(cluster_id_x());
+  const int npairs = static_cast<int>(nclusters_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < TC2_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(tmem_slot, TC2_TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nkb = (g.K + TC2_BK - 1) / TC2_BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_par = 0;
+      bool ok = true;
+      for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
+        int mb, nb;
+        tc_tile_coords(g, tile, mb, nb);
+        const int m0 = mb * TC2_TILE_M + static_cast<int>(rank) * 128;
+        const int n0 = nb * TC2_TILE_N + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = smem + stage * TC2_STAGE_BYTES;
+          uint8_t* sB = sA + TC2_A_BYTES;
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * TC2_STAGE_BYTES);
+          const uint32_t bar = mapa_u32(&full[stage], 0);
+          const int k0 = kb * TC2_BK;
+          if (!A_MN) {
+            tma_load_2d_pair(sA, &tmA, bar, k0, m0);
+          } else {
+            tma_load_2d_pair(sA, &tmA, bar, m0, k0);
+            tma_load_2d_pair(sA + 8192, &tmA, bar, m0 + 64, k0);
+          }
+          if (!B_MN) {
+            tma_load_2d_pair(sB, &tmB, bar, k0, n0);
+          } else {
+            tma_load_2d_pair(sB, &tmB, bar, n0, k0);
+            tma_load_2d_pair(sB + 8192, &tmB, bar, n0 + 64, k0);
+          }
+          issued_mask |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == TC2_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: a stage's copies have landed once the MMAs that read it are
+      // done, which arrives on this CTA's empty barrier.
+      for (int s = 0; s < TC2_STAGES; ++s)
+        if (issued_mask & (1u << s)) mbar_wait_cluster_drain(&empty[s], (issued_par >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA only)
+      constexpr uint32_t kIdesc = idesc_bf16_f32(TC2_TILE_M, TC2_TILE_N, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = pair; tile < g.num_tiles && ok; tile += npairs, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_par = (it >> 1) & 1;
+        if (!mbar_wait_cluster(&tempty[acc], acc_par ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * TC2_TILE_N;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_cluster(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * TC2_STAGE_BYTES);
+          const uint32_t b_base = a_base + TC2_A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < TC2_BK / 16; ++kk) {
+            const uint64_t adesc = A_MN ? sdesc_sw128(a_base + kk * 2048, 8192, 1024)
+                                        : sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc = B_MN ? sdesc_sw128(b_base + kk * 2048, 8192, 1024)
+                                        : sdesc_sw128(b_base + kk * 32, 16, 1024);
+            tc_mma_bf16_pair(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(&empty[stage], 0x3);
+          if (++stage == TC2_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) tc_commit_pair_mc(&tfull[acc], 0x3);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue (both CTAs): this CTA's 128 rows of the tile
+    const int q = warp & 3;
+    int it = 0;
+    for (int tile = pair; tile < g.num_tiles; tile += npairs, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_par = (it >> 1) & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_cluster(&tfull[acc], acc_par, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      int mb, nb;
+      tc_tile_coords(g, tile, mb, nb);
+      const int64_t row = static_cast<int64_t>(mb) * TC2_TILE_M + rank * 128 + q * 32 + lane;
+      const int64_t col0 = static_cast<int64_t>(nb) * TC2_TILE_N;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TC2_TILE_N;
+      Epi::template run<TC2_TILE_N / 32>(ep, row, col0, nb,
+                                         [&](int c, float (&v)[32]) { tmem_ld32(taddr + c * 32, v); });
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_u32(&tempty[acc], 0));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA frees or leaves while its peer may still use it
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc_pair(tmem_base, TC2_TMEM_COLS);
+  if (threadIdx.x == 0 && *abort_flag && g.status != nullptr) atomicOr(g.status, kStatusTimeout);
+}
+
+}  // namespace lce

@@ -113,8 +113,8 @@ def test_host_argument_errors(lib):
     assert ce(FAKE, FAKE, 4, 8, lce.LCE_F32, lce.LCE_RED_NONE, -100, None, FAKE, FAKE, 1 << 20, None) == 5
     assert ce(FAKE, FAKE, 4, 8, lce.LCE_F32, lce.LCE_RED_MEAN, -100, None, FAKE, FAKE, 16, None) == 6
     assert lib.lce_read_device_status(None, None) == 1
-    assert lib.lce_test_gemm_bf16(FAKE, FAKE, FAKE, 8, 8, 12, 0, 0, None, None) == 9
-    assert lib.lce_test_gemm_bf16(None, FAKE, FAKE, 8, 8, 8, 0, 0, None, None) == 1
+    assert lib.lce_test_gemm_bf16(FAKE, FAKE, FAKE, 8, 8, 12, 0, 0, 0, None, None) == 9
+    assert lib.lce_test_gemm_bf16(None, FAKE, FAKE, 8, 8, 8, 0, 0, 1, None, None) == 1
 
 
 def test_profile_api_without_launches(lib):

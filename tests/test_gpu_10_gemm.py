@@ -27,12 +27,13 @@ def _operands(M, N, K, a_mn, b_mn, dtype, seed):
     return A, B, Am @ Bm.T
 
 
+@pytest.mark.parametrize("pair", [False, True])
 @pytest.mark.parametrize("a_mn,b_mn", LAYOUTS)
-@pytest.mark.parametrize("M,N,K", SHAPES)
-def test_tcgen05_gemm(cuda_lib, a_mn, b_mn, M, N, K):
+@pytest.mark.parametrize("M,N,K", SHAPES + [(600, 800, 136)])
+def test_tcgen05_gemm(cuda_lib, a_mn, b_mn, M, N, K, pair):
     A, B, ref = _operands(M, N, K, a_mn, b_mn, torch.bfloat16, 11 + M + N + K)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = cuda_lib.test_gemm_bf16(A, B, M, N, K, a_mn, b_mn, status=status)
+    out = cuda_lib.test_gemm_bf16(A, B, M, N, K, a_mn, b_mn, status=status, cta_pair=pair)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert rel_max(out.double().cpu().numpy(), ref) < 1e-5
