@@ -36,6 +36,43 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+// Merge two (max, sum of exp(x - max)) pairs.
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  const float a = (m == -INFINITY) ? 0.0f : s * fast_exp2((m - mn) * kLog2e);
+  const float b = (m2 == -INFINITY) ? 0.0f : s2 * fast_exp2((m2 - mn) * kLog2e);
+  m = mn;
+  s = a + b;
+}
+// Block-wide merge of per-thread (max, sum-exp) pairs in one reduction;
+// every thread gets the block's pair.
+__device__ __forceinline__ void block_merge_ms(float& m, float& s, float2* scratch2) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    merge_ms(m, s, m2, s2);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) scratch2[warp] = make_float2(m, s);
+  __syncthreads();
+  const int nw = blockDim.x >> 5;
+  m = -INFINITY;
+  s = 0.0f;
+  if (lane < nw) {
+    const float2 p = scratch2[lane];
+    m = p.x;
+    s = p.y;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    merge_ms(m, s, m2, s2);
+  }
+}
+
 // Block-wide reductions over CE_THREADS threads; every thread gets the result.
 __device__ __forceinline__ float block_max(float v, float* scratch) {
   v = warp_max(v);
@@ -96,7 +133,7 @@ template <class T>
 __global__ void __launch_bounds__(CE_THREADS, 2) ce_resident_kernel(const CeArgs a, int cs) {
   constexpr int VE = 16 / static_cast<int>(sizeof(T));
   constexpr int NV = CE_EPT / VE;
-  __shared__ float scratch[32];
+  __shared__ float2 scratch2[32];
   __shared__ float xch[2][2];
   __shared__ float bc[2];
   const uint32_t rank = cluster_ctarank();
@@ -123,16 +160,16 @@ __global__ void __launch_bounds__(CE_THREADS, 2) ce_resident_kernel(const CeArgs
     const bool valid = target_valid(t, a.ignore_index, V);
     float zt = 0.0f;
     if (rank == 0 && tid == 0 && valid) zt = to_f32(rowp[t]);  // read before any CTA writes the row
-    float m = -INFINITY;
+    // per-thread (max, sum-exp), then one block-wide merge of the pairs
+    float cm = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < CE_EPT; ++i) m = fmaxf(m, x[i]);
-    const float cm = block_max(m, scratch);
-    float s = 0.0f;
-    if (cm != -INFINITY) {  // a slice wholly past V holds only padding
+    for (int i = 0; i < CE_EPT; ++i) cm = fmaxf(cm, x[i]);
+    float csum = 0.0f;
+    if (cm != -INFINITY) {  // all-padding threads (past V) contribute nothing
 #pragma unroll
-      for (int i = 0; i < CE_EPT; ++i) s += fast_exp2((x[i] - cm) * kLog2e);
+      for (int i = 0; i < CE_EPT; ++i) csum += fast_exp2((x[i] - cm) * kLog2e);
     }
-    const float csum = block_sum(s, scratch);
+    block_merge_ms(cm, csum, scratch2);
     if (tid == 0) {
       xch[iter & 1][0] = cm;
       xch[iter & 1][1] = csum;
