@@ -1,0 +1,93 @@
+"""PyTorch autograd on top of the C ABI.
+
+``linear_cross_entropy(input, weight, target, bias=None, reduction="mean",
+ignore_index=-100)`` returns the loss of the fused linear + cross-entropy
+as a differentiable tensor. Every step of the computation runs in
+liblce.so; this module only decides what to compute when, following the
+split of the batch-chunked op in PyTorch's ``linear_cross_entropy.py``:
+
+* reduction "mean" / "sum": the forward computes the loss and, in the same
+  library call, the gradients of every input that requires one (the scalar
+  ops of the page precompute the gradients); the backward scales them by
+  the upstream gradient (returned as they are when it is 1).
+* reduction "none": the forward computes only the per-row losses and keeps
+  the inputs; the backward recomputes the logits tile by tile and forms the
+  vector-Jacobian product with the per-row upstream gradient in one call
+  (the page's reduction="none" backward, which cannot keep the per-sample
+  softmax).
+
+Leading dimensions of ``input`` are flattened (``input.reshape(-1, D)``), as
+in PyTorch commit ddfa80bd "Fix NJT linear_backward() memory usage".
+Higher-order gradients are not supported.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import lce_forward, lce_forward_backward
+
+
+class _ScalarReduction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, X, W, b, target, reduction, ignore_index):
+        want_dx, want_dw, want_db = ctx.needs_input_grad[0], ctx.needs_input_grad[1], ctx.needs_input_grad[2]
+        if want_dx or want_dw or want_db:
+            loss, dX, dW, db = lce_forward_backward(X, W, b, target, reduction, ignore_index, None,
+                                                    want_dx=want_dx, want_dw=want_dw,
+                                                    want_db=want_db and b is not None)
+        else:
+            loss, dX, dW, db = lce_forward(X, W, b, target, reduction, ignore_index), None, None, None
+        ctx.grads = (dX, dW, db)
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad_loss):
+        dX, dW, db = ctx.grads
+        if not torch.equal(grad_loss, torch.ones_like(grad_loss)):
+            g = grad_loss.to(torch.float32)
+            dX = None if dX is None else (dX.float() * g).to(dX.dtype)
+            dW = None if dW is None else (dW.float() * g).to(dW.dtype)
+            db = None if db is None else (db.float() * g).to(db.dtype)
+        return dX, dW, db, None, None, None
+
+
+class _NoReduction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, X, W, b, target, ignore_index):
+        loss = lce_forward(X, W, b, target, "none", ignore_index)
+        ctx.save_for_backward(X, W, b, target)
+        ctx.ignore_index = ignore_index
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad_loss):
+        X, W, b, target = ctx.saved_tensors
+        need = ctx.needs_input_grad
+        _, dX, dW, db = lce_forward_backward(X, W, b, target, "none", ctx.ignore_index,
+                                             grad_loss.to(torch.float32).contiguous(),
+                                             want_dx=need[0], want_dw=need[1],
+                                             want_db=need[2] and b is not None)
+        return dX, dW, db, None, None
+
+
+def linear_cross_entropy(input, weight, target, bias=None, reduction="mean", ignore_index=-100):
+    """Loss of cross_entropy(input @ weight.T + bias, target) without the
+    [rows, classes] logits, differentiable in input, weight and bias.
+
+    input [..., D] (fp32 or bf16), weight [C, D], bias [C] or None (same
+    dtype), target [...] int64. Returns a float32 scalar (mean, sum) or a
+    float32 tensor of target's shape (none).
+    """
+    if reduction not in ("mean", "sum", "none"):
+        raise ValueError(f"reduction must be mean, sum or none, got {reduction!r}")
+    D = input.shape[-1]
+    X = input.reshape(-1, D).contiguous()
+    t = target.reshape(-1).contiguous()
+    if t.shape[0] != X.shape[0]:
+        raise ValueError("target must have one entry per row of input")
+    W = weight.contiguous()
+    b = None if bias is None else bias.contiguous()
+    if reduction == "none":
+        return _NoReduction.apply(X, W, b, t, ignore_index).reshape(target.shape)
+    return _ScalarReduction.apply(X, W, b, t, reduction, ignore_index)

@@ -1,0 +1,58 @@
+"""The autograd wrapper over the C ABI: loss and .grad of input, weight and
+bias against the float64 oracle, with leading dimensions, an upstream
+gradient, reduction none and retain_graph."""
+
+import numpy as np
+import pytest
+import torch
+
+from linear_cross_entropy_lce_gb300.autograd import linear_cross_entropy
+from linear_cross_entropy_lce_gb300.workloads import make_linear_inputs
+from oracle import lce_oracle as O
+from tests.util import TOL, rel_max, rel_scalar, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+def test_autograd_matches_oracle(cuda_lib, dtype, reduction):
+    inp = make_linear_inputs(6 * 50, 64, 700, dtype, "cuda", seed=31, bias=True, w_std=0.3, b_std=0.2,
+                             n_ignored=9)
+    X = inp["X"].reshape(6, 50, 64).requires_grad_(True)  # leading dims are flattened
+    W = inp["W"].clone().requires_grad_(True)
+    b = inp["b"].clone().requires_grad_(True)
+    t = inp["target"].reshape(6, 50)
+    loss = linear_cross_entropy(X, W, t, b, reduction)
+    if reduction == "none":
+        assert loss.shape == (6, 50)
+        g = torch.randn(6, 50, device="cuda")
+        loss.backward(g)
+        gn = to64(g).reshape(-1)
+    else:
+        (loss * 1.5).backward()
+        gn = 1.5
+    rl, rX, rW, rb = O.lce_forward_backward(to64(X.detach()).reshape(-1, 64), to64(W.detach()),
+                                            to64(b.detach()), t.reshape(-1).cpu().numpy(), reduction, -100, gn)
+    tol = TOL[dtype]
+    if reduction == "none":
+        assert rel_max(to64(loss.detach()).reshape(-1), rl) < tol["loss"]
+    else:
+        assert rel_scalar(loss.item(), rl) < tol["loss"]
+    assert X.grad.shape == X.shape and X.grad.dtype == dtype
+    assert rel_max(to64(X.grad).reshape(-1, 64), rX) < tol["grad"]
+    assert rel_max(to64(W.grad), rW) < tol["grad"]
+    assert rel_max(to64(b.grad), rb) < tol["grad"]
+
+
+def test_autograd_retain_graph_and_partial_grads(cuda_lib):
+    inp = make_linear_inputs(128, 32, 300, torch.bfloat16, "cuda", seed=32, w_std=0.4)
+    X = inp["X"].requires_grad_(True)
+    W = inp["W"]  # no gradient wanted for the weight
+    loss = linear_cross_entropy(X, W, inp["target"], reduction="mean")
+    loss.backward(retain_graph=True)
+    g1 = X.grad.clone()
+    X.grad = None
+    loss.backward()
+    assert torch.equal(g1, X.grad)
+    assert W.grad is None
