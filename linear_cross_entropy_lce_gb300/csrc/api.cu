@@ -283,10 +283,12 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
     el.ptilde_bf16 = dtype == LCE_BF16;
     if (p.tc) {
       const void* Xc = static_cast<const __nv_bfloat16*>(X) + row0 * D;
-      CUtensorMap tmX_k;
+      CUtensorMap tmX_k, tmL;
       if (!encode_tmap_bf16(&tmX_k, Xc, D, rows, D, TC_BM)) return LCE_ERR_CUDA;
-      LCE_TRY(launch_tc_logits(tmX_k, tmW_k, static_cast<int>(rows), static_cast<int>(C), static_cast<int>(D),
-                               &hdr->status, el, pair, s));
+      const bool tma_out = pair && backward;
+      if (tma_out && !encode_tmap_bf16_store(&tmL, Lbuf, p.C_pad, rows, p.C_pad)) return LCE_ERR_CUDA;
+      LCE_TRY(launch_tc_logits(tmX_k, tmW_k, tma_out ? &tmL : nullptr, static_cast<int>(rows), static_cast<int>(C),
+                               static_cast<int>(D), &hdr->status, el, pair, s));
     } else {
       const float* Xc = static_cast<const float*>(X) + row0 * D;
       LCE_TRY(launch_simt_logits(Xc, static_cast<const float*>(W), D, D, rows, C, D, el, s));
@@ -337,10 +339,12 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       es.cols = D;
       es.vec_ok = aligned16(dX) && ((D * gsz) % 16 == 0);
       if (p.tc) {
-        CUtensorMap tmG_k;
+        CUtensorMap tmG_k, tmdX;
         if (!encode_tmap_bf16(&tmG_k, Lbuf, C, rows, p.C_pad, TC_BM)) return LCE_ERR_CUDA;
-        LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmW_n, static_cast<int>(rows), static_cast<int>(D),
-                                static_cast<int>(C), &hdr->status, es, pair, s));
+        const bool tma_out = pair && es.out_bf16 && es.vec_ok;
+        if (tma_out && !encode_tmap_bf16_store(&tmdX, es.out, D, rows, D)) return LCE_ERR_CUDA;
+        LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmW_n, tma_out ? &tmdX : nullptr, static_cast<int>(rows),
+                                static_cast<int>(D), static_cast<int>(C), &hdr->status, es, pair, s));
       } else {
         LCE_TRY(launch_simt_store(TC_DX, static_cast<const float*>(Lbuf), static_cast<const float*>(W), p.C_pad, D,
                                   rows, D, C, es, s));
@@ -367,11 +371,13 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       }
       if (p.tc) {
         const void* Xc = static_cast<const __nv_bfloat16*>(X) + row0 * D;
-        CUtensorMap tmG_m, tmX_n;
+        CUtensorMap tmG_m, tmX_n, tmdW;
         if (!encode_tmap_bf16(&tmG_m, Lbuf, C, rows, p.C_pad, 64)) return LCE_ERR_CUDA;
         if (!encode_tmap_bf16(&tmX_n, Xc, D, rows, D, 64)) return LCE_ERR_CUDA;
-        LCE_TRY(launch_tc_store(TC_DW, tmG_m, tmX_n, static_cast<int>(C), static_cast<int>(D),
-                                static_cast<int>(rows), &hdr->status, es, pair, s));
+        const bool tma_out = pair && es.mode == 0 && es.out_bf16 && es.vec_ok;
+        if (tma_out && !encode_tmap_bf16_store(&tmdW, dW, D, C, D)) return LCE_ERR_CUDA;
+        LCE_TRY(launch_tc_store(TC_DW, tmG_m, tmX_n, tma_out ? &tmdW : nullptr, static_cast<int>(C),
+                                static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s));
       } else {
         const float* Xc = static_cast<const float*>(X) + row0 * D;
         LCE_TRY(launch_simt_store(TC_DW, static_cast<const float*>(Lbuf), Xc, p.C_pad, D, C, D, rows, es, s));
@@ -561,8 +567,9 @@ int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t M, int6
   es.cols = N;
   es.vec_ok = (N % 4) == 0;
   const int op = a_mn_major ? (b_mn_major ? TC_TEST_MM : TC_TEST_MK) : (b_mn_major ? TC_TEST_KM : TC_TEST_KK);
-  return from_cuda(launch_tc_store(op, ta, tb, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                   dev_status, es, cta_pair != 0, static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_tc_store(op, ta, tb, nullptr, static_cast<int>(M), static_cast<int>(N),
+                                   static_cast<int>(K), dev_status, es, cta_pair != 0,
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 int lce_test_gemm_f32(const float* A, const float* B, float* out, int64_t M, int64_t N, int64_t K, int a_mn_major,

@@ -12,6 +12,51 @@
 
 namespace lce {
 
+// Output path of one epilogue warp. With tmap == NULL every thread stores
+// its row directly. Otherwise bf16 results go out per 32-column chunk
+// through a TMA store of the warp's 32 x 32 box: the warp stages the chunk
+// in a 2 KB buffer (32 rows x 64 B, 64-byte swizzle, so the 16-byte writes
+// of the 32 lanes hit distinct banks) and lane 0 issues the store; two
+// buffers alternate, and a buffer is rewritten only after the store issued
+// from it two chunks earlier has finished reading it. Calls are
+// warp-collective; rows and columns outside the tensor are not written.
+struct EpiIO {
+  const CUtensorMap* tmap;
+  uint8_t* stage;    // 2 x 2048 B, 1024-byte aligned
+  int64_t row_base;  // first output row of this warp
+  int lane;
+  int nst;           // stores issued so far (buffer parity)
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void stage_store_bf16(EpiIO& io, const float (&v)[32], int64_t col) {
+  uint8_t* buf = io.stage + (io.nst & 1) * 2048;
+  if (io.lane == 0) bulk_wait_read_le1();
+  __syncwarp();
+  const uint32_t row_addr = smem_u32(buf) + io.lane * 64;
+  const int sw = (io.lane >> 1) & 3;  // 64-byte swizzle: 16-byte chunk index ^= (row / 2) % 4
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    st_shared_v4(row_addr + ((q ^ sw) << 4), u);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (io.lane == 0) {
+    tma_store_2d(io.tmap, buf, static_cast<int32_t>(col), static_cast<int32_t>(io.row_base));
+    bulk_commit_group();
+  }
+  ++io.nst;
+}
+
 // ---------------------------------------------------------------------------
 // Logits epilogue of the forward GEMM (z = X W^T + b).
 //
@@ -48,7 +93,7 @@ struct EpiLse {
 
   template <int NCHUNK, class Loader>
   __device__ static __forceinline__ void run(const Params& p, int64_t row, int64_t col0, int64_t seg,
-                                             Loader&& load) {
+                                             Loader&& load, EpiIO& io) {
     const bool row_ok = row < p.rows;
     const int64_t t = row_ok ? p.target[row] : -1;
     const int tl = (t >= col0 && t < col0 + NCHUNK * 32 && t < p.C) ? static_cast<int>(t - col0) : -1;
@@ -79,7 +124,9 @@ struct EpiLse {
         s += e;
         v[i] = e;
       }
-      if (p.ptilde != nullptr && row_ok) {
+      if (p.ptilde != nullptr && io.tmap != nullptr) {
+        stage_store_bf16(io, v, col0 + 32 * c);
+      } else if (p.ptilde != nullptr && row_ok) {
         const int64_t off = row * p.ld_p + col0 + 32 * c;
         if (p.ptilde_bf16) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.ptilde) + off);
@@ -146,12 +193,16 @@ struct EpiStore {
 
   template <int NCHUNK, class Loader>
   __device__ static __forceinline__ void run(const Params& p, int64_t row, int64_t col0, int64_t /*seg*/,
-                                             Loader&& load) {
+                                             Loader&& load, EpiIO& io) {
     const bool row_ok = row < p.rows;
     float v[32];
 #pragma unroll 1
     for (int c = 0; c < NCHUNK; ++c) {
       load(c, v);
+      if (io.tmap != nullptr) {  // bf16, mode 0 (the host only sets tmap then)
+        stage_store_bf16(io, v, col0 + 32 * c);
+        continue;
+      }
       if (!row_ok) continue;
       const int64_t cb = col0 + 32 * c;
       const int64_t base = row * p.ldo + cb;

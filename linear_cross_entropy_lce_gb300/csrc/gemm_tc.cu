@@ -47,6 +47,7 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int
   g.num_tiles = g.num_m_blocks * g.num_n_blocks;
   g.m_inner = m_inner;
   g.status = status;
+  g.use_tma_out = 0;
   if (g.num_tiles == 0) return cudaSuccess;
   const int grid = g.num_tiles < num_sms() ? g.num_tiles : num_sms();
   prof_before(kid, s, 2.0 * M * N * static_cast<double>(K));
@@ -57,8 +58,8 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int
 }
 
 template <bool A_MN, bool B_MN, class Epi>
-cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, int m_inner,
-                       int* status, const typename Epi::Params& ep, int kid, cudaStream_t s) {
+cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M, int N,
+                       int K, int m_inner, int* status, const typename Epi::Params& ep, int kid, cudaStream_t s) {
   auto kern = tc2_gemm_kernel<A_MN, B_MN, Epi>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -75,6 +76,7 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, in
   g.num_tiles = g.num_m_blocks * g.num_n_blocks;
   g.m_inner = m_inner;
   g.status = status;
+  g.use_tma_out = tmOut != nullptr ? 1 : 0;
   if (g.num_tiles == 0) return cudaSuccess;
   const int max_pairs = num_sms() / 2;
   const int pairs = g.num_tiles < max_pairs ? g.num_tiles : max_pairs;
@@ -91,7 +93,7 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, in
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   prof_before(kid, s, 2.0 * M * N * static_cast<double>(K));
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, g, ep);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmOut != nullptr ? *tmOut : tmA, g, ep);
   prof_after(kid, s);
   return e;
 }
@@ -121,30 +123,43 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
   return r == CUDA_SUCCESS;
 }
 
+bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64_t rows, uint64_t ld) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // logits: A = X [M rows, K] K-major, B = W [N rows, K] K-major; consecutive
 // tiles walk down the rows so the CTAs in flight share one W panel.
-cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, int M, int N, int K, int* status,
-                             const EpiLse::Params& ep, bool pair, cudaStream_t s) {
-  if (pair) return launch_tc2<false, false, EpiLse>(tmX, tmW, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s);
+cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
+                             int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s) {
+  if (pair) return launch_tc2<false, false, EpiLse>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s);
   return launch_tc<false, false, EpiLse>(tmX, tmW, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s);
 }
 
-cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
-                            int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s) {
+cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M,
+                            int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s) {
   if (pair) {
     switch (op) {
       case TC_DX:
-        return launch_tc2<false, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_DX_TC, s);
+        return launch_tc2<false, true, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DX_TC, s);
       case TC_DW:
-        return launch_tc2<true, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_DW_TC, s);
+        return launch_tc2<true, true, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DW_TC, s);
       case TC_TEST_KK:
-        return launch_tc2<false, false, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+        return launch_tc2<false, false, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_TEST, s);
       case TC_TEST_KM:
-        return launch_tc2<false, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+        return launch_tc2<false, true, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_TEST, s);
       case TC_TEST_MK:
-        return launch_tc2<true, false, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+        return launch_tc2<true, false, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_TEST, s);
       case TC_TEST_MM:
-        return launch_tc2<true, true, EpiStore>(tmA, tmB, M, N, K, 0, status, ep, K_GEMM_TEST, s);
+        return launch_tc2<true, true, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_TEST, s);
       default:
         return cudaErrorInvalidValue;
     }

@@ -48,10 +48,14 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
                       uint32_t box_rows);
 // pair: run the CTA-pair kernel (256 x 256 tiles, cta_group::2); its B
 // operand maps use boxes of 128 rows (K-major) instead of 256.
-cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, int M, int N, int K, int* status,
-                             const EpiLse::Params& ep, bool pair, cudaStream_t s);
-cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
-                            int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s);
+// tmOut (pair kernel only; NULL = direct stores): bf16 output tensor map
+// with 32 x 32 boxes and 64-byte swizzle (encode_tmap_bf16_store) through
+// which the epilogue writes P~ (logits) or the mode-0 bf16 result (store).
+cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
+                             int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s);
+cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M,
+                            int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s);
+bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64_t rows, uint64_t ld);
 // Whether the fused path uses the CTA-pair GEMM (default yes; LCE_TC_PAIR=0 selects the one-CTA kernel).
 bool tc_pair_default();
 

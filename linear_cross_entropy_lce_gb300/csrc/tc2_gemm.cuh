@@ -27,7 +27,8 @@ constexpr int TC2_STAGES = 6;
 constexpr int TC2_A_BYTES = 128 * TC2_BK * 2;  // this CTA's 128 rows of A
 constexpr int TC2_B_BYTES = 128 * TC2_BK * 2;  // this CTA's 128 rows of the 256-row B tile
 constexpr int TC2_STAGE_BYTES = TC2_A_BYTES + TC2_B_BYTES;
-constexpr int TC2_SMEM_BYTES = TC2_STAGES * TC2_STAGE_BYTES + 1024 + 512;
+constexpr int TC2_STAGING_BYTES = 4 * 2 * 2048;  // epilogue: 2 x 2 KB per epilogue warp
+constexpr int TC2_SMEM_BYTES = TC2_STAGES * TC2_STAGE_BYTES + TC2_STAGING_BYTES + 1024 + 512;
 constexpr int TC2_THREADS = 256;
 constexpr int TC2_TMEM_COLS = 512;
 constexpr int TC2_TILE_M = 256;  // rows per pair tile (128 per CTA)
@@ -36,10 +37,12 @@ constexpr int TC2_TILE_N = 256;
 template <bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(TC2_THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const TcGemmArgs g, const typename Epi::Params ep) {
+                    const __grid_constant__ CUtensorMap tmOut, const TcGemmArgs g,
+                    const typename Epi::Params ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TC2_STAGES * TC2_STAGE_BYTES);
+  uint8_t* staging = smem + TC2_STAGES * TC2_STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + TC2_STAGING_BYTES);
   uint64_t* empty = full + TC2_STAGES;
   uint64_t* tfull = empty + TC2_STAGES;
   uint64_t* tempty = tfull + 2;
@@ -168,6 +171,7 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
   } else if (warp >= 4) {
     // ---------------- epilogue (both CTAs): this CTA's 128 rows of the tile
     const int q = warp & 3;
+    EpiIO io{g.use_tma_out ? &tmOut : nullptr, staging + q * 4096, 0, lane, 0};
     int it = 0;
     for (int tile = pair; tile < g.num_tiles; tile += npairs, ++it) {
       const int acc = it & 1;
@@ -182,12 +186,15 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
       const int64_t row = static_cast<int64_t>(mb) * TC2_TILE_M + rank * 128 + q * 32 + lane;
       const int64_t col0 = static_cast<int64_t>(nb) * TC2_TILE_N;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TC2_TILE_N;
-      Epi::template run<TC2_TILE_N / 32>(ep, row, col0, nb,
-                                         [&](int c, float (&v)[32]) { tmem_ld32(taddr + c * 32, v); });
+      io.row_base = static_cast<int64_t>(mb) * TC2_TILE_M + rank * 128 + q * 32;
+      Epi::template run<TC2_TILE_N / 32>(
+          ep, row, col0, nb, [&](int c, float (&v)[32]) { tmem_ld32(taddr + c * 32, v); }, io);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_u32(&tempty[acc], 0));
     }
+    if (lane == 0) bulk_wait_all();  // every TMA store of this warp has landed
+    __syncwarp();
   }
 
   tc_fence_before();

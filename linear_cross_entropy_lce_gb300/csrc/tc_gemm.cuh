@@ -38,6 +38,7 @@ struct TcGemmArgs {
   int num_m_blocks, num_n_blocks, num_tiles;
   int m_inner;  // 1: consecutive tiles walk down M (share a B panel); 0: walk along N
   int* status;  // device status word or NULL
+  int use_tma_out;  // CTA-pair kernel: epilogue stores bf16 results through the output tensor map
 };
 
 __device__ __forceinline__ void tc_tile_coords(const TcGemmArgs& g, int tile, int& mb, int& nb) {
@@ -196,8 +197,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int64_t row = static_cast<int64_t>(mb) * TC_BM + q * 32 + lane;
       const int64_t col0 = static_cast<int64_t>(nb) * TC_BN;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TC_BN;
+      EpiIO io{nullptr, nullptr, 0, lane, 0};
       Epi::template run<TC_BN / 32>(ep, row, col0, nb,
-                                    [&](int c, float (&v)[32]) { tmem_ld32(taddr + c * 32, v); });
+                                    [&](int c, float (&v)[32]) { tmem_ld32(taddr + c * 32, v); }, io);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
