@@ -38,14 +38,7 @@ METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor
 # DRAM bytes (read + write) per launch of a kernel, from an ncu capture of
 # the same command: {(workload, kernel): bytes}. An entry is removed when the
 # kernel changes after its capture.
-MEASURED_TRAFFIC = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (CTA-pair GEMM build),
-    # see profiles/tc2_gemm_bf16_head_N2048_D4096_C32768.md
-    ("bf16_llm_head", "gemm_logits_tc"): 8988454656 + 2123299072,
-    ("bf16_llm_head", "gemm_dx_tc"): 12589023488 + 60022528,
-    ("bf16_llm_head", "gemm_dw_tc"): 9717467392 + 1043529472,
-    ("bf16_llm_head", "grad_logits"): 2134378496 + 2036349952,
-}
+MEASURED_TRAFFIC = {}
 
 
 def _peaks():

@@ -268,65 +268,86 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
   for (int64_t ci = 0; ci < p.nchunks; ++ci) {
     const int64_t row0 = ci * p.Bc;
     const int64_t rows = std::min(p.Bc, N - row0);
-    // ---- logits GEMM with the (max, sum-exp) epilogue
-    EpiLse::Params el;
-    el.bias = b;
-    el.bias_bf16 = dtype == LCE_BF16;
-    el.target = target + row0;
-    el.C = C;
-    el.rows = static_cast<int>(rows);
-    el.partial = partial;
-    el.partial_ld = p.Bc;
-    el.zt = zt;
-    el.ptilde = backward ? Lbuf : nullptr;
-    el.ld_p = p.C_pad;
-    el.ptilde_bf16 = dtype == LCE_BF16;
-    if (p.tc) {
-      const void* Xc = static_cast<const __nv_bfloat16*>(X) + row0 * D;
-      CUtensorMap tmX_k, tmL;
-      if (!encode_tmap_bf16(&tmX_k, Xc, D, rows, D, TC_BM)) return LCE_ERR_CUDA;
-      const bool tma_out = pair && backward;
-      if (tma_out && !encode_tmap_bf16_store(&tmL, Lbuf, p.C_pad, rows, p.C_pad)) return LCE_ERR_CUDA;
-      LCE_TRY(launch_tc_logits(tmX_k, tmW_k, tma_out ? &tmL : nullptr, static_cast<int>(rows), static_cast<int>(C),
-                               static_cast<int>(D), &hdr->status, el, pair, s));
-    } else {
-      const float* Xc = static_cast<const float*>(X) + row0 * D;
-      LCE_TRY(launch_simt_logits(Xc, static_cast<const float*>(W), D, D, rows, C, D, el, s));
+    // ---- logits, row lse / loss, and G, over row slabs of the chunk. On the
+    // CTA-pair path with a backward, the chunk is cut into 4 slabs and the
+    // idle warps of slab k's logits GEMM form G for slab k-1, so only the
+    // last slab's G formation runs as a kernel of its own.
+    const bool slabbed = p.tc && pair && backward && rows >= 1024;
+    const int64_t slab = slabbed ? ceil_div(ceil_div(rows, 4), 256) * 256 : rows;
+    const int64_t nslab = ceil_div(rows, slab);
+    GradArgs ga_prev;
+    bool have_prev = false;
+    for (int64_t si = 0; si < nslab; ++si) {
+      const int64_t so = si * slab;                      // slab offset within the chunk
+      const int64_t sr = std::min(slab, rows - so);      // rows in the slab
+      EpiLse::Params el;
+      el.bias = b;
+      el.bias_bf16 = dtype == LCE_BF16;
+      el.target = target + row0 + so;
+      el.C = C;
+      el.rows = static_cast<int>(sr);
+      el.partial = partial + so;
+      el.partial_ld = p.Bc;
+      el.zt = zt + so;
+      el.ptilde = backward ? static_cast<uint8_t*>(Lbuf) + static_cast<size_t>(so) * p.C_pad * esize(dtype)
+                           : nullptr;
+      el.ld_p = p.C_pad;
+      el.ptilde_bf16 = dtype == LCE_BF16;
+      if (p.tc) {
+        const void* Xc = static_cast<const __nv_bfloat16*>(X) + (row0 + so) * D;
+        CUtensorMap tmX_k, tmL;
+        if (!encode_tmap_bf16(&tmX_k, Xc, D, sr, D, TC_BM)) return LCE_ERR_CUDA;
+        const bool tma_out = pair && backward;
+        if (tma_out && !encode_tmap_bf16_store(&tmL, el.ptilde, p.C_pad, sr, p.C_pad)) return LCE_ERR_CUDA;
+        SideGrad side;
+        side.a = ga_prev;
+        side.enabled = have_prev ? 1 : 0;
+        LCE_TRY(launch_tc_logits(tmX_k, tmW_k, tma_out ? &tmL : nullptr, static_cast<int>(sr), static_cast<int>(C),
+                                 static_cast<int>(D), &hdr->status, el, pair, s, have_prev ? &side : nullptr));
+      } else {
+        const float* Xc = static_cast<const float*>(X) + (row0 + so) * D;
+        LCE_TRY(launch_simt_logits(Xc, static_cast<const float*>(W), D, D, sr, C, D, el, s));
+      }
+      CombineArgs ca;
+      ca.partial = partial + so;
+      ca.ld = p.Bc;
+      ca.nseg = p.nseg;
+      ca.rows = sr;
+      ca.row0 = row0 + so;
+      ca.zt = zt + so;
+      ca.tcol = tcol + so;
+      ca.gt = gt + so;
+      ca.target = target;
+      ca.ignore_index = ignore_index;
+      ca.C = C;
+      ca.rw = rw;
+      ca.hdr = hdr;
+      ca.loss_rows = rows_out;
+      ca.lse_out = lse_out;
+      ca.backward = backward ? 1 : 0;
+      LCE_TRY(launch_combine(ca, s));
+      if (!backward) continue;
+      GradArgs ga;
+      ga.L = el.ptilde;
+      ga.ld = p.C_pad;
+      ga.rows = sr;
+      ga.C = C;
+      ga.segw = p.segw;
+      ga.nseg = p.nseg;
+      ga.scale = partial + so;
+      ga.sld = p.Bc;
+      ga.tcol = tcol + so;
+      ga.gt = gt + so;
+      ga.db_acc = want_db ? db_acc : nullptr;
+      if (slabbed && si + 1 < nslab) {
+        ga_prev = ga;  // formed by the next slab's GEMM
+        have_prev = true;
+      } else {
+        LCE_TRY(launch_grad_logits(ga, dtype == LCE_BF16, s));
+        have_prev = false;
+      }
     }
-    // ---- row lse, loss, scales
-    CombineArgs ca;
-    ca.partial = partial;
-    ca.ld = p.Bc;
-    ca.nseg = p.nseg;
-    ca.rows = rows;
-    ca.row0 = row0;
-    ca.zt = zt;
-    ca.tcol = tcol;
-    ca.gt = gt;
-    ca.target = target;
-    ca.ignore_index = ignore_index;
-    ca.C = C;
-    ca.rw = rw;
-    ca.hdr = hdr;
-    ca.loss_rows = rows_out;
-    ca.lse_out = lse_out;
-    ca.backward = backward ? 1 : 0;
-    LCE_TRY(launch_combine(ca, s));
     if (!backward) continue;
-    // ---- G in place
-    GradArgs ga;
-    ga.L = Lbuf;
-    ga.ld = p.C_pad;
-    ga.rows = rows;
-    ga.C = C;
-    ga.segw = p.segw;
-    ga.nseg = p.nseg;
-    ga.scale = partial;
-    ga.sld = p.Bc;
-    ga.tcol = tcol;
-    ga.gt = gt;
-    ga.db_acc = want_db ? db_acc : nullptr;
-    LCE_TRY(launch_grad_logits(ga, dtype == LCE_BF16, s));
     // ---- dX = G W
     if (want_dx) {
       EpiStore::Params es;

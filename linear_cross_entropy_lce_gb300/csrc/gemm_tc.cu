@@ -1,5 +1,6 @@
 // gemm_tc.cu -- instantiations and host launchers of the tcgen05 GEMM.
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -59,7 +60,8 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int
 
 template <bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M, int N,
-                       int K, int m_inner, int* status, const typename Epi::Params& ep, int kid, cudaStream_t s) {
+                       int K, int m_inner, int* status, const typename Epi::Params& ep, int kid, cudaStream_t s,
+                       const SideGrad* side = nullptr) {
   auto kern = tc2_gemm_kernel<A_MN, B_MN, Epi>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -93,7 +95,13 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   prof_before(kid, s, 2.0 * M * N * static_cast<double>(K));
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmOut != nullptr ? *tmOut : tmA, g, ep);
+  SideGrad sd;
+  if (side != nullptr) {
+    sd = *side;
+  } else {
+    memset(&sd, 0, sizeof(sd));
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmOut != nullptr ? *tmOut : tmA, g, ep, sd);
   prof_after(kid, s);
   return e;
 }
@@ -139,8 +147,10 @@ bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64
 // logits: A = X [M rows, K] K-major, B = W [N rows, K] K-major; consecutive
 // tiles walk down the rows so the CTAs in flight share one W panel.
 cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
-                             int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s) {
-  if (pair) return launch_tc2<false, false, EpiLse>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s);
+                             int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s,
+                             const SideGrad* side) {
+  if (pair)
+    return launch_tc2<false, false, EpiLse>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s, side);
   return launch_tc<false, false, EpiLse>(tmX, tmW, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s);
 }
 

@@ -40,6 +40,8 @@ void prof_after(int id, cudaStream_t s);
 
 int num_sms();
 
+struct SideGrad;
+
 // ---- tcgen05 GEMM (gemm_tc.cu)
 enum TcOp { TC_LOGITS = 0, TC_DX = 1, TC_DW = 2, TC_TEST_KK = 3, TC_TEST_KM = 4, TC_TEST_MK = 5, TC_TEST_MM = 6 };
 // Encodes a 2-D bf16 tensor map over a row-major matrix with `rows` rows of
@@ -52,7 +54,8 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
 // with 32 x 32 boxes and 64-byte swizzle (encode_tmap_bf16_store) through
 // which the epilogue writes P~ (logits) or the mode-0 bf16 result (store).
 cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
-                             int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s);
+                             int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s,
+                             const SideGrad* side = nullptr);
 cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M,
                             int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s);
 bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64_t rows, uint64_t ld);
@@ -102,6 +105,12 @@ struct GradArgs {
   float* db_acc;  // [C] or NULL
 };
 cudaError_t launch_grad_logits(const GradArgs& a, bool bf16, cudaStream_t s);
+// G formation for a row slab (bf16, 256-column segments) done by the idle
+// warps of the CTA-pair logits GEMM of the next slab.
+struct SideGrad {
+  GradArgs a;
+  int enabled;
+};
 cudaError_t launch_loss_finalize(const float* loss_rows, int64_t N, int reduction, const WsHeader* hdr,
                                  float* loss_out, cudaStream_t s);
 cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, bool bf16, cudaStream_t s);

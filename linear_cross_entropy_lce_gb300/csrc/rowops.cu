@@ -2,6 +2,7 @@
 // valid-target count, merge of the per-segment (max, sum-exp) pairs into
 // the row log-sum-exp and loss, formation of the gradient tile G, and the
 // final loss / bias-gradient reductions.
+#include "grad_unit.cuh"
 #include "internal.h"
 
 namespace lce {
@@ -104,65 +105,12 @@ __global__ void combine_kernel(const CombineArgs a) {
   }
 }
 
-// G[r, j] = P~[r, j] * scale[seg(j), r], replaced by gt[r] at the target
-// column, written in place over P~ (linear_cross_entropy.py: logits scaled
-// by w / denominator, then the one-hot corrections). Optionally adds the
-// column sums of G over the block's rows into db_acc (fp32 atomics, one per
-// column per block).
+// Stand-alone G formation: one (segment, 64-row block) unit per CTA.
 template <class T, int SEGW>
 __global__ void __launch_bounds__(256) grad_logits_kernel(const GradArgs a) {
-  constexpr int VE = 16 / static_cast<int>(sizeof(T));
-  constexpr int TPR = SEGW / VE;
-  constexpr int RPP = 256 / TPR;
-  constexpr int RB = 64;
-  __shared__ float red[RPP][TPR * VE];
-  const int seg = blockIdx.x;
-  const int64_t r_begin = static_cast<int64_t>(blockIdx.y) * RB;
-  const int64_t r_end = (r_begin + RB < a.rows) ? r_begin + RB : a.rows;
-  const int lt = threadIdx.x % TPR;
-  const int rsub = threadIdx.x / TPR;
-  const int64_t col = static_cast<int64_t>(seg) * SEGW + lt * VE;
-  constexpr int NR = RB / RPP;  // rows per thread, all loaded before any store
-  float colsum[VE];
-#pragma unroll
-  for (int i = 0; i < VE; ++i) colsum[i] = 0.0f;
-  uint4 raw[NR];
-  float sc[NR];
-  int tc[NR];
-#pragma unroll
-  for (int k = 0; k < NR; ++k) {
-    const int64_t r = r_begin + rsub + k * RPP;
-    if (r < r_end) {
-      raw[k] = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.L) + r * a.ld + col);
-      sc[k] = a.scale[seg * a.sld + r].x;
-      tc[k] = a.tcol[r];
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < NR; ++k) {
-    const int64_t r = r_begin + rsub + k * RPP;
-    if (r >= r_end) continue;
-    T* e = reinterpret_cast<T*>(&raw[k]);
-#pragma unroll
-    for (int i = 0; i < VE; ++i) {
-      float gv = to_f32(e[i]) * sc[k];
-      if (col + i == tc[k]) gv = a.gt[r];
-      e[i] = from_f32<T>(gv);
-      colsum[i] += to_f32(e[i]);
-    }
-    *reinterpret_cast<uint4*>(static_cast<T*>(a.L) + r * a.ld + col) = raw[k];
-  }
-  if (a.db_acc == nullptr) return;
-#pragma unroll
-  for (int i = 0; i < VE; ++i) red[rsub][lt * VE + i] = colsum[i];
-  __syncthreads();
-  for (int c = threadIdx.x; c < TPR * VE; c += 256) {
-    float acc = 0.0f;
-#pragma unroll 4
-    for (int q = 0; q < RPP; ++q) acc += red[q][c];
-    const int64_t gc = static_cast<int64_t>(seg) * SEGW + c;
-    if (gc < a.C) atomicAdd(&a.db_acc[gc], acc);
-  }
+  __shared__ float red[256 / (SEGW / (16 / sizeof(T)))][SEGW];
+  grad_unit<T, SEGW, 256, 64>(a, blockIdx.x, static_cast<int64_t>(blockIdx.y) * 64, threadIdx.x, &red[0][0],
+                              [] { __syncthreads(); });
 }
 
 // Deterministic single-block sum of the per-row losses in fp64; mean

@@ -18,6 +18,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "grad_unit.cuh"
 #include "ptx.cuh"
 
 namespace lce {
@@ -28,7 +29,8 @@ constexpr int TC2_A_BYTES = 128 * TC2_BK * 2;  // this CTA's 128 rows of A
 constexpr int TC2_B_BYTES = 128 * TC2_BK * 2;  // this CTA's 128 rows of the 256-row B tile
 constexpr int TC2_STAGE_BYTES = TC2_A_BYTES + TC2_B_BYTES;
 constexpr int TC2_STAGING_BYTES = 4 * 2 * 2048;  // epilogue: 2 x 2 KB per epilogue warp
-constexpr int TC2_SMEM_BYTES = TC2_STAGES * TC2_STAGE_BYTES + TC2_STAGING_BYTES + 1024 + 512;
+constexpr int TC2_SIDE_BYTES = 2 * 256 * 4;       // warps 2-3: column-sum scratch of the G formation
+constexpr int TC2_SMEM_BYTES = TC2_STAGES * TC2_STAGE_BYTES + TC2_STAGING_BYTES + TC2_SIDE_BYTES + 1024 + 512;
 constexpr int TC2_THREADS = 256;
 constexpr int TC2_TMEM_COLS = 512;
 constexpr int TC2_TILE_M = 256;  // rows per pair tile (128 per CTA)
@@ -38,11 +40,12 @@ template <bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(TC2_THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmOut, const TcGemmArgs g,
-                    const typename Epi::Params ep) {
+                    const typename Epi::Params ep, const SideGrad side) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + TC2_STAGES * TC2_STAGE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + TC2_STAGING_BYTES);
+  float* side_red = reinterpret_cast<float*>(staging + TC2_STAGING_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + TC2_STAGING_BYTES + TC2_SIDE_BYTES);
   uint64_t* empty = full + TC2_STAGES;
   uint64_t* tfull = empty + TC2_STAGES;
   uint64_t* tempty = tfull + 2;
@@ -166,6 +169,18 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
           }
         }
         if (ok) tc_commit_pair_mc(&tfull[acc], 0x3);
+      }
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ---------------- side job: G formation of the previous row slab
+    if (side.enabled) {
+      const int tid = threadIdx.x - 64;
+      const int64_t nunits = ((side.a.rows + 63) / 64) * side.a.nseg;
+      for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
+        const int seg = static_cast<int>(u % side.a.nseg);
+        const int64_t rb = u / side.a.nseg;
+        grad_unit<__nv_bfloat16, 256, 64, 64>(side.a, seg, rb * 64, tid, side_red,
+                                              [] { asm volatile("bar.sync 1, 64;" ::: "memory"); });
       }
     }
   } else if (warp >= 4) {

@@ -194,3 +194,12 @@ def test_outputs_fully_written(cuda_lib):
     torch.cuda.synchronize()
     assert torch.isfinite(dX).all() and torch.isfinite(dW).all() and torch.isfinite(db).all()
     assert math.isfinite(loss.item())
+
+
+@pytest.mark.parametrize("N,chunk_rows,reduction", [(1500, 0, "mean"), (2500, 1024, "sum"), (1100, 0, "none")])
+def test_row_slabs(cuda_lib, N, chunk_rows, reduction):
+    # bf16 backward over >= 1024 rows: the chunk is cut into row slabs and the
+    # logits GEMM of slab k forms G of slab k-1 (with the bias gradient)
+    inp = make_linear_inputs(N, 128, 2000, torch.bfloat16, "cuda", seed=N, bias=True, w_std=0.1, b_std=0.2,
+                             n_ignored=N // 20)
+    _check(cuda_lib, inp, reduction, chunk_rows=chunk_rows)
