@@ -13,7 +13,10 @@ step in float64 with numpy (the matmul is the only library primitive used):
   lse_n     = m_n + log sum_j exp(z[n, j] - m_n),  m_n = max_j z[n, j]
   loss_n    = valid_n ? lse_n - z[n, target_n] : 0
   loss      = none: loss_n | sum: sum_n loss_n | mean: sum_n loss_n / n_valid
-  w_n       = valid_n * (mean: g / n_valid | sum: g | none: g_n)
+  w_n       = c_n * (mean: g / sum_n c_n | sum: g | none: g_n),
+              c_n = valid_n * weight[target_n] (weight = 1 without class weights)
+  (with class weights loss_n is c_n (lse_n - z[n, target_n]) and mean
+   divides by sum_n c_n)
   G[n, j]   = w_n * (exp(z[n, j] - lse_n) - [j == target_n])
   dX = G W ,  dW = G^T X ,  db = sum_n G[n, :]
 
@@ -95,20 +98,34 @@ def corrected_target(target: np.ndarray, valid: np.ndarray) -> np.ndarray:
     return np.where(valid, np.asarray(target, dtype=np.int64), 0)
 
 
-def row_weights(target, num_classes, reduction, ignore_index=DEFAULT_IGNORE_INDEX, grad_out=None):
+def class_weight_of_rows(target, valid, class_weight):
+    """c_n = weight[target_n] on valid rows (1 without class weights), 0 on
+    ignored rows (linear_cross_entropy.py, neg_weight_target: the masked
+    index_select of the per-class weight)."""
+    v = valid.astype(np.float64)
+    if class_weight is None:
+        return v
+    cw = _f64(class_weight).reshape(-1)
+    return v * cw[corrected_target(target, valid)]
+
+
+def row_weights(target, num_classes, reduction, ignore_index=DEFAULT_IGNORE_INDEX, grad_out=None,
+                class_weight=None):
     """Per-row loss weight w_n, with the upstream gradient folded in.
 
-    linear_cross_entropy.py, ``_ChunkContext.neg_weight_target`` (no class
-    weights): ignored rows get 0; mean divides by d = n_valid and gives NaN
-    for every row when d == 0; sum uses 1; none uses grad_output[n] in the
-    backward. For mean and sum the scalar upstream gradient multiplies the
-    precomputed gradients (``_linear_cross_entropy_batch_chunked_backward``:
+    linear_cross_entropy.py, ``_ChunkContext.neg_weight_target``: ignored
+    rows get 0, valid rows the class weight weight[target_n] (1 without
+    class weights); mean divides by d = sum of those weights and gives NaN
+    for every row when d == 0; sum uses them as they are; none multiplies
+    them by grad_output[n] in the backward. For mean and sum the scalar
+    upstream gradient multiplies the precomputed gradients
+    (``_linear_cross_entropy_batch_chunked_backward``:
     ``grad.mul_(grad_output)``); it is folded into w_n here. grad_out=None
     means 1.0 for mean/sum and is required for none.
     """
     _check_reduction(reduction)
     valid = valid_mask(target, num_classes, ignore_index)
-    v = valid.astype(np.float64)
+    v = class_weight_of_rows(np.asarray(target, dtype=np.int64), valid, class_weight)
     if reduction == "none":
         if grad_out is None:
             raise OracleError("reduction='none' needs a per-row upstream gradient")
@@ -141,13 +158,15 @@ def log_sum_exp(z: np.ndarray) -> np.ndarray:
         return m + np.log(np.exp(z - m[:, None]).sum(axis=1))
 
 
-def _reduce(loss_rows: np.ndarray, valid: np.ndarray, reduction: str):
+def _reduce(loss_rows: np.ndarray, c: np.ndarray, reduction: str):
+    """c: per-row class weights (0 on ignored rows; the valid mask without
+    class weights); mean divides by their sum."""
     if reduction == "none":
         return loss_rows
     total = float(loss_rows.sum())
     if reduction == "sum":
         return total
-    d = float(valid.sum())
+    d = float(np.asarray(c, dtype=np.float64).sum())
     # mean over the valid rows; N == 0 or all rows ignored gives NaN
     # (linear_cross_entropy.py: the empty-batch mean and neg_weight_target's
     # d == 0 case).
@@ -155,7 +174,7 @@ def _reduce(loss_rows: np.ndarray, valid: np.ndarray, reduction: str):
 
 
 def ce_from_logits(logits, target, reduction="mean", ignore_index=DEFAULT_IGNORE_INDEX,
-                   grad_out=None, want_grad=True):
+                   grad_out=None, want_grad=True, class_weight=None):
     """Cross entropy on given logits [N, V], and the gradient that replaces them.
 
     Liger-Kernel issue #343: one pass gives the loss and writes
@@ -168,26 +187,27 @@ def ce_from_logits(logits, target, reduction="mean", ignore_index=DEFAULT_IGNORE
     target = np.asarray(target, dtype=np.int64).reshape(-1)
     valid = valid_mask(target, V, ignore_index)
     tc = corrected_target(target, valid)
+    c = class_weight_of_rows(target, valid, class_weight)
     loss_rows = np.zeros(N)
     grad = np.zeros_like(z) if want_grad else None
     w = None
     if want_grad:
-        w = row_weights(target, V, reduction, ignore_index, grad_out)
+        w = row_weights(target, V, reduction, ignore_index, grad_out, class_weight)
     for r0 in range(0, N, ROW_BLOCK):
         r1 = min(N, r0 + ROW_BLOCK)
         zb = z[r0:r1]
         lse = log_sum_exp(zb)
         rows = np.arange(r1 - r0)
         zt = zb[rows, tc[r0:r1]]
-        loss_rows[r0:r1] = np.where(valid[r0:r1], lse - zt, 0.0)
+        loss_rows[r0:r1] = np.where(valid[r0:r1], c[r0:r1] * (lse - zt), 0.0)
         if want_grad:
             P = np.exp(zb - lse[:, None])
             P[rows, tc[r0:r1]] -= valid[r0:r1].astype(np.float64)
             grad[r0:r1] = w[r0:r1, None] * P
-    return _reduce(loss_rows, valid, reduction), grad
+    return _reduce(loss_rows, c, reduction), grad
 
 
-def lce_forward(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE_INDEX):
+def lce_forward(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE_INDEX, class_weight=None):
     """Loss of the fused linear + cross-entropy, and lse per row.
 
     Returns (loss, lse[N]); loss is a float for sum/mean and loss_n [N] for
@@ -203,6 +223,7 @@ def lce_forward(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE_I
     target = np.asarray(target, dtype=np.int64).reshape(-1)
     valid = valid_mask(target, C, ignore_index)
     tc = corrected_target(target, valid)
+    c = class_weight_of_rows(target, valid, class_weight)
     lse = np.zeros(N)
     loss_rows = np.zeros(N)
     for r0 in range(0, N, ROW_BLOCK):
@@ -210,12 +231,12 @@ def lce_forward(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE_I
         z = logits_block(X[r0:r1], W, b)
         lse[r0:r1] = log_sum_exp(z)
         zt = z[np.arange(r1 - r0), tc[r0:r1]]
-        loss_rows[r0:r1] = np.where(valid[r0:r1], lse[r0:r1] - zt, 0.0)
-    return _reduce(loss_rows, valid, reduction), lse
+        loss_rows[r0:r1] = np.where(valid[r0:r1], c[r0:r1] * (lse[r0:r1] - zt), 0.0)
+    return _reduce(loss_rows, c, reduction), lse
 
 
 def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE_INDEX,
-                         grad_out=None):
+                         grad_out=None, class_weight=None):
     """Loss and all gradients (dX, dW, db) of the fused linear + cross-entropy.
 
     Returns (loss, dX[N, D], dW[C, D], db[C] or None). For mean/sum the
@@ -235,7 +256,8 @@ def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=DEFAULT
     target = np.asarray(target, dtype=np.int64).reshape(-1)
     valid = valid_mask(target, C, ignore_index)
     tc = corrected_target(target, valid)
-    w = row_weights(target, C, reduction, ignore_index, grad_out)
+    c = class_weight_of_rows(target, valid, class_weight)
+    w = row_weights(target, C, reduction, ignore_index, grad_out, class_weight)
     loss_rows = np.zeros(N)
     dX = np.zeros((N, D))
     dW = np.zeros((C, D))
@@ -246,7 +268,7 @@ def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=DEFAULT
         z = logits_block(X[r0:r1], W, b)
         lse = log_sum_exp(z)
         zt = z[rows, tc[r0:r1]]
-        loss_rows[r0:r1] = np.where(valid[r0:r1], lse - zt, 0.0)
+        loss_rows[r0:r1] = np.where(valid[r0:r1], c[r0:r1] * (lse - zt), 0.0)
         G = np.exp(z - lse[:, None])
         G[rows, tc[r0:r1]] -= valid[r0:r1].astype(np.float64)
         G *= w[r0:r1, None]
@@ -254,7 +276,7 @@ def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=DEFAULT
         dW += G.T @ X[r0:r1]
         if db is not None:
             db += G.sum(axis=0)
-    return _reduce(loss_rows, valid, reduction), dX, dW, db
+    return _reduce(loss_rows, c, reduction), dX, dW, db
 
 
 # --------------------------------------------------------------------------
@@ -296,7 +318,7 @@ def forward_stats(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE
     return {
         "lse": lse,
         "loss_rows": loss_rows,
-        "loss": _reduce(loss_rows, valid, reduction),
+        "loss": _reduce(loss_rows, valid.astype(np.float64), reduction),
         "w": w,
         "valid": valid,
         "db": db,

@@ -293,7 +293,7 @@ def _mut_transposed_weight_grad(X, W, b, t, reduction, ignore_index, grad_out):
     return loss, dX, dW[::-1].copy(), db
 
 
-def _mut_mean_over_all_rows(target, num_classes, reduction, ignore_index=-100, grad_out=None):
+def _mut_mean_over_all_rows(target, num_classes, reduction, ignore_index=-100, grad_out=None, class_weight=None):
     valid = O.valid_mask(target, num_classes, ignore_index).astype(np.float64)
     if reduction == "mean":
         return valid / len(valid)
@@ -313,3 +313,44 @@ def test_planted_mistakes_are_caught(monkeypatch, mutant):
     elif mutant == "mean_denominator":
         monkeypatch.setattr(O, "row_weights", _mut_mean_over_all_rows)
     assert not _matches_torch(fb, X, W, b, t, "mean", -100, None)
+
+
+@pytest.mark.parametrize("reduction,ignore_index,g", [("mean", -100, None), ("sum", 3, 0.5), ("none", -100, "vec")])
+def test_class_weights_against_torch(reduction, ignore_index, g):
+    # per-class weights (the page's ``weight``): w_n = weight[t_n]; mean divides by sum of weight[t_n]
+    X, W, b, t = _rand_case(N=17, D=6, C=9, ignore_index=ignore_index, seed=41)
+    cw = np.random.default_rng(42).uniform(0.2, 2.0, 9)
+    if g == "vec":
+        g = np.random.default_rng(43).standard_normal(17)
+    loss, dX, dW, db = O.lce_forward_backward(X, W, b, t, reduction, ignore_index, g, class_weight=cw)
+    Xt = torch.tensor(X, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    bt = torch.tensor(b, requires_grad=True)
+    l = F.cross_entropy(F.linear(Xt, Wt, bt), torch.tensor(t), weight=torch.tensor(cw), reduction=reduction,
+                        ignore_index=ignore_index)
+    if reduction == "none":
+        l.backward(torch.tensor(g))
+    else:
+        (l * (1.0 if g is None else g)).backward()
+    np.testing.assert_allclose(loss, l.detach().numpy(), rtol=1e-12)
+    np.testing.assert_allclose(dX, Xt.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dW, Wt.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(db, bt.grad.numpy(), rtol=1e-10, atol=1e-13)
+    lf, _ = O.lce_forward(X, W, b, t, reduction, ignore_index, class_weight=cw)
+    np.testing.assert_allclose(lf, loss, rtol=1e-13)
+    z = X @ W.T + b
+    lc, gc = O.ce_from_logits(z, t, reduction, ignore_index, g, class_weight=cw)
+    np.testing.assert_allclose(lc, loss, rtol=1e-12)
+    np.testing.assert_allclose(gc @ W, dX, rtol=1e-10, atol=1e-13)
+    # weight 1 everywhere is the unweighted loss
+    l1, dX1, _, _ = O.lce_forward_backward(X, W, b, t, reduction, ignore_index, g, class_weight=np.ones(9))
+    l0, dX0, _, _ = O.lce_forward_backward(X, W, b, t, reduction, ignore_index, g)
+    np.testing.assert_allclose(l1, l0, rtol=1e-13)
+    np.testing.assert_allclose(dX1, dX0, rtol=1e-13)
+
+
+def test_class_weights_zero_sum_is_nan():
+    X, W, b, t = _rand_case(N=5, D=3, C=4, n_ign=0, seed=44)
+    cw = np.zeros(4)
+    loss, dX, _, _ = O.lce_forward_backward(X, W, b, t, "mean", class_weight=cw)
+    assert math.isnan(loss) and np.isnan(dX).all()
