@@ -193,6 +193,32 @@ LCE_API int lce_cross_entropy_from_logits_noalloc(void* logits_inout, const int6
                                                   int64_t ignore_index, const float* grad_out,
                                                   float* loss_out, int* device_status, void* stream);
 
+/*
+ * Per-class weights (the page's `weight` argument of cross entropy).
+ * Same as lce_forward / lce_forward_backward / lce_cross_entropy_from_logits
+ * with one more input, class_weight: NULL (no class weights) or a device
+ * fp32 [C] (or [V]) array. A valid row n then has loss weight
+ * c_n = class_weight[target_n]: loss_n = c_n (lse_n - z[n, target_n]),
+ * mean divides by the sum of c_n over the valid rows (NaN when that sum is
+ * 0), and the gradients carry c_n in w_n (linear_cross_entropy.py,
+ * neg_weight_target: the per-row weight is the class weight of the target,
+ * divided by their sum for mean).
+ */
+LCE_API int lce_forward_ex(const void* X, const void* W, const void* b, const int64_t* target,
+                           const float* class_weight, int64_t N, int64_t D, int64_t C, int dtype,
+                           int acc_dtype, int reduction, int64_t ignore_index, float* loss_out,
+                           float* lse_out, void* workspace, size_t ws_bytes, void* stream);
+LCE_API int lce_forward_backward_ex(const void* X, const void* W, const void* b, const int64_t* target,
+                                    const float* class_weight, int64_t N, int64_t D, int64_t C,
+                                    int dtype, int acc_dtype, int reduction, int64_t ignore_index,
+                                    const float* grad_out, float* loss_out, void* dX, void* dW, void* db,
+                                    int grad_dtype, void* workspace, size_t ws_bytes, void* stream);
+LCE_API int lce_cross_entropy_from_logits_ex(void* logits_inout, const int64_t* target,
+                                             const float* class_weight, int64_t N, int64_t V, int dtype,
+                                             int reduction, int64_t ignore_index, const float* grad_out,
+                                             float* loss_out, void* workspace, size_t ws_bytes,
+                                             void* stream);
+
 /* Human-readable text of a status code (static storage). */
 LCE_API const char* lce_status_string(int status);
 

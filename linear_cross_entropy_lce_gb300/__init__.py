@@ -55,6 +55,13 @@ _SIGNATURES = {
                                      c_int, c_void_p, c_size_t, c_void_p]),
     "lce_cross_entropy_from_logits": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_int64,
                                               c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "lce_forward_ex": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int,
+                               c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "lce_forward_backward_ex": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64,
+                                        c_int, c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
+    "lce_cross_entropy_from_logits_ex": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int, c_int,
+                                                 c_int64, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "lce_cross_entropy_from_logits_noalloc": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int,
                                                       c_int64, c_void_p, c_void_p, c_void_p, c_void_p]),
     "lce_status_string": (ctypes.c_char_p, [c_int]),
@@ -140,6 +147,15 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
+def _class_weight(cw, C, device):
+    if cw is None:
+        return None
+    cw = torch.as_tensor(cw, dtype=torch.float32, device=device).reshape(-1).contiguous()
+    if cw.numel() != C:
+        raise ValueError(f"class_weight must have {C} entries")
+    return cw
+
+
 def _check_inputs(X, W, b, target):
     if X.dim() != 2 or W.dim() != 2 or X.shape[1] != W.shape[1]:
         raise ValueError("expected X [N, D] and W [C, D]")
@@ -155,8 +171,9 @@ def _check_inputs(X, W, b, target):
 
 
 def lce_forward(X, W, b, target, reduction="mean", ignore_index=-100, want_lse=False,
-                workspace=None, stream=None):
-    """Loss (fp32 scalar, or [N] for 'none') and optionally lse [N]."""
+                workspace=None, stream=None, class_weight=None):
+    """Loss (fp32 scalar, or [N] for 'none') and optionally lse [N].
+    class_weight: optional per-class weights [C] (fp32)."""
     lib = load_library()
     _check_inputs(X, W, b, target)
     N, D = X.shape
@@ -168,15 +185,17 @@ def lce_forward(X, W, b, target, reduction="mean", ignore_index=-100, want_lse=F
     lse = torch.empty(N, dtype=torch.float32, device=dev) if want_lse else None
     nbytes = lib.lce_workspace_size(LCE_OP_FORWARD, N, D, C, dt, red, LCE_F32, 0)
     ws = _workspace(nbytes, dev, workspace)
-    _check(lib.lce_forward(_ptr(X), _ptr(W), _ptr(b), _ptr(target), N, D, C, dt, LCE_F32, red, ignore_index,
-                           _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), "lce_forward")
+    cw = _class_weight(class_weight, C, dev)
+    _check(lib.lce_forward_ex(_ptr(X), _ptr(W), _ptr(b), _ptr(target), _ptr(cw), N, D, C, dt, LCE_F32, red,
+                              ignore_index, _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)),
+           "lce_forward")
     loss = loss if red == LCE_RED_NONE else loss[0]
     return (loss, lse) if want_lse else loss
 
 
 def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=-100, grad_out=None,
                          want_dx=True, want_dw=True, want_db=True, grad_dtype=None, chunk_rows=0,
-                         workspace=None, stream=None):
+                         workspace=None, stream=None, class_weight=None):
     """Loss and (dX, dW, db); a gradient not wanted (or db without bias) is None.
 
     grad_out: None (= 1) or a scalar / 1-element tensor for sum and mean; a
@@ -202,14 +221,15 @@ def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=-100, g
     db = torch.empty(C, dtype=gtype, device=dev) if (want_db and b is not None) else None
     nbytes = lib.lce_workspace_size(LCE_OP_FORWARD_BACKWARD, N, D, C, dt, red, gdt, chunk_rows)
     ws = _workspace(nbytes, dev, workspace)
-    _check(lib.lce_forward_backward(_ptr(X), _ptr(W), _ptr(b), _ptr(target), N, D, C, dt, LCE_F32, red,
-                                    ignore_index, _ptr(g), _ptr(loss), _ptr(dX), _ptr(dW), _ptr(db), gdt,
-                                    _ptr(ws), ws.numel(), _stream(stream)), "lce_forward_backward")
+    cw = _class_weight(class_weight, C, dev)
+    _check(lib.lce_forward_backward_ex(_ptr(X), _ptr(W), _ptr(b), _ptr(target), _ptr(cw), N, D, C, dt, LCE_F32,
+                                       red, ignore_index, _ptr(g), _ptr(loss), _ptr(dX), _ptr(dW), _ptr(db), gdt,
+                                       _ptr(ws), ws.numel(), _stream(stream)), "lce_forward_backward")
     return (loss if red == LCE_RED_NONE else loss[0]), dX, dW, db
 
 
 def lce_cross_entropy_from_logits(logits, target, reduction="mean", ignore_index=-100, grad_out=None,
-                                  workspace=None, stream=None):
+                                  workspace=None, stream=None, class_weight=None):
     """Loss; the gradient overwrites ``logits`` in place."""
     lib = load_library()
     if logits.dim() != 2 or not logits.is_contiguous():
@@ -226,8 +246,9 @@ def lce_cross_entropy_from_logits(logits, target, reduction="mean", ignore_index
     loss = torch.empty(N if red == LCE_RED_NONE else 1, dtype=torch.float32, device=dev)
     nbytes = lib.lce_workspace_size(LCE_OP_CE_FROM_LOGITS, N, 1, V, dt, red, dt, 0)
     ws = _workspace(nbytes, dev, workspace)
-    _check(lib.lce_cross_entropy_from_logits(_ptr(logits), _ptr(target), N, V, dt, red, ignore_index, _ptr(g),
-                                             _ptr(loss), _ptr(ws), ws.numel(), _stream(stream)),
+    cw = _class_weight(class_weight, V, dev)
+    _check(lib.lce_cross_entropy_from_logits_ex(_ptr(logits), _ptr(target), _ptr(cw), N, V, dt, red, ignore_index,
+                                                _ptr(g), _ptr(loss), _ptr(ws), ws.numel(), _stream(stream)),
            "lce_cross_entropy_from_logits")
     return loss if red == LCE_RED_NONE else loss[0]
 

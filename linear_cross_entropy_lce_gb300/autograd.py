@@ -30,14 +30,15 @@ from . import lce_forward, lce_forward_backward
 
 class _ScalarReduction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, X, W, b, target, reduction, ignore_index):
+    def forward(ctx, X, W, b, target, reduction, ignore_index, class_weight):
         want_dx, want_dw, want_db = ctx.needs_input_grad[0], ctx.needs_input_grad[1], ctx.needs_input_grad[2]
         if want_dx or want_dw or want_db:
             loss, dX, dW, db = lce_forward_backward(X, W, b, target, reduction, ignore_index, None,
                                                     want_dx=want_dx, want_dw=want_dw,
-                                                    want_db=want_db and b is not None)
+                                                    want_db=want_db and b is not None, class_weight=class_weight)
         else:
-            loss, dX, dW, db = lce_forward(X, W, b, target, reduction, ignore_index), None, None, None
+            loss = lce_forward(X, W, b, target, reduction, ignore_index, class_weight=class_weight)
+            dX = dW = db = None
         ctx.grads = (dX, dW, db)
         return loss
 
@@ -49,15 +50,16 @@ class _ScalarReduction(torch.autograd.Function):
             dX = None if dX is None else (dX.float() * g).to(dX.dtype)
             dW = None if dW is None else (dW.float() * g).to(dW.dtype)
             db = None if db is None else (db.float() * g).to(db.dtype)
-        return dX, dW, db, None, None, None
+        return dX, dW, db, None, None, None, None
 
 
 class _NoReduction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, X, W, b, target, ignore_index):
-        loss = lce_forward(X, W, b, target, "none", ignore_index)
+    def forward(ctx, X, W, b, target, ignore_index, class_weight):
+        loss = lce_forward(X, W, b, target, "none", ignore_index, class_weight=class_weight)
         ctx.save_for_backward(X, W, b, target)
         ctx.ignore_index = ignore_index
+        ctx.class_weight = class_weight
         return loss
 
     @staticmethod
@@ -67,17 +69,18 @@ class _NoReduction(torch.autograd.Function):
         _, dX, dW, db = lce_forward_backward(X, W, b, target, "none", ctx.ignore_index,
                                              grad_loss.to(torch.float32).contiguous(),
                                              want_dx=need[0], want_dw=need[1],
-                                             want_db=need[2] and b is not None)
-        return dX, dW, db, None, None
+                                             want_db=need[2] and b is not None, class_weight=ctx.class_weight)
+        return dX, dW, db, None, None, None
 
 
-def linear_cross_entropy(input, weight, target, bias=None, reduction="mean", ignore_index=-100):
+def linear_cross_entropy(input, weight, target, bias=None, reduction="mean", ignore_index=-100, class_weight=None):
     """Loss of cross_entropy(input @ weight.T + bias, target) without the
     [rows, classes] logits, differentiable in input, weight and bias.
 
     input [..., D] (fp32 or bf16), weight [C, D], bias [C] or None (same
-    dtype), target [...] int64. Returns a float32 scalar (mean, sum) or a
-    float32 tensor of target's shape (none).
+    dtype), target [...] int64, class_weight [C] or None (per-class weights
+    of cross entropy, not differentiated). Returns a float32 scalar (mean,
+    sum) or a float32 tensor of target's shape (none).
     """
     if reduction not in ("mean", "sum", "none"):
         raise ValueError(f"reduction must be mean, sum or none, got {reduction!r}")
@@ -89,5 +92,5 @@ def linear_cross_entropy(input, weight, target, bias=None, reduction="mean", ign
     W = weight.contiguous()
     b = None if bias is None else bias.contiguous()
     if reduction == "none":
-        return _NoReduction.apply(X, W, b, t, ignore_index).reshape(target.shape)
-    return _ScalarReduction.apply(X, W, b, t, reduction, ignore_index)
+        return _NoReduction.apply(X, W, b, t, ignore_index, class_weight).reshape(target.shape)
+    return _ScalarReduction.apply(X, W, b, t, reduction, ignore_index, class_weight)

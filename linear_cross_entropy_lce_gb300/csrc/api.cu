@@ -201,8 +201,9 @@ int check_common(int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype, int 
   } while (0)
 
 // The shared body of lce_forward and lce_forward_backward.
-int run_lce(bool backward, const void* X, const void* W, const void* b, const int64_t* target, int64_t N,
-            int64_t D, int64_t C, int dtype, int acc_dtype, int reduction, int64_t ignore_index,
+int run_lce(bool backward, const void* X, const void* W, const void* b, const int64_t* target,
+            const float* class_weight, int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype, int reduction,
+            int64_t ignore_index,
             const float* grad_out, float* loss_out, float* lse_out, void* dX, void* dW, void* db, int grad_dtype,
             void* workspace, size_t ws_bytes, void* stream) {
   int st = check_common(N, D, C, dtype, acc_dtype, reduction);
@@ -244,17 +245,19 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
 
   LCE_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
   if (N == 0) {
-    if (reduction != LCE_RED_NONE) LCE_TRY(launch_loss_finalize(loss_rows, 0, reduction, hdr, loss_out, s));
+    if (reduction != LCE_RED_NONE)
+      LCE_TRY(launch_loss_finalize(loss_rows, 0, reduction, hdr, class_weight != nullptr, loss_out, s));
     if (want_dw) LCE_TRY(cudaMemsetAsync(dW, 0, static_cast<size_t>(C) * D * gsz, s));
     if (want_db) LCE_TRY(cudaMemsetAsync(db, 0, static_cast<size_t>(C) * gsz, s));
     return LCE_OK;
   }
-  LCE_TRY(launch_prep(target, N, C, ignore_index, hdr, s));
+  LCE_TRY(launch_prep(target, N, C, ignore_index, class_weight, hdr, s));
   if (want_db) LCE_TRY(cudaMemsetAsync(db_acc, 0, static_cast<size_t>(C) * 4, s));
   float* rows_out = reduction == LCE_RED_NONE ? loss_out : loss_rows;
 
   RowWeight rw;
   rw.grad_out = grad_out;
+  rw.class_weight = class_weight;
   rw.reduction = reduction;
   rw.grad_is_vector = reduction == LCE_RED_NONE ? 1 : 0;
 
@@ -405,7 +408,8 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       }
     }
   }
-  if (reduction != LCE_RED_NONE) LCE_TRY(launch_loss_finalize(loss_rows, N, reduction, hdr, loss_out, s));
+  if (reduction != LCE_RED_NONE)
+    LCE_TRY(launch_loss_finalize(loss_rows, N, reduction, hdr, class_weight != nullptr, loss_out, s));
   if (want_db) LCE_TRY(launch_db_finalize(db_acc, db, C, grad_dtype == LCE_BF16, s));
   return LCE_OK;
 }
@@ -446,21 +450,44 @@ size_t lce_workspace_size(int op, int64_t N, int64_t D, int64_t C, int dtype, in
 int lce_forward(const void* X, const void* W, const void* b, const int64_t* target, int64_t N, int64_t D, int64_t C,
                 int dtype, int acc_dtype, int reduction, int64_t ignore_index, float* loss_out, float* lse_out,
                 void* workspace, size_t ws_bytes, void* stream) {
-  return run_lce(false, X, W, b, target, N, D, C, dtype, acc_dtype, reduction, ignore_index, nullptr, loss_out,
-                 lse_out, nullptr, nullptr, nullptr, LCE_F32, workspace, ws_bytes, stream);
+  return run_lce(false, X, W, b, target, nullptr, N, D, C, dtype, acc_dtype, reduction, ignore_index, nullptr,
+                 loss_out, lse_out, nullptr, nullptr, nullptr, LCE_F32, workspace, ws_bytes, stream);
+}
+
+int lce_forward_ex(const void* X, const void* W, const void* b, const int64_t* target, const float* class_weight,
+                   int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype, int reduction, int64_t ignore_index,
+                   float* loss_out, float* lse_out, void* workspace, size_t ws_bytes, void* stream) {
+  return run_lce(false, X, W, b, target, class_weight, N, D, C, dtype, acc_dtype, reduction, ignore_index, nullptr,
+                 loss_out, lse_out, nullptr, nullptr, nullptr, LCE_F32, workspace, ws_bytes, stream);
 }
 
 int lce_forward_backward(const void* X, const void* W, const void* b, const int64_t* target, int64_t N, int64_t D,
                          int64_t C, int dtype, int acc_dtype, int reduction, int64_t ignore_index,
                          const float* grad_out, float* loss_out, void* dX, void* dW, void* db, int grad_dtype,
                          void* workspace, size_t ws_bytes, void* stream) {
-  return run_lce(true, X, W, b, target, N, D, C, dtype, acc_dtype, reduction, ignore_index, grad_out, loss_out,
-                 nullptr, dX, dW, db, grad_dtype, workspace, ws_bytes, stream);
+  return run_lce(true, X, W, b, target, nullptr, N, D, C, dtype, acc_dtype, reduction, ignore_index, grad_out,
+                 loss_out, nullptr, dX, dW, db, grad_dtype, workspace, ws_bytes, stream);
+}
+
+int lce_forward_backward_ex(const void* X, const void* W, const void* b, const int64_t* target,
+                            const float* class_weight, int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype,
+                            int reduction, int64_t ignore_index, const float* grad_out, float* loss_out, void* dX,
+                            void* dW, void* db, int grad_dtype, void* workspace, size_t ws_bytes, void* stream) {
+  return run_lce(true, X, W, b, target, class_weight, N, D, C, dtype, acc_dtype, reduction, ignore_index, grad_out,
+                 loss_out, nullptr, dX, dW, db, grad_dtype, workspace, ws_bytes, stream);
 }
 
 int lce_cross_entropy_from_logits(void* logits_inout, const int64_t* target, int64_t N, int64_t V, int dtype,
                                   int reduction, int64_t ignore_index, const float* grad_out, float* loss_out,
                                   void* workspace, size_t ws_bytes, void* stream) {
+  return lce_cross_entropy_from_logits_ex(logits_inout, target, nullptr, N, V, dtype, reduction, ignore_index,
+                                          grad_out, loss_out, workspace, ws_bytes, stream);
+}
+
+int lce_cross_entropy_from_logits_ex(void* logits_inout, const int64_t* target, const float* class_weight,
+                                     int64_t N, int64_t V, int dtype, int reduction, int64_t ignore_index,
+                                     const float* grad_out, float* loss_out, void* workspace, size_t ws_bytes,
+                                     void* stream) {
   if (dtype != LCE_F32 && dtype != LCE_BF16) return LCE_ERR_DTYPE;
   if (reduction != LCE_RED_NONE && reduction != LCE_RED_SUM && reduction != LCE_RED_MEAN) return LCE_ERR_REDUCTION;
   if (N < 0 || V < 1 || N > (int64_t(1) << 40) || V > (int64_t(1) << 40)) return LCE_ERR_SHAPE;
@@ -479,7 +506,7 @@ int lce_cross_entropy_from_logits(void* logits_inout, const int64_t* target, int
   float* loss_rows = reinterpret_cast<float*>(ws + align_up(sizeof(WsHeader)));
   LCE_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
   if (N > 0) {
-    LCE_TRY(launch_prep(target, N, V, ignore_index, hdr, s));
+    LCE_TRY(launch_prep(target, N, V, ignore_index, class_weight, hdr, s));
     CeArgs a;
     a.logits = logits_inout;
     a.N = N;
@@ -487,6 +514,7 @@ int lce_cross_entropy_from_logits(void* logits_inout, const int64_t* target, int
     a.target = target;
     a.ignore_index = ignore_index;
     a.rw.grad_out = grad_out;
+    a.rw.class_weight = class_weight;
     a.rw.reduction = reduction;
     a.rw.grad_is_vector = reduction == LCE_RED_NONE ? 1 : 0;
     a.hdr = hdr;
@@ -494,7 +522,8 @@ int lce_cross_entropy_from_logits(void* logits_inout, const int64_t* target, int
     a.status = &hdr->status;
     LCE_TRY(launch_ce_logits(a, dtype == LCE_BF16, s));
   }
-  if (reduction != LCE_RED_NONE) LCE_TRY(launch_loss_finalize(loss_rows, N, reduction, hdr, loss_out, s));
+  if (reduction != LCE_RED_NONE)
+    LCE_TRY(launch_loss_finalize(loss_rows, N, reduction, hdr, class_weight != nullptr, loss_out, s));
   return LCE_OK;
 }
 

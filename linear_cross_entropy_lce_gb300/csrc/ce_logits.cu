@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(CE_THREADS, 2) ce_resident_kernel(const CeArgs
       const float S = warp_sum((lane < cs && pm != -INFINITY) ? ps * expf(pm - M) : 0.0f);
       if (lane == 0) {
         bc[0] = M + logf(S);
-        bc[1] = row_weight(a.rw, &a.hdr->n_valid, row, valid);
+        bc[1] = row_weight(a.rw, a.hdr, row, t, valid);
       }
     }
     __syncthreads();
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(CE_THREADS, 2) ce_resident_kernel(const CeArgs
           if (col + i < V) rowp[col + i] = from_f32<T>(gv[i]);
       }
     }
-    if (rank == 0 && tid == 0) a.loss_rows[row] = valid ? lse - zt : 0.0f;
+    if (rank == 0 && tid == 0) a.loss_rows[row] = valid ? class_w(a.rw, t, true) * (lse - zt) : 0.0f;
   }
   cluster_sync();  // no CTA leaves while a peer may still read its xch
 }
@@ -237,13 +237,13 @@ __global__ void __launch_bounds__(CE_THREADS) ce_stream_kernel(const CeArgs a) {
     const float M = block_max(m, scratch);
     const float S = block_sum(m == -INFINITY ? 0.0f : s * fast_exp2((m - M) * kLog2e), scratch);
     const float lse = M + logf(S);
-    const float w = row_weight(a.rw, &a.hdr->n_valid, row, valid);
+    const float w = row_weight(a.rw, a.hdr, row, t, valid);
     const float zt = s_zt;
     for (int64_t j = tid; j < V; j += CE_THREADS) {
       const float p = fast_exp2((to_f32(rowp[j]) - lse) * kLog2e);
       rowp[j] = from_f32<T>(w * ((valid && j == t) ? p - 1.0f : p));
     }
-    if (tid == 0) a.loss_rows[row] = valid ? lse - zt : 0.0f;
+    if (tid == 0) a.loss_rows[row] = valid ? class_w(a.rw, t, true) * (lse - zt) : 0.0f;
     __syncthreads();  // s_zt is rewritten for the next row
   }
 }

@@ -22,15 +22,18 @@ constexpr int kStatusTimeout = 2;
 struct WsHeader {
   int status;       // kStatus* bits, OR-ed by kernels
   int n_valid;      // rows whose target is a class index (not ignored, in range)
-  double loss_sum;  // unused padding for alignment / future use
+  double weight_sum;  // sum of class weights over valid rows (class-weighted calls)
   int pad[60];
 };
 static_assert(sizeof(WsHeader) <= 256, "header must fit 256 bytes");
 
-// Per-row weight parameters: w_n = valid ? base * (vec ? g[n] : g0) : 0,
-// with base = 1 (sum, none) or 1 / n_valid (mean; NaN when n_valid == 0).
+// Per-row weight parameters: w_n = valid ? c_n * base * (vec ? g[n] : g0) : 0,
+// with c_n = class_weight[target_n] (1 without class weights) and base = 1
+// (sum, none) or 1 / d (mean; d = n_valid, or the sum of c_n over valid rows
+// with class weights; NaN for every row when d == 0).
 struct RowWeight {
-  const float* grad_out;  // device scalar (sum/mean) or [N] (none); may be NULL
+  const float* grad_out;      // device scalar (sum/mean) or [N] (none); may be NULL
+  const float* class_weight;  // [C] or NULL
   int reduction;
   int grad_is_vector;
 };
@@ -49,20 +52,31 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
 }
 
-__device__ __forceinline__ float row_weight(const RowWeight& rw, const int* n_valid_ptr, int64_t n, bool valid) {
+// Class weight of a row: class_weight[t] on valid rows (1 without class
+// weights), 0 on ignored rows.
+__device__ __forceinline__ float class_w(const RowWeight& rw, int64_t t, bool valid) {
+  if (!valid) return 0.0f;
+  return rw.class_weight != nullptr ? rw.class_weight[t] : 1.0f;
+}
+
+__device__ __forceinline__ float row_weight(const RowWeight& rw, const WsHeader* hdr, int64_t n, int64_t t,
+                                            bool valid) {
+  const bool mean = rw.reduction == LCE_RED_MEAN;
+  const bool empty = rw.class_weight != nullptr ? hdr->weight_sum == 0.0 : hdr->n_valid == 0;
   if (!valid) {
-    // an ignored row still sees NaN under mean with no valid row
-    if (rw.reduction == LCE_RED_MEAN && *n_valid_ptr == 0) return __int_as_float(0x7fc00000);
-    return 0.0f;
+    // an ignored row still sees NaN under mean when the divisor is 0
+    return (mean && empty) ? __int_as_float(0x7fc00000) : 0.0f;
   }
   float g = 1.0f;
   if (rw.grad_out != nullptr) g = rw.grad_is_vector ? rw.grad_out[n] : rw.grad_out[0];
-  if (rw.reduction == LCE_RED_MEAN) {
-    const int nv = *n_valid_ptr;
-    const float base = nv == 0 ? __int_as_float(0x7fc00000) : 1.0f / static_cast<float>(nv);
-    return base * g;
+  const float c = rw.class_weight != nullptr ? rw.class_weight[t] : 1.0f;
+  if (mean) {
+    if (empty) return __int_as_float(0x7fc00000);
+    const float d = rw.class_weight != nullptr ? static_cast<float>(hdr->weight_sum)
+                                               : static_cast<float>(hdr->n_valid);
+    return c * (1.0f / d) * g;
   }
-  return g;
+  return c * g;
 }
 
 // A row's target is valid iff it is not ignore_index; a target outside

@@ -70,8 +70,8 @@ cudaError_t launch_simt_store(int op, const float* A, const float* B, int64_t ld
                               int64_t N, int64_t K, const EpiStore::Params& ep, cudaStream_t s);
 
 // ---- row kernels (rowops.cu)
-cudaError_t launch_prep(const int64_t* target, int64_t N, int64_t C, int64_t ignore_index, WsHeader* hdr,
-                        cudaStream_t s);
+cudaError_t launch_prep(const int64_t* target, int64_t N, int64_t C, int64_t ignore_index, const float* cw,
+                        WsHeader* hdr, cudaStream_t s);
 struct CombineArgs {
   float2* partial;  // [nseg][ld]; overwritten: .x = w_n exp(m - lse) when backward
   int64_t ld;
@@ -112,7 +112,7 @@ struct SideGrad {
   int enabled;
 };
 cudaError_t launch_loss_finalize(const float* loss_rows, int64_t N, int reduction, const WsHeader* hdr,
-                                 float* loss_out, cudaStream_t s);
+                                 bool weighted, float* loss_out, cudaStream_t s);
 cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, bool bf16, cudaStream_t s);
 
 // ---- cross entropy on given logits (ce_logits.cu)

@@ -13,43 +13,53 @@ namespace {
 // ignore_index nor in [0, C) sets the target-range status bit
 // (linear_cross_entropy.py: the _mask / corrected_target / neg_weight_target
 // d = sum of unmasked weights).
-__global__ void prep_kernel(const int64_t* __restrict__ target, int64_t N, int64_t C, int64_t ign, WsHeader* hdr) {
+__global__ void prep_kernel(const int64_t* __restrict__ target, int64_t N, int64_t C, int64_t ign,
+                            const float* __restrict__ cw, WsHeader* hdr) {
   __shared__ int s_cnt[32];
   __shared__ int s_bad[32];
+  __shared__ double s_ws[32];
   int cnt = 0, bad = 0;
+  double ws = 0.0;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < N;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t t = target[i];
     if (t != ign) {
-      if (t >= 0 && t < C)
+      if (t >= 0 && t < C) {
         ++cnt;
-      else
+        if (cw != nullptr) ws += cw[t];
+      } else {
         bad = 1;
+      }
     }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
     bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    ws += __shfl_xor_sync(0xffffffffu, ws, o);
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) {
     s_cnt[warp] = cnt;
     s_bad[warp] = bad;
+    s_ws[warp] = ws;
   }
   __syncthreads();
   if (warp == 0) {
     const int nw = blockDim.x >> 5;
     cnt = lane < nw ? s_cnt[lane] : 0;
     bad = lane < nw ? s_bad[lane] : 0;
+    ws = lane < nw ? s_ws[lane] : 0.0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
       bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+      ws += __shfl_xor_sync(0xffffffffu, ws, o);
     }
     if (lane == 0) {
       if (cnt) atomicAdd(&hdr->n_valid, cnt);
       if (bad) atomicOr(&hdr->status, kStatusTargetRange);
+      if (cw != nullptr && ws != 0.0) atomicAdd(&hdr->weight_sum, ws);
     }
   }
 }
@@ -89,11 +99,11 @@ __global__ void combine_kernel(const CombineArgs a) {
   const bool valid = target_valid(t, a.ignore_index, a.C);
   const float zt = valid ? a.zt[r] : 0.0f;
   if (lane == 0) {
-    a.loss_rows[g] = valid ? lse - zt : 0.0f;
+    a.loss_rows[g] = valid ? class_w(a.rw, t, true) * (lse - zt) : 0.0f;
     if (a.lse_out != nullptr) a.lse_out[g] = lse;
   }
   if (a.backward) {
-    const float w = row_weight(a.rw, &a.hdr->n_valid, g, valid);
+    const float w = row_weight(a.rw, a.hdr, g, t, valid);
     for (int s = lane; s < a.nseg; s += 32) {
       float2* p = &a.partial[s * a.ld + r];
       p->x = w * expf(p->x - lse);
@@ -116,7 +126,7 @@ __global__ void __launch_bounds__(256) grad_logits_kernel(const GradArgs a) {
 // Deterministic single-block sum of the per-row losses in fp64; mean
 // divides by n_valid (NaN when it is 0).
 __global__ void loss_finalize_kernel(const float* __restrict__ loss_rows, int64_t N, int reduction,
-                                     const WsHeader* hdr, float* loss_out) {
+                                     const WsHeader* hdr, int weighted, float* loss_out) {
   __shared__ double s[32];
   double acc = 0.0;
   for (int64_t i = threadIdx.x; i < N; i += blockDim.x) acc += loss_rows[i];
@@ -134,8 +144,9 @@ __global__ void loss_finalize_kernel(const float* __restrict__ loss_rows, int64_
       if (reduction == LCE_RED_SUM) {
         loss_out[0] = static_cast<float>(acc);
       } else {
-        const int nv = hdr->n_valid;
-        loss_out[0] = nv == 0 ? __int_as_float(0x7fc00000) : static_cast<float>(acc / nv);
+        // mean over the valid rows, or over their class weights
+        const double d = weighted ? hdr->weight_sum : static_cast<double>(hdr->n_valid);
+        loss_out[0] = d == 0.0 ? __int_as_float(0x7fc00000) : static_cast<float>(acc / d);
       }
     }
   }
@@ -150,13 +161,13 @@ __global__ void db_finalize_kernel(const float* __restrict__ db_acc, T* db, int6
 
 }  // namespace
 
-cudaError_t launch_prep(const int64_t* target, int64_t N, int64_t C, int64_t ignore_index, WsHeader* hdr,
-                        cudaStream_t s) {
+cudaError_t launch_prep(const int64_t* target, int64_t N, int64_t C, int64_t ignore_index, const float* cw,
+                        WsHeader* hdr, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   int64_t blocks = (N + 1023) / 1024;
   if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
   prof_before(K_PREP, s, 8.0 * N);
-  prep_kernel<<<static_cast<unsigned>(blocks), 1024, 0, s>>>(target, N, C, ignore_index, hdr);
+  prep_kernel<<<static_cast<unsigned>(blocks), 1024, 0, s>>>(target, N, C, ignore_index, cw, hdr);
   cudaError_t e = cudaGetLastError();
   prof_after(K_PREP, s);
   return e;
@@ -189,9 +200,9 @@ cudaError_t launch_grad_logits(const GradArgs& a, bool bf16, cudaStream_t s) {
 }
 
 cudaError_t launch_loss_finalize(const float* loss_rows, int64_t N, int reduction, const WsHeader* hdr,
-                                 float* loss_out, cudaStream_t s) {
+                                 bool weighted, float* loss_out, cudaStream_t s) {
   prof_before(K_LOSS_FINALIZE, s, 4.0 * N);
-  loss_finalize_kernel<<<1, 1024, 0, s>>>(loss_rows, N, reduction, hdr, loss_out);
+  loss_finalize_kernel<<<1, 1024, 0, s>>>(loss_rows, N, reduction, hdr, weighted ? 1 : 0, loss_out);
   cudaError_t e = cudaGetLastError();
   prof_after(K_LOSS_FINALIZE, s);
   return e;
