@@ -164,6 +164,15 @@ def _make_resized(w):
                               w.scale_by_sqrt_d, w.target_dist, w.zipf_s, w.n_ignored, w.grad_out_std)
 
 
+def aggregate_ms(ms, dist=None, device=None):
+    """Per-step time of the whole job: the maximum over ranks."""
+    if dist is None:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -286,11 +295,7 @@ def run_gpu(args):
     lce.profile_enable(False)
     launches = lce.launch_count() - launches0
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = aggregate_ms(e0.elapsed_time(e1) / args.steps, dist, dev)
     prof = lce.profile_summary()
     lce.profile_reset()
 
@@ -327,11 +332,7 @@ def run_gpu(args):
             e2e_step()
         f1.record(stream)
         barrier()
-        ems = f0.elapsed_time(f1) / args.steps
-        if dist is not None:
-            tt = torch.tensor([ems], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
+        ems = aggregate_ms(f0.elapsed_time(f1) / args.steps, dist, dev)
         e2e = {"value": ws * N / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": ems}
     else:
@@ -355,7 +356,7 @@ def run_gpu(args):
             e2e_step()
         f1.record(stream)
         barrier()
-        ems = f0.elapsed_time(f1) / args.steps
+        ems = aggregate_ms(f0.elapsed_time(f1) / args.steps, dist, dev)
         e2e = {"value": ws * N / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": 4, "ms_per_step": ems}
 
@@ -400,7 +401,7 @@ def run_gpu(args):
     # ---- CPU baseline: the oracle on a bounded sample, rank 0, N=1 only
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
-        rows = args.ref_rows
+        rows = args.cpu_rows
         sec = _oracle_sample_seconds(args.workload, rows, inp)
         cpu = {"value": rows / sec, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
                "sample": f"{rows} of {w.N} rows, full method (loss and all gradients for those rows) in "
@@ -448,7 +449,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="bf16_llm_head", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--ref-rows", type=int, default=32, help="rows per step of the --impl reference arm")
+    ap.add_argument("--cpu-rows", type=int, default=256, help="rows of the oracle sample in cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=0, help="override N (profiling a smaller case)")
     ap.add_argument("--dim", type=int, default=0, help="override D")
