@@ -161,8 +161,9 @@ struct EpiLse {
 // Store epilogue for the dX = G W and dW = G^T X contractions (and the GEMM
 // tests). mode 0: out = acc; 1: acc32 = acc (first chunk of a dW
 // accumulated over chunks); 2: acc32 += acc; 3: out = acc32 + acc (last
-// chunk). out is bf16 or fp32; acc32 is fp32 with the same leading
-// dimension as out.
+// chunk); 4: out += acc with fp32 atomics (one split of a split-K GEMM
+// into a zeroed fp32 out). out is bf16 or fp32; acc32 is fp32 with the
+// same leading dimension as out.
 // ---------------------------------------------------------------------------
 struct EpiStore {
   struct Params {
@@ -176,6 +177,10 @@ struct EpiStore {
   };
 
   __device__ static __forceinline__ void put(const Params& p, int64_t idx, float x) {
+    if (p.mode == 4) {  // split-K partial: add into the zeroed fp32 output
+      atomicAdd(static_cast<float*>(p.out) + idx, x);
+      return;
+    }
     if (p.mode == 1) {
       p.acc32[idx] = x;
       return;
@@ -206,7 +211,7 @@ struct EpiStore {
       if (!row_ok) continue;
       const int64_t cb = col0 + 32 * c;
       const int64_t base = row * p.ldo + cb;
-      if (p.vec_ok && cb + 32 <= p.cols) {
+      if (p.vec_ok && cb + 32 <= p.cols && p.mode != 4) {
         if (p.mode == 0 && p.out_bf16) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + base);
 #pragma unroll
