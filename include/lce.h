@@ -40,12 +40,17 @@
  *    recorded in the workspace and read back with lce_read_device_status;
  *    rows with such a target get loss 0 and gradient 0 and do not count
  *    toward n_valid.
- *  - Types: dtype LCE_F32 or LCE_BF16 for X, W, b (or for logits);
- *    acc_dtype must be LCE_F32 (accumulation is always fp32);
- *    grad_dtype (dX, dW, db) LCE_F32 or LCE_BF16. Loss and lse are fp32.
- *  - LCE_BF16 inputs run on the tcgen05 tensor cores and need D % 8 == 0
- *    and 16-byte aligned X, W, dX, dW (else LCE_ERR_ALIGN). LCE_F32
- *    inputs run exact fp32 FMA on the CUDA cores and accept any shape.
+ *  - Types: dtype LCE_F32, LCE_BF16 or LCE_F16 for X, W, b (or for
+ *    logits); acc_dtype must be LCE_F32 (accumulation is always fp32);
+ *    grad_dtype (dX, dW, db) LCE_F32, LCE_BF16 or LCE_F16. Loss and lse
+ *    are fp32.
+ *  - LCE_BF16 and LCE_F16 inputs run on the tcgen05 tensor cores and need
+ *    D % 8 == 0 and 16-byte aligned X, W, dX, dW (else LCE_ERR_ALIGN).
+ *    LCE_F32 inputs run exact fp32 FMA on the CUDA cores and accept any
+ *    shape. With LCE_F16 the backward keeps the per-row weights w_n out of
+ *    the 16-bit gradient tile (1/n_valid is below fp16's normal range for
+ *    large batches; linear_cross_entropy.py keeps the per-row weight in
+ *    fp32 for the same reason) and applies them in fp32 afterwards.
  *  - Device: compute capability 10.3 (GB300, sm_103a); else LCE_ERR_DEVICE.
  */
 #ifndef LCE_H_
@@ -68,7 +73,7 @@ extern "C" {
 
 /* Element types (linear_cross_entropy.py supports fp32 accumulation for
  * fp16/bf16 inputs, and accumulation in the input type otherwise). */
-enum lce_dtype_e { LCE_F32 = 0, LCE_BF16 = 1 };
+enum lce_dtype_e { LCE_F32 = 0, LCE_BF16 = 1, LCE_F16 = 2 };
 
 /* Reductions accepted by linear_cross_entropy.py: "none", "sum", "mean". */
 enum lce_reduction_e { LCE_RED_NONE = 0, LCE_RED_SUM = 1, LCE_RED_MEAN = 2 };

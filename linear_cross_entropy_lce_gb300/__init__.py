@@ -28,7 +28,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblce.so")
 
-LCE_F32, LCE_BF16 = 0, 1
+LCE_F32, LCE_BF16, LCE_F16 = 0, 1, 2
 LCE_RED_NONE, LCE_RED_SUM, LCE_RED_MEAN = 0, 1, 2
 LCE_OP_FORWARD, LCE_OP_FORWARD_BACKWARD, LCE_OP_CE_FROM_LOGITS = 0, 1, 2
 LCE_NOALLOC_MAX_ROWS = 1 << 20
@@ -38,8 +38,8 @@ STATUS = {
     9: "LCE_ERR_ALIGN", 10: "LCE_ERR_TIMEOUT", 11: "LCE_ERR_DEVICE",
 }
 _REDUCTION = {"none": LCE_RED_NONE, "sum": LCE_RED_SUM, "mean": LCE_RED_MEAN}
-_DTYPE = {torch.float32: LCE_F32, torch.bfloat16: LCE_BF16}
-_TORCH_DTYPE = {LCE_F32: torch.float32, LCE_BF16: torch.bfloat16}
+_DTYPE = {torch.float32: LCE_F32, torch.bfloat16: LCE_BF16, torch.float16: LCE_F16}
+_TORCH_DTYPE = {LCE_F32: torch.float32, LCE_BF16: torch.bfloat16, LCE_F16: torch.float16}
 
 _lib = None
 
@@ -131,7 +131,7 @@ def _stream(stream=None):
 
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype not in _DTYPE:
-        raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+        raise TypeError(f"unsupported dtype {t.dtype}: use float32, bfloat16 or float16")
     return _DTYPE[t.dtype]
 
 

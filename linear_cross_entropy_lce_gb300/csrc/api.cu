@@ -77,7 +77,7 @@ std::atomic<int64_t> g_launches{0};
 const char* kNames[K_NUM_IDS] = {
     "prep",          "gemm_logits_tc", "gemm_dx_tc",  "gemm_dw_tc",      "gemm_logits_simt",
     "gemm_dx_simt",  "gemm_dw_simt",   "lse_combine", "grad_logits",     "loss_finalize",
-    "db_finalize",   "ce_resident",    "ce_stream",   "gemm_test"};
+    "db_finalize",   "ce_resident",    "ce_stream",   "gemm_test",       "row_scale"};
 }  // namespace
 
 const char* kernel_id_name(int id) { return (id >= 0 && id < K_NUM_IDS) ? kNames[id] : "?"; }
@@ -104,10 +104,10 @@ constexpr int64_t kDefaultChunkBytes = int64_t(8) << 30;  // chunk buffer budget
 
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-inline int esize(int dt) { return dt == LCE_BF16 ? 2 : 4; }
+inline int esize(int dt) { return dt == LCE_F32 ? 4 : 2; }
 
 struct Plan {
-  bool tc;          // tensor-core (bf16) path
+  bool tc;          // tensor-core (bf16 / fp16) path
   int segw;         // columns per (max, sum-exp) segment
   int nseg;
   int64_t C_pad;    // chunk buffer row pitch (elements)
@@ -115,6 +115,9 @@ struct Plan {
   int64_t nchunks;
   bool dw_acc;      // fp32 dW accumulator in the workspace
   size_t off_loss, off_zt, off_tcol, off_gt, off_partial, off_L, off_dw, off_db, total;
+  // fp16 backward: per-row weights [Bc], their max |w| (one float), and the
+  // rows of X scaled by w / max|w| for dW ([Bc, D] fp16)
+  size_t off_wrow, off_wbar, off_xs;
 };
 
 // Bytes for chunk size Bc. backward: chunk buffer and gradient scratch;
@@ -122,14 +125,14 @@ struct Plan {
 bool make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, bool want_dw, bool want_db,
                int64_t Bc, Plan* p) {
   const bool backward = op == LCE_OP_FORWARD_BACKWARD;
-  p->tc = dtype == LCE_BF16;
+  p->tc = dtype != LCE_F32;
   p->segw = p->tc ? 256 : 64;
   p->nseg = static_cast<int>(ceil_div(C, p->segw));
   p->C_pad = p->tc ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
   if (N == 0) Bc = 0;
   p->Bc = Bc;
   p->nchunks = Bc > 0 ? ceil_div(N, Bc) : 0;
-  p->dw_acc = backward && want_dw && p->nchunks > 1 && grad_dtype == LCE_BF16;
+  p->dw_acc = backward && want_dw && p->nchunks > 1 && grad_dtype != LCE_F32;
   size_t off = align_up(sizeof(WsHeader));
   p->off_loss = off;
   off = align_up(off + static_cast<size_t>(N) * 4);
@@ -147,13 +150,20 @@ bool make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtyp
   if (p->dw_acc) off = align_up(off + static_cast<size_t>(C) * static_cast<size_t>(D) * 4);
   p->off_db = off;
   if (backward && want_db) off = align_up(off + static_cast<size_t>(C) * 4);
+  const bool f16bw = backward && dtype == LCE_F16;
+  p->off_wrow = off;
+  if (f16bw) off = align_up(off + static_cast<size_t>(Bc) * 4);
+  p->off_wbar = off;
+  if (f16bw) off = align_up(off + 4);
+  p->off_xs = off;
+  if (f16bw && want_dw) off = align_up(off + static_cast<size_t>(Bc) * static_cast<size_t>(D) * 2);
   p->total = off;
   return true;
 }
 
 int64_t default_chunk(int op, int64_t N, int64_t C, int dtype) {
   if (N == 0) return 0;
-  const int64_t C_pad = dtype == LCE_BF16 ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
+  const int64_t C_pad = dtype != LCE_F32 ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
   const int64_t per_row = (op == LCE_OP_FORWARD_BACKWARD ? C_pad * esize(dtype) : 0) + ceil_div(C, 64) * 8;
   if (N * per_row <= kDefaultChunkBytes) return N;
   int64_t bc = 128;
@@ -186,7 +196,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? LCE_OK : LCE_ERR_CUDA; }
 
 int check_common(int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype, int reduction) {
-  if (dtype != LCE_F32 && dtype != LCE_BF16) return LCE_ERR_DTYPE;
+  if (dtype != LCE_F32 && dtype != LCE_BF16 && dtype != LCE_F16) return LCE_ERR_DTYPE;
   if (acc_dtype != LCE_F32) return LCE_ERR_DTYPE;
   if (reduction != LCE_RED_NONE && reduction != LCE_RED_SUM && reduction != LCE_RED_MEAN) return LCE_ERR_REDUCTION;
   if (N < 0 || D < 1 || C < 1) return LCE_ERR_SHAPE;
@@ -208,7 +218,7 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
             void* workspace, size_t ws_bytes, void* stream) {
   int st = check_common(N, D, C, dtype, acc_dtype, reduction);
   if (st != LCE_OK) return st;
-  if (backward && grad_dtype != LCE_F32 && grad_dtype != LCE_BF16) return LCE_ERR_DTYPE;
+  if (backward && grad_dtype != LCE_F32 && grad_dtype != LCE_BF16 && grad_dtype != LCE_F16) return LCE_ERR_DTYPE;
   if (N > 0 && (X == nullptr || W == nullptr || target == nullptr || loss_out == nullptr)) return LCE_ERR_NULL;
   if (reduction != LCE_RED_NONE && loss_out == nullptr) return LCE_ERR_NULL;
   if (backward && reduction == LCE_RED_NONE && N > 0 && grad_out == nullptr) return LCE_ERR_GRAD_OUT;
@@ -217,7 +227,7 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
   const bool want_dx = backward && dX != nullptr;
   const bool want_dw = backward && dW != nullptr;
   const bool want_db = backward && db != nullptr && b != nullptr;
-  if (dtype == LCE_BF16) {
+  if (dtype != LCE_F32) {
     if (D % 8 != 0) return LCE_ERR_ALIGN;
     if (N > 0 && (!aligned16(X) || !aligned16(W))) return LCE_ERR_ALIGN;
     if ((want_dx && !aligned16(dX)) || (want_dw && !aligned16(dW))) return LCE_ERR_ALIGN;
@@ -241,7 +251,11 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
   void* Lbuf = ws + p.off_L;
   float* dw_acc = reinterpret_cast<float*>(ws + p.off_dw);
   float* db_acc = reinterpret_cast<float*>(ws + p.off_db);
-  const int gsz = grad_dtype == LCE_BF16 ? 2 : 4;
+  const bool f16 = dtype == LCE_F16;
+  float* wrow = f16 && backward ? reinterpret_cast<float*>(ws + p.off_wrow) : nullptr;
+  float* wbar = reinterpret_cast<float*>(ws + p.off_wbar);
+  void* Xs = ws + p.off_xs;
+  const int gsz = esize(grad_dtype);
 
   LCE_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
   if (N == 0) {
@@ -262,10 +276,10 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
   rw.grad_is_vector = reduction == LCE_RED_NONE ? 1 : 0;
 
   CUtensorMap tmW_k, tmW_n;
-  const bool pair = tc_pair_default();
+  const bool pair = tc_pair_default() || f16;  // fp16 runs on the CTA-pair kernel only
   if (p.tc) {
-    if (!encode_tmap_bf16(&tmW_k, W, D, C, D, pair ? 128 : TC_BN)) return LCE_ERR_CUDA;
-    if (want_dx && !encode_tmap_bf16(&tmW_n, W, D, C, D, 64)) return LCE_ERR_CUDA;
+    if (!encode_tmap_bf16(&tmW_k, W, D, C, D, pair ? 128 : TC_BN, dtype)) return LCE_ERR_CUDA;
+    if (want_dx && !encode_tmap_bf16(&tmW_n, W, D, C, D, 64, dtype)) return LCE_ERR_CUDA;
   }
 
   for (int64_t ci = 0; ci < p.nchunks; ++ci) {
@@ -285,7 +299,7 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       const int64_t sr = std::min(slab, rows - so);      // rows in the slab
       EpiLse::Params el;
       el.bias = b;
-      el.bias_bf16 = dtype == LCE_BF16;
+      el.bias_dt = dtype;
       el.target = target + row0 + so;
       el.C = C;
       el.rows = static_cast<int>(sr);
@@ -295,18 +309,18 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       el.ptilde = backward ? static_cast<uint8_t*>(Lbuf) + static_cast<size_t>(so) * p.C_pad * esize(dtype)
                            : nullptr;
       el.ld_p = p.C_pad;
-      el.ptilde_bf16 = dtype == LCE_BF16;
+      el.ptilde_dt = dtype;
       if (p.tc) {
-        const void* Xc = static_cast<const __nv_bfloat16*>(X) + (row0 + so) * D;
+        const void* Xc = static_cast<const uint16_t*>(X) + (row0 + so) * D;
         CUtensorMap tmX_k, tmL;
-        if (!encode_tmap_bf16(&tmX_k, Xc, D, sr, D, TC_BM)) return LCE_ERR_CUDA;
+        if (!encode_tmap_bf16(&tmX_k, Xc, D, sr, D, TC_BM, dtype)) return LCE_ERR_CUDA;
         const bool tma_out = pair && backward;
-        if (tma_out && !encode_tmap_bf16_store(&tmL, el.ptilde, p.C_pad, sr, p.C_pad)) return LCE_ERR_CUDA;
+        if (tma_out && !encode_tmap_bf16_store(&tmL, el.ptilde, p.C_pad, sr, p.C_pad, dtype)) return LCE_ERR_CUDA;
         SideGrad side;
         side.a = ga_prev;
         side.enabled = have_prev ? 1 : 0;
         LCE_TRY(launch_tc_logits(tmX_k, tmW_k, tma_out ? &tmL : nullptr, static_cast<int>(sr), static_cast<int>(C),
-                                 static_cast<int>(D), &hdr->status, el, pair, s, have_prev ? &side : nullptr));
+                                 static_cast<int>(D), &hdr->status, el, pair, s, have_prev ? &side : nullptr, f16));
       } else {
         const float* Xc = static_cast<const float*>(X) + (row0 + so) * D;
         LCE_TRY(launch_simt_logits(Xc, static_cast<const float*>(W), D, D, sr, C, D, el, s));
@@ -328,6 +342,7 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       ca.loss_rows = rows_out;
       ca.lse_out = lse_out;
       ca.backward = backward ? 1 : 0;
+      ca.wrow = wrow != nullptr ? wrow + so : nullptr;
       LCE_TRY(launch_combine(ca, s));
       if (!backward) continue;
       GradArgs ga;
@@ -342,11 +357,12 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       ga.tcol = tcol + so;
       ga.gt = gt + so;
       ga.db_acc = want_db ? db_acc : nullptr;
+      ga.wrow = wrow != nullptr ? wrow + so : nullptr;
       if (slabbed && si + 1 < nslab) {
         ga_prev = ga;  // formed by the next slab's GEMM
         have_prev = true;
       } else {
-        LCE_TRY(launch_grad_logits(ga, dtype == LCE_BF16, s));
+        LCE_TRY(launch_grad_logits(ga, dtype, s));
         have_prev = false;
       }
     }
@@ -355,20 +371,22 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
     if (want_dx) {
       EpiStore::Params es;
       es.out = static_cast<uint8_t*>(dX) + static_cast<size_t>(row0) * D * gsz;
-      es.out_bf16 = grad_dtype == LCE_BF16;
+      es.out_dt = grad_dtype;
       es.ldo = D;
       es.acc32 = nullptr;
       es.mode = 0;
       es.rows = rows;
       es.cols = D;
       es.vec_ok = aligned16(dX) && ((D * gsz) % 16 == 0);
+      es.row_scale = wrow;  // fp16: G without the row weights
+      es.scalar_scale = nullptr;
       if (p.tc) {
         CUtensorMap tmG_k, tmdX;
-        if (!encode_tmap_bf16(&tmG_k, Lbuf, C, rows, p.C_pad, TC_BM)) return LCE_ERR_CUDA;
-        const bool tma_out = pair && es.out_bf16 && es.vec_ok;
-        if (tma_out && !encode_tmap_bf16_store(&tmdX, es.out, D, rows, D)) return LCE_ERR_CUDA;
+        if (!encode_tmap_bf16(&tmG_k, Lbuf, C, rows, p.C_pad, TC_BM, dtype)) return LCE_ERR_CUDA;
+        const bool tma_out = pair && es.out_dt != LCE_F32 && es.vec_ok;
+        if (tma_out && !encode_tmap_bf16_store(&tmdX, es.out, D, rows, D, grad_dtype)) return LCE_ERR_CUDA;
         LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmW_n, tma_out ? &tmdX : nullptr, static_cast<int>(rows),
-                                static_cast<int>(D), static_cast<int>(C), &hdr->status, es, pair, s));
+                                static_cast<int>(D), static_cast<int>(C), &hdr->status, es, pair, s, f16));
       } else {
         LCE_TRY(launch_simt_store(TC_DX, static_cast<const float*>(Lbuf), static_cast<const float*>(W), p.C_pad, D,
                                   rows, D, C, es, s));
@@ -378,11 +396,13 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
     if (want_dw) {
       EpiStore::Params es;
       es.out = dW;
-      es.out_bf16 = grad_dtype == LCE_BF16;
+      es.out_dt = grad_dtype;
       es.ldo = D;
       es.rows = C;
       es.cols = D;
       es.vec_ok = aligned16(dW) && ((D * gsz) % 16 == 0);
+      es.row_scale = nullptr;
+      es.scalar_scale = f16 ? wbar : nullptr;  // fp16: dW = max|w| * G^T (X * w / max|w|)
       if (p.nchunks == 1) {
         es.mode = 0;
         es.acc32 = nullptr;
@@ -394,14 +414,18 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
         es.acc32 = dw_acc;
       }
       if (p.tc) {
-        const void* Xc = static_cast<const __nv_bfloat16*>(X) + row0 * D;
+        const void* Xc = static_cast<const uint16_t*>(X) + row0 * D;
+        if (f16) {
+          LCE_TRY(launch_row_scale(Xc, wrow, wbar, Xs, rows, D, s));
+          Xc = Xs;
+        }
         CUtensorMap tmG_m, tmX_n, tmdW;
-        if (!encode_tmap_bf16(&tmG_m, Lbuf, C, rows, p.C_pad, 64)) return LCE_ERR_CUDA;
-        if (!encode_tmap_bf16(&tmX_n, Xc, D, rows, D, 64)) return LCE_ERR_CUDA;
-        const bool tma_out = pair && es.mode == 0 && es.out_bf16 && es.vec_ok;
-        if (tma_out && !encode_tmap_bf16_store(&tmdW, dW, D, C, D)) return LCE_ERR_CUDA;
+        if (!encode_tmap_bf16(&tmG_m, Lbuf, C, rows, p.C_pad, 64, dtype)) return LCE_ERR_CUDA;
+        if (!encode_tmap_bf16(&tmX_n, Xc, D, rows, D, 64, dtype)) return LCE_ERR_CUDA;
+        const bool tma_out = pair && es.mode == 0 && es.out_dt != LCE_F32 && es.vec_ok;
+        if (tma_out && !encode_tmap_bf16_store(&tmdW, dW, D, C, D, grad_dtype)) return LCE_ERR_CUDA;
         LCE_TRY(launch_tc_store(TC_DW, tmG_m, tmX_n, tma_out ? &tmdW : nullptr, static_cast<int>(C),
-                                static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s));
+                                static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s, f16));
       } else {
         const float* Xc = static_cast<const float*>(X) + row0 * D;
         LCE_TRY(launch_simt_store(TC_DW, static_cast<const float*>(Lbuf), Xc, p.C_pad, D, C, D, rows, es, s));
@@ -410,7 +434,7 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
   }
   if (reduction != LCE_RED_NONE)
     LCE_TRY(launch_loss_finalize(loss_rows, N, reduction, hdr, class_weight != nullptr, loss_out, s));
-  if (want_db) LCE_TRY(launch_db_finalize(db_acc, db, C, grad_dtype == LCE_BF16, s));
+  if (want_db) LCE_TRY(launch_db_finalize(db_acc, db, C, grad_dtype, s));
   return LCE_OK;
 }
 
@@ -429,7 +453,8 @@ size_t lce_workspace_size(int op, int64_t N, int64_t D, int64_t C, int dtype, in
   }
   if (op != LCE_OP_FORWARD && op != LCE_OP_FORWARD_BACKWARD) return 0;
   if (check_common(N, D, C, dtype, LCE_F32, reduction) != LCE_OK) return 0;
-  if (op == LCE_OP_FORWARD_BACKWARD && grad_dtype != LCE_F32 && grad_dtype != LCE_BF16) return 0;
+  if (op == LCE_OP_FORWARD_BACKWARD && grad_dtype != LCE_F32 && grad_dtype != LCE_BF16 && grad_dtype != LCE_F16)
+    return 0;
   if (chunk_rows < 0) return 0;
   int64_t bc;
   if (chunk_rows == 0) {
@@ -488,7 +513,7 @@ int lce_cross_entropy_from_logits_ex(void* logits_inout, const int64_t* target, 
                                      int64_t N, int64_t V, int dtype, int reduction, int64_t ignore_index,
                                      const float* grad_out, float* loss_out, void* workspace, size_t ws_bytes,
                                      void* stream) {
-  if (dtype != LCE_F32 && dtype != LCE_BF16) return LCE_ERR_DTYPE;
+  if (dtype != LCE_F32 && dtype != LCE_BF16 && dtype != LCE_F16) return LCE_ERR_DTYPE;
   if (reduction != LCE_RED_NONE && reduction != LCE_RED_SUM && reduction != LCE_RED_MEAN) return LCE_ERR_REDUCTION;
   if (N < 0 || V < 1 || N > (int64_t(1) << 40) || V > (int64_t(1) << 40)) return LCE_ERR_SHAPE;
   if (N > 0 && (logits_inout == nullptr || target == nullptr || loss_out == nullptr)) return LCE_ERR_NULL;
@@ -520,7 +545,7 @@ int lce_cross_entropy_from_logits_ex(void* logits_inout, const int64_t* target, 
     a.hdr = hdr;
     a.loss_rows = reduction == LCE_RED_NONE ? loss_out : loss_rows;
     a.status = &hdr->status;
-    LCE_TRY(launch_ce_logits(a, dtype == LCE_BF16, s));
+    LCE_TRY(launch_ce_logits(a, dtype, s));
   }
   if (reduction != LCE_RED_NONE)
     LCE_TRY(launch_loss_finalize(loss_rows, N, reduction, hdr, class_weight != nullptr, loss_out, s));
@@ -609,7 +634,9 @@ int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t M, int6
   if (!ok) return LCE_ERR_CUDA;
   EpiStore::Params es;
   es.out = out;
-  es.out_bf16 = 0;
+  es.out_dt = LCE_F32;
+  es.row_scale = nullptr;
+  es.scalar_scale = nullptr;
   es.ldo = N;
   es.acc32 = nullptr;
   es.mode = 0;
@@ -630,7 +657,9 @@ int lce_test_gemm_f32(const float* A, const float* B, float* out, int64_t M, int
   if (st != LCE_OK) return st;
   EpiStore::Params es;
   es.out = out;
-  es.out_bf16 = 0;
+  es.out_dt = LCE_F32;
+  es.row_scale = nullptr;
+  es.scalar_scale = nullptr;
   es.ldo = N;
   es.acc32 = nullptr;
   es.mode = 0;

@@ -114,8 +114,27 @@ __device__ __forceinline__ void load_vec<__nv_bfloat16>(const __nv_bfloat16* p, 
     x[2 * i + 1] = f.y;
   }
 }
+template <>
+__device__ __forceinline__ void load_vec<__half>(const __half* p, float* x) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
 template <class T>
 __device__ __forceinline__ void store_vec(T* p, const float* x);
+template <>
+__device__ __forceinline__ void store_vec<__half>(__half* p, const float* x) {
+  uint4 v;
+  __half2* h = reinterpret_cast<__half2*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = v;
+}
 template <>
 __device__ __forceinline__ void store_vec<float>(float* p, const float* x) {
   *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
@@ -290,9 +309,11 @@ cudaError_t launch_ce_t(const CeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_ce_logits(const CeArgs& a, bool bf16, cudaStream_t s) {
+cudaError_t launch_ce_logits(const CeArgs& a, int dt, cudaStream_t s) {
   if (a.N == 0) return cudaSuccess;
-  return bf16 ? launch_ce_t<__nv_bfloat16>(a, s) : launch_ce_t<float>(a, s);
+  if (dt == LCE_BF16) return launch_ce_t<__nv_bfloat16>(a, s);
+  if (dt == LCE_F16) return launch_ce_t<__half>(a, s);
+  return launch_ce_t<float>(a, s);
 }
 
 }  // namespace lce

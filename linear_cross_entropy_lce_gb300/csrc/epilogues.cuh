@@ -5,15 +5,60 @@
 // accumulators of columns [col0 + 32c, col0 + 32c + 32) of that row. The
 // loads must be called by every lane of a warp in the same order (the
 // tcgen05 loads are warp-collective), so row validity only guards stores.
+// Element types are the lce_dtype_e codes: 0 fp32, 1 bf16, 2 fp16.
 #pragma once
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
 
 namespace lce {
 
+__device__ __forceinline__ float load_elem(const void* p, int64_t i, int dt) {
+  if (dt == LCE_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+  if (dt == LCE_F16) return __half2float(static_cast<const __half*>(p)[i]);
+  return static_cast<const float*>(p)[i];
+}
+__device__ __forceinline__ void store_elem(void* p, int64_t i, float x, int dt) {
+  if (dt == LCE_BF16)
+    static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
+  else if (dt == LCE_F16)
+    static_cast<__half*>(p)[i] = __float2half_rn(x);
+  else
+    static_cast<float*>(p)[i] = x;
+}
+// Two floats as one 32-bit word of two 16-bit values (bf16 or fp16).
+__device__ __forceinline__ uint32_t pack2(float a, float b, int dt) {
+  if (dt == LCE_F16) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// 32 floats -> 64 bytes of 16-bit values at dst (16-byte aligned).
+__device__ __forceinline__ void store32_16bit(void* dst, const float (&v)[32], int dt) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack2(v[8 * q + 0], v[8 * q + 1], dt);
+    u.y = pack2(v[8 * q + 2], v[8 * q + 3], dt);
+    u.z = pack2(v[8 * q + 4], v[8 * q + 5], dt);
+    u.w = pack2(v[8 * q + 6], v[8 * q + 7], dt);
+    d[q] = u;
+  }
+}
+// 32 floats -> 128 bytes of fp32 at dst (16-byte aligned).
+__device__ __forceinline__ void store32_f32(float* dst, const float (&v)[32]) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
 // Output path of one epilogue warp. With tmap == NULL every thread stores
-// its row directly. Otherwise bf16 results go out per 32-column chunk
+// its row directly. Otherwise 16-bit results go out per 32-column chunk
 // through a TMA store of the warp's 32 x 32 box: the warp stages the chunk
 // in a 2 KB buffer (32 rows x 64 B, 64-byte swizzle, so the 16-byte writes
 // of the 32 lanes hit distinct banks) and lane 0 issues the store; two
@@ -28,12 +73,7 @@ struct EpiIO {
   int nst;           // stores issued so far (buffer parity)
 };
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ void stage_store_bf16(EpiIO& io, const float (&v)[32], int64_t col) {
+__device__ __forceinline__ void stage_store_16bit(EpiIO& io, const float (&v)[32], int64_t col, int dt) {
   uint8_t* buf = io.stage + (io.nst & 1) * 2048;
   if (io.lane == 0) bulk_wait_read_le1();
   __syncwarp();
@@ -42,10 +82,10 @@ __device__ __forceinline__ void stage_store_bf16(EpiIO& io, const float (&v)[32]
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint4 u;
-    u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-    u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-    u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-    u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    u.x = pack2(v[8 * q + 0], v[8 * q + 1], dt);
+    u.y = pack2(v[8 * q + 2], v[8 * q + 3], dt);
+    u.z = pack2(v[8 * q + 4], v[8 * q + 5], dt);
+    u.w = pack2(v[8 * q + 6], v[8 * q + 7], dt);
     st_shared_v4(row_addr + ((q ^ sw) << 4), u);
   }
   fence_proxy_async_smem();
@@ -72,23 +112,22 @@ __device__ __forceinline__ void stage_store_bf16(EpiIO& io, const float (&v)[32]
 // ---------------------------------------------------------------------------
 struct EpiLse {
   struct Params {
-    const void* bias;        // [C] (bf16 or fp32, see bias_bf16) or NULL
-    int bias_bf16;
+    const void* bias;        // [C] of bias_dt, or NULL
+    int bias_dt;
     const int64_t* target;   // chunk-local: target[row]
     int64_t C;
     int rows;                // valid rows in this chunk
     float2* partial;         // [nseg][partial_ld] (m, s)
     int64_t partial_ld;
     float* zt;               // [rows] logit at the target column
-    void* ptilde;            // [rows][ld_p] or NULL (forward only)
+    void* ptilde;            // [rows][ld_p] of ptilde_dt, or NULL (forward only)
     int64_t ld_p;
-    int ptilde_bf16;
+    int ptilde_dt;
   };
 
   __device__ static __forceinline__ float bias_at(const Params& p, int64_t col) {
     if (p.bias == nullptr || col >= p.C) return 0.0f;
-    return p.bias_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.bias)[col])
-                       : static_cast<const float*>(p.bias)[col];
+    return load_elem(p.bias, col, p.bias_dt);
   }
 
   template <int NCHUNK, class Loader>
@@ -125,29 +164,13 @@ struct EpiLse {
         v[i] = e;
       }
       if (p.ptilde != nullptr && io.tmap != nullptr) {
-        stage_store_bf16(io, v, col0 + 32 * c);
+        stage_store_16bit(io, v, col0 + 32 * c, p.ptilde_dt);
       } else if (p.ptilde != nullptr && row_ok) {
         const int64_t off = row * p.ld_p + col0 + 32 * c;
-        if (p.ptilde_bf16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.ptilde) + off);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 u;
-            __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
-            __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
-            __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
-            u.x = *reinterpret_cast<uint32_t*>(&h0);
-            u.y = *reinterpret_cast<uint32_t*>(&h1);
-            u.z = *reinterpret_cast<uint32_t*>(&h2);
-            u.w = *reinterpret_cast<uint32_t*>(&h3);
-            dst[q] = u;
-          }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.ptilde) + off);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
+        if (p.ptilde_dt == LCE_F32)
+          store32_f32(static_cast<float*>(p.ptilde) + off, v);
+        else
+          store32_16bit(static_cast<uint16_t*>(p.ptilde) + off, v, p.ptilde_dt);
       }
     }
     if (row_ok && col0 < p.C) {
@@ -162,18 +185,23 @@ struct EpiLse {
 // tests). mode 0: out = acc; 1: acc32 = acc (first chunk of a dW
 // accumulated over chunks); 2: acc32 += acc; 3: out = acc32 + acc (last
 // chunk); 4: out += acc with fp32 atomics (one split of a split-K GEMM
-// into a zeroed fp32 out). out is bf16 or fp32; acc32 is fp32 with the
-// same leading dimension as out.
+// into a zeroed fp32 out). out is fp32, bf16 or fp16 (out_dt); acc32 is
+// fp32 with the same leading dimension as out. Before any of this the
+// accumulator may be scaled per row (row_scale[row]) and by one device
+// scalar (scalar_scale[0]): the fp16 backward stores G without the row
+// weights, so dX takes them per row and dW as one scalar.
 // ---------------------------------------------------------------------------
 struct EpiStore {
   struct Params {
     void* out;
-    int out_bf16;
+    int out_dt;
     int64_t ldo;
     float* acc32;
     int mode;
-    int64_t rows, cols;  // valid output region
-    int vec_ok;          // rows of out / acc32 are 16-byte aligned
+    int64_t rows, cols;         // valid output region
+    int vec_ok;                 // rows of out / acc32 are 16-byte aligned
+    const float* row_scale;     // [rows] or NULL
+    const float* scalar_scale;  // device scalar or NULL
   };
 
   __device__ static __forceinline__ void put(const Params& p, int64_t idx, float x) {
@@ -190,53 +218,42 @@ struct EpiStore {
       return;
     }
     if (p.mode == 3) x += p.acc32[idx];
-    if (p.out_bf16)
-      static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(x);
-    else
-      static_cast<float*>(p.out)[idx] = x;
+    store_elem(p.out, idx, x, p.out_dt);
   }
 
   template <int NCHUNK, class Loader>
   __device__ static __forceinline__ void run(const Params& p, int64_t row, int64_t col0, int64_t /*seg*/,
                                              Loader&& load, EpiIO& io) {
     const bool row_ok = row < p.rows;
+    float scale = 1.0f;
+    if (p.row_scale != nullptr) scale = row_ok ? p.row_scale[row] : 0.0f;
+    if (p.scalar_scale != nullptr) scale *= p.scalar_scale[0];
+    const bool scaled = p.row_scale != nullptr || p.scalar_scale != nullptr;
     float v[32];
 #pragma unroll 1
     for (int c = 0; c < NCHUNK; ++c) {
       load(c, v);
-      if (io.tmap != nullptr) {  // bf16, mode 0 (the host only sets tmap then)
-        stage_store_bf16(io, v, col0 + 32 * c);
+      if (scaled) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= scale;
+      }
+      if (io.tmap != nullptr) {  // 16-bit, mode 0 (the host only sets tmap then)
+        stage_store_16bit(io, v, col0 + 32 * c, p.out_dt);
         continue;
       }
       if (!row_ok) continue;
       const int64_t cb = col0 + 32 * c;
       const int64_t base = row * p.ldo + cb;
       if (p.vec_ok && cb + 32 <= p.cols && p.mode != 4) {
-        if (p.mode == 0 && p.out_bf16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + base);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 u;
-            __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
-            __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
-            __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
-            u.x = *reinterpret_cast<uint32_t*>(&h0);
-            u.y = *reinterpret_cast<uint32_t*>(&h1);
-            u.z = *reinterpret_cast<uint32_t*>(&h2);
-            u.w = *reinterpret_cast<uint32_t*>(&h3);
-            dst[q] = u;
-          }
+        if (p.mode == 0 && p.out_dt != LCE_F32) {
+          store32_16bit(static_cast<uint16_t*>(p.out) + base, v, p.out_dt);
           continue;
         }
         if (p.mode == 0 || p.mode == 1) {
-          float* o = (p.mode == 1) ? p.acc32 : static_cast<float*>(p.out);
-          float4* dst = reinterpret_cast<float4*>(o + base);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          store32_f32((p.mode == 1 ? p.acc32 : static_cast<float*>(p.out)) + base, v);
           continue;
         }
-        if (p.mode == 2 || (p.mode == 3 && !p.out_bf16)) {
+        if (p.mode == 2 || (p.mode == 3 && p.out_dt == LCE_F32)) {
           float4* a = reinterpret_cast<float4*>(p.acc32 + base);
           float4* o = reinterpret_cast<float4*>((p.mode == 2 ? p.acc32 : static_cast<float*>(p.out)) + base);
 #pragma unroll

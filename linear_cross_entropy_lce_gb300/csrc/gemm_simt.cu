@@ -41,7 +41,7 @@ cudaError_t launch_simt_store(int op, const float* A, const float* B, int64_t ld
       // few output tiles and a long K (= C): split K over z so every SM has
       // work; the splits add into the zeroed fp32 output (mode 4)
       const int64_t tiles = ((M + SG_BM - 1) / SG_BM) * ((N + SG_BN - 1) / SG_BN);
-      if (ep.mode == 0 && !ep.out_bf16 && tiles < 2 * num_sms() && K >= 1024) {
+      if (ep.mode == 0 && ep.out_dt == LCE_F32 && ep.row_scale == nullptr && tiles < 2 * num_sms() && K >= 1024) {
         int64_t splits = (2 * num_sms() + tiles - 1) / tiles;
         if (splits > 16) splits = 16;
         if (splits > K / 256) splits = K / 256;

@@ -58,11 +58,11 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int
   return e;
 }
 
-template <bool A_MN, bool B_MN, class Epi>
+template <bool A_MN, bool B_MN, class Epi, bool F16 = false>
 cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M, int N,
                        int K, int m_inner, int* status, const typename Epi::Params& ep, int kid, cudaStream_t s,
                        const SideGrad* side = nullptr) {
-  auto kern = tc2_gemm_kernel<A_MN, B_MN, Epi>;
+  auto kern = tc2_gemm_kernel<A_MN, B_MN, Epi, F16>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TC2_SMEM_BYTES);
@@ -117,30 +117,33 @@ bool tc_pair_default() {
   return v == 1;
 }
 
+static CUtensorMapDataType map_dtype(int dt) {
+  return dt == LCE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
-                      uint32_t box_rows) {
+                      uint32_t box_rows, int dt) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {ld * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = fn(map, map_dtype(dt), 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64_t rows, uint64_t ld) {
+bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64_t rows, uint64_t ld, int dt) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {ld * 2};
   cuuint32_t box[2] = {32, 32};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(map, map_dtype(dt), 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -148,14 +151,28 @@ bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64
 // tiles walk down the rows so the CTAs in flight share one W panel.
 cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
                              int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s,
-                             const SideGrad* side) {
+                             const SideGrad* side, bool f16) {
+  if (f16)
+    return launch_tc2<false, false, EpiLse, true>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s,
+                                                  side);
   if (pair)
     return launch_tc2<false, false, EpiLse>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s, side);
   return launch_tc<false, false, EpiLse>(tmX, tmW, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s);
 }
 
 cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M,
-                            int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s) {
+                            int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s,
+                            bool f16) {
+  if (f16) {  // fp16 operands: CTA-pair kernel only
+    switch (op) {
+      case TC_DX:
+        return launch_tc2<false, true, EpiStore, true>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DX_TC, s);
+      case TC_DW:
+        return launch_tc2<true, true, EpiStore, true>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DW_TC, s);
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
   if (pair) {
     switch (op) {
       case TC_DX:

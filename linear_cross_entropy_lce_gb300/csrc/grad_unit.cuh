@@ -5,7 +5,8 @@
 // column, written in place over P~ (linear_cross_entropy.py: logits scaled
 // by w / denominator, then the one-hot correction). With db_acc the column
 // sums of G over the unit's rows are added to db_acc (one fp32 atomic per
-// column per unit). Used by the stand-alone kernel (256 threads) and by the
+// column per unit); when G is stored without the row weights (wrow given)
+// each row's contribution is multiplied by wrow[r]. Used by the stand-alone kernel (256 threads) and by the
 // otherwise idle warps 2-3 of the CTA-pair GEMM (64 threads), which convert
 // one row slab while the next slab's logits are being computed.
 #pragma once
@@ -36,6 +37,7 @@ __device__ __forceinline__ void grad_unit(const GradArgs& a, int seg, int64_t r_
     uint4 raw[NR];
     float sc[NR];
     int tc[NR];
+    float wr[NR];
 #pragma unroll
     for (int k = 0; k < NR; ++k) {
       const int64_t r = rp + k * RPP;
@@ -43,6 +45,7 @@ __device__ __forceinline__ void grad_unit(const GradArgs& a, int seg, int64_t r_
         raw[k] = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.L) + r * a.ld + col);
         sc[k] = a.scale[seg * a.sld + r].x;
         tc[k] = a.tcol[r];
+        wr[k] = a.wrow != nullptr ? a.wrow[r] : 1.0f;
       }
     }
 #pragma unroll
@@ -55,7 +58,7 @@ __device__ __forceinline__ void grad_unit(const GradArgs& a, int seg, int64_t r_
         float gv = to_f32(e[i]) * sc[k];
         if (col + i == tc[k]) gv = a.gt[r];
         e[i] = from_f32<T>(gv);
-        colsum[i] += to_f32(e[i]);
+        colsum[i] += wr[k] * to_f32(e[i]);
       }
       *reinterpret_cast<uint4*>(static_cast<T*>(a.L) + r * a.ld + col) = raw[k];
     }

@@ -29,6 +29,7 @@ enum KernelId {
   K_CE_RESIDENT,
   K_CE_STREAM,
   K_GEMM_TEST,
+  K_ROW_SCALE,
   K_NUM_IDS
 };
 const char* kernel_id_name(int id);
@@ -47,18 +48,21 @@ enum TcOp { TC_LOGITS = 0, TC_DX = 1, TC_DW = 2, TC_TEST_KK = 3, TC_TEST_KM = 4,
 // Encodes a 2-D bf16 tensor map over a row-major matrix with `rows` rows of
 // `inner` elements, row pitch `ld` elements, box {64, box_rows}, 128B swizzle.
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
-                      uint32_t box_rows);
+                      uint32_t box_rows, int dt = LCE_BF16);
 // pair: run the CTA-pair kernel (256 x 256 tiles, cta_group::2); its B
 // operand maps use boxes of 128 rows (K-major) instead of 256.
 // tmOut (pair kernel only; NULL = direct stores): bf16 output tensor map
 // with 32 x 32 boxes and 64-byte swizzle (encode_tmap_bf16_store) through
 // which the epilogue writes P~ (logits) or the mode-0 bf16 result (store).
+// f16: fp16 operands (CTA-pair kernel); otherwise bf16.
 cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
                              int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s,
-                             const SideGrad* side = nullptr);
+                             const SideGrad* side = nullptr, bool f16 = false);
 cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M,
-                            int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s);
-bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64_t rows, uint64_t ld);
+                            int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s,
+                            bool f16 = false);
+bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64_t rows, uint64_t ld,
+                            int dt = LCE_BF16);
 // Whether the fused path uses the CTA-pair GEMM (default yes; LCE_TC_PAIR=0 selects the one-CTA kernel).
 bool tc_pair_default();
 
@@ -89,6 +93,9 @@ struct CombineArgs {
   float* loss_rows;          // global [N]
   float* lse_out;            // global [N] or NULL
   int backward;
+  // fp16 backward: scales and G at the target leave out w_n, which goes to
+  // wrow[r] instead (NULL otherwise)
+  float* wrow;
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 struct GradArgs {
@@ -102,18 +109,23 @@ struct GradArgs {
   int64_t sld;
   const int* tcol;
   const float* gt;
-  float* db_acc;  // [C] or NULL
+  float* db_acc;       // [C] or NULL
+  const float* wrow;   // [rows] row weights when G is stored without them (fp16), else NULL
 };
-cudaError_t launch_grad_logits(const GradArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_grad_logits(const GradArgs& a, int dt, cudaStream_t s);
 // G formation for a row slab (bf16, 256-column segments) done by the idle
 // warps of the CTA-pair logits GEMM of the next slab.
 struct SideGrad {
   GradArgs a;
   int enabled;
 };
+// fp16 backward: wbar = max_r |w_r| over the chunk rows (NaN if any w_r is
+// NaN), then Xs[r, :] = (w_r / wbar) X[r, :] in fp16 (0 when wbar is 0).
+cudaError_t launch_row_scale(const void* X, const float* wrow, float* wbar, void* Xs, int64_t rows, int64_t D,
+                             cudaStream_t s);
 cudaError_t launch_loss_finalize(const float* loss_rows, int64_t N, int reduction, const WsHeader* hdr,
                                  bool weighted, float* loss_out, cudaStream_t s);
-cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, bool bf16, cudaStream_t s);
+cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, int dt, cudaStream_t s);
 
 // ---- cross entropy on given logits (ce_logits.cu)
 struct CeArgs {
@@ -126,6 +138,6 @@ struct CeArgs {
   float* loss_rows;  // [N]
   int* status;
 };
-cudaError_t launch_ce_logits(const CeArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_ce_logits(const CeArgs& a, int dt, cudaStream_t s);
 
 }  // namespace lce

@@ -114,13 +114,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A and B and an fp32
-// accumulator: D format F32 (bits 4-5 = 1), A and B format BF16 (bits 7-9,
-// 10-12 = 1), A / B major-ness (bit 15 / 16: 1 = MN-major), N >> 3 in bits
-// 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor for kind::f16 with 16-bit A and B and an fp32
+// accumulator: D format F32 (bits 4-5 = 1), A and B format (bits 7-9,
+// 10-12: 0 = F16, 1 = BF16), A / B major-ness (bit 15 / 16: 1 = MN-major),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_16_f32(int M, int N, bool a_mn, bool b_mn, bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one CTA, issued by a single thread.

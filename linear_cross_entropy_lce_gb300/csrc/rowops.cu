@@ -104,13 +104,16 @@ __global__ void combine_kernel(const CombineArgs a) {
   }
   if (a.backward) {
     const float w = row_weight(a.rw, a.hdr, g, t, valid);
+    // with wrow the stored G leaves w_n out: unit weight on valid rows, 0 on the others
+    const float ws = a.wrow != nullptr ? (valid ? 1.0f : 0.0f) : w;
     for (int s = lane; s < a.nseg; s += 32) {
       float2* p = &a.partial[s * a.ld + r];
-      p->x = w * expf(p->x - lse);
+      p->x = ws * expf(p->x - lse);
     }
     if (lane == 0) {
       a.tcol[r] = valid ? static_cast<int>(t) : -1;
-      a.gt[r] = valid ? w * expm1f(zt - lse) : 0.0f;
+      a.gt[r] = valid ? ws * expm1f(zt - lse) : 0.0f;
+      if (a.wrow != nullptr) a.wrow[r] = w;
     }
   }
 }
@@ -121,6 +124,61 @@ __global__ void __launch_bounds__(256) grad_logits_kernel(const GradArgs a) {
   __shared__ float red[256 / (SEGW / (16 / sizeof(T)))][SEGW];
   grad_unit<T, SEGW, 256, 64>(a, blockIdx.x, static_cast<int64_t>(blockIdx.y) * 64, threadIdx.x, &red[0][0],
                               [] { __syncthreads(); });
+}
+
+// max |w| over the rows, NaN if any w is NaN (single block).
+__global__ void wmax_kernel(const float* __restrict__ w, int64_t rows, float* out) {
+  __shared__ float s_m[32];
+  __shared__ int s_nan[32];
+  float m = 0.0f;
+  int nan = 0;
+  for (int64_t i = threadIdx.x; i < rows; i += blockDim.x) {
+    const float x = w[i];
+    nan |= isnan(x) ? 1 : 0;
+    m = fmaxf(m, fabsf(x));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    nan |= __shfl_xor_sync(0xffffffffu, nan, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_nan[warp] = nan;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    m = lane < nw ? s_m[lane] : 0.0f;
+    nan = lane < nw ? s_nan[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      nan |= __shfl_xor_sync(0xffffffffu, nan, o);
+    }
+    if (lane == 0) out[0] = nan ? __int_as_float(0x7fc00000) : m;
+  }
+}
+
+// Xs[r, :] = (w_r / wbar) X[r, :], fp16, 8 elements per thread (D % 8 == 0).
+__global__ void scale_rows_kernel(const __half* __restrict__ X, const float* __restrict__ w,
+                                  const float* __restrict__ wbar, __half* __restrict__ Xs, int64_t rows, int64_t D) {
+  const int64_t nvec = rows * (D / 8);
+  const float wb = wbar[0];
+  for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < nvec;
+       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = v / (D / 8);
+    const float f = wb > 0.0f ? w[r] / wb : (isnan(wb) ? wb : 0.0f);
+    uint4 raw = reinterpret_cast<const uint4*>(X)[v];
+    __half2* h = reinterpret_cast<__half2*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __half22float2(h[i]);
+      h[i] = __floats2half2_rn(x.x * f, x.y * f);
+    }
+    reinterpret_cast<uint4*>(Xs)[v] = raw;
+  }
 }
 
 // Deterministic single-block sum of the per-row losses in fp64; mean
@@ -183,19 +241,36 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   return e;
 }
 
-cudaError_t launch_grad_logits(const GradArgs& a, bool bf16, cudaStream_t s) {
+cudaError_t launch_grad_logits(const GradArgs& a, int dt, cudaStream_t s) {
+  const bool bf16 = dt != LCE_F32;
   if (a.rows == 0) return cudaSuccess;
   const int64_t gy = (a.rows + 63) / 64;
   if (gy > 65535) return cudaErrorInvalidValue;
   if (a.segw != (bf16 ? 256 : 64)) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(a.nseg), static_cast<unsigned>(gy));
-  prof_before(K_GRAD_LOGITS, s, 2.0 * (bf16 ? 2 : 4) * a.rows * static_cast<double>(a.ld));
-  if (bf16)
+  prof_before(K_GRAD_LOGITS, s, 2.0 * (bf16 ? 2 : 4) * a.rows * static_cast<double>(a.ld));  // 16-bit or fp32
+  if (dt == LCE_F16)
+    grad_logits_kernel<__half, 256><<<grid, 256, 0, s>>>(a);
+  else if (dt == LCE_BF16)
     grad_logits_kernel<__nv_bfloat16, 256><<<grid, 256, 0, s>>>(a);
   else
     grad_logits_kernel<float, 64><<<grid, 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   prof_after(K_GRAD_LOGITS, s);
+  return e;
+}
+
+cudaError_t launch_row_scale(const void* X, const float* wrow, float* wbar, void* Xs, int64_t rows, int64_t D,
+                             cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  prof_before(K_ROW_SCALE, s, 4.0 * rows * static_cast<double>(D) + 4.0 * rows);
+  wmax_kernel<<<1, 1024, 0, s>>>(wrow, rows, wbar);
+  int64_t blocks = (rows * (D / 8) + 255) / 256;
+  if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
+  scale_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const __half*>(X), wrow, wbar,
+                                                                 static_cast<__half*>(Xs), rows, D);
+  cudaError_t e = cudaGetLastError();
+  prof_after(K_ROW_SCALE, s);
   return e;
 }
 
@@ -208,13 +283,15 @@ cudaError_t launch_loss_finalize(const float* loss_rows, int64_t N, int reductio
   return e;
 }
 
-cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, bool bf16, cudaStream_t s) {
+cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, int dt, cudaStream_t s) {
   int64_t blocks = (C + 255) / 256;
   if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
-  prof_before(K_DB_FINALIZE, s, (bf16 ? 6.0 : 8.0) * C);
-  if (bf16)
+  prof_before(K_DB_FINALIZE, s, (dt == LCE_F32 ? 8.0 : 6.0) * C);
+  if (dt == LCE_BF16)
     db_finalize_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         db_acc, static_cast<__nv_bfloat16*>(db), C);
+  else if (dt == LCE_F16)
+    db_finalize_kernel<__half><<<static_cast<unsigned>(blocks), 256, 0, s>>>(db_acc, static_cast<__half*>(db), C);
   else
     db_finalize_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, s>>>(db_acc, static_cast<float*>(db), C);
   cudaError_t e = cudaGetLastError();

@@ -36,7 +36,7 @@ constexpr int TC2_TMEM_COLS = 512;
 constexpr int TC2_TILE_M = 256;  // rows per pair tile (128 per CTA)
 constexpr int TC2_TILE_N = 256;
 
-template <bool A_MN, bool B_MN, class Epi>
+template <bool A_MN, bool B_MN, class Epi, bool F16>
 __global__ void __launch_bounds__(TC2_THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmOut, const TcGemmArgs g,
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (even CTA only)
-      constexpr uint32_t kIdesc = idesc_bf16_f32(TC2_TILE_M, TC2_TILE_N, A_MN, B_MN);
+      constexpr uint32_t kIdesc = idesc_16_f32(TC2_TILE_M, TC2_TILE_N, A_MN, B_MN, F16);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -179,8 +179,11 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
       for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
         const int seg = static_cast<int>(u % side.a.nseg);
         const int64_t rb = u / side.a.nseg;
-        grad_unit<__nv_bfloat16, 256, 64, 64>(side.a, seg, rb * 64, tid, side_red,
-                                              [] { asm volatile("bar.sync 1, 64;" ::: "memory"); });
+        auto bar = [] { asm volatile("bar.sync 1, 64;" ::: "memory"); };
+        if (F16)
+          grad_unit<__half, 256, 64, 64>(side.a, seg, rb * 64, tid, side_red, bar);
+        else
+          grad_unit<__nv_bfloat16, 256, 64, 64>(side.a, seg, rb * 64, tid, side_red, bar);
       }
     }
   } else if (warp >= 4) {

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t kIdesc = idesc_bf16_f32(TC_BM, TC_BN, A_MN, B_MN);
+      constexpr uint32_t kIdesc = idesc_16_f32(TC_BM, TC_BN, A_MN, B_MN, false);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
