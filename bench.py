@@ -392,6 +392,17 @@ def run_gpu(args):
                         "peak_source": peaks["source"] + " bf16_tflops_sustained (the kernel runs inside a "
                                                          "long sequence of back-to-back steps)",
                         "algorithmic_flops_per_launch": per_launch}
+        elif dominant.startswith("gemm_") and dominant.endswith("_3xtf32"):
+            # fp32 product as three TF32 tensor-core products: the ceiling for
+            # its algorithmic flop is the TF32 peak / 3; TF32 peak = measured
+            # bf16 sustained x the nominal dense TF32 / bf16 ratio (1.1 / 2.25)
+            achieved = per_launch / avg_s / 1e12
+            peak = peaks["bf16_tflops_sustained"] * (1.1 / 2.25) / 3.0
+            roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak, "traffic": traffic, "kernel": dominant,
+                        "peak_source": peaks["source"] + " bf16_tflops_sustained x 1.1/2.25 (nominal TF32/bf16) "
+                                                         "/ 3 (TF32 products per fp32 product)",
+                        "algorithmic_flops_per_launch": per_launch}
         elif dominant.startswith("gemm_"):
             # exact fp32 FMA on the CUDA cores: SMs x 128 FP32 lanes x 2 flop x max SM clock
             sms = torch.cuda.get_device_properties(dev).multi_processor_count

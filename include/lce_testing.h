@@ -23,11 +23,19 @@
  *   Needs the contiguous dimension of each operand to be a multiple of 8 and
  *   16-byte aligned pointers.
  * lce_test_gemm_f32: fp32 A, B with fp32 FMA on the CUDA cores; any shape.
+ * lce_test_gemm_tf32x3: fp32 A, B on the tensor cores as three TF32
+ *   products (hi*hi + hi*lo + lo*hi, hi = x rounded to TF32, lo = the
+ *   rounded remainder; Ootomo & Yokota 2022), accumulated in fp32. The
+ *   operands are first split into K-major hi / lo copies in `workspace`
+ *   (device, 16-byte aligned, at least 2 * (M + N) * ceil(K / 4) * 16 + 1024
+ *   bytes); k_splits > 1 splits K over that many work items per tile which
+ *   add into the zeroed output. Any shape up to 2^30 per dimension.
  * Return an lce_status_e code.
  */
 #ifndef LCE_TESTING_H_
 #define LCE_TESTING_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifndef LCE_API
@@ -48,6 +56,10 @@ LCE_API int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t
 
 LCE_API int lce_test_gemm_f32(const float* A, const float* B, float* out, int64_t M, int64_t N,
                       int64_t K, int a_mn_major, int b_mn_major, void* stream);
+
+LCE_API int lce_test_gemm_tf32x3(const float* A, const float* B, float* out, int64_t M, int64_t N,
+                         int64_t K, int a_mn_major, int b_mn_major, int k_splits, void* workspace,
+                         size_t ws_bytes, int* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

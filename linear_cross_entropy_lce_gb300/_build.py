@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblce.so")
-UNITS = ["api.cu", "gemm_tc.cu", "gemm_simt.cu", "rowops.cu", "ce_logits.cu", "noalloc.cu"]
+UNITS = ["api.cu", "gemm_tc.cu", "gemm_tf32.cu", "gemm_simt.cu", "rowops.cu", "ce_logits.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

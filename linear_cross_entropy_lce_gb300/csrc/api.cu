@@ -77,7 +77,8 @@ std::atomic<int64_t> g_launches{0};
 const char* kNames[K_NUM_IDS] = {
     "prep",          "gemm_logits_tc", "gemm_dx_tc",  "gemm_dw_tc",      "gemm_logits_simt",
     "gemm_dx_simt",  "gemm_dw_simt",   "lse_combine", "grad_logits",     "loss_finalize",
-    "db_finalize",   "ce_resident",    "ce_stream",   "gemm_test",       "row_scale"};
+    "db_finalize",   "ce_resident",    "ce_stream",   "gemm_test",       "row_scale",
+    "gemm_logits_3xtf32", "gemm_dx_3xtf32", "gemm_dw_3xtf32", "split_tf32"};
 }  // namespace
 
 const char* kernel_id_name(int id) { return (id >= 0 && id < K_NUM_IDS) ? kNames[id] : "?"; }
@@ -108,6 +109,7 @@ inline int esize(int dt) { return dt == LCE_F32 ? 4 : 2; }
 
 struct Plan {
   bool tc;          // tensor-core (bf16 / fp16) path
+  bool tf32;        // fp32 inputs on the tensor cores (3xTF32)
   int segw;         // columns per (max, sum-exp) segment
   int nseg;
   int64_t C_pad;    // chunk buffer row pitch (elements)
@@ -118,17 +120,23 @@ struct Plan {
   // fp16 backward: per-row weights [Bc], their max |w| (one float), and the
   // rows of X scaled by w / max|w| for dW ([Bc, D] fp16)
   size_t off_wrow, off_wbar, off_xs;
+  // 3xTF32: TF32 hi / lo parts of W [C, ldD], W^T [D, ldC] (dX), the chunk's
+  // X [Bc, ldD] and X^T [D, ldB] (dW), the lo part of G [Bc, C_pad] (its hi
+  // part replaces G in the chunk buffer) and G^T [C, ldB] (dW)
+  int64_t ldD, ldC, ldB;
+  size_t off_wh, off_wl, off_wth, off_wtl, off_xh, off_xl, off_xth, off_xtl, off_gl, off_gth, off_gtl;
 };
 
 // Bytes for chunk size Bc. backward: chunk buffer and gradient scratch;
 // need_dw_acc_if_multi: a bf16 dW needs an fp32 accumulator once Bc < N.
-bool make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, bool want_dw, bool want_db,
-               int64_t Bc, Plan* p) {
+bool make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, bool want_dx, bool want_dw,
+               bool want_db, int64_t Bc, Plan* p) {
   const bool backward = op == LCE_OP_FORWARD_BACKWARD;
   p->tc = dtype != LCE_F32;
-  p->segw = p->tc ? 256 : 64;
+  p->tf32 = dtype == LCE_F32 && f32_tensor_default();
+  p->segw = (p->tc || p->tf32) ? 256 : 64;
   p->nseg = static_cast<int>(ceil_div(C, p->segw));
-  p->C_pad = p->tc ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
+  p->C_pad = (p->tc || p->tf32) ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
   if (N == 0) Bc = 0;
   p->Bc = Bc;
   p->nchunks = Bc > 0 ? ceil_div(N, Bc) : 0;
@@ -157,14 +165,45 @@ bool make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtyp
   if (f16bw) off = align_up(off + 4);
   p->off_xs = off;
   if (f16bw && want_dw) off = align_up(off + static_cast<size_t>(Bc) * static_cast<size_t>(D) * 2);
+  p->ldD = ceil_div(D, 4) * 4;
+  p->ldC = ceil_div(C, 4) * 4;
+  p->ldB = ceil_div(Bc, 4) * 4;
+  const bool tx = p->tf32;
+  const bool tx_dx = tx && backward && want_dx;
+  const bool tx_dw = tx && backward && want_dw;
+  auto take = [&off](bool on, size_t bytes) {
+    const size_t at = off;
+    if (on) off = align_up(off + bytes);
+    return at;
+  };
+  const size_t w_bytes = static_cast<size_t>(C) * p->ldD * 4;
+  const size_t wt_bytes = static_cast<size_t>(D) * p->ldC * 4;
+  const size_t x_bytes = static_cast<size_t>(Bc) * p->ldD * 4;
+  const size_t xt_bytes = static_cast<size_t>(D) * p->ldB * 4;
+  const size_t gl_bytes = static_cast<size_t>(Bc) * p->C_pad * 4;
+  const size_t gt_bytes = static_cast<size_t>(C) * p->ldB * 4;
+  p->off_wh = take(tx, w_bytes);
+  p->off_wl = take(tx, w_bytes);
+  p->off_wth = take(tx_dx, wt_bytes);
+  p->off_wtl = take(tx_dx, wt_bytes);
+  p->off_xh = take(tx, x_bytes);
+  p->off_xl = take(tx, x_bytes);
+  p->off_xth = take(tx_dw, xt_bytes);
+  p->off_xtl = take(tx_dw, xt_bytes);
+  p->off_gl = take(tx_dx, gl_bytes);
+  p->off_gth = take(tx_dw, gt_bytes);
+  p->off_gtl = take(tx_dw, gt_bytes);
   p->total = off;
   return true;
 }
 
-int64_t default_chunk(int op, int64_t N, int64_t C, int dtype) {
+int64_t default_chunk(int op, int64_t N, int64_t D, int64_t C, int dtype) {
   if (N == 0) return 0;
-  const int64_t C_pad = dtype != LCE_F32 ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
-  const int64_t per_row = (op == LCE_OP_FORWARD_BACKWARD ? C_pad * esize(dtype) : 0) + ceil_div(C, 64) * 8;
+  const bool tf32 = dtype == LCE_F32 && f32_tensor_default();
+  const bool bw = op == LCE_OP_FORWARD_BACKWARD;
+  const int64_t C_pad = (dtype != LCE_F32 || tf32) ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
+  int64_t per_row = (bw ? C_pad * esize(dtype) : 0) + ceil_div(C, 64) * 8;
+  if (tf32) per_row += 8 * D + (bw ? 4 * C_pad + 8 * C + 8 * D : 0);  // TF32 parts of X, G, X^T, G^T
   if (N * per_row <= kDefaultChunkBytes) return N;
   int64_t bc = 128;
   while (bc * 2 * per_row <= kDefaultChunkBytes && bc * 2 < N) bc *= 2;
@@ -172,10 +211,10 @@ int64_t default_chunk(int op, int64_t N, int64_t C, int dtype) {
 }
 
 // Largest chunk (N itself, else 128 * 2^k < N) whose plan fits ws_bytes.
-bool choose_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, bool want_dw, bool want_db,
-                 size_t ws_bytes, Plan* p) {
+bool choose_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, bool want_dx, bool want_dw,
+                 bool want_db, size_t ws_bytes, Plan* p) {
   if (N == 0) {
-    make_plan(op, 0, D, C, dtype, grad_dtype, want_dw, want_db, 0, p);
+    make_plan(op, 0, D, C, dtype, grad_dtype, want_dx, want_dw, want_db, 0, p);
     return p->total <= ws_bytes;
   }
   std::vector<int64_t> cands;
@@ -185,7 +224,7 @@ bool choose_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dt
   for (; bc >= 128; bc /= 2)
     if (bc < N) cands.push_back(bc);
   for (int64_t c : cands) {
-    make_plan(op, N, D, C, dtype, grad_dtype, want_dw, want_db, c, p);
+    make_plan(op, N, D, C, dtype, grad_dtype, want_dx, want_dw, want_db, c, p);
     if (p->total <= ws_bytes) return true;
   }
   return false;
@@ -233,8 +272,8 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
     if ((want_dx && !aligned16(dX)) || (want_dw && !aligned16(dW))) return LCE_ERR_ALIGN;
   }
   Plan p;
-  if (!choose_plan(backward ? LCE_OP_FORWARD_BACKWARD : LCE_OP_FORWARD, N, D, C, dtype, grad_dtype, want_dw,
-                   want_db, ws_bytes, &p))
+  if (!choose_plan(backward ? LCE_OP_FORWARD_BACKWARD : LCE_OP_FORWARD, N, D, C, dtype, grad_dtype, want_dx,
+                   want_dw, want_db, ws_bytes, &p))
     return LCE_ERR_WORKSPACE;
   if (p.Bc > 2147483647LL) return LCE_ERR_SHAPE;
   st = check_device();
@@ -281,6 +320,28 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
     if (!encode_tmap_bf16(&tmW_k, W, D, C, D, pair ? 128 : TC_BN, dtype)) return LCE_ERR_CUDA;
     if (want_dx && !encode_tmap_bf16(&tmW_n, W, D, C, D, 64, dtype)) return LCE_ERR_CUDA;
   }
+  // 3xTF32: every operand as K-major TF32 hi / lo parts in the workspace
+  auto wsf = [ws](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  TxOperands tx_lg, tx_dx, tx_dw;
+  if (p.tf32) {
+    SplitArgs sa;
+    sa.src = static_cast<const float*>(W);
+    sa.rows = C;
+    sa.cols = D;
+    sa.lds = D;
+    sa.hi = wsf(p.off_wh);
+    sa.lo = wsf(p.off_wl);
+    sa.ldo = p.ldD;
+    sa.hiT = want_dx ? wsf(p.off_wth) : nullptr;
+    sa.loT = want_dx ? wsf(p.off_wtl) : nullptr;
+    sa.ldt = p.ldC;
+    LCE_TRY(launch_split_tf32(sa, s));
+    bool ok = encode_tmap_f32(&tx_lg.bh, sa.hi, D, C, p.ldD, 128) && encode_tmap_f32(&tx_lg.bl, sa.lo, D, C, p.ldD, 128);
+    if (want_dx)
+      ok = ok && encode_tmap_f32(&tx_dx.bh, sa.hiT, C, D, p.ldC, 128) &&
+           encode_tmap_f32(&tx_dx.bl, sa.loT, C, D, p.ldC, 128);
+    if (!ok) return LCE_ERR_CUDA;
+  }
 
   for (int64_t ci = 0; ci < p.nchunks; ++ci) {
     const int64_t row0 = ci * p.Bc;
@@ -289,6 +350,20 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
     // CTA-pair path with a backward, the chunk is cut into 4 slabs and the
     // idle warps of slab k's logits GEMM form G for slab k-1, so only the
     // last slab's G formation runs as a kernel of its own.
+    if (p.tf32) {  // TF32 parts of the chunk's rows of X (and of X^T for dW)
+      SplitArgs sa;
+      sa.src = static_cast<const float*>(X) + row0 * D;
+      sa.rows = rows;
+      sa.cols = D;
+      sa.lds = D;
+      sa.hi = wsf(p.off_xh);
+      sa.lo = wsf(p.off_xl);
+      sa.ldo = p.ldD;
+      sa.hiT = want_dw ? wsf(p.off_xth) : nullptr;
+      sa.loT = want_dw ? wsf(p.off_xtl) : nullptr;
+      sa.ldt = p.ldB;
+      LCE_TRY(launch_split_tf32(sa, s));
+    }
     const bool slabbed = p.tc && pair && backward && rows >= 1024;
     const int64_t slab = slabbed ? ceil_div(ceil_div(rows, 4), 256) * 256 : rows;
     const int64_t nslab = ceil_div(rows, slab);
@@ -321,6 +396,13 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
         side.enabled = have_prev ? 1 : 0;
         LCE_TRY(launch_tc_logits(tmX_k, tmW_k, tma_out ? &tmL : nullptr, static_cast<int>(sr), static_cast<int>(C),
                                  static_cast<int>(D), &hdr->status, el, pair, s, have_prev ? &side : nullptr, f16));
+      } else if (p.tf32) {
+        const float* xh = wsf(p.off_xh) + so * p.ldD;
+        const float* xl = wsf(p.off_xl) + so * p.ldD;
+        if (!encode_tmap_f32(&tx_lg.ah, xh, D, sr, p.ldD, 128) || !encode_tmap_f32(&tx_lg.al, xl, D, sr, p.ldD, 128))
+          return LCE_ERR_CUDA;
+        LCE_TRY(launch_tx_logits(tx_lg, static_cast<int>(sr), static_cast<int>(C), static_cast<int>(D), &hdr->status,
+                                 el, s));
       } else {
         const float* Xc = static_cast<const float*>(X) + (row0 + so) * D;
         LCE_TRY(launch_simt_logits(Xc, static_cast<const float*>(W), D, D, sr, C, D, el, s));
@@ -367,6 +449,20 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       }
     }
     if (!backward) continue;
+    if (p.tf32 && (want_dx || want_dw)) {  // TF32 parts of G (hi over G itself) and of G^T
+      SplitArgs sa;
+      sa.src = static_cast<const float*>(Lbuf);
+      sa.rows = rows;
+      sa.cols = C;
+      sa.lds = p.C_pad;
+      sa.hi = want_dx ? static_cast<float*>(Lbuf) : nullptr;
+      sa.lo = want_dx ? wsf(p.off_gl) : nullptr;
+      sa.ldo = p.C_pad;
+      sa.hiT = want_dw ? wsf(p.off_gth) : nullptr;
+      sa.loT = want_dw ? wsf(p.off_gtl) : nullptr;
+      sa.ldt = p.ldB;
+      LCE_TRY(launch_split_tf32(sa, s));
+    }
     // ---- dX = G W
     if (want_dx) {
       EpiStore::Params es;
@@ -387,6 +483,12 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
         if (tma_out && !encode_tmap_bf16_store(&tmdX, es.out, D, rows, D, grad_dtype)) return LCE_ERR_CUDA;
         LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmW_n, tma_out ? &tmdX : nullptr, static_cast<int>(rows),
                                 static_cast<int>(D), static_cast<int>(C), &hdr->status, es, pair, s, f16));
+      } else if (p.tf32) {
+        if (!encode_tmap_f32(&tx_dx.ah, Lbuf, C, rows, p.C_pad, 128) ||
+            !encode_tmap_f32(&tx_dx.al, wsf(p.off_gl), C, rows, p.C_pad, 128))
+          return LCE_ERR_CUDA;
+        LCE_TRY(launch_tx_store(TC_DX, tx_dx, static_cast<int>(rows), static_cast<int>(D), static_cast<int>(C),
+                                &hdr->status, es, s));
       } else {
         LCE_TRY(launch_simt_store(TC_DX, static_cast<const float*>(Lbuf), static_cast<const float*>(W), p.C_pad, D,
                                   rows, D, C, es, s));
@@ -426,6 +528,14 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
         if (tma_out && !encode_tmap_bf16_store(&tmdW, dW, D, C, D, grad_dtype)) return LCE_ERR_CUDA;
         LCE_TRY(launch_tc_store(TC_DW, tmG_m, tmX_n, tma_out ? &tmdW : nullptr, static_cast<int>(C),
                                 static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s, f16));
+      } else if (p.tf32) {
+        bool ok = encode_tmap_f32(&tx_dw.ah, wsf(p.off_gth), rows, C, p.ldB, 128) &&
+                  encode_tmap_f32(&tx_dw.al, wsf(p.off_gtl), rows, C, p.ldB, 128) &&
+                  encode_tmap_f32(&tx_dw.bh, wsf(p.off_xth), rows, D, p.ldB, 128) &&
+                  encode_tmap_f32(&tx_dw.bl, wsf(p.off_xtl), rows, D, p.ldB, 128);
+        if (!ok) return LCE_ERR_CUDA;
+        LCE_TRY(launch_tx_store(TC_DW, tx_dw, static_cast<int>(C), static_cast<int>(D), static_cast<int>(rows),
+                                &hdr->status, es, s));
       } else {
         const float* Xc = static_cast<const float*>(X) + row0 * D;
         LCE_TRY(launch_simt_store(TC_DW, static_cast<const float*>(Lbuf), Xc, p.C_pad, D, C, D, rows, es, s));
@@ -458,7 +568,7 @@ size_t lce_workspace_size(int op, int64_t N, int64_t D, int64_t C, int dtype, in
   if (chunk_rows < 0) return 0;
   int64_t bc;
   if (chunk_rows == 0) {
-    bc = default_chunk(op, N, C, dtype);
+    bc = default_chunk(op, N, D, C, dtype);
   } else if (chunk_rows >= N) {
     bc = N;
   } else {
@@ -468,7 +578,7 @@ size_t lce_workspace_size(int op, int64_t N, int64_t D, int64_t C, int dtype, in
     if (bc >= N) bc = N;
   }
   Plan p;
-  make_plan(op, N, D, C, dtype, grad_dtype, true, true, bc, &p);
+  make_plan(op, N, D, C, dtype, grad_dtype, true, true, true, bc, &p);
   return p.total;
 }
 
@@ -647,6 +757,58 @@ int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t M, int6
   return from_cuda(launch_tc_store(op, ta, tb, nullptr, static_cast<int>(M), static_cast<int>(N),
                                    static_cast<int>(K), dev_status, es, cta_pair != 0,
                                    static_cast<cudaStream_t>(stream)));
+}
+
+int lce_test_gemm_tf32x3(const float* A, const float* B, float* out, int64_t M, int64_t N, int64_t K,
+                         int a_mn_major, int b_mn_major, int k_splits, void* workspace, size_t ws_bytes,
+                         int* dev_status, void* stream) {
+  if (A == nullptr || B == nullptr || out == nullptr || workspace == nullptr) return LCE_ERR_NULL;
+  if (M < 1 || N < 1 || K < 1 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return LCE_ERR_SHAPE;
+  if (!aligned16(workspace)) return LCE_ERR_ALIGN;
+  const int64_t ldk = ceil_div(K, 4) * 4;
+  const size_t a_bytes = align_up(static_cast<size_t>(M) * ldk * 4);
+  const size_t b_bytes = align_up(static_cast<size_t>(N) * ldk * 4);
+  if (ws_bytes < 2 * a_bytes + 2 * b_bytes) return LCE_ERR_WORKSPACE;
+  int st = check_device();
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* parts[4] = {reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + a_bytes),
+                     reinterpret_cast<float*>(ws + 2 * a_bytes), reinterpret_cast<float*>(ws + 2 * a_bytes + b_bytes)};
+  // K-major parts: an MN-major operand ([K, rows] in memory) goes through the transposing split
+  for (int op = 0; op < 2; ++op) {
+    const bool mn = op == 0 ? a_mn_major != 0 : b_mn_major != 0;
+    const int64_t rows = op == 0 ? M : N;
+    SplitArgs sa;
+    sa.src = op == 0 ? A : B;
+    sa.rows = mn ? K : rows;
+    sa.cols = mn ? rows : K;
+    sa.lds = sa.cols;
+    sa.hi = mn ? nullptr : parts[2 * op];
+    sa.lo = mn ? nullptr : parts[2 * op + 1];
+    sa.ldo = ldk;
+    sa.hiT = mn ? parts[2 * op] : nullptr;
+    sa.loT = mn ? parts[2 * op + 1] : nullptr;
+    sa.ldt = ldk;
+    if (launch_split_tf32(sa, s) != cudaSuccess) return LCE_ERR_CUDA;
+  }
+  TxOperands o;
+  bool ok = encode_tmap_f32(&o.ah, parts[0], K, M, ldk, 128) && encode_tmap_f32(&o.al, parts[1], K, M, ldk, 128) &&
+            encode_tmap_f32(&o.bh, parts[2], K, N, ldk, 128) && encode_tmap_f32(&o.bl, parts[3], K, N, ldk, 128);
+  if (!ok) return LCE_ERR_CUDA;
+  EpiStore::Params es;
+  es.out = out;
+  es.out_dt = LCE_F32;
+  es.row_scale = nullptr;
+  es.scalar_scale = nullptr;
+  es.ldo = N;
+  es.acc32 = nullptr;
+  es.mode = 0;
+  es.rows = M;
+  es.cols = N;
+  es.vec_ok = aligned16(out) && (N % 4) == 0;
+  return from_cuda(launch_tx_store(TC_TEST_KK, o, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                                   dev_status, es, s, k_splits));
 }
 
 int lce_test_gemm_f32(const float* A, const float* B, float* out, int64_t M, int64_t N, int64_t K, int a_mn_major,

@@ -30,6 +30,10 @@ enum KernelId {
   K_CE_STREAM,
   K_GEMM_TEST,
   K_ROW_SCALE,
+  K_GEMM_LOGITS_TX,
+  K_GEMM_DX_TX,
+  K_GEMM_DW_TX,
+  K_SPLIT_TF32,
   K_NUM_IDS
 };
 const char* kernel_id_name(int id);
@@ -65,6 +69,43 @@ bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64
                             int dt = LCE_BF16);
 // Whether the fused path uses the CTA-pair GEMM (default yes; LCE_TC_PAIR=0 selects the one-CTA kernel).
 bool tc_pair_default();
+
+// ---- fp32 GEMM on the tensor cores by three TF32 products (gemm_tf32.cu)
+// Encodes a 2-D fp32 tensor map over a row-major matrix (rows x inner, row
+// pitch ld elements, ld * 4 a multiple of 16 bytes), box {32, box_rows},
+// 128B swizzle.
+bool encode_tmap_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
+                     uint32_t box_rows);
+// Operands as hi / lo pairs of tensor maps (box rows 128), all K-major:
+// A [M, K], B [N, K]. op: TC_LOGITS (EpiLse), TC_DX or TC_DW (EpiStore);
+// TC_DX with an fp32 mode-0 output and few tiles splits K over work items
+// that add into the output after zeroing it; TC_TEST_KK does the same with
+// test_splits work items per tile when test_splits > 1 (fp32 mode-0 output).
+struct TxOperands {
+  CUtensorMap ah, al, bh, bl;
+};
+cudaError_t launch_tx_logits(const TxOperands& o, int M, int N, int K, int* status, const EpiLse::Params& ep,
+                             cudaStream_t s);
+cudaError_t launch_tx_store(int op, const TxOperands& o, int M, int N, int K, int* status,
+                            const EpiStore::Params& ep, cudaStream_t s, int test_splits = 0);
+// Splits an fp32 matrix src [rows, cols] (pitch lds) into TF32 hi / lo parts:
+// hi[r, c] = x rounded to TF32, lo[r, c] = (x - hi) rounded to TF32, written
+// row-major (hi / lo, pitch ldo; hi may be src itself with ldo == lds) and /
+// or transposed (hiT / loT [cols, rows], pitch ldt). A NULL pair is skipped.
+struct SplitArgs {
+  const float* src;
+  int64_t rows, cols, lds;
+  float* hi;
+  float* lo;
+  int64_t ldo;
+  float* hiT;
+  float* loT;
+  int64_t ldt;
+};
+cudaError_t launch_split_tf32(const SplitArgs& a, cudaStream_t s);
+// Whether fp32 inputs take the 3xTF32 tensor-core path (default) or the
+// SIMT fp32 GEMM (LCE_F32_SIMT=1).
+bool f32_tensor_default();
 
 // ---- SIMT fp32 GEMM (gemm_simt.cu); op as TcOp (LOGITS: A K-major, B
 // K-major; DX: A K-major, B N-major; DW: A M-major, B N-major).

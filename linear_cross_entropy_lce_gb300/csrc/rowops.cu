@@ -246,13 +246,15 @@ cudaError_t launch_grad_logits(const GradArgs& a, int dt, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;
   const int64_t gy = (a.rows + 63) / 64;
   if (gy > 65535) return cudaErrorInvalidValue;
-  if (a.segw != (bf16 ? 256 : 64)) return cudaErrorInvalidValue;
+  if (bf16 ? a.segw != 256 : (a.segw != 64 && a.segw != 256)) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(a.nseg), static_cast<unsigned>(gy));
   prof_before(K_GRAD_LOGITS, s, 2.0 * (bf16 ? 2 : 4) * a.rows * static_cast<double>(a.ld));  // 16-bit or fp32
   if (dt == LCE_F16)
     grad_logits_kernel<__half, 256><<<grid, 256, 0, s>>>(a);
   else if (dt == LCE_BF16)
     grad_logits_kernel<__nv_bfloat16, 256><<<grid, 256, 0, s>>>(a);
+  else if (a.segw == 256)  // fp32 on the tensor cores: 256-column segments
+    grad_logits_kernel<float, 256><<<grid, 256, 0, s>>>(a);
   else
     grad_logits_kernel<float, 64><<<grid, 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();

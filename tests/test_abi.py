@@ -115,6 +115,11 @@ def test_host_argument_errors(lib):
     assert lib.lce_read_device_status(None, None) == 1
     assert lib.lce_test_gemm_bf16(FAKE, FAKE, FAKE, 8, 8, 12, 0, 0, 0, None, None) == 9
     assert lib.lce_test_gemm_bf16(None, FAKE, FAKE, 8, 8, 8, 0, 0, 1, None, None) == 1
+    tx = lib.lce_test_gemm_tf32x3
+    assert tx(FAKE, FAKE, FAKE, 8, 8, 8, 0, 0, 1, None, 1 << 20, None, None) == 1
+    assert tx(FAKE, FAKE, FAKE, 0, 8, 8, 0, 0, 1, FAKE, 1 << 20, None, None) == 2
+    assert tx(FAKE, FAKE, FAKE, 8, 8, 8, 0, 0, 1, ctypes.c_void_p(4100), 1 << 20, None, None) == 9
+    assert tx(FAKE, FAKE, FAKE, 8, 8, 8, 0, 0, 1, FAKE, 1000, None, None) == 6
 
 
 def test_profile_api_without_launches(lib):

@@ -1,6 +1,6 @@
-"""The two GEMM engines on their own: tcgen05 (bf16, TMA + tensor memory) and
-SIMT (fp32), in the four operand layouts, against a float64 matmul of the
-same values."""
+"""The GEMM engines on their own: tcgen05 (bf16, TMA + tensor memory),
+3xTF32 on the tensor cores (fp32) and SIMT (fp32), in the four operand
+layouts, against a float64 matmul of the same values."""
 
 import numpy as np
 import pytest
@@ -46,3 +46,29 @@ def test_simt_gemm(cuda_lib, a_mn, b_mn, M, N, K):
     out = cuda_lib.test_gemm_f32(A, B, M, N, K, a_mn, b_mn)
     torch.cuda.synchronize()
     assert rel_max(out.double().cpu().numpy(), ref) < 1e-5
+
+
+@pytest.mark.parametrize("a_mn,b_mn", LAYOUTS)
+@pytest.mark.parametrize("M,N,K,splits", [(256, 256, 32, 1), (300, 517, 203, 1), (7, 3, 5, 1),
+                                          (1000, 600, 3000, 1), (520, 260, 4100, 5)])
+def test_tf32x3_gemm(cuda_lib, a_mn, b_mn, M, N, K, splits):
+    """Three TF32 products reach fp32 accuracy: the error bound of the split
+    (about 2^-21 of |A||B| per product) keeps the result within 1e-5 of the
+    float64 matmul relative to its largest entry."""
+    A, B, ref = _operands(M, N, K, a_mn, b_mn, torch.float32, 17 + M + N + K)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = cuda_lib.test_gemm_tf32x3(A, B, M, N, K, a_mn, b_mn, k_splits=splits, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert rel_max(out.double().cpu().numpy(), ref) < 1e-5
+
+
+def test_tf32x3_beats_one_tf32_product(cuda_lib):
+    """The lo parts matter: with them the error is far below what a single
+    TF32 product (about 2^-11 relative per element) would give."""
+    M, N, K = 512, 512, 1024
+    A, B, ref = _operands(M, N, K, 0, 0, torch.float32, 99)
+    out = cuda_lib.test_gemm_tf32x3(A, B, M, N, K, 0, 0)
+    torch.cuda.synchronize()
+    err = np.abs(out.double().cpu().numpy() - ref).max() / np.abs(ref).max()
+    assert err < 2e-6
