@@ -244,6 +244,12 @@ struct EpiStore {
       if (!row_ok) continue;
       const int64_t cb = col0 + 32 * c;
       const int64_t base = row * p.ldo + cb;
+      if (p.vec_ok && cb + 32 <= p.cols && p.mode == 4) {  // split-K partial: 8 vector reductions
+        float* o = static_cast<float*>(p.out) + base;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) red_add_v4(o + 4 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        continue;
+      }
       if (p.vec_ok && cb + 32 <= p.cols && p.mode != 4) {
         if (p.mode == 0 && p.out_dt != LCE_F32) {
           store32_16bit(static_cast<uint16_t*>(p.out) + base, v, p.out_dt);

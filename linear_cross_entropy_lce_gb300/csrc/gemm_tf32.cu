@@ -23,43 +23,90 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
   }
 }
 
-// One 32 x 32 tile of src per iteration, 256 threads (8 rows of 32 lanes,
-// 4 rows each); the transposed outputs go through shared memory so both the
-// reads and the writes are coalesced.
-__global__ void __launch_bounds__(256) split_tf32_kernel(const SplitArgs a) {
-  __shared__ float th[32][33];
-  __shared__ float tl[32][33];
-  const int tx = threadIdx.x & 31;
-  const int ty = threadIdx.x >> 5;
-  const int64_t tiles_c = (a.cols + 31) / 32;
-  const int64_t ntiles = ((a.rows + 31) / 32) * tiles_c;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const int64_t r0 = (t / tiles_c) * 32;
-    const int64_t c0 = (t % tiles_c) * 32;
-    const int64_t c = c0 + tx;
+// One 64 x 64 tile of src per iteration, 256 threads. Reads and row-major
+// writes move float4s (16 threads per 64-float row segment) when the row
+// pitches and base pointers allow it; the transposed outputs go through
+// shared memory and are written as float4 runs along their rows, so every
+// global access is coalesced. Scalar code covers ragged tile edges.
+constexpr int SP_T = 64;
+__global__ void __launch_bounds__(256) split_tf32_kernel(const SplitArgs a, int vec_in, int vec_t) {
+  __shared__ float th[SP_T][SP_T + 1];
+  __shared__ float tl[SP_T][SP_T + 1];
+  const int t = threadIdx.x;
+  const int64_t tiles_c = (a.cols + SP_T - 1) / SP_T;
+  const int64_t ntiles = ((a.rows + SP_T - 1) / SP_T) * tiles_c;
+  const int cq = (t & 15) * 4;  // column of this thread's float4 within the tile
+  const int rq = t >> 4;        // first row (of 16) within the tile
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t r0 = (tile / tiles_c) * SP_T;
+    const int64_t c0 = (tile % tiles_c) * SP_T;
+    const bool full_c = vec_in && c0 + cq + 4 <= a.cols;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int64_t r = r0 + ty + 8 * k;
-      float hi = 0.0f, lo = 0.0f;
-      if (r < a.rows && c < a.cols) {
-        split_tf32(a.src[r * a.lds + c], hi, lo);
-        if (a.hi != nullptr) {
-          a.hi[r * a.ldo + c] = hi;
-          a.lo[r * a.ldo + c] = lo;
+      const int lr = rq + 16 * k;
+      const int64_t r = r0 + lr;
+      float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (r < a.rows) {
+        if (full_c) {
+          const float4 v = *reinterpret_cast<const float4*>(a.src + r * a.lds + c0 + cq);
+          x[0] = v.x;
+          x[1] = v.y;
+          x[2] = v.z;
+          x[3] = v.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (c0 + cq + e < a.cols) x[e] = a.src[r * a.lds + c0 + cq + e];
         }
       }
-      th[ty + 8 * k][tx] = hi;
-      tl[ty + 8 * k][tx] = lo;
+      float h[4], l[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split_tf32(x[e], h[e], l[e]);
+      if (a.hi != nullptr && r < a.rows) {
+        if (full_c) {
+          *reinterpret_cast<float4*>(a.hi + r * a.ldo + c0 + cq) = make_float4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<float4*>(a.lo + r * a.ldo + c0 + cq) = make_float4(l[0], l[1], l[2], l[3]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (c0 + cq + e < a.cols) {
+              a.hi[r * a.ldo + c0 + cq + e] = h[e];
+              a.lo[r * a.ldo + c0 + cq + e] = l[e];
+            }
+          }
+        }
+      }
+      if (a.hiT != nullptr) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          th[lr][cq + e] = h[e];
+          tl[lr][cq + e] = l[e];
+        }
+      }
     }
     if (a.hiT != nullptr) {
       __syncthreads();
+      // transposed: output row cc (a column of src) holds the tile's 64 rows
+      const int j = (t & 15) * 4;  // first src row of this thread's float4
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int64_t cc = c0 + ty + 8 * k;  // row of the transposed outputs
-        const int64_t rr = r0 + tx;
-        if (cc < a.cols && rr < a.rows) {
-          a.hiT[cc * a.ldt + rr] = th[tx][ty + 8 * k];
-          a.loT[cc * a.ldt + rr] = tl[tx][ty + 8 * k];
+      for (int p = 0; p < 4; ++p) {
+        const int lc = (t >> 4) + 16 * p;
+        const int64_t cc = c0 + lc;
+        if (cc >= a.cols) continue;
+        const int64_t rr = r0 + j;
+        float* dh = a.hiT + cc * a.ldt + rr;
+        float* dl = a.loT + cc * a.ldt + rr;
+        if (vec_t && rr + 4 <= a.rows) {
+          *reinterpret_cast<float4*>(dh) = make_float4(th[j][lc], th[j + 1][lc], th[j + 2][lc], th[j + 3][lc]);
+          *reinterpret_cast<float4*>(dl) = make_float4(tl[j][lc], tl[j + 1][lc], tl[j + 2][lc], tl[j + 3][lc]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (rr + e < a.rows) {
+              dh[e] = th[j + e][lc];
+              dl[e] = tl[j + e][lc];
+            }
+          }
         }
       }
     }
@@ -126,12 +173,16 @@ bool f32_tensor_default() {
 
 cudaError_t launch_split_tf32(const SplitArgs& a, cudaStream_t s) {
   if (a.rows == 0 || a.cols == 0) return cudaSuccess;
-  const int64_t ntiles = ((a.rows + 31) / 32) * ((a.cols + 31) / 32);
-  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  const int vec_in = (a.lds % 4 == 0) && al16(a.src) &&
+                     (a.hi == nullptr || ((a.ldo % 4 == 0) && al16(a.hi) && al16(a.lo)));
+  const int vec_t = a.hiT != nullptr && (a.ldt % 4 == 0) && al16(a.hiT) && al16(a.loT);
+  const int64_t ntiles = ((a.rows + SP_T - 1) / SP_T) * ((a.cols + SP_T - 1) / SP_T);
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 6;
   const int grid = static_cast<int>(ntiles < cap ? ntiles : cap);
   const double outs = (a.hi != nullptr ? 2.0 : 0.0) + (a.hiT != nullptr ? 2.0 : 0.0);
   prof_before(K_SPLIT_TF32, s, 4.0 * (1.0 + outs) * a.rows * static_cast<double>(a.cols));
-  split_tf32_kernel<<<grid, 256, 0, s>>>(a);
+  split_tf32_kernel<<<grid, 256, 0, s>>>(a, vec_in, vec_t);
   cudaError_t e = cudaGetLastError();
   prof_after(K_SPLIT_TF32, s);
   return e;
@@ -148,12 +199,18 @@ cudaError_t launch_tx_store(int op, const TxOperands& o, int M, int N, int K, in
     // few output tiles and a long K (= C): split K so that every SM pair has
     // work; the splits add into the zeroed fp32 output (mode 4)
     const int64_t tiles = static_cast<int64_t>((M + 255) / 256) * ((N + 255) / 256);
-    const int pairs = num_sms() / 2;
+    const int64_t pairs = num_sms() / 2;
     if (ep.mode == 0 && ep.out_dt == LCE_F32 && ep.row_scale == nullptr && ep.scalar_scale == nullptr &&
         tiles < pairs && K >= 1024) {
-      int64_t splits = (pairs + tiles - 1) / tiles;
-      if (splits > 16) splits = 16;
-      if (splits > K / 512) splits = K / 512;
+      // cost of a split count: K blocks on the busiest pair (waves x K
+      // blocks per work item); take the fewest splits (fewest output
+      // atomics) within 10 % of the best, at most 16, >= 16 K blocks each
+      const int64_t nkb = (K + TX_BK - 1) / TX_BK;
+      auto cost = [&](int64_t sp) { return ((tiles * sp + pairs - 1) / pairs) * ((nkb + sp - 1) / sp); };
+      int64_t best = nkb;
+      for (int64_t sp = 2; sp <= 16 && nkb / sp >= 16; ++sp) best = cost(sp) < best ? cost(sp) : best;
+      int64_t splits = 1;
+      while (cost(splits) * 10 > best * 11) ++splits;
       if (splits > 1) {
         EpiStore::Params e2 = ep;
         e2.mode = 4;

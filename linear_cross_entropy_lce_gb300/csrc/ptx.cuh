@@ -415,3 +415,12 @@ __device__ __forceinline__ void tmem_ld64x2(uint32_t ta, uint32_t tb, float (&a)
   }
 }
 }  // namespace lce
+
+namespace lce {
+// Four fp32 additions to 16-byte aligned global memory in one reduction
+// operation (no return value).
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+}  // namespace lce

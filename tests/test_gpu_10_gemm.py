@@ -64,11 +64,12 @@ def test_tf32x3_gemm(cuda_lib, a_mn, b_mn, M, N, K, splits):
 
 
 def test_tf32x3_beats_one_tf32_product(cuda_lib):
-    """The lo parts matter: with them the error is far below what a single
-    TF32 product (about 2^-11 relative per element) would give."""
+    """The lo parts matter: a single TF32 product per element (relative
+    error about 2^-11 each) leaves about 1e-4 of the largest entry at this
+    K; the three products with folded partial sums stay below 1e-5."""
     M, N, K = 512, 512, 1024
     A, B, ref = _operands(M, N, K, 0, 0, torch.float32, 99)
     out = cuda_lib.test_gemm_tf32x3(A, B, M, N, K, 0, 0)
     torch.cuda.synchronize()
     err = np.abs(out.double().cpu().numpy() - ref).max() / np.abs(ref).max()
-    assert err < 2e-6
+    assert err < 1e-5
