@@ -41,9 +41,6 @@ METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor
 MEASURED_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the full-size
     # step (row-slab build), per launch; see profiles/tc2_gemm_bf16_llm_head_traffic.md
-    ("bf16_llm_head", "gemm_logits_tc"): (6262746112 + 3627991296) / 4,  # mean of the 4 slab launches
-    ("bf16_llm_head", "gemm_dx_tc"): 16404365312 + 62007296,
-    ("bf16_llm_head", "gemm_dw_tc"): 10727093248 + 1043881728,
     ("bf16_llm_head", "grad_logits"): 533614848 + 460472064,
 }
 

@@ -1,10 +1,11 @@
 // epilogues.cuh -- per-row epilogues shared by the tcgen05 and the SIMT GEMMs.
 //
 // Both GEMMs hand each epilogue thread one output row of a tile segment of
-// NCHUNK*32 columns starting at col0; load(c, v) fills v with the fp32
-// accumulators of columns [col0 + 32c, col0 + 32c + 32) of that row. The
-// loads must be called by every lane of a warp in the same order (the
-// tcgen05 loads are warp-collective), so row validity only guards stores.
+// NCHUNK*32 columns starting at col0, read in groups of GW chunks:
+// load(g, v) fills v[GW*32] with the fp32 accumulators of columns
+// [col0 + 32 GW g, col0 + 32 GW (g + 1)) of that row. The loads must be
+// called by every lane of a warp in the same order (the tcgen05 loads are
+// warp-collective), so row validity only guards stores.
 // Element types are the lce_dtype_e codes: 0 fp32, 1 bf16, 2 fp16.
 #pragma once
 
@@ -130,47 +131,77 @@ struct EpiLse {
     return load_elem(p.bias, col, p.bias_dt);
   }
 
-  template <int NCHUNK, class Loader>
+  // NCHUNK 32-column chunks, read GW chunks at a time: load(g, v) fills
+  // v[GW * 32] with columns [col0 + 32 GW g, col0 + 32 GW (g + 1)).
+  template <int NCHUNK, int GW, class Loader>
   __device__ static __forceinline__ void run(const Params& p, int64_t row, int64_t col0, int64_t seg,
                                              Loader&& load, EpiIO& io) {
+    static_assert(NCHUNK % GW == 0, "chunk groups");
+    constexpr int NG = NCHUNK / GW;
+    constexpr int W = GW * 32;
     const bool row_ok = row < p.rows;
     const int64_t t = row_ok ? p.target[row] : -1;
     const int tl = (t >= col0 && t < col0 + NCHUNK * 32 && t < p.C) ? static_cast<int>(t - col0) : -1;
-    float v[32];
+    // no bias and no padding column: the common case, without per-column tests
+    const bool plain = p.bias == nullptr && col0 + NCHUNK * 32 <= p.C;
+    float v[W];
     // pass 1: segment max
     float m = -INFINITY;
 #pragma unroll 1
-    for (int c = 0; c < NCHUNK; ++c) {
-      load(c, v);
+    for (int g = 0; g < NG; ++g) {
+      load(g, v);
+      if (plain) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int64_t col = col0 + 32 * c + i;
-        const float z = v[i] + bias_at(p, col);
-        m = (col < p.C) ? fmaxf(m, z) : m;
+        for (int i = 0; i < W; ++i) m = fmaxf(m, v[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+          const int64_t col = col0 + W * g + i;
+          const float z = v[i] + bias_at(p, col);
+          m = (col < p.C) ? fmaxf(m, z) : m;
+        }
       }
     }
     // pass 2: sum of exp(z - m), target logit, optional P~ store
     float s = 0.0f, ztv = 0.0f;
 #pragma unroll 1
-    for (int c = 0; c < NCHUNK; ++c) {
-      load(c, v);
+    for (int g = 0; g < NG; ++g) {
+      load(g, v);
+      if (!plain) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int64_t col = col0 + 32 * c + i;
-        const float z = v[i] + bias_at(p, col);
-        const float e = (col < p.C) ? fast_exp2((z - m) * kLog2e) : 0.0f;
-        ztv = (32 * c + i == tl) ? z : ztv;
-        s += e;
-        v[i] = e;
+        for (int i = 0; i < W; ++i) v[i] += bias_at(p, col0 + W * g + i);
       }
-      if (p.ptilde != nullptr && io.tmap != nullptr) {
-        stage_store_16bit(io, v, col0 + 32 * c, p.ptilde_dt);
-      } else if (p.ptilde != nullptr && row_ok) {
-        const int64_t off = row * p.ld_p + col0 + 32 * c;
-        if (p.ptilde_dt == LCE_F32)
-          store32_f32(static_cast<float*>(p.ptilde) + off, v);
-        else
-          store32_16bit(static_cast<uint16_t*>(p.ptilde) + off, v, p.ptilde_dt);
+      if (tl >= W * g && tl < W * (g + 1)) {  // at most one group of one segment per row
+#pragma unroll
+        for (int i = 0; i < W; ++i) ztv = (W * g + i == tl) ? v[i] : ztv;
+      }
+      if (plain) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+          v[i] = fast_exp2((v[i] - m) * kLog2e);
+          s += v[i];
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+          v[i] = (col0 + W * g + i < p.C) ? fast_exp2((v[i] - m) * kLog2e) : 0.0f;
+          s += v[i];
+        }
+      }
+      if (p.ptilde == nullptr) continue;
+#pragma unroll
+      for (int c = 0; c < GW; ++c) {
+        float(&vc)[32] = *reinterpret_cast<float(*)[32]>(&v[32 * c]);
+        const int64_t cc = col0 + W * g + 32 * c;
+        if (io.tmap != nullptr) {
+          stage_store_16bit(io, vc, cc, p.ptilde_dt);
+        } else if (row_ok) {
+          const int64_t off = row * p.ld_p + cc;
+          if (p.ptilde_dt == LCE_F32)
+            store32_f32(static_cast<float*>(p.ptilde) + off, vc);
+          else
+            store32_16bit(static_cast<uint16_t*>(p.ptilde) + off, vc, p.ptilde_dt);
+        }
       }
     }
     if (row_ok && col0 < p.C) {
@@ -221,58 +252,64 @@ struct EpiStore {
     store_elem(p.out, idx, x, p.out_dt);
   }
 
-  template <int NCHUNK, class Loader>
+  template <int NCHUNK, int GW, class Loader>
   __device__ static __forceinline__ void run(const Params& p, int64_t row, int64_t col0, int64_t /*seg*/,
                                              Loader&& load, EpiIO& io) {
+    static_assert(NCHUNK % GW == 0, "chunk groups");
+    constexpr int W = GW * 32;
     const bool row_ok = row < p.rows;
     float scale = 1.0f;
     if (p.row_scale != nullptr) scale = row_ok ? p.row_scale[row] : 0.0f;
     if (p.scalar_scale != nullptr) scale *= p.scalar_scale[0];
     const bool scaled = p.row_scale != nullptr || p.scalar_scale != nullptr;
-    float v[32];
+    float vg[W];
 #pragma unroll 1
-    for (int c = 0; c < NCHUNK; ++c) {
-      load(c, v);
+    for (int g = 0; g < NCHUNK / GW; ++g) {
+      load(g, vg);
       if (scaled) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= scale;
+        for (int i = 0; i < W; ++i) vg[i] *= scale;
       }
-      if (io.tmap != nullptr) {  // 16-bit, mode 0 (the host only sets tmap then)
-        stage_store_16bit(io, v, col0 + 32 * c, p.out_dt);
-        continue;
-      }
-      if (!row_ok) continue;
-      const int64_t cb = col0 + 32 * c;
-      const int64_t base = row * p.ldo + cb;
-      if (p.vec_ok && cb + 32 <= p.cols && p.mode == 4) {  // split-K partial: 8 vector reductions
-        float* o = static_cast<float*>(p.out) + base;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) red_add_v4(o + 4 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        continue;
-      }
-      if (p.vec_ok && cb + 32 <= p.cols && p.mode != 4) {
-        if (p.mode == 0 && p.out_dt != LCE_F32) {
-          store32_16bit(static_cast<uint16_t*>(p.out) + base, v, p.out_dt);
+      for (int c = 0; c < GW; ++c) {
+        float(&v)[32] = *reinterpret_cast<float(*)[32]>(&vg[32 * c]);
+        const int64_t cb = col0 + W * g + 32 * c;
+        if (io.tmap != nullptr) {  // 16-bit, mode 0 (the host only sets tmap then)
+          stage_store_16bit(io, v, cb, p.out_dt);
           continue;
         }
-        if (p.mode == 0 || p.mode == 1) {
-          store32_f32((p.mode == 1 ? p.acc32 : static_cast<float*>(p.out)) + base, v);
+        if (!row_ok) continue;
+        const int64_t base = row * p.ldo + cb;
+        if (p.vec_ok && cb + 32 <= p.cols && p.mode == 4) {  // split-K partial: 8 vector reductions
+          float* o = static_cast<float*>(p.out) + base;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) red_add_v4(o + 4 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           continue;
         }
-        if (p.mode == 2 || (p.mode == 3 && p.out_dt == LCE_F32)) {
-          float4* a = reinterpret_cast<float4*>(p.acc32 + base);
-          float4* o = reinterpret_cast<float4*>((p.mode == 2 ? p.acc32 : static_cast<float*>(p.out)) + base);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float4 x = a[q];
-            o[q] = make_float4(x.x + v[4 * q], x.y + v[4 * q + 1], x.z + v[4 * q + 2], x.w + v[4 * q + 3]);
+        if (p.vec_ok && cb + 32 <= p.cols && p.mode != 4) {
+          if (p.mode == 0 && p.out_dt != LCE_F32) {
+            store32_16bit(static_cast<uint16_t*>(p.out) + base, v, p.out_dt);
+            continue;
           }
-          continue;
-        }
-      }
+          if (p.mode == 0 || p.mode == 1) {
+            store32_f32((p.mode == 1 ? p.acc32 : static_cast<float*>(p.out)) + base, v);
+            continue;
+          }
+          if (p.mode == 2 || (p.mode == 3 && p.out_dt == LCE_F32)) {
+            float4* a = reinterpret_cast<float4*>(p.acc32 + base);
+            float4* o = reinterpret_cast<float4*>((p.mode == 2 ? p.acc32 : static_cast<float*>(p.out)) + base);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (cb + i < p.cols) put(p, base + i, v[i]);
+            for (int q = 0; q < 8; ++q) {
+              float4 x = a[q];
+              o[q] = make_float4(x.x + v[4 * q], x.y + v[4 * q + 1], x.z + v[4 * q + 2], x.w + v[4 * q + 3]);
+            }
+            continue;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (cb + i < p.cols) put(p, base + i, v[i]);
+        }
       }
     }
   }

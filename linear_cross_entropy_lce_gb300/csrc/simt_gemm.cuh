@@ -135,11 +135,11 @@ __global__ void __launch_bounds__(SG_THREADS)
   const int r = tid >> 1, half = tid & 1;
   const int64_t col0 = n0 + half * SG_SEG;
   EpiIO io{nullptr, nullptr, 0, static_cast<int>(threadIdx.x & 31), 0};
-  Epi::template run<SG_SEG / 32>(
+  Epi::template run<SG_SEG / 32, SG_SEG / 32>(
       ep, m0 + r, col0, col0 / SG_SEG,
-      [&](int c, float (&v)[32]) {
+      [&](int, float (&v)[SG_SEG]) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = Ct[r * SG_CT_LD + half * SG_SEG + c * 32 + i];
+        for (int i = 0; i < SG_SEG; ++i) v[i] = Ct[r * SG_CT_LD + half * SG_SEG + i];
       },
       io);
 }

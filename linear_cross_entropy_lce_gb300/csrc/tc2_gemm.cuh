@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
       const int64_t col0 = static_cast<int64_t>(nb) * TC2_TILE_N;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TC2_TILE_N;
       io.row_base = static_cast<int64_t>(mb) * TC2_TILE_M + rank * 128 + q * 32;
-      Epi::template run<TC2_TILE_N / 32>(
-          ep, row, col0, nb, [&](int c, float (&v)[32]) { tmem_ld32(taddr + c * 32, v); }, io);
+      Epi::template run<TC2_TILE_N / 32, 4>(
+          ep, row, col0, nb, [&](int g, float (&v)[128]) { tmem_ld128(taddr + g * 128, v); }, io);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_u32(&tempty[acc], 0));

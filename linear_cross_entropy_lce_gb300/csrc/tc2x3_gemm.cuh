@@ -238,8 +238,8 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
       if (!ok) break;
       const int64_t row = static_cast<int64_t>(mb) * 256 + rank * 128 + qw * 32 + lane;
       const int64_t col0 = static_cast<int64_t>(nb) * 256;
-      Epi::template run<8>(
-          ep, row, col0, nb, [&](int c, float (&v)[32]) { tmem_ld32(tR + c * 32, v); }, io);
+      Epi::template run<8, 4>(
+          ep, row, col0, nb, [&](int g, float (&v)[128]) { tmem_ld128(tR + g * 128, v); }, io);
     }
   }
 

@@ -198,8 +198,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int64_t col0 = static_cast<int64_t>(nb) * TC_BN;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TC_BN;
       EpiIO io{nullptr, nullptr, 0, lane, 0};
-      Epi::template run<TC_BN / 32>(ep, row, col0, nb,
-                                    [&](int c, float (&v)[32]) { tmem_ld32(taddr + c * 32, v); }, io);
+      Epi::template run<TC_BN / 32, 4>(
+          ep, row, col0, nb, [&](int g, float (&v)[128]) { tmem_ld128(taddr + g * 128, v); }, io);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
