@@ -367,8 +367,9 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
     const bool slabbed = p.tc && pair && backward && rows >= 1024;
     const int64_t slab = slabbed ? ceil_div(ceil_div(rows, 4), 256) * 256 : rows;
     const int64_t nslab = ceil_div(rows, slab);
-    GradArgs ga_prev;
-    bool have_prev = false;
+    GradArgs ga_prev, ga_last;
+    bool have_prev = false, have_last = false;
+    int64_t last_row0 = 0;
     for (int64_t si = 0; si < nslab; ++si) {
       const int64_t so = si * slab;                      // slab offset within the chunk
       const int64_t sr = std::min(slab, rows - so);      // rows in the slab
@@ -394,6 +395,9 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
         SideGrad side;
         side.a = ga_prev;
         side.enabled = have_prev ? 1 : 0;
+        side.claim = nullptr;
+        side.done = nullptr;
+        side.dep_row0 = 0;
         LCE_TRY(launch_tc_logits(tmX_k, tmW_k, tma_out ? &tmL : nullptr, static_cast<int>(sr), static_cast<int>(C),
                                  static_cast<int>(D), &hdr->status, el, pair, s, have_prev ? &side : nullptr, f16));
       } else if (p.tf32) {
@@ -443,6 +447,10 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       if (slabbed && si + 1 < nslab) {
         ga_prev = ga;  // formed by the next slab's GEMM
         have_prev = true;
+      } else if (slabbed && want_dx) {
+        ga_last = ga;  // formed by the dX GEMM's idle warps before it reads these rows
+        have_last = true;
+        last_row0 = so;
       } else {
         LCE_TRY(launch_grad_logits(ga, dtype, s));
         have_prev = false;
@@ -481,8 +489,18 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
         if (!encode_tmap_bf16(&tmG_k, Lbuf, C, rows, p.C_pad, TC_BM, dtype)) return LCE_ERR_CUDA;
         const bool tma_out = pair && es.out_dt != LCE_F32 && es.vec_ok;
         if (tma_out && !encode_tmap_bf16_store(&tmdX, es.out, D, rows, D, grad_dtype)) return LCE_ERR_CUDA;
+        SideGrad side;
+        if (have_last) {
+          LCE_TRY(cudaMemsetAsync(&hdr->side_claim, 0, 2 * sizeof(int), s));
+          side.a = ga_last;
+          side.enabled = 1;
+          side.claim = &hdr->side_claim;
+          side.done = &hdr->side_done;
+          side.dep_row0 = last_row0;
+        }
         LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmW_n, tma_out ? &tmdX : nullptr, static_cast<int>(rows),
-                                static_cast<int>(D), static_cast<int>(C), &hdr->status, es, pair, s, f16));
+                                static_cast<int>(D), static_cast<int>(C), &hdr->status, es, pair, s, f16,
+                                have_last ? &side : nullptr));
       } else if (p.tf32) {
         if (!encode_tmap_f32(&tx_dx.ah, Lbuf, C, rows, p.C_pad, 128) ||
             !encode_tmap_f32(&tx_dx.al, wsf(p.off_gl), C, rows, p.C_pad, 128))

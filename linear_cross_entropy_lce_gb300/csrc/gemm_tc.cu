@@ -176,11 +176,13 @@ cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, con
 
 cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M,
                             int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s,
-                            bool f16) {
+                            bool f16, const SideGrad* side) {
+  if (side != nullptr && !(op == TC_DX && (pair || f16))) return cudaErrorInvalidValue;
   if (f16) {  // fp16 operands: CTA-pair kernel only
     switch (op) {
       case TC_DX:
-        return launch_tc2<false, true, EpiStore, true>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DX_TC, s);
+        return launch_tc2<false, true, EpiStore, true>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DX_TC, s,
+                                                       side);
       case TC_DW:
         return launch_tc2<true, true, EpiStore, true>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DW_TC, s);
       default:
@@ -190,7 +192,7 @@ cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& t
   if (pair) {
     switch (op) {
       case TC_DX:
-        return launch_tc2<false, true, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DX_TC, s);
+        return launch_tc2<false, true, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DX_TC, s, side);
       case TC_DW:
         return launch_tc2<true, true, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DW_TC, s);
       case TC_TEST_KK:

@@ -62,9 +62,11 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
 cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
                              int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s,
                              const SideGrad* side = nullptr, bool f16 = false);
+// side (TC_DX on the pair kernel only): G formation run in the GEMM's idle
+// warps, in the dynamic form of SideGrad.
 cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M,
                             int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s,
-                            bool f16 = false);
+                            bool f16 = false, const SideGrad* side = nullptr);
 bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64_t rows, uint64_t ld,
                             int dt = LCE_BF16);
 // Whether the fused path uses the CTA-pair GEMM (default yes; LCE_TC_PAIR=0 selects the one-CTA kernel).
@@ -159,6 +161,13 @@ cudaError_t launch_grad_logits(const GradArgs& a, int dt, cudaStream_t s);
 struct SideGrad {
   GradArgs a;
   int enabled;
+  // Dynamic form (the dX GEMM): units are claimed from *claim and counted in
+  // *done once their G is stored; the GEMM's producer loads A rows
+  // [dep_row0, dep_row0 + a.rows) only after *done reaches the unit count.
+  // claim == NULL: units are taken by block index, with no dependency.
+  int* claim;
+  int* done;
+  int64_t dep_row0;
 };
 // fp16 backward: wbar = max_r |w_r| over the chunk rows (NaN if any w_r is
 // NaN), then Xs[r, :] = (w_r / wbar) X[r, :] in fp16 (0 when wbar is 0).

@@ -465,3 +465,15 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
 }  // namespace lce
+
+namespace lce {
+// Acquire load of a global int at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Orders this thread's generic-proxy memory accesses with its async-proxy
+// (TMA) accesses, in every state space.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+}  // namespace lce

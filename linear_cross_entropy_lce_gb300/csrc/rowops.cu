@@ -64,56 +64,93 @@ __global__ void prep_kernel(const int64_t* __restrict__ target, int64_t N, int64
   }
 }
 
-// One warp per chunk row: the lanes merge the row's per-segment (max,
-// sum-exp) pairs into lse = M + log sum_s s_s exp(m_s - M), then
-// loss_n = lse - z_t (0 on ignored rows). For the backward each pair becomes
-// the scale w_n exp(m_s - lse) that maps the stored P~ to G, and G at the
-// target column is w_n (softmax_t - 1) from the fp32 target logit (expm1
-// keeps it accurate when softmax_t ~ 1).
+// Merge of a row's per-segment (max, sum-exp) pairs into lse = M + log
+// sum_s s_s exp(m_s - M), then loss_n = lse - z_t (0 on ignored rows). For
+// the backward each pair becomes the scale w_n exp(m_s - lse) that maps the
+// stored P~ to G, and G at the target column is w_n (softmax_t - 1) from
+// the fp32 target logit (expm1 keeps it accurate when softmax_t ~ 1).
+//
+// A block holds 32 consecutive rows x COMBINE_SL segment lanes: the 32
+// threads of a warp take the same segment of 32 rows, so every access to
+// the [segment][row] partials is one coalesced 256-byte row of the array.
+// Lane sl merges segments sl, sl + COMBINE_SL, ...; the lanes' pairs meet
+// in shared memory.
 __device__ __forceinline__ void merge_pair(float& M, float& S, float m2, float s2) {
-  const float Mn = fmaxf(M, m2);
-  const float a = (M == -INFINITY) ? 0.0f : S * expf(M - Mn);
-  const float b = (m2 == -INFINITY) ? 0.0f : s2 * expf(m2 - Mn);
-  M = Mn;
-  S = a + b;
+  if (m2 == -INFINITY) return;  // an empty pair (also covers M == m2 == -inf)
+  if (m2 > M) {
+    S = (M == -INFINITY ? 0.0f : S * expf(M - m2)) + s2;
+    M = m2;
+  } else {
+    S += s2 * expf(m2 - M);
+  }
 }
 
-__global__ void combine_kernel(const CombineArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
-  if (r >= a.rows) return;  // warp-uniform
+constexpr int COMBINE_SL = 32;
+
+__global__ void __launch_bounds__(32 * COMBINE_SL) combine_kernel(const CombineArgs a) {
+  __shared__ float sM[COMBINE_SL][33];
+  __shared__ float sS[COMBINE_SL][33];
+  __shared__ float sLse[32];
+  __shared__ float sW[32];
+  const int rl = threadIdx.x & 31;
+  const int sl = threadIdx.x >> 5;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 32 + rl;
+  const bool in = r < a.rows;
   float M = -INFINITY, S = 0.0f;
-  for (int s = lane; s < a.nseg; s += 32) {
-    const float2 p = a.partial[s * a.ld + r];
-    merge_pair(M, S, p.x, p.y);
-  }
+  if (in) {
+    // 8 independent loads in flight per batch instead of one dependent chain
+    for (int s0 = sl; s0 < a.nseg; s0 += 8 * COMBINE_SL) {
+      float2 p[8];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-    merge_pair(M, S, m2, s2);
+      for (int k = 0; k < 8; ++k) {
+        const int s = s0 + k * COMBINE_SL;
+        p[k] = s < a.nseg ? a.partial[s * a.ld + r] : make_float2(-INFINITY, 0.0f);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) merge_pair(M, S, p[k].x, p[k].y);
+    }
   }
-  const float lse = M + logf(S);
-  const int64_t g = a.row0 + r;
-  const int64_t t = a.target[g];
-  const bool valid = target_valid(t, a.ignore_index, a.C);
-  const float zt = valid ? a.zt[r] : 0.0f;
-  if (lane == 0) {
+  sM[sl][rl] = M;
+  sS[sl][rl] = S;
+  __syncthreads();
+  if (sl == 0 && in) {
+#pragma unroll 1
+    for (int k = 1; k < COMBINE_SL; ++k) merge_pair(M, S, sM[k][rl], sS[k][rl]);
+    const float lse = M + logf(S);
+    const int64_t g = a.row0 + r;
+    const int64_t t = a.target[g];
+    const bool valid = target_valid(t, a.ignore_index, a.C);
+    const float zt = valid ? a.zt[r] : 0.0f;
     a.loss_rows[g] = valid ? class_w(a.rw, t, true) * (lse - zt) : 0.0f;
     if (a.lse_out != nullptr) a.lse_out[g] = lse;
-  }
-  if (a.backward) {
-    const float w = row_weight(a.rw, a.hdr, g, t, valid);
-    // with wrow the stored G leaves w_n out: unit weight on valid rows, 0 on the others
-    const float ws = a.wrow != nullptr ? (valid ? 1.0f : 0.0f) : w;
-    for (int s = lane; s < a.nseg; s += 32) {
-      float2* p = &a.partial[s * a.ld + r];
-      p->x = ws * expf(p->x - lse);
-    }
-    if (lane == 0) {
+    if (a.backward) {
+      const float w = row_weight(a.rw, a.hdr, g, t, valid);
+      // with wrow the stored G leaves w_n out: unit weight on valid rows, 0 on the others
+      const float ws = a.wrow != nullptr ? (valid ? 1.0f : 0.0f) : w;
       a.tcol[r] = valid ? static_cast<int>(t) : -1;
       a.gt[r] = valid ? ws * expm1f(zt - lse) : 0.0f;
       if (a.wrow != nullptr) a.wrow[r] = w;
+      sLse[rl] = lse;
+      sW[rl] = ws;
+    }
+  }
+  if (!a.backward) return;  // uniform over the grid
+  __syncthreads();
+  if (in) {
+    const float lse = sLse[rl];
+    const float ws = sW[rl];
+    for (int s0 = sl; s0 < a.nseg; s0 += 8 * COMBINE_SL) {
+      float m[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int s = s0 + k * COMBINE_SL;
+        m[k] = s < a.nseg ? a.partial[s * a.ld + r].x : 0.0f;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int s = s0 + k * COMBINE_SL;
+        if (s < a.nseg) a.partial[s * a.ld + r].x = ws * expf(m[k] - lse);
+      }
     }
   }
 }
@@ -233,9 +270,9 @@ cudaError_t launch_prep(const int64_t* target, int64_t N, int64_t C, int64_t ign
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;
-  const int64_t blocks = (a.rows + 7) / 8;  // 8 warps, one row each
+  const int64_t blocks = (a.rows + 31) / 32;  // 32 rows per block
   prof_before(K_LSE_COMBINE, s, 8.0 * a.rows * a.nseg * (a.backward ? 2 : 1));
-  combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  combine_kernel<<<static_cast<unsigned>(blocks), 32 * COMBINE_SL, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   prof_after(K_LSE_COMBINE, s);
   return e;

@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* unit_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);  // side job: claimed unit
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -92,11 +93,27 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_par = 0;
       bool ok = true;
+      // rows of A formed by the side job of this launch: wait for all its units once
+      bool dep_wait = side.enabled && side.claim != nullptr;
+      const int dep_units = static_cast<int>(((side.a.rows + 63) / 64) * side.a.nseg);
       for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
         int mb, nb;
         tc_tile_coords(g, tile, mb, nb);
         const int m0 = mb * TC2_TILE_M + static_cast<int>(rank) * 128;
         const int n0 = nb * TC2_TILE_N + static_cast<int>(rank) * 128;
+        if (dep_wait && m0 + 128 > side.dep_row0 && m0 < side.dep_row0 + side.a.rows) {
+          const long long t0 = clock64();
+          while (ld_acquire_gpu(side.done) < dep_units) {
+            if (*abort_flag || clock64() - t0 > kWaitLimitCycles) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          fence_proxy_async_all();  // the TMA loads below see the side job's G stores
+          dep_wait = false;
+        }
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -176,14 +193,31 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
     if (side.enabled) {
       const int tid = threadIdx.x - 64;
       const int64_t nunits = ((side.a.rows + 63) / 64) * side.a.nseg;
-      for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
+      auto bar = [] { asm volatile("bar.sync 1, 64;" ::: "memory"); };
+      auto unit = [&](int64_t u) {
         const int seg = static_cast<int>(u % side.a.nseg);
         const int64_t rb = u / side.a.nseg;
-        auto bar = [] { asm volatile("bar.sync 1, 64;" ::: "memory"); };
         if (F16)
           grad_unit<__half, 256, 64, 64>(side.a, seg, rb * 64, tid, side_red, bar);
         else
           grad_unit<__nv_bfloat16, 256, 64, 64>(side.a, seg, rb * 64, tid, side_red, bar);
+      };
+      if (side.claim == nullptr) {
+        for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) unit(u);
+      } else {
+        // claimed units: progress does not depend on which CTAs are resident
+        while (true) {
+          if (tid == 0) *unit_slot = atomicAdd(side.claim, 1);
+          bar();
+          const int64_t u = *unit_slot;
+          bar();  // every thread has read the slot before it is rewritten
+          if (u >= nunits) break;
+          unit(u);
+          fence_proxy_async_all();  // G stores visible to the TMA loads of other CTAs
+          __threadfence();
+          bar();
+          if (tid == 0) atomicAdd(side.done, 1);
+        }
       }
     }
   } else if (warp >= 4) {

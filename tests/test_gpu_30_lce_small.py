@@ -203,3 +203,25 @@ def test_row_slabs(cuda_lib, N, chunk_rows, reduction):
     inp = make_linear_inputs(N, 128, 2000, torch.bfloat16, "cuda", seed=N, bias=True, w_std=0.1, b_std=0.2,
                              n_ignored=N // 20)
     _check(cuda_lib, inp, reduction, chunk_rows=chunk_rows)
+
+
+@pytest.mark.parametrize("want", [(True, False, False), (False, True, True), (True, True, False), (False, False, True)])
+def test_row_slabs_grad_subsets(cuda_lib, want):
+    # the last slab's G is formed inside the dX GEMM when dX is wanted, by
+    # its own kernel otherwise; either way dW and db see all of G
+    want_dx, want_dw, want_db = want
+    N, D, C = 2100, 64, 3000
+    inp = make_linear_inputs(N, D, C, torch.bfloat16, "cuda", seed=77, bias=True, w_std=0.1, b_std=0.2,
+                             n_ignored=40)
+    X, W, b, t = inp["X"], inp["W"], inp["b"], inp["target"]
+    loss, dX, dW, db = cuda_lib.lce_forward_backward(X, W, b, t, "mean", want_dx=want_dx, want_dw=want_dw,
+                                                     want_db=want_db)
+    torch.cuda.synchronize()
+    rl, rX, rW, rb = O.lce_forward_backward(to64(X), to64(W), to64(b), t.cpu().numpy(), "mean")
+    tol = TOL[torch.bfloat16]
+    assert rel_scalar(loss.item(), rl) < tol["loss"]
+    for on, got, ref in ((want_dx, dX, rX), (want_dw, dW, rW), (want_db, db, rb)):
+        if on:
+            assert rel_max(to64(got), ref) < tol["grad"]
+        else:
+            assert got is None
