@@ -263,10 +263,12 @@ def run_gpu(args):
 
         P = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())
 
-        def step():
+        def step(mark=None):
             if red == 0:  # reduction none: forward, then forward+backward with the upstream vector
                 lce._check(lib.lce_forward(P(X), P(W), P(b), P(t), N, D, C, dt, 0, red, -100, P(loss), None,
                                            P(wsbuf), nbytes, ctypes.c_void_p(stream.cuda_stream)), "fwd")
+                if mark is not None:
+                    mark()  # CUDA event between the two parts
             lce._check(lib.lce_forward_backward(P(X), P(W), P(b), P(t), N, D, C, dt, 0, red, -100, P(g), P(loss),
                                                 P(dX), P(dW), P(db), dt, P(wsbuf), nbytes,
                                                 ctypes.c_void_p(stream.cuda_stream)), "fwd+bwd")
@@ -293,9 +295,18 @@ def run_gpu(args):
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    part_events = []  # reduction none: (start, between, end) per step
+    split_parts = w.kind == "linear" and w.reduction == "none"
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        if split_parts:
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
+            step(mark=lambda: ev[1].record(stream))
+            ev[2].record(stream)
+            part_events.append(ev)
+        else:
+            step()
     e1.record(stream)
     barrier()
     lce.profile_enable(False)
@@ -460,6 +471,12 @@ def run_gpu(args):
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in sorted(prof.items(), key=lambda kv: -kv[1][1])},
         "kernels_launches_per_step": {k: v[0] / args.steps for k, v in prof.items()},
     }
+    if part_events:
+        fwd_ms = sum(ev[0].elapsed_time(ev[1]) for ev in part_events) / len(part_events)
+        fb_ms = sum(ev[1].elapsed_time(ev[2]) for ev in part_events) / len(part_events)
+        ndc2 = 2.0 * w.N * w.D * w.C
+        line["parts"] = {"forward_ms": fwd_ms, "forward_tflops": ndc2 / (fwd_ms / 1e3) / 1e12,
+                         "forward_backward_ms": fb_ms, "forward_backward_tflops": 3 * ndc2 / (fb_ms / 1e3) / 1e12}
     if flops:
         line["tflops"] = flops * ws / (ms / 1e3) / 1e12
         line["pct_bf16_peak"] = 100.0 * line["tflops"] / ws / peaks["bf16_tflops"]

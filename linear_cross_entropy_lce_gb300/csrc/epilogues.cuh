@@ -72,6 +72,7 @@ struct EpiIO {
   int64_t row_base;  // first output row of this warp
   int lane;
   int nst;           // stores issued so far (buffer parity)
+  float* bias_s;     // NULL, or this warp's shared buffer for one segment of bias (NCHUNK * 32 floats)
 };
 
 __device__ __forceinline__ void stage_store_16bit(EpiIO& io, const float (&v)[32], int64_t col, int dt) {
@@ -142,8 +143,17 @@ struct EpiLse {
     const bool row_ok = row < p.rows;
     const int64_t t = row_ok ? p.target[row] : -1;
     const int tl = (t >= col0 && t < col0 + NCHUNK * 32 && t < p.C) ? static_cast<int>(t - col0) : -1;
-    // no bias and no padding column: the common case, without per-column tests
-    const bool plain = p.bias == nullptr && col0 + NCHUNK * 32 <= p.C;
+    const bool full = col0 + NCHUNK * 32 <= p.C;  // no padding column in the segment
+    // the segment's bias, staged once per tile by the warp in shared memory
+    float* bs = (p.bias != nullptr && full) ? io.bias_s : nullptr;
+    if (bs != nullptr) {
+      __syncwarp();  // the previous tile's reads are done
+#pragma unroll
+      for (int k = 0; k < NCHUNK; ++k) bs[io.lane + 32 * k] = load_elem(p.bias, col0 + io.lane + 32 * k, p.bias_dt);
+      __syncwarp();
+    }
+    // no per-column tests: no bias, or a full segment with its bias staged
+    const bool plain = full && (p.bias == nullptr || bs != nullptr);
     float v[W];
     // pass 1: segment max
     float m = -INFINITY;
@@ -151,6 +161,10 @@ struct EpiLse {
     for (int g = 0; g < NG; ++g) {
       load(g, v);
       if (plain) {
+        if (bs != nullptr) {
+#pragma unroll
+          for (int i = 0; i < W; ++i) v[i] += bs[W * g + i];
+        }
 #pragma unroll
         for (int i = 0; i < W; ++i) m = fmaxf(m, v[i]);
       } else {
@@ -167,7 +181,10 @@ struct EpiLse {
 #pragma unroll 1
     for (int g = 0; g < NG; ++g) {
       load(g, v);
-      if (!plain) {
+      if (bs != nullptr) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] += bs[W * g + i];
+      } else if (!plain) {
 #pragma unroll
         for (int i = 0; i < W; ++i) v[i] += bias_at(p, col0 + W * g + i);
       }

@@ -46,7 +46,7 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int
   g.num_m_blocks = (M + TC_BM - 1) / TC_BM;
   g.num_n_blocks = (N + TC_BN - 1) / TC_BN;
   g.num_tiles = g.num_m_blocks * g.num_n_blocks;
-  g.m_inner = m_inner;
+  g.m_inner = m_inner ? m_group_for(g.num_m_blocks, TC_BM, K, 2) : 0;
   g.status = status;
   g.use_tma_out = 0;
   if (g.num_tiles == 0) return cudaSuccess;
@@ -76,7 +76,7 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   g.num_m_blocks = (M + TC2_TILE_M - 1) / TC2_TILE_M;
   g.num_n_blocks = (N + TC2_TILE_N - 1) / TC2_TILE_N;
   g.num_tiles = g.num_m_blocks * g.num_n_blocks;
-  g.m_inner = m_inner;
+  g.m_inner = m_inner ? m_group_for(g.num_m_blocks, TC2_TILE_M, K, 2) : 0;
   g.status = status;
   g.use_tma_out = tmOut != nullptr ? 1 : 0;
   if (g.num_tiles == 0) return cudaSuccess;

@@ -137,7 +137,7 @@ cudaError_t launch_tx(const TxOperands& o, int M, int N, int K, int m_inner, int
   g.kb_per_split = (nkb + splits - 1) / splits;
   splits = (nkb + g.kb_per_split - 1) / g.kb_per_split;  // no empty work item
   g.num_tiles = g.mn_tiles * splits;
-  g.m_inner = m_inner;
+  g.m_inner = m_inner ? m_group_for(g.num_m_blocks, 256, K, 8) : 0;  // hi + lo fp32 parts of A
   g.status = status;
   if (g.mn_tiles == 0 || nkb == 0) return cudaSuccess;
   const int max_pairs = num_sms() / 2;

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(SG_THREADS)
   __syncthreads();
   const int r = tid >> 1, half = tid & 1;
   const int64_t col0 = n0 + half * SG_SEG;
-  EpiIO io{nullptr, nullptr, 0, static_cast<int>(threadIdx.x & 31), 0};
+  EpiIO io{nullptr, nullptr, 0, static_cast<int>(threadIdx.x & 31), 0, nullptr};
   Epi::template run<SG_SEG / 32, SG_SEG / 32>(
       ep, m0 + r, col0, col0 / SG_SEG,
       [&](int, float (&v)[SG_SEG]) {

@@ -30,7 +30,9 @@ constexpr int TC2_B_BYTES = 128 * TC2_BK * 2;  // this CTA's 128 rows of the 256
 constexpr int TC2_STAGE_BYTES = TC2_A_BYTES + TC2_B_BYTES;
 constexpr int TC2_STAGING_BYTES = 4 * 2 * 2048;  // epilogue: 2 x 2 KB per epilogue warp
 constexpr int TC2_SIDE_BYTES = 2 * 256 * 4;       // warps 2-3: column-sum scratch of the G formation
-constexpr int TC2_SMEM_BYTES = TC2_STAGES * TC2_STAGE_BYTES + TC2_STAGING_BYTES + TC2_SIDE_BYTES + 1024 + 512;
+constexpr int TC2_BIAS_BYTES = 4 * 256 * 4;       // epilogue: one segment of bias per epilogue warp
+constexpr int TC2_SMEM_BYTES =
+    TC2_STAGES * TC2_STAGE_BYTES + TC2_STAGING_BYTES + TC2_SIDE_BYTES + TC2_BIAS_BYTES + 1024 + 512;
 constexpr int TC2_THREADS = 256;
 constexpr int TC2_TMEM_COLS = 512;
 constexpr int TC2_TILE_M = 256;  // rows per pair tile (128 per CTA)
@@ -45,7 +47,8 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + TC2_STAGES * TC2_STAGE_BYTES;
   float* side_red = reinterpret_cast<float*>(staging + TC2_STAGING_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + TC2_STAGING_BYTES + TC2_SIDE_BYTES);
+  float* bias_s = side_red + TC2_SIDE_BYTES / 4;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + TC2_STAGING_BYTES + TC2_SIDE_BYTES + TC2_BIAS_BYTES);
   uint64_t* empty = full + TC2_STAGES;
   uint64_t* tfull = empty + TC2_STAGES;
   uint64_t* tempty = tfull + 2;
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
   } else if (warp >= 4) {
     // ---------------- epilogue (both CTAs): this CTA's 128 rows of the tile
     const int q = warp & 3;
-    EpiIO io{g.use_tma_out ? &tmOut : nullptr, staging + q * 4096, 0, lane, 0};
+    EpiIO io{g.use_tma_out ? &tmOut : nullptr, staging + q * 4096, 0, lane, 0, bias_s + q * 256};
     int it = 0;
     for (int tile = pair; tile < g.num_tiles; tile += npairs, ++it) {
       const int acc = it & 1;

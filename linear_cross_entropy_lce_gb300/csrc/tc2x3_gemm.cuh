@@ -28,6 +28,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tc_gemm.cuh"
 
 namespace lce {
 
@@ -37,7 +38,7 @@ struct TxArgs {
   int mn_tiles;                    // num_m_blocks * num_n_blocks
   int num_tiles;                   // mn_tiles * k_splits
   int kb_per_split;                // 32-wide K blocks per work item
-  int m_inner;                     // 1: consecutive tiles walk down M (share a B panel)
+  int m_inner;                     // as TcGemmArgs::m_inner (0, or row blocks per group)
   int* status;
 };
 
@@ -45,8 +46,13 @@ __device__ __forceinline__ void tx_tile(const TxArgs& g, int tile, int& mb, int&
   const int mn = tile % g.mn_tiles;
   const int ks = tile / g.mn_tiles;
   if (g.m_inner) {
-    mb = mn % g.num_m_blocks;
-    nb = mn / g.num_m_blocks;
+    const int per_group = g.m_inner * g.num_n_blocks;
+    const int grp = mn / per_group;
+    const int m_first = grp * g.m_inner;
+    const int rows_in = g.m_inner < g.num_m_blocks - m_first ? g.m_inner : g.num_m_blocks - m_first;
+    const int r = mn - grp * per_group;
+    mb = m_first + r % rows_in;
+    nb = r / rows_in;
   } else {
     nb = mn % g.num_n_blocks;
     mb = mn / g.num_n_blocks;
@@ -199,7 +205,7 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
     const int qw = warp & 3;
     const uint32_t tP = tmem_base + (static_cast<uint32_t>(qw * 32) << 16);
     const uint32_t tR = tP + 256;
-    EpiIO io{nullptr, nullptr, 0, lane, 0};
+    EpiIO io{nullptr, nullptr, 0, lane, 0, nullptr};
     uint32_t q = 0;
     bool ok = true;
     for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {

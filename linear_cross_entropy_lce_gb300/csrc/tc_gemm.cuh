@@ -33,18 +33,35 @@ constexpr int TC_SMEM_BYTES = TC_STAGES * TC_STAGE_BYTES + 1024 + 256;
 constexpr int TC_THREADS = 256;
 constexpr int TC_TMEM_COLS = 512;
 
+// Row blocks per group for the grouped M-inner walk: the A rows of a group
+// (block_rows x K x a_bytes each) within about 40 MB of L2.
+inline int m_group_for(int num_m_blocks, int block_rows, int K, int a_bytes) {
+  const double per_block = static_cast<double>(block_rows) * K * a_bytes;
+  int gm = static_cast<int>((40.0 * 1024 * 1024) / per_block);
+  if (gm < 1) gm = 1;
+  return gm < num_m_blocks ? gm : num_m_blocks;
+}
+
 struct TcGemmArgs {
   int M, N, K;
   int num_m_blocks, num_n_blocks, num_tiles;
-  int m_inner;  // 1: consecutive tiles walk down M (share a B panel); 0: walk along N
+  // 0: consecutive tiles walk along N. k >= 1: they walk down M in groups of
+  // k row blocks (all N blocks of one group before the next group), so the
+  // CTAs in flight share a B panel and the group's A rows stay in L2.
+  int m_inner;
   int* status;  // device status word or NULL
   int use_tma_out;  // CTA-pair kernel: epilogue stores bf16 results through the output tensor map
 };
 
 __device__ __forceinline__ void tc_tile_coords(const TcGemmArgs& g, int tile, int& mb, int& nb) {
   if (g.m_inner) {
-    mb = tile % g.num_m_blocks;
-    nb = tile / g.num_m_blocks;
+    const int per_group = g.m_inner * g.num_n_blocks;
+    const int grp = tile / per_group;
+    const int m_first = grp * g.m_inner;
+    const int rows_in = g.m_inner < g.num_m_blocks - m_first ? g.m_inner : g.num_m_blocks - m_first;
+    const int r = tile - grp * per_group;
+    mb = m_first + r % rows_in;
+    nb = r / rows_in;
   } else {
     nb = tile % g.num_n_blocks;
     mb = tile / g.num_n_blocks;
@@ -197,7 +214,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int64_t row = static_cast<int64_t>(mb) * TC_BM + q * 32 + lane;
       const int64_t col0 = static_cast<int64_t>(nb) * TC_BN;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TC_BN;
-      EpiIO io{nullptr, nullptr, 0, lane, 0};
+      EpiIO io{nullptr, nullptr, 0, lane, 0, nullptr};
       Epi::template run<TC_BN / 32, 4>(
           ep, row, col0, nb, [&](int g, float (&v)[128]) { tmem_ld128(taddr + g * 128, v); }, io);
       tc_fence_before();
