@@ -311,6 +311,32 @@ def run_gpu(args):
     clocks = sampler.stop()
     ms = aggregate_ms(e0.elapsed_time(e1) / args.steps, dist, dev)
 
+    # ---- the same step captured once in a CUDA graph and replayed (the
+    # library allocates and synchronizes nothing, so its calls capture):
+    # reported for short steps, where launch overhead is visible
+    graph_ms = None
+    if ms < 5.0 and dist is None:
+        cap_stream = torch.cuda.Stream()
+        cap_stream.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        prev = stream
+        stream = cap_stream  # step() launches on `stream`
+        with torch.cuda.graph(graph, stream=cap_stream):
+            step()
+        stream = prev
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        graph_ms = g0.elapsed_time(g1) / args.steps
+        del graph
+
     # ---- per-kernel times: a separate pass with the library's CUDA-event
     # profiler (its events would add to the timed region on small steps)
     prof_steps = min(args.steps, 10)
@@ -478,6 +504,8 @@ def run_gpu(args):
         "kernels_ms_per_step": {k: v[1] / prof_steps for k, v in sorted(prof.items(), key=lambda kv: -kv[1][1])},
         "kernels_launches_per_step": {k: v[0] / prof_steps for k, v in prof.items()},
     }
+    if graph_ms is not None:
+        line["graph_replay_ms_per_step"] = graph_ms
     if part_events:
         fwd_ms = sum(ev[0].elapsed_time(ev[1]) for ev in part_events) / len(part_events)
         fb_ms = sum(ev[1].elapsed_time(ev[2]) for ev in part_events) / len(part_events)
