@@ -106,6 +106,10 @@ constexpr int64_t kDefaultChunkBytes = int64_t(8) << 30;  // chunk buffer budget
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int esize(int dt) { return dt == LCE_F32 ? 4 : 2; }
+// Work counters of the idle-warp side jobs, per chunk: (claimed, done) for
+// the merge of slabs 0..3 at [2k, 2k + 1], for the last slab's G formation
+// in the dX GEMM at [8, 9].
+constexpr int kCountersPerChunk = 16;
 
 struct Plan {
   bool tc;          // tensor-core (bf16 / fp16) path
@@ -116,7 +120,7 @@ struct Plan {
   int64_t Bc;       // rows per chunk
   int64_t nchunks;
   bool dw_acc;      // fp32 dW accumulator in the workspace
-  size_t off_loss, off_zt, off_tcol, off_gt, off_partial, off_L, off_dw, off_db, total;
+  size_t off_cnt, off_loss, off_zt, off_tcol, off_gt, off_partial, off_L, off_dw, off_db, total;
   // fp16 backward: per-row weights [Bc], their max |w| (one float), and the
   // rows of X scaled by w / max|w| for dW ([Bc, D] fp16)
   size_t off_wrow, off_wbar, off_xs;
@@ -142,6 +146,8 @@ bool make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtyp
   p->nchunks = Bc > 0 ? ceil_div(N, Bc) : 0;
   p->dw_acc = backward && want_dw && p->nchunks > 1 && grad_dtype != LCE_F32;
   size_t off = align_up(sizeof(WsHeader));
+  p->off_cnt = off;  // zeroed with the header at the start of every call
+  off = align_up(off + static_cast<size_t>(p->nchunks) * kCountersPerChunk * sizeof(int));
   p->off_loss = off;
   off = align_up(off + static_cast<size_t>(N) * 4);
   p->off_zt = off;
@@ -296,7 +302,8 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
   void* Xs = ws + p.off_xs;
   const int gsz = esize(grad_dtype);
 
-  LCE_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
+  LCE_TRY(cudaMemsetAsync(hdr, 0, p.off_cnt + static_cast<size_t>(p.nchunks) * kCountersPerChunk * sizeof(int), s));
+  int* counters = reinterpret_cast<int*>(ws + p.off_cnt);
   if (N == 0) {
     if (reduction != LCE_RED_NONE)
       LCE_TRY(launch_loss_finalize(loss_rows, 0, reduction, hdr, class_weight != nullptr, loss_out, s));
@@ -368,8 +375,10 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
     const int64_t slab = slabbed ? ceil_div(ceil_div(rows, 4), 256) * 256 : rows;
     const int64_t nslab = ceil_div(rows, slab);
     GradArgs ga_prev, ga_last;
+    CombineArgs ca_prev, ca_last;  // merges deferred into the next GEMM's idle warps
     bool have_prev = false, have_last = false;
-    int64_t last_row0 = 0;
+    int64_t last_row0 = 0, last_si = 0;
+    int* cnt = counters + ci * kCountersPerChunk;
     for (int64_t si = 0; si < nslab; ++si) {
       const int64_t so = si * slab;                      // slab offset within the chunk
       const int64_t sr = std::min(slab, rows - so);      // rows in the slab
@@ -398,6 +407,10 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
         side.claim = nullptr;
         side.done = nullptr;
         side.dep_row0 = 0;
+        side.ca = ca_prev;  // merge of slab si - 1, then its G formation
+        side.comb = have_prev ? 1 : 0;
+        side.cclaim = cnt + 2 * (si - 1);
+        side.cdone = cnt + 2 * (si - 1) + 1;
         LCE_TRY(launch_tc_logits(tmX_k, tmW_k, tma_out ? &tmL : nullptr, static_cast<int>(sr), static_cast<int>(C),
                                  static_cast<int>(D), &hdr->status, el, pair, s, have_prev ? &side : nullptr, f16));
       } else if (p.tf32) {
@@ -429,7 +442,9 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       ca.lse_out = lse_out;
       ca.backward = backward ? 1 : 0;
       ca.wrow = wrow != nullptr ? wrow + so : nullptr;
-      LCE_TRY(launch_combine(ca, s));
+      // on the slabbed path the merge runs in the next GEMM's idle warps
+      const bool defer = slabbed && (si + 1 < nslab || want_dx);
+      if (!defer) LCE_TRY(launch_combine(ca, s));
       if (!backward) continue;
       GradArgs ga;
       ga.L = el.ptilde;
@@ -445,12 +460,15 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       ga.db_acc = want_db ? db_acc : nullptr;
       ga.wrow = wrow != nullptr ? wrow + so : nullptr;
       if (slabbed && si + 1 < nslab) {
-        ga_prev = ga;  // formed by the next slab's GEMM
+        ga_prev = ga;  // merged and formed by the next slab's GEMM
+        ca_prev = ca;
         have_prev = true;
       } else if (slabbed && want_dx) {
-        ga_last = ga;  // formed by the dX GEMM's idle warps before it reads these rows
+        ga_last = ga;  // merged and formed by the dX GEMM's idle warps before it reads these rows
+        ca_last = ca;
         have_last = true;
         last_row0 = so;
+        last_si = si;
       } else {
         LCE_TRY(launch_grad_logits(ga, dtype, s));
         have_prev = false;
@@ -491,12 +509,15 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
         if (tma_out && !encode_tmap_bf16_store(&tmdX, es.out, D, rows, D, grad_dtype)) return LCE_ERR_CUDA;
         SideGrad side;
         if (have_last) {
-          LCE_TRY(cudaMemsetAsync(&hdr->side_claim, 0, 2 * sizeof(int), s));
           side.a = ga_last;
           side.enabled = 1;
-          side.claim = &hdr->side_claim;
-          side.done = &hdr->side_done;
+          side.claim = cnt + 8;
+          side.done = cnt + 9;
           side.dep_row0 = last_row0;
+          side.ca = ca_last;
+          side.comb = 1;
+          side.cclaim = cnt + 2 * last_si;
+          side.cdone = cnt + 2 * last_si + 1;
         }
         LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmW_n, tma_out ? &tmdX : nullptr, static_cast<int>(rows),
                                 static_cast<int>(D), static_cast<int>(C), &hdr->status, es, pair, s, f16,

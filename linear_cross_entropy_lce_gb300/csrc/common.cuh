@@ -24,9 +24,7 @@ struct WsHeader {
   int status;       // kStatus* bits, OR-ed by kernels
   int n_valid;      // rows whose target is a class index (not ignored, in range)
   double weight_sum;  // sum of class weights over valid rows (class-weighted calls)
-  int side_claim;   // G-formation units claimed / finished in the dX GEMM's idle warps
-  int side_done;
-  int pad[58];
+  int pad[60];
 };
 static_assert(sizeof(WsHeader) <= 256, "header must fit 256 bytes");
 

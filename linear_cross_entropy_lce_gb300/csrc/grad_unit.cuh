@@ -15,13 +15,16 @@
 
 namespace lce {
 
-template <class T, int SEGW, int NT, int RB, class Bar>
+// NRMAX: rows per thread loaded before any store (bytes in flight); the
+// 64-thread idle-warp form takes 16 so that few threads keep enough loads
+// in flight.
+template <class T, int SEGW, int NT, int RB, int NRMAX = 8, class Bar>
 __device__ __forceinline__ void grad_unit(const GradArgs& a, int seg, int64_t r_begin, int tid, float* red,
                                           Bar&& bar) {
   constexpr int VE = 16 / static_cast<int>(sizeof(T));
   constexpr int TPR = SEGW / VE;          // threads per row
   constexpr int RPP = NT / TPR;           // rows per pass of all threads
-  constexpr int NR = (RB / RPP) < 8 ? (RB / RPP) : 8;  // rows per thread loaded before any store
+  constexpr int NR = (RB / RPP) < NRMAX ? (RB / RPP) : NRMAX;
   constexpr int PASSES = RB / (RPP * NR);
   static_assert(NT % TPR == 0 && RB % (RPP * NR) == 0, "unit shape");
   const int64_t r_end = (r_begin + RB < a.rows) ? r_begin + RB : a.rows;
@@ -38,6 +41,7 @@ __device__ __forceinline__ void grad_unit(const GradArgs& a, int seg, int64_t r_
     float sc[NR];
     int tc[NR];
     float wr[NR];
+    float gtv[NR];
 #pragma unroll
     for (int k = 0; k < NR; ++k) {
       const int64_t r = rp + k * RPP;
@@ -46,6 +50,7 @@ __device__ __forceinline__ void grad_unit(const GradArgs& a, int seg, int64_t r_
         sc[k] = a.scale[seg * a.sld + r].x;
         tc[k] = a.tcol[r];
         wr[k] = a.wrow != nullptr ? a.wrow[r] : 1.0f;
+        gtv[k] = a.gt[r];
       }
     }
 #pragma unroll
@@ -56,7 +61,7 @@ __device__ __forceinline__ void grad_unit(const GradArgs& a, int seg, int64_t r_
 #pragma unroll
       for (int i = 0; i < VE; ++i) {
         float gv = to_f32(e[i]) * sc[k];
-        if (col + i == tc[k]) gv = a.gt[r];
+        if (col + i == tc[k]) gv = gtv[k];
         e[i] = from_f32<T>(gv);
         colsum[i] += wr[k] * to_f32(e[i]);
       }

@@ -168,6 +168,14 @@ struct SideGrad {
   int* claim;
   int* done;
   int64_t dep_row0;
+  // Optional merge phase first (comb != 0): the rows of `ca` in blocks of
+  // 32, claimed from *cclaim and counted in *cdone; the G formation starts
+  // once *cdone reaches the block count (the merging threads fence before
+  // counting; the waiting thread fences after its acquiring wait).
+  CombineArgs ca;
+  int comb;
+  int* cclaim;
+  int* cdone;
 };
 // fp16 backward: wbar = max_r |w_r| over the chunk rows (NaN if any w_r is
 // NaN), then Xs[r, :] = (w_r / wbar) X[r, :] in fp16 (0 when wbar is 0).

@@ -2,6 +2,7 @@
 // valid-target count, merge of the per-segment (max, sum-exp) pairs into
 // the row log-sum-exp and loss, formation of the gradient tile G, and the
 // final loss / bias-gradient reductions.
+#include "combine_unit.cuh"
 #include "grad_unit.cuh"
 #include "internal.h"
 
@@ -64,95 +65,13 @@ __global__ void prep_kernel(const int64_t* __restrict__ target, int64_t N, int64
   }
 }
 
-// Merge of a row's per-segment (max, sum-exp) pairs into lse = M + log
-// sum_s s_s exp(m_s - M), then loss_n = lse - z_t (0 on ignored rows). For
-// the backward each pair becomes the scale w_n exp(m_s - lse) that maps the
-// stored P~ to G, and G at the target column is w_n (softmax_t - 1) from
-// the fp32 target logit (expm1 keeps it accurate when softmax_t ~ 1).
-//
-// A block holds 32 consecutive rows x COMBINE_SL segment lanes: the 32
-// threads of a warp take the same segment of 32 rows, so every access to
-// the [segment][row] partials is one coalesced 256-byte row of the array.
-// Lane sl merges segments sl, sl + COMBINE_SL, ...; the lanes' pairs meet
-// in shared memory.
-__device__ __forceinline__ void merge_pair(float& M, float& S, float m2, float s2) {
-  if (m2 == -INFINITY) return;  // an empty pair (also covers M == m2 == -inf)
-  if (m2 > M) {
-    S = (M == -INFINITY ? 0.0f : S * expf(M - m2)) + s2;
-    M = m2;
-  } else {
-    S += s2 * expf(m2 - M);
-  }
-}
-
+// Stand-alone per-row merge: 32 rows x COMBINE_SL segment lanes per block.
 constexpr int COMBINE_SL = 32;
 
 __global__ void __launch_bounds__(32 * COMBINE_SL) combine_kernel(const CombineArgs a) {
-  __shared__ float sM[COMBINE_SL][33];
-  __shared__ float sS[COMBINE_SL][33];
-  __shared__ float sLse[32];
-  __shared__ float sW[32];
-  const int rl = threadIdx.x & 31;
-  const int sl = threadIdx.x >> 5;
-  const int64_t r = static_cast<int64_t>(blockIdx.x) * 32 + rl;
-  const bool in = r < a.rows;
-  float M = -INFINITY, S = 0.0f;
-  if (in) {
-    // 8 independent loads in flight per batch instead of one dependent chain
-    for (int s0 = sl; s0 < a.nseg; s0 += 8 * COMBINE_SL) {
-      float2 p[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int s = s0 + k * COMBINE_SL;
-        p[k] = s < a.nseg ? a.partial[s * a.ld + r] : make_float2(-INFINITY, 0.0f);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) merge_pair(M, S, p[k].x, p[k].y);
-    }
-  }
-  sM[sl][rl] = M;
-  sS[sl][rl] = S;
-  __syncthreads();
-  if (sl == 0 && in) {
-#pragma unroll 1
-    for (int k = 1; k < COMBINE_SL; ++k) merge_pair(M, S, sM[k][rl], sS[k][rl]);
-    const float lse = M + logf(S);
-    const int64_t g = a.row0 + r;
-    const int64_t t = a.target[g];
-    const bool valid = target_valid(t, a.ignore_index, a.C);
-    const float zt = valid ? a.zt[r] : 0.0f;
-    a.loss_rows[g] = valid ? class_w(a.rw, t, true) * (lse - zt) : 0.0f;
-    if (a.lse_out != nullptr) a.lse_out[g] = lse;
-    if (a.backward) {
-      const float w = row_weight(a.rw, a.hdr, g, t, valid);
-      // with wrow the stored G leaves w_n out: unit weight on valid rows, 0 on the others
-      const float ws = a.wrow != nullptr ? (valid ? 1.0f : 0.0f) : w;
-      a.tcol[r] = valid ? static_cast<int>(t) : -1;
-      a.gt[r] = valid ? ws * expm1f(zt - lse) : 0.0f;
-      if (a.wrow != nullptr) a.wrow[r] = w;
-      sLse[rl] = lse;
-      sW[rl] = ws;
-    }
-  }
-  if (!a.backward) return;  // uniform over the grid
-  __syncthreads();
-  if (in) {
-    const float lse = sLse[rl];
-    const float ws = sW[rl];
-    for (int s0 = sl; s0 < a.nseg; s0 += 8 * COMBINE_SL) {
-      float m[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int s = s0 + k * COMBINE_SL;
-        m[k] = s < a.nseg ? a.partial[s * a.ld + r].x : 0.0f;
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int s = s0 + k * COMBINE_SL;
-        if (s < a.nseg) a.partial[s * a.ld + r].x = ws * expf(m[k] - lse);
-      }
-    }
-  }
+  __shared__ float sm[2 * 32 * COMBINE_SL + 64];
+  combine_rows32<32 * COMBINE_SL>(a, static_cast<int64_t>(blockIdx.x) * 32, threadIdx.x, sm,
+                                  [] { __syncthreads(); });
 }
 
 // Stand-alone G formation: one (segment, 64-row block) unit per CTA.

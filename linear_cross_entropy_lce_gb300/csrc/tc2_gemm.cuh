@@ -18,6 +18,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "combine_unit.cuh"
 #include "grad_unit.cuh"
 #include "ptx.cuh"
 
@@ -197,15 +198,52 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
       const int tid = threadIdx.x - 64;
       const int64_t nunits = ((side.a.rows + 63) / 64) * side.a.nseg;
       auto bar = [] { asm volatile("bar.sync 1, 64;" ::: "memory"); };
+      bool go = true;
+      if (side.comb) {
+        // merge phase: claimed 32-row blocks, then wait until every block
+        // (merged by any CTA) is done before forming G from the scales
+        const int64_t nblk = (side.ca.rows + 31) / 32;
+        while (true) {
+          if (tid == 0) *unit_slot = atomicAdd(side.cclaim, 1);
+          bar();
+          const int64_t u = *unit_slot;
+          bar();
+          if (u >= nblk) break;
+          combine_rows32<64>(side.ca, u * 32, tid, side_red, bar);
+          __threadfence();
+          bar();
+          if (tid == 0) atomicAdd(side.cdone, 1);
+        }
+        if (tid == 0) {
+          int ok = 1;
+          const long long t0 = clock64();
+          while (ld_acquire_gpu(side.cdone) < nblk) {
+            if (*abort_flag || clock64() - t0 > kWaitLimitCycles) {
+              *abort_flag = 1;
+              ok = 0;
+              break;
+            }
+          }
+          // with the barrier below, the other threads' plain loads of the
+          // merged rows see what the merging CTAs wrote before counting
+          __threadfence();
+          *unit_slot = ok;
+        }
+        bar();
+        go = *unit_slot != 0;
+        bar();
+      }
       auto unit = [&](int64_t u) {
         const int seg = static_cast<int>(u % side.a.nseg);
         const int64_t rb = u / side.a.nseg;
         if (F16)
-          grad_unit<__half, 256, 64, 64>(side.a, seg, rb * 64, tid, side_red, bar);
+          grad_unit<__half, 256, 64, 64, 16>(side.a, seg, rb * 64, tid, side_red, bar);
         else
-          grad_unit<__nv_bfloat16, 256, 64, 64>(side.a, seg, rb * 64, tid, side_red, bar);
+          grad_unit<__nv_bfloat16, 256, 64, 64, 16>(side.a, seg, rb * 64, tid, side_red, bar);
       };
-      if (side.claim == nullptr) {
+      if (!go) {
+        // a merge wait gave up: the launch reports a timeout
+      } else if (side.claim == nullptr) {
         for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) unit(u);
       } else {
         // claimed units: progress does not depend on which CTAs are resident
