@@ -30,6 +30,15 @@
  *   (device, 16-byte aligned, at least 2 * (M + N) * ceil(K / 4) * 16 + 1024
  *   bytes); k_splits > 1 splits K over that many work items per tile which
  *   add into the zeroed output. Any shape up to 2^30 per dimension.
+ * lce_test_gemm_bf16_unmet_dependency: the CTA-pair GEMM in its dX form
+ *   (A K-major [M, K], B MN-major [K, N]) with its side job's dependency
+ *   made unsatisfiable: counters[0] (claimed units, preset by the caller to
+ *   a value >= ceil(M / 64)) lets no unit run and counters[1] (finished
+ *   units, preset to 0) never reaches the count the producer waits for. The
+ *   producer's bounded wait (about 2 s of SM clock) gives up, every role of
+ *   the kernel unwinds through its own bounded waits, and dev_status
+ *   receives the timeout bit (2); the context stays usable. For tests of
+ *   the failure path only; out is left unspecified.
  * Return an lce_status_e code.
  */
 #ifndef LCE_TESTING_H_
@@ -56,6 +65,10 @@ LCE_API int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t
 
 LCE_API int lce_test_gemm_f32(const float* A, const float* B, float* out, int64_t M, int64_t N,
                       int64_t K, int a_mn_major, int b_mn_major, void* stream);
+
+LCE_API int lce_test_gemm_bf16_unmet_dependency(const void* A, const void* B, float* out, int64_t M,
+                                        int64_t N, int64_t K, int* counters, int* dev_status,
+                                        void* stream);
 
 LCE_API int lce_test_gemm_tf32x3(const float* A, const float* B, float* out, int64_t M, int64_t N,
                          int64_t K, int a_mn_major, int b_mn_major, int k_splits, void* workspace,

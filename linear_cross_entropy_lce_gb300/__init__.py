@@ -77,6 +77,8 @@ _SIGNATURES = {
                                    c_int, c_void_p, c_void_p]),
     "lce_test_gemm_f32": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int,
                                   c_void_p]),
+    "lce_test_gemm_bf16_unmet_dependency": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64,
+                                                    c_void_p, c_void_p, c_void_p]),
     "lce_test_gemm_tf32x3": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int,
                                      c_int, c_void_p, c_size_t, c_void_p, c_void_p]),
 }
@@ -297,6 +299,15 @@ def test_gemm_bf16(A, B, M, N, K, a_mn_major, b_mn_major, status=None, cta_pair=
     out = torch.empty(M, N, dtype=torch.float32, device=A.device)
     _check(lib.lce_test_gemm_bf16(_ptr(A), _ptr(B), _ptr(out), M, N, K, int(a_mn_major), int(b_mn_major),
                                   int(cta_pair), _ptr(status), _stream(stream)), "lce_test_gemm_bf16")
+    return out
+
+
+def test_gemm_bf16_unmet_dependency(A, B, M, N, K, counters, status, stream=None):
+    lib = load_library()
+    out = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    _check(lib.lce_test_gemm_bf16_unmet_dependency(_ptr(A), _ptr(B), _ptr(out), M, N, K, _ptr(counters),
+                                                   _ptr(status), _stream(stream)),
+           "lce_test_gemm_bf16_unmet_dependency")
     return out
 
 

@@ -798,6 +798,41 @@ int lce_test_gemm_bf16(const void* A, const void* B, float* out, int64_t M, int6
                                    static_cast<cudaStream_t>(stream)));
 }
 
+int lce_test_gemm_bf16_unmet_dependency(const void* A, const void* B, float* out, int64_t M, int64_t N, int64_t K,
+                                        int* counters, int* dev_status, void* stream) {
+  if (A == nullptr || B == nullptr || out == nullptr || counters == nullptr || dev_status == nullptr)
+    return LCE_ERR_NULL;
+  if (M < 1 || N < 1 || K < 1 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return LCE_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return LCE_ERR_ALIGN;
+  if (K % 8 != 0 || N % 8 != 0) return LCE_ERR_ALIGN;
+  int st = check_device();
+  if (st != LCE_OK) return st;
+  CUtensorMap ta, tb;
+  if (!encode_tmap_bf16(&ta, A, K, M, K, TC_BM) || !encode_tmap_bf16(&tb, B, N, K, N, 64)) return LCE_ERR_CUDA;
+  EpiStore::Params es;
+  es.out = out;
+  es.out_dt = LCE_F32;
+  es.row_scale = nullptr;
+  es.scalar_scale = nullptr;
+  es.ldo = N;
+  es.acc32 = nullptr;
+  es.mode = 0;
+  es.rows = M;
+  es.cols = N;
+  es.vec_ok = (N % 4) == 0;
+  SideGrad side;
+  memset(&side, 0, sizeof(side));
+  side.enabled = 1;
+  side.a.rows = M;  // the dependency covers every A row
+  side.a.nseg = 1;
+  side.claim = counters;
+  side.done = counters + 1;
+  side.dep_row0 = 0;
+  return from_cuda(launch_tc_store(TC_DX, ta, tb, nullptr, static_cast<int>(M), static_cast<int>(N),
+                                   static_cast<int>(K), dev_status, es, true, static_cast<cudaStream_t>(stream),
+                                   false, &side));
+}
+
 int lce_test_gemm_tf32x3(const float* A, const float* B, float* out, int64_t M, int64_t N, int64_t K,
                          int a_mn_major, int b_mn_major, int k_splits, void* workspace, size_t ws_bytes,
                          int* dev_status, void* stream) {

@@ -115,6 +115,10 @@ def test_host_argument_errors(lib):
     assert lib.lce_read_device_status(None, None) == 1
     assert lib.lce_test_gemm_bf16(FAKE, FAKE, FAKE, 8, 8, 12, 0, 0, 0, None, None) == 9
     assert lib.lce_test_gemm_bf16(None, FAKE, FAKE, 8, 8, 8, 0, 0, 1, None, None) == 1
+    ud = lib.lce_test_gemm_bf16_unmet_dependency
+    assert ud(FAKE, FAKE, FAKE, 8, 8, 8, None, FAKE, None) == 1
+    assert ud(FAKE, FAKE, FAKE, 0, 8, 8, FAKE, FAKE, None) == 2
+    assert ud(FAKE, FAKE, FAKE, 8, 8, 12, FAKE, FAKE, None) == 9
     tx = lib.lce_test_gemm_tf32x3
     assert tx(FAKE, FAKE, FAKE, 8, 8, 8, 0, 0, 1, None, 1 << 20, None, None) == 1
     assert tx(FAKE, FAKE, FAKE, 0, 8, 8, 0, 0, 1, FAKE, 1 << 20, None, None) == 2
