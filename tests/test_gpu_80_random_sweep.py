@@ -2,8 +2,11 @@
 float64 oracle: input dtype (fp32 / bf16 / fp16), reduction, bias, ignored
 rows, class weights, chunk size, gradient dtype, the subset of gradients
 wanted, target distribution, and shapes with ragged tails on every
-dimension (including row counts that take the row-slab path). Each case is
-drawn from its own seed, so a failure names a reproducible configuration."""
+dimension (including row counts that take the row-slab path); and the same
+for cross entropy on given logits (dtype, reduction, ignored rows, class
+weights, logit scale, and class counts on both sides of the resident /
+streaming kernel boundary). Each case is drawn from its own seed, so a
+failure names a reproducible configuration."""
 
 import random
 
@@ -11,7 +14,7 @@ import numpy as np
 import pytest
 import torch
 
-from linear_cross_entropy_lce_gb300.workloads import make_linear_inputs
+from linear_cross_entropy_lce_gb300.workloads import make_linear_inputs, make_logits_inputs
 from oracle import lce_oracle as O
 from tests.util import TOL, rel_max, rel_scalar, to64
 
@@ -86,3 +89,45 @@ def test_random_case(cuda_lib, i):
             assert rel_max(to64(got), ref) < gtol, (name, rel_max(to64(got), ref), what)
         else:
             assert got is None, (name, what)
+
+
+def _ce_case(i):
+    r = random.Random(5000 + i)
+    dtype = r.choice([torch.float32, torch.bfloat16, torch.float16])
+    N = r.choice([1, 5, 64, 300])
+    V = r.choice([1, 2, 31, 1000, 16384, 16385, 40000, 131072, 140000])
+    red = r.choice(["mean", "sum", "none"])
+    n_ign = r.choice([0, 1, N // 3])
+    if red == "mean":
+        n_ign = min(n_ign, N - 1)
+    return dict(dtype=dtype, N=N, V=V, reduction=red, n_ignored=n_ign, class_weight=r.random() < 0.3,
+                std=r.choice([0.5, 2.0, 8.0]), seed=r.randrange(1 << 30))
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_ce_case(cuda_lib, i):
+    c = _ce_case(i)
+    inp = make_logits_inputs(c["N"], c["V"], c["dtype"], "cuda", seed=c["seed"], std=c["std"],
+                             n_ignored=c["n_ignored"])
+    logits, t = inp["logits"], inp["target"]
+    N, V = c["N"], c["V"]
+    g = None
+    if c["reduction"] == "none":
+        g = torch.randn(N, generator=torch.Generator(device="cuda").manual_seed(c["seed"]), device="cuda")
+    elif c["reduction"] == "sum":
+        g = torch.tensor(1.5, device="cuda")
+    cw = None
+    if c["class_weight"]:
+        cw = torch.rand(V, generator=torch.Generator(device="cuda").manual_seed(c["seed"] + 1),
+                        device="cuda") * 1.8 + 0.2
+    snap = to64(logits)
+    loss = cuda_lib.lce_cross_entropy_from_logits(logits, t, c["reduction"], -100, g, class_weight=cw)
+    torch.cuda.synchronize()
+    rl, rg = O.ce_from_logits(snap, t.cpu().numpy(), c["reduction"], -100, to64(g), class_weight=to64(cw))
+    tol = TOL[c["dtype"]]
+    what = str(c)
+    if c["reduction"] == "none":
+        assert rel_max(to64(loss), rl) < tol["loss"], what
+    else:
+        assert rel_scalar(loss.item(), rl) < tol["loss"], what
+    assert rel_max(to64(logits), rg) < tol["grad"], what
