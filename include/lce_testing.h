@@ -32,8 +32,8 @@
  *   add into the zeroed output. Any shape up to 2^30 per dimension.
  * lce_test_gemm_bf16_unmet_dependency: the CTA-pair GEMM in its dX form
  *   (A K-major [M, K], B MN-major [K, N]) with its side job's dependency
- *   made unsatisfiable: counters[0] (claimed units, preset by the caller to
- *   a value >= ceil(M / 64)) lets no unit run and counters[1] (finished
+ *   made unsatisfiable: counters[0] (claimed work chunks, preset by the
+ *   caller to a value >= ceil(M / 512), e.g. 1 << 20) lets no chunk run and counters[1] (finished
  *   units, preset to 0) never reaches the count the producer waits for. The
  *   producer's bounded wait (about 2 s of SM clock) gives up, every role of
  *   the kernel unwinds through its own bounded waits, and dev_status

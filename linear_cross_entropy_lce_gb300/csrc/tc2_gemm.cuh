@@ -24,6 +24,16 @@
 
 namespace lce {
 
+// G formation in idle warps: work chunks of side_rb_group 64-row blocks of
+// one column segment. With a bias gradient, 8 blocks share one flush of the
+// column sums; without one, single blocks keep the CTAs working at the same
+// time on neighbouring segments of the same 64 rows (better DRAM locality).
+__host__ __device__ inline int64_t side_rb_group(const GradArgs& a) { return a.db_acc != nullptr ? 8 : 1; }
+__host__ __device__ inline int64_t side_chunks(const GradArgs& a) {
+  const int64_t rows_per_chunk = 64 * side_rb_group(a);
+  return ((a.rows + rows_per_chunk - 1) / rows_per_chunk) * a.nseg;
+}
+
 constexpr int TC2_BK = 64;
 constexpr int TC2_STAGES = 6;
 constexpr int TC2_A_BYTES = 128 * TC2_BK * 2;  // this CTA's 128 rows of A
@@ -99,7 +109,7 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
       bool ok = true;
       // rows of A formed by the side job of this launch: wait for all its units once
       bool dep_wait = side.enabled && side.claim != nullptr;
-      const int dep_units = static_cast<int>(((side.a.rows + 63) / 64) * side.a.nseg);
+      const int dep_units = static_cast<int>(side_chunks(side.a));
       for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
         int mb, nb;
         tc_tile_coords(g, tile, mb, nb);
@@ -196,7 +206,6 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
     // ---------------- side job: G formation of the previous row slab
     if (side.enabled) {
       const int tid = threadIdx.x - 64;
-      const int64_t nunits = ((side.a.rows + 63) / 64) * side.a.nseg;
       auto bar = [] { asm volatile("bar.sync 1, 64;" ::: "memory"); };
       bool go = true;
       if (side.comb) {
@@ -233,27 +242,45 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
         go = *unit_slot != 0;
         bar();
       }
-      auto unit = [&](int64_t u) {
-        const int seg = static_cast<int>(u % side.a.nseg);
-        const int64_t rb = u / side.a.nseg;
+      // Work chunks ordered row-group-major (chunk c -> row group c / nseg,
+      // segment c % nseg): the column sums are flushed once per chunk and the
+      // CTAs working at the same time read neighbouring segments of the same
+      // rows.
+      const int64_t nrb = (side.a.rows + 63) / 64;
+      const int64_t nchunks = side_chunks(side.a);
+      const int64_t kRbGroup = side_rb_group(side.a);
+      auto run_chunk = [&](int64_t c) {
+        using U16 = GradUnit<__half, 256, 64, 64, 16>;
+        using UB = GradUnit<__nv_bfloat16, 256, 64, 64, 16>;
+        const int seg = static_cast<int>(c % side.a.nseg);
+        const int64_t rb0 = (c / side.a.nseg) * kRbGroup;
+        float colsum[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) colsum[i] = 0.0f;
+        for (int64_t rb = rb0; rb < rb0 + kRbGroup && rb < nrb; ++rb) {
+          if (F16)
+            U16::form(side.a, seg, rb * 64, tid, colsum);
+          else
+            UB::form(side.a, seg, rb * 64, tid, colsum);
+        }
         if (F16)
-          grad_unit<__half, 256, 64, 64, 16>(side.a, seg, rb * 64, tid, side_red, bar);
+          U16::flush(side.a, seg, tid, colsum, side_red, bar);
         else
-          grad_unit<__nv_bfloat16, 256, 64, 64, 16>(side.a, seg, rb * 64, tid, side_red, bar);
+          UB::flush(side.a, seg, tid, colsum, side_red, bar);
       };
       if (!go) {
         // a merge wait gave up: the launch reports a timeout
       } else if (side.claim == nullptr) {
-        for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) unit(u);
+        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) run_chunk(c);
       } else {
-        // claimed units: progress does not depend on which CTAs are resident
+        // claimed chunks: progress does not depend on which CTAs are resident
         while (true) {
           if (tid == 0) *unit_slot = atomicAdd(side.claim, 1);
           bar();
-          const int64_t u = *unit_slot;
+          const int64_t c = *unit_slot;
           bar();  // every thread has read the slot before it is rewritten
-          if (u >= nunits) break;
-          unit(u);
+          if (c >= nchunks) break;
+          run_chunk(c);
           fence_proxy_async_all();  // G stores visible to the TMA loads of other CTAs
           __threadfence();
           bar();
