@@ -14,7 +14,11 @@
 //     multicast to the "empty" / "accumulator full" barriers of both CTAs;
 //     both CTAs' epilogue warps release an accumulator on the even CTA's
 //     "accumulator empty" barrier (8 arrivals).
-// Every wait is bounded as in tc_gemm.cuh.
+// Warps: 0 TMA producer, 1 MMA issuer (even CTA), 2 tensor-memory
+// allocation, 2-3 an optional side job (the per-row merge and G formation
+// of another row slab, see SideGrad), 4-7 epilogue (128-column tensor-memory
+// loads, stores through TMA where an output map is given). Every wait is
+// bounded as in tc_gemm.cuh.
 #pragma once
 
 #include "common.cuh"
