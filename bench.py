@@ -185,6 +185,13 @@ def _cores():
         return os.cpu_count()
 
 
+def _config(w, ws):
+    """The workload description both arms print."""
+    return {"workload": w.name, "N": w.N, "D": w.D, "C": w.C, "reduction": w.reduction,
+            "bias": w.bias, "targets": w.target_dist, "parallelism": "replicas" if ws > 1 else "single",
+            "l2": "inputs larger than L2 (W is %.2f GB)" % (w.C * max(w.D, 1) * 2 / 1e9)}
+
+
 def run_reference(args):
     ws, rank = _dist()
     if rank != 0:
@@ -202,7 +209,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": name, "N": w.N, "D": w.D, "C": w.C, "reduction": w.reduction},
+        "config": _config(w, ws),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
                          "sample": f"{rows} of {w.N} rows per step, full method (loss and all gradients "
                                    f"for those rows) in float64 numpy"},
@@ -492,9 +499,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic",
-        "config": {"workload": name, "N": w.N, "D": w.D, "C": w.C, "reduction": w.reduction,
-                   "bias": w.bias, "targets": w.target_dist, "parallelism": "replicas" if ws > 1 else "single",
-                   "l2": "inputs larger than L2 (W is %.2f GB)" % (w.C * max(w.D, 1) * 2 / 1e9)},
+        "config": _config(w, ws),
         "gpu_launches": launches,
         "clocks": clocks,
         "roofline": roofline,
