@@ -53,6 +53,111 @@ constexpr int TC2_TMEM_COLS = 512;
 constexpr int TC2_TILE_M = 256;  // rows per pair tile (128 per CTA)
 constexpr int TC2_TILE_N = 256;
 
+// The side job of warps 2-3 (64 threads, named barrier 1): an optional
+// merge phase, then the G formation of side.a (see SideGrad).
+template <bool F16>
+__device__ __forceinline__ void run_side_job(const SideGrad& side, float* side_red, volatile int* unit_slot,
+                                          volatile int* abort_flag) {
+  const int tid = threadIdx.x - 64;
+  auto bar = [] { asm volatile("bar.sync 1, 64;" ::: "memory"); };
+  bool go = true;
+  if (side.comb) {
+    // merge phase: claimed 32-row blocks, then wait until every block
+    // (merged by any CTA) is done before forming G from the scales
+    const int64_t nblk = (side.ca.rows + 31) / 32;
+    while (true) {
+      if (tid == 0) *unit_slot = atomicAdd(side.cclaim, 1);
+      bar();
+      const int64_t u = *unit_slot;
+      bar();
+      if (u >= nblk) break;
+      combine_rows32<64>(side.ca, u * 32, tid, side_red, bar);
+      __threadfence();
+      bar();
+      if (tid == 0) atomicAdd(side.cdone, 1);
+    }
+    if (tid == 0) {
+      int ok = 1;
+      const long long t0 = clock64();
+      while (ld_acquire_gpu(side.cdone) < nblk) {
+        if (*abort_flag || clock64() - t0 > kWaitLimitCycles) {
+          *abort_flag = 1;
+          ok = 0;
+          break;
+        }
+      }
+      // with the barrier below, the other threads' plain loads of the
+      // merged rows see what the merging CTAs wrote before counting
+      __threadfence();
+      *unit_slot = ok;
+    }
+    bar();
+    go = *unit_slot != 0;
+    bar();
+  }
+  // Work chunks ordered row-group-major (chunk c -> row group c / nseg,
+  // segment c % nseg): the column sums are flushed once per chunk and the
+  // CTAs working at the same time read neighbouring segments of the same
+  // rows.
+  const int64_t nrb = (side.a.rows + 63) / 64;
+  const int64_t nchunks = side_chunks(side.a);
+  const int64_t kRbGroup = side_rb_group(side.a);
+  auto run_chunk = [&](int64_t c) {
+    using U16 = GradUnit<__half, 256, 64, 64, 16>;
+    using UB = GradUnit<__nv_bfloat16, 256, 64, 64, 16>;
+    const int seg = static_cast<int>(c % side.a.nseg);
+    const int64_t rb0 = (c / side.a.nseg) * kRbGroup;
+    float colsum[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) colsum[i] = 0.0f;
+    for (int64_t rb = rb0; rb < rb0 + kRbGroup && rb < nrb; ++rb) {
+      if (F16)
+        U16::form(side.a, seg, rb * 64, tid, colsum);
+      else
+        UB::form(side.a, seg, rb * 64, tid, colsum);
+    }
+    if (F16)
+      U16::flush(side.a, seg, tid, colsum, side_red, bar);
+    else
+      UB::flush(side.a, seg, tid, colsum, side_red, bar);
+  };
+  if (!go) {
+    // a merge wait gave up: the launch reports a timeout
+  } else if (side.claim == nullptr) {
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) run_chunk(c);
+  } else {
+    // claimed chunks: progress does not depend on which CTAs are resident
+    while (true) {
+      if (tid == 0) *unit_slot = atomicAdd(side.claim, 1);
+      bar();
+      const int64_t c = *unit_slot;
+      bar();  // every thread has read the slot before it is rewritten
+      if (c >= nchunks) break;
+      run_chunk(c);
+      fence_proxy_async_all();  // G stores visible to the TMA loads of other CTAs
+      __threadfence();
+      bar();
+      if (tid == 0) atomicAdd(side.done, 1);
+    }
+  }
+}
+
+// Bounded wait of a producer until the side job's G formation is complete
+// (all chunks counted), then the proxy fence that lets its TMA loads see
+// the G stores. False (abort flag set) when the wait gives up.
+__device__ __forceinline__ bool wait_side_done(const SideGrad& side, volatile int* abort_flag) {
+  const int target = static_cast<int>(side_chunks(side.a));
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(side.done) < target) {
+    if (*abort_flag || clock64() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  fence_proxy_async_all();
+  return true;
+}
+
 template <bool A_MN, bool B_MN, class Epi, bool F16>
 __global__ void __launch_bounds__(TC2_THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -113,23 +218,16 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
       bool ok = true;
       // rows of A formed by the side job of this launch: wait for all its units once
       bool dep_wait = side.enabled && side.claim != nullptr;
-      const int dep_units = static_cast<int>(side_chunks(side.a));
       for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
         int mb, nb;
         tc_tile_coords(g, tile, mb, nb);
         const int m0 = mb * TC2_TILE_M + static_cast<int>(rank) * 128;
         const int n0 = nb * TC2_TILE_N + static_cast<int>(rank) * 128;
         if (dep_wait && m0 + 128 > side.dep_row0 && m0 < side.dep_row0 + side.a.rows) {
-          const long long t0 = clock64();
-          while (ld_acquire_gpu(side.done) < dep_units) {
-            if (*abort_flag || clock64() - t0 > kWaitLimitCycles) {
-              *abort_flag = 1;
-              ok = false;
-              break;
-            }
+          if (!wait_side_done(side, abort_flag)) {
+            ok = false;
+            break;
           }
-          if (!ok) break;
-          fence_proxy_async_all();  // the TMA loads below see the side job's G stores
           dep_wait = false;
         }
         for (int kb = 0; kb < nkb; ++kb) {
@@ -207,91 +305,8 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
       }
     }
   } else if (warp == 2 || warp == 3) {
-    // ---------------- side job: G formation of the previous row slab
-    if (side.enabled) {
-      const int tid = threadIdx.x - 64;
-      auto bar = [] { asm volatile("bar.sync 1, 64;" ::: "memory"); };
-      bool go = true;
-      if (side.comb) {
-        // merge phase: claimed 32-row blocks, then wait until every block
-        // (merged by any CTA) is done before forming G from the scales
-        const int64_t nblk = (side.ca.rows + 31) / 32;
-        while (true) {
-          if (tid == 0) *unit_slot = atomicAdd(side.cclaim, 1);
-          bar();
-          const int64_t u = *unit_slot;
-          bar();
-          if (u >= nblk) break;
-          combine_rows32<64>(side.ca, u * 32, tid, side_red, bar);
-          __threadfence();
-          bar();
-          if (tid == 0) atomicAdd(side.cdone, 1);
-        }
-        if (tid == 0) {
-          int ok = 1;
-          const long long t0 = clock64();
-          while (ld_acquire_gpu(side.cdone) < nblk) {
-            if (*abort_flag || clock64() - t0 > kWaitLimitCycles) {
-              *abort_flag = 1;
-              ok = 0;
-              break;
-            }
-          }
-          // with the barrier below, the other threads' plain loads of the
-          // merged rows see what the merging CTAs wrote before counting
-          __threadfence();
-          *unit_slot = ok;
-        }
-        bar();
-        go = *unit_slot != 0;
-        bar();
-      }
-      // Work chunks ordered row-group-major (chunk c -> row group c / nseg,
-      // segment c % nseg): the column sums are flushed once per chunk and the
-      // CTAs working at the same time read neighbouring segments of the same
-      // rows.
-      const int64_t nrb = (side.a.rows + 63) / 64;
-      const int64_t nchunks = side_chunks(side.a);
-      const int64_t kRbGroup = side_rb_group(side.a);
-      auto run_chunk = [&](int64_t c) {
-        using U16 = GradUnit<__half, 256, 64, 64, 16>;
-        using UB = GradUnit<__nv_bfloat16, 256, 64, 64, 16>;
-        const int seg = static_cast<int>(c % side.a.nseg);
-        const int64_t rb0 = (c / side.a.nseg) * kRbGroup;
-        float colsum[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) colsum[i] = 0.0f;
-        for (int64_t rb = rb0; rb < rb0 + kRbGroup && rb < nrb; ++rb) {
-          if (F16)
-            U16::form(side.a, seg, rb * 64, tid, colsum);
-          else
-            UB::form(side.a, seg, rb * 64, tid, colsum);
-        }
-        if (F16)
-          U16::flush(side.a, seg, tid, colsum, side_red, bar);
-        else
-          UB::flush(side.a, seg, tid, colsum, side_red, bar);
-      };
-      if (!go) {
-        // a merge wait gave up: the launch reports a timeout
-      } else if (side.claim == nullptr) {
-        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) run_chunk(c);
-      } else {
-        // claimed chunks: progress does not depend on which CTAs are resident
-        while (true) {
-          if (tid == 0) *unit_slot = atomicAdd(side.claim, 1);
-          bar();
-          const int64_t c = *unit_slot;
-          bar();  // every thread has read the slot before it is rewritten
-          if (c >= nchunks) break;
-          run_chunk(c);
-          fence_proxy_async_all();  // G stores visible to the TMA loads of other CTAs
-          __threadfence();
-          bar();
-          if (tid == 0) atomicAdd(side.done, 1);
-        }
-      }
-    }
+    // ---------------- side job: merge and G formation of another row slab
+    if (side.enabled) run_side_job<F16>(side, side_red, unit_slot, abort_flag);
   } else if (warp >= 4) {
     // ---------------- epilogue (both CTAs): this CTA's 128 rows of the tile
     const int q = warp & 3;
