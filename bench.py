@@ -41,10 +41,10 @@ METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor
 MEASURED_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the full-size
     # step, per launch; see profiles/tc2_gemm_bf16_llm_head_traffic.md
-    ("bf16_llm_head", "gemm_logits_tc"): (1135656192 + 517704704 + 1812763904 + 1048631296 + 1837804544
-                                          + 1049351936 + 1808848128 + 1049269760) / 4,  # mean of 4 slabs
-    ("bf16_llm_head", "gemm_dx_tc"): 16933255424 + 595223808,
-    ("bf16_llm_head", "gemm_dw_tc"): 10297675776 + 1042369024,
+    ("bf16_llm_head", "gemm_logits_tc"): (1258640128 + 519451648 + 2606860544 + 1053282816 + 2437540096
+                                          + 1052864256 + 2464549376 + 1052785152) / 4,  # mean of 4 slabs
+    ("bf16_llm_head", "gemm_dx_tc"): 21192143104 + 596788224,
+    ("bf16_llm_head", "gemm_dw_tc"): 13933914880 + 1042174464,
     # see profiles/tc2x3_gemm_fp32_mid.md
     ("fp32_mid", "gemm_logits_3xtf32"): 42238208 + 10453504,
     ("fp32_mid", "gemm_dx_3xtf32"): 176070656 + 531968,
