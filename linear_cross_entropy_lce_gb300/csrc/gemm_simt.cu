@@ -10,11 +10,9 @@ template <bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_sg(const float* A, const float* B, int64_t lda, int64_t ldb, int64_t M, int64_t N, int64_t K,
                       const typename Epi::Params& ep, int kid, cudaStream_t s, int splits = 1) {
   auto kern = simt_gemm_kernel<A_MN, B_MN, Epi>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SG_SMEM_BYTES);
+  {
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), SG_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   if (M == 0 || N == 0) return cudaSuccess;
   const int64_t gx = (N + SG_BN - 1) / SG_BN, gy = (M + SG_BM - 1) / SG_BM;

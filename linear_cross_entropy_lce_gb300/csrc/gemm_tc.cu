@@ -33,11 +33,9 @@ template <bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, int m_inner,
                       int* status, const typename Epi::Params& ep, int kid, cudaStream_t s) {
   auto kern = tc_gemm_kernel<A_MN, B_MN, Epi>;
-  static bool attr_set = false;  // one device per process is assumed for the attribute cache
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_BYTES);
+  {
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), TC_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   TcGemmArgs g;
   g.M = M;
@@ -63,11 +61,9 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
                        int K, int m_inner, int* status, const typename Epi::Params& ep, int kid, cudaStream_t s,
                        const SideGrad* side = nullptr) {
   auto kern = tc2_gemm_kernel<A_MN, B_MN, Epi, F16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TC2_SMEM_BYTES);
+  {
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), TC2_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   TcGemmArgs g;
   g.M = M;

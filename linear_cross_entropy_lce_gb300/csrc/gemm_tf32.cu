@@ -118,11 +118,9 @@ template <class Epi>
 cudaError_t launch_tx(const TxOperands& o, int M, int N, int K, int m_inner, int splits, int* status,
                       const typename Epi::Params& ep, int kid, cudaStream_t s) {
   auto kern = tc2x3_gemm_kernel<Epi>;
-  static bool attr_set = false;  // one device per process is assumed for the attribute cache
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TX_SMEM_BYTES);
+  {
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), TX_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   TxArgs g;
   g.M = M;

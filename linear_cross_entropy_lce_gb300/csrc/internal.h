@@ -45,6 +45,11 @@ void prof_after(int id, cudaStream_t s);
 
 int num_sms();
 
+// Sets the kernel's maximum dynamic shared memory on the current device the
+// first time the kernel is launched there (a per-device, per-kernel cache,
+// so one process may use the library on several GPUs).
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
 struct SideGrad;
 
 // ---- tcgen05 GEMM (gemm_tc.cu)
