@@ -45,6 +45,11 @@ MEASURED_TRAFFIC = {
                                           + 1052864256 + 2464549376 + 1052785152) / 4,  # mean of 4 slabs
     ("bf16_llm_head", "gemm_dx_tc"): 21192143104 + 596788224,
     ("bf16_llm_head", "gemm_dw_tc"): 13933914880 + 1042174464,
+    # see profiles/tc2_gemm_bf16_large_head.md: mean of the 5 logits launches of a step
+    ("bf16_large_head", "gemm_logits_tc"): (24336470272 + 3735230208 + 7337553920 + 7294764544
+                                            + 7505232128) / 5,
+    ("bf16_large_head", "gemm_dx_tc"): 52641719296 + 1227354112,
+    ("bf16_large_head", "gemm_dw_tc"): 45915678976 + 1071470848,
     # see profiles/tc2x3_gemm_fp32_mid.md
     ("fp32_mid", "gemm_logits_3xtf32"): 42238208 + 10453504,
     ("fp32_mid", "gemm_dx_3xtf32"): 176070656 + 531968,
