@@ -50,7 +50,7 @@ MEASURED_TRAFFIC = {
                                             + 7505232128) / 5,
     ("bf16_large_head", "gemm_dx_tc"): 52641719296 + 1227354112,
     ("bf16_large_head", "gemm_dw_tc"): 45915678976 + 1071470848,
-    # see profiles/ce_resident_logits_fp32_N2048_V131072.md (full-size 1-pass capture)
+    # see profiles/ce_resident_ce_logits_fp32.md (full-size 1-pass capture)
     ("ce_logits_fp32", "ce_resident"): 8590645760 + 8527984384,
     # see profiles/tc2x3_gemm_fp32_mid.md
     ("fp32_mid", "gemm_logits_3xtf32"): 42238208 + 10453504,
