@@ -295,6 +295,7 @@ def profile_summary() -> dict:
 # ---- building-block checks (include/lce_testing.h)
 
 def test_gemm_bf16(A, B, M, N, K, a_mn_major, b_mn_major, status=None, cta_pair=False, stream=None):
+    """lce_test_gemm_bf16: fp32 [M, N] = A B^T on the tcgen05 engine (layouts as in lce_testing.h)."""
     lib = load_library()
     out = torch.empty(M, N, dtype=torch.float32, device=A.device)
     _check(lib.lce_test_gemm_bf16(_ptr(A), _ptr(B), _ptr(out), M, N, K, int(a_mn_major), int(b_mn_major),
@@ -303,6 +304,7 @@ def test_gemm_bf16(A, B, M, N, K, a_mn_major, b_mn_major, status=None, cta_pair=
 
 
 def test_gemm_bf16_unmet_dependency(A, B, M, N, K, counters, status, stream=None):
+    """lce_test_gemm_bf16_unmet_dependency: the failure path of the bounded waits (see lce_testing.h)."""
     lib = load_library()
     out = torch.empty(M, N, dtype=torch.float32, device=A.device)
     _check(lib.lce_test_gemm_bf16_unmet_dependency(_ptr(A), _ptr(B), _ptr(out), M, N, K, _ptr(counters),
@@ -312,6 +314,7 @@ def test_gemm_bf16_unmet_dependency(A, B, M, N, K, counters, status, stream=None
 
 
 def test_gemm_tf32x3(A, B, M, N, K, a_mn_major, b_mn_major, k_splits=1, status=None, stream=None):
+    """lce_test_gemm_tf32x3: fp32 [M, N] = A B^T as three TF32 products on the tensor cores."""
     lib = load_library()
     out = torch.empty(M, N, dtype=torch.float32, device=A.device)
     ldk = (K + 3) // 4 * 4
@@ -324,6 +327,7 @@ def test_gemm_tf32x3(A, B, M, N, K, a_mn_major, b_mn_major, k_splits=1, status=N
 
 
 def test_gemm_f32(A, B, M, N, K, a_mn_major, b_mn_major, stream=None):
+    """lce_test_gemm_f32: fp32 [M, N] = A B^T with fp32 FMA on the CUDA cores."""
     lib = load_library()
     out = torch.empty(M, N, dtype=torch.float32, device=A.device)
     _check(lib.lce_test_gemm_f32(_ptr(A), _ptr(B), _ptr(out), M, N, K, int(a_mn_major), int(b_mn_major),
