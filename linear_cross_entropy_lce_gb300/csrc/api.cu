@@ -375,9 +375,10 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
     const int64_t row0 = ci * p.Bc;
     const int64_t rows = std::min(p.Bc, N - row0);
     // ---- logits, row lse / loss, and G, over row slabs of the chunk. On the
-    // CTA-pair path with a backward, the chunk is cut into 4 slabs and the
-    // idle warps of slab k's logits GEMM form G for slab k-1, so only the
-    // last slab's G formation runs as a kernel of its own.
+    // CTA-pair path with a backward (>= 1024 rows), the chunk is cut into up
+    // to 4 slabs; the idle warps of slab k's logits GEMM merge the rows of
+    // slab k-1 and form its G, and those of the dX GEMM do the same for the
+    // last slab.
     if (p.tf32) {  // TF32 parts of the chunk's rows of X (and of X^T for dW)
       SplitArgs sa;
       sa.src = static_cast<const float*>(X) + row0 * D;
@@ -393,16 +394,32 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       LCE_TRY(launch_split_tf32(sa, s));
     }
     const bool slabbed = p.tc && pair && backward && rows >= 1024;
-    const int64_t slab = slabbed ? ceil_div(ceil_div(rows, 4), 256) * 256 : rows;
-    const int64_t nslab = ceil_div(rows, slab);
+    // Slab k's G formation runs beside slab k+1's logits GEMM, so the slabs
+    // grow (about 4 : 7 : 9 : 12 of the rows, in multiples of 256): each side
+    // job forms fewer rows than the GEMM beside it computes, and the largest,
+    // last slab goes to the long dX GEMM.
+    int64_t slab_off[5] = {0, rows, rows, rows, rows};
+    int64_t nslab = 1;
+    if (slabbed) {
+      static const int64_t kSlabWeight[4] = {4, 7, 9, 12};  // of 32
+      int64_t off = 0;
+      nslab = 0;
+      for (int k = 0; k < 4 && off < rows; ++k) {
+        int64_t sz = k == 3 ? rows - off : ceil_div(ceil_div(rows * kSlabWeight[k], 32), 256) * 256;
+        if (sz > rows - off) sz = rows - off;
+        slab_off[nslab++] = off;
+        off += sz;
+      }
+      slab_off[nslab] = rows;
+    }
     GradArgs ga_prev, ga_last;
     CombineArgs ca_prev, ca_last;  // merges deferred into the next GEMM's idle warps
     bool have_prev = false, have_last = false;
     int64_t last_row0 = 0, last_si = 0;
     int* cnt = counters + ci * kCountersPerChunk;
     for (int64_t si = 0; si < nslab; ++si) {
-      const int64_t so = si * slab;                      // slab offset within the chunk
-      const int64_t sr = std::min(slab, rows - so);      // rows in the slab
+      const int64_t so = slab_off[si];                   // slab offset within the chunk
+      const int64_t sr = slab_off[si + 1] - so;          // rows in the slab
       EpiLse::Params el;
       el.bias = b;
       el.bias_dt = dtype;
