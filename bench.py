@@ -41,15 +41,16 @@ METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor
 MEASURED_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the full-size
     # step, per launch; see profiles/tc2_gemm_bf16_llm_head_traffic.md
-    ("bf16_llm_head", "gemm_logits_tc"): (1258640128 + 519451648 + 2606860544 + 1053282816 + 2437540096
-                                          + 1052864256 + 2464549376 + 1052785152) / 4,  # mean of 4 slabs
-    ("bf16_llm_head", "gemm_dx_tc"): 21192143104 + 596788224,
-    ("bf16_llm_head", "gemm_dw_tc"): 13933914880 + 1042174464,
+    ("bf16_llm_head", "gemm_logits_tc"): (1085808384 + 252943616 + 1376624896 + 714537728 + 1619247616
+                                          + 1047489280 + 1890603776 + 1382050304) / 4,  # mean of 4 slabs
+    ("bf16_llm_head", "gemm_dx_tc"): 17544397312 + 862763264,
+    ("bf16_llm_head", "gemm_dw_tc"): 11263625216 + 1043292160,
     # see profiles/tc2_gemm_bf16_large_head.md: mean of the 5 logits launches of a step
-    ("bf16_large_head", "gemm_logits_tc"): (24336470272 + 3735230208 + 7337553920 + 7294764544
-                                            + 7505232128) / 5,
-    ("bf16_large_head", "gemm_dx_tc"): 52641719296 + 1227354112,
-    ("bf16_large_head", "gemm_dw_tc"): 45915678976 + 1071470848,
+    ("bf16_large_head", "gemm_logits_tc"): (19411388160 + 70922496 + 1130574336 + 524168704 + 2069232128
+                                            + 1482686720 + 3842266624 + 2168438528 + 8193454848
+                                            + 2856722432) / 5,
+    ("bf16_large_head", "gemm_dx_tc"): 47722717696 + 1773781760,
+    ("bf16_large_head", "gemm_dw_tc"): 41360279808 + 1070604544,
     # see profiles/ce_resident_ce_logits_fp32.md (full-size 1-pass capture)
     ("ce_logits_fp32", "ce_resident"): 8590645760 + 8527984384,
     # see profiles/tc2x3_gemm_fp32_mid.md
