@@ -13,7 +13,7 @@
 //     dW GEMM       dW (+)= G^T X_c
 //   loss finalize, bias-gradient finalize
 // On the bf16 / fp16 CTA-pair path with >= 1024 chunk rows the logits GEMM
-// runs over 4 row slabs, and combine + grad of slab k run in the idle warps
+// runs over up to 4 row slabs of growing size, and combine + grad of slab k run in the idle warps
 // of the GEMM that follows it (slab k+1's logits GEMM, or the dX GEMM for
 // the last slab, whose producer waits for those rows), so no combine or
 // grad kernel is launched. fp32 inputs add the TF32 hi / lo splits of W,
