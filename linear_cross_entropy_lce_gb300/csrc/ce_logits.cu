@@ -5,13 +5,14 @@
 // logits with dLoss/dlogits during the forward. Here the whole row is read
 // from HBM once and written once:
 //
-//  * resident kernel: a thread-block cluster of CS CTAs (CS = 1..8) owns a
+//  * resident kernel: a thread-block cluster of CS CTAs (CS = 1..16) owns a
 //    row; each CTA holds a 16384-element slice in registers (512 threads x
 //    32 elements, 16-byte vector loads), reduces its slice to (max, sum-exp),
 //    exchanges the pairs through distributed shared memory, and writes
 //    g * w_n * (softmax - onehot) back from registers. Clusters walk the
-//    rows persistently. Needs V <= 8 * 16384 and 16-byte aligned rows.
-//  * streaming kernel (any V, any alignment): one CTA per row, online
+//    rows persistently. Needs V <= 16 * 16384 and 16-byte aligned rows.
+//  * streaming kernel (any V, any alignment; used when V > 262144, rows are
+//    not 16-byte aligned, or no cluster fits): one CTA per row, online
 //    (max, sum-exp) in a first pass, gradient in a second pass that reads
 //    the row again (largely from L2).
 #include <cfloat>
@@ -271,9 +272,19 @@ template <class T>
 cudaError_t launch_ce_t(const CeArgs& a, cudaStream_t s) {
   const size_t esz = sizeof(T);
   const bool aligned = (reinterpret_cast<uintptr_t>(a.logits) % 16 == 0) && ((a.V * esz) % 16 == 0);
-  int cs = 1;
-  while (static_cast<int64_t>(cs) * CE_SLICE < a.V && cs < 8) cs *= 2;
-  if (aligned && static_cast<int64_t>(cs) * CE_SLICE >= a.V) {
+  // one 16384-element slice per CTA: a cluster of ceil(V / 16384) CTAs,
+  // up to 16 (above 8 a non-portable cluster size, allowed per kernel; the
+  // occupancy query below falls back to streaming when no cluster fits)
+  const int64_t need = (a.V + CE_SLICE - 1) / CE_SLICE;
+  int cs = need < 16 ? static_cast<int>(need) : 16;
+  if (cs > 8) {
+    cudaError_t e = cudaFuncSetAttribute(ce_resident_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      cs = 0;  // stream the rows instead
+    }
+  }
+  if (aligned && cs > 0 && static_cast<int64_t>(cs) * CE_SLICE >= a.V) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

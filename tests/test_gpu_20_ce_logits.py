@@ -19,7 +19,11 @@ CASES = [
     (64, 40000, torch.float32, "sum", 5),       # cluster of 4
     (16, 131072, torch.float32, "mean", 0),     # cluster of 8
     (19, 1001, torch.float32, "mean", 2),       # V % 4 != 0: streaming kernel
-    (9, 200003, torch.float32, "sum", 1),       # V > 8 * 16384: streaming kernel
+    (9, 200003, torch.float32, "sum", 1),       # V * 4 bytes not a multiple of 16: streaming kernel
+    (12, 150000, torch.float32, "mean", 2),     # cluster of 16 (non-portable size)
+    (6, 262144, torch.float32, "none", 1),      # cluster of 16, full slices
+    (10, 200000, torch.bfloat16, "sum", 1),     # cluster of 16, bf16
+    (5, 262148, torch.float32, "mean", 1),      # V > 16 * 16384: streaming kernel
     (33, 50000, torch.bfloat16, "mean", 4),
     (20, 777, torch.bfloat16, "none", 2),       # streaming (V % 8 != 0)
     (25, 4096, torch.float32, "none", 3),
