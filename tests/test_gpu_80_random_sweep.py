@@ -37,7 +37,9 @@ def _case(i):
     case = dict(
         dtype=dtype, N=N, D=D, C=C, reduction=red, bias=r.random() < 0.5, n_ignored=n_ign,
         class_weight=r.random() < 0.3, chunk_rows=r.choice([0, 0, 128, 512]),
-        grad_dtype=(torch.float32 if r.random() < 0.2 else None),
+        grad_dtype=(torch.float32 if r.random() < 0.2 else
+                    (r.choice([torch.bfloat16, torch.float16]) if dtype == torch.float32 and r.random() < 0.25
+                     else None)),
         want=(tuple(r.random() < 0.7 for _ in range(3)) if r.random() < 0.2 else (True, True, True)),
         zipf=r.random() < 0.3, w_std=r.choice([0.05, 0.3, 1.0]), seed=r.randrange(1 << 30))
     return case
@@ -75,8 +77,8 @@ def test_random_case(cuda_lib, i):
                                             to64(g), class_weight=to64(cw))
     tol = TOL[c["dtype"]]
     gtol = tol["grad"]
-    if c["grad_dtype"] is None and c["dtype"] == torch.bfloat16:
-        gtol = TOL[torch.bfloat16]["grad"]
+    if c["grad_dtype"] in (torch.bfloat16, torch.float16):  # 16-bit gradient storage
+        gtol = max(gtol, TOL[c["grad_dtype"]]["grad"])
     what = _describe(c)
     if c["reduction"] == "none":
         assert rel_max(to64(loss), rl) < tol["loss"], what
