@@ -10,7 +10,8 @@
 //    32 elements, 16-byte vector loads), reduces its slice to (max, sum-exp),
 //    exchanges the pairs through distributed shared memory, and writes
 //    g * w_n * (softmax - onehot) back from registers. Clusters walk the
-//    rows persistently. Needs V <= 16 * 16384 and 16-byte aligned rows.
+//    rows persistently, each CTA prefetching its slice of the next row into
+//    L2 with the copy engine. Needs V <= 16 * 16384 and 16-byte aligned rows.
 //  * streaming kernel (any V, any alignment; used when V > 262144, rows are
 //    not 16-byte aligned, or no cluster fits): one CTA per row, online
 //    (max, sum-exp) in a first pass, gradient in a second pass that reads
@@ -37,41 +38,12 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
-// Merge two (max, sum of exp(x - max)) pairs.
-__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
-  const float mn = fmaxf(m, m2);
-  const float a = (m == -INFINITY) ? 0.0f : s * fast_exp2((m - mn) * kLog2e);
-  const float b = (m2 == -INFINITY) ? 0.0f : s2 * fast_exp2((m2 - mn) * kLog2e);
-  m = mn;
-  s = a + b;
-}
-// Block-wide merge of per-thread (max, sum-exp) pairs in one reduction;
-// every thread gets the block's pair.
-__device__ __forceinline__ void block_merge_ms(float& m, float& s, float2* scratch2) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    merge_ms(m, s, m2, s2);
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) scratch2[warp] = make_float2(m, s);
-  __syncthreads();
-  const int nw = blockDim.x >> 5;
-  m = -INFINITY;
-  s = 0.0f;
-  if (lane < nw) {
-    const float2 p = scratch2[lane];
-    m = p.x;
-    s = p.y;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    merge_ms(m, s, m2, s2);
-  }
+// Warp-wide merge of per-lane (max, sum of exp(x - max)) pairs: the warp's
+// max first, then one rescale per lane and a sum. Every lane gets the pair.
+__device__ __forceinline__ void warp_merge_ms(float& m, float& s) {
+  const float wm = warp_max(m);
+  s = warp_sum(m == -INFINITY ? 0.0f : s * fast_exp2((m - wm) * kLog2e));
+  m = wm;
 }
 
 // Block-wide reductions over CE_THREADS threads; every thread gets the result.
@@ -180,19 +152,39 @@ __global__ void __launch_bounds__(CE_THREADS, 2) ce_resident_kernel(const CeArgs
     const bool valid = target_valid(t, a.ignore_index, V);
     float zt = 0.0f;
     if (rank == 0 && tid == 0 && valid) zt = to_f32(rowp[t]);  // read before any CTA writes the row
-    // per-thread (max, sum-exp), then one block-wide merge of the pairs
+    // One thread starts the copy engine fetching this CTA's slice of its
+    // next row into L2, so that those loads find it there; the prefetch
+    // holds no registers and no barrier waits for it.
+    if (tid == 0 && row + ncl < a.N && sbeg < V) {
+      const int64_t n = (V - sbeg < CE_SLICE ? V - sbeg : CE_SLICE) * static_cast<int64_t>(sizeof(T));
+      bulk_prefetch_l2(rowp + static_cast<int64_t>(ncl) * V + sbeg, static_cast<uint32_t>(n));
+    }
+    // Per-thread max cm; x[i] is replaced by e_i = exp(x_i - cm), so that
+    // the gradient needs one more exponential per thread, not one per
+    // element: softmax_i = e_i * exp(cm - lse). A thread whose values are
+    // all -inf (padding past V, or -inf logits) takes no shift: its e_i = 0.
     float cm = -INFINITY;
 #pragma unroll
     for (int i = 0; i < CE_EPT; ++i) cm = fmaxf(cm, x[i]);
+    const float cm2 = (cm == -INFINITY) ? 0.0f : cm * kLog2e;
     float csum = 0.0f;
-    if (cm != -INFINITY) {  // all-padding threads (past V) contribute nothing
 #pragma unroll
-      for (int i = 0; i < CE_EPT; ++i) csum += fast_exp2((x[i] - cm) * kLog2e);
+    for (int i = 0; i < CE_EPT; ++i) {
+      x[i] = fast_exp2(fmaf(x[i], kLog2e, -cm2));
+      csum += x[i];
     }
-    block_merge_ms(cm, csum, scratch2);
-    if (tid == 0) {
-      xch[iter & 1][0] = cm;
-      xch[iter & 1][1] = csum;
+    // warp pairs, then warp 0 merges the CTA's pairs for the cluster exchange
+    float wm = cm, wsum = csum;
+    warp_merge_ms(wm, wsum);
+    if (lane == 0) scratch2[warp] = make_float2(wm, wsum);
+    __syncthreads();
+    if (warp == 0) {
+      float2 pr = (lane < CE_THREADS / 32) ? scratch2[lane] : make_float2(-INFINITY, 0.0f);
+      warp_merge_ms(pr.x, pr.y);
+      if (lane == 0) {
+        xch[iter & 1][0] = pr.x;
+        xch[iter & 1][1] = pr.y;
+      }
     }
     cluster_sync();
     if (warp == 0) {
@@ -210,15 +202,16 @@ __global__ void __launch_bounds__(CE_THREADS, 2) ce_resident_kernel(const CeArgs
     }
     __syncthreads();
     const float lse = bc[0], w = bc[1];
-    const float lse2 = lse * kLog2e;
+    // w * exp(cm - lse): 0 for all-padding threads (cm = -inf)
+    const float ws = w * fast_exp2((cm - lse) * kLog2e);
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int64_t col = sbeg + static_cast<int64_t>(tid + k * CE_THREADS) * VE;
       float gv[VE];
 #pragma unroll
       for (int i = 0; i < VE; ++i) {
-        const float p = fast_exp2(fmaf(x[k * VE + i], kLog2e, -lse2));
-        gv[i] = w * ((valid && col + i == t) ? p - 1.0f : p);
+        const float e = x[k * VE + i];
+        gv[i] = (valid && col + i == t) ? fmaf(e, ws, -w) : e * ws;
       }
       if (col + VE <= V) {
         store_vec<T>(rowp + col, gv);
@@ -250,7 +243,7 @@ __global__ void __launch_bounds__(CE_THREADS) ce_stream_kernel(const CeArgs a) {
       if (x > m) {
         s = s * fast_exp2((m - x) * kLog2e) + 1.0f;
         m = x;
-      } else {
+      } else if (m != -INFINITY) {  // x = m = -inf adds exp(-inf) = 0, not exp(NaN)
         s += fast_exp2((x - m) * kLog2e);
       }
     }

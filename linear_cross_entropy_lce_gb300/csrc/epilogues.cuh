@@ -176,7 +176,10 @@ struct EpiLse {
         }
       }
     }
-    // pass 2: sum of exp(z - m), target logit, optional P~ store
+    // pass 2: sum of exp(z - m), target logit, optional P~ store. A segment
+    // whose logits are all -inf (a bias of -inf masks classes) is shifted
+    // by 0, so that it stores P~ = exp(-inf) = 0 and sums to 0, not NaN.
+    if (m == -INFINITY) m = 0.0f;
     float s = 0.0f, ztv = 0.0f;
 #pragma unroll 1
     for (int g = 0; g < NG; ++g) {
@@ -222,7 +225,7 @@ struct EpiLse {
       }
     }
     if (row_ok && col0 < p.C) {
-      p.partial[seg * p.partial_ld + row] = make_float2(m, s);
+      p.partial[seg * p.partial_ld + row] = make_float2(s == 0.0f ? -INFINITY : m, s);
       if (tl >= 0) p.zt[row] = ztv;
     }
   }

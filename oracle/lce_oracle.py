@@ -199,7 +199,8 @@ def ce_from_logits(logits, target, reduction="mean", ignore_index=DEFAULT_IGNORE
         lse = log_sum_exp(zb)
         rows = np.arange(r1 - r0)
         zt = zb[rows, tc[r0:r1]]
-        loss_rows[r0:r1] = np.where(valid[r0:r1], c[r0:r1] * (lse - zt), 0.0)
+        with np.errstate(invalid="ignore"):  # an ignored row's placeholder column may be -inf
+            loss_rows[r0:r1] = np.where(valid[r0:r1], c[r0:r1] * (lse - zt), 0.0)
         if want_grad:
             P = np.exp(zb - lse[:, None])
             P[rows, tc[r0:r1]] -= valid[r0:r1].astype(np.float64)
@@ -231,7 +232,8 @@ def lce_forward(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE_I
         z = logits_block(X[r0:r1], W, b)
         lse[r0:r1] = log_sum_exp(z)
         zt = z[np.arange(r1 - r0), tc[r0:r1]]
-        loss_rows[r0:r1] = np.where(valid[r0:r1], c[r0:r1] * (lse[r0:r1] - zt), 0.0)
+        with np.errstate(invalid="ignore"):  # an ignored row's placeholder column may be -inf
+            loss_rows[r0:r1] = np.where(valid[r0:r1], c[r0:r1] * (lse[r0:r1] - zt), 0.0)
     return _reduce(loss_rows, c, reduction), lse
 
 
@@ -268,7 +270,8 @@ def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=DEFAULT
         z = logits_block(X[r0:r1], W, b)
         lse = log_sum_exp(z)
         zt = z[rows, tc[r0:r1]]
-        loss_rows[r0:r1] = np.where(valid[r0:r1], c[r0:r1] * (lse - zt), 0.0)
+        with np.errstate(invalid="ignore"):  # an ignored row's placeholder column may be -inf
+            loss_rows[r0:r1] = np.where(valid[r0:r1], c[r0:r1] * (lse - zt), 0.0)
         G = np.exp(z - lse[:, None])
         G[rows, tc[r0:r1]] -= valid[r0:r1].astype(np.float64)
         G *= w[r0:r1, None]

@@ -96,3 +96,41 @@ def test_ce_logits_edge_cases(cuda_lib):
                                                   workspace=ws)
     assert cuda_lib.lce_read_device_status(ws) == 8
     assert loss[2].item() == 0.0 and (logits[2] == 0).all()
+
+
+@pytest.mark.parametrize("V,dtype", [
+    (40000, torch.float32),     # resident, cluster of 4
+    (131072, torch.float32),    # resident, cluster of 8
+    (50000, torch.bfloat16),    # resident, bf16
+    (1001, torch.float32),      # streaming
+])
+def test_ce_logits_masked_columns(cuda_lib, V, dtype):
+    """Logits masked with -inf (a vocabulary mask): a contiguous block that
+    covers whole per-thread slices of the resident kernel, scattered entries
+    on every other row, and one row that is -inf everywhere but its target.
+    Masked columns get probability 0, hence gradient 0; the last row has
+    loss 0 and gradient 0."""
+    N = 9
+    inp = make_logits_inputs(N, V, dtype, "cuda", seed=V + 7, std=2.0, n_ignored=1)
+    logits, t = inp["logits"], inp["target"].clone()
+    logits[:, V // 4: V // 2] = -math.inf
+    logits[::2, ::3] = -math.inf
+    # targets in columns that stay finite: j < V // 4 and j % 3 == 1
+    valid = t != -100
+    t[valid] = 1 + 3 * (torch.arange(int(valid.sum()), device="cuda") * 37 % (V // 12))
+    r = int(torch.nonzero(valid)[-1])
+    keep = logits[r, t[r]].clone()
+    logits[r] = -math.inf
+    logits[r, t[r]] = keep
+    snap = to64(logits)
+    tn = t.cpu().numpy()
+    loss = cuda_lib.lce_cross_entropy_from_logits(logits, t, "none", -100, torch.ones(N, device="cuda"))
+    torch.cuda.synchronize()
+    ref_loss, ref_grad = O.ce_from_logits(snap, tn, "none", -100, np.ones(N))
+    tol = TOL[dtype]
+    got = to64(logits)
+    assert np.isfinite(got).all()
+    assert rel_max(to64(loss), ref_loss) < tol["loss"]
+    assert rel_max(got, ref_grad) < tol["grad"]
+    assert (got[np.isneginf(snap)] == 0).all()
+    assert loss[r].item() == 0.0 and (got[r] == 0).all()

@@ -225,3 +225,29 @@ def test_row_slabs_grad_subsets(cuda_lib, want):
             assert rel_max(to64(got), ref) < tol["grad"]
         else:
             assert got is None
+
+
+@pytest.mark.parametrize("dtype,N", [(torch.bfloat16, 1500), (torch.float32, 700), (torch.float16, 1300)])
+def test_classes_masked_by_bias(cuda_lib, dtype, N):
+    """A bias of -inf masks classes: two whole 256-column segments and every
+    seventh class. Masked classes get probability 0, so their dW rows and db
+    entries are 0 and everything else matches the oracle (no NaN from a
+    segment whose logits are all -inf). bf16 at 1500 rows runs the row slabs."""
+    D, C = 64, 3000
+    inp = make_linear_inputs(N, D, C, dtype, "cuda", seed=N + 5, bias=True, w_std=0.1, b_std=0.2,
+                             n_ignored=N // 25)
+    b = inp["b"]
+    masked = torch.zeros(C, dtype=torch.bool, device="cuda")
+    masked[256:768] = True
+    masked[3::7] = True
+    b[masked] = -math.inf
+    t = inp["target"]
+    valid = t != -100
+    free = torch.nonzero(~masked).flatten()
+    t[valid] = free[t[valid] % free.numel()]
+    for reduction in ("mean", "none"):
+        _check(cuda_lib, inp, reduction)
+    loss, dX, dW, db = cuda_lib.lce_forward_backward(inp["X"], inp["W"], b, t, "mean")
+    torch.cuda.synchronize()
+    assert torch.isfinite(loss) and torch.isfinite(dX).all() and torch.isfinite(dW).all()
+    assert (dW[masked] == 0).all() and (db[masked] == 0).all()

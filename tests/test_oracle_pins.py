@@ -354,3 +354,35 @@ def test_class_weights_zero_sum_is_nan():
     cw = np.zeros(4)
     loss, dX, _, _ = O.lce_forward_backward(X, W, b, t, "mean", class_weight=cw)
     assert math.isnan(loss) and np.isnan(dX).all()
+
+
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+def test_masked_classes_equal_deleted_classes(reduction):
+    """A bias of -inf on a set of classes gives those classes probability 0:
+    loss and dX equal those of the problem with the classes deleted (with
+    targets renumbered), and the masked classes' dW rows and db entries are
+    0. The same holds for cross entropy on logits masked column-wise."""
+    X, W, b, t = _rand_case(N=17, D=6, C=19, n_ign=3, seed=31)
+    masked = np.zeros(19, dtype=bool)
+    masked[[2, 5, 6, 13]] = True
+    t[t >= 0] = np.flatnonzero(~masked)[t[t >= 0] % (~masked).sum()]
+    g = np.random.default_rng(5).standard_normal(17) if reduction == "none" else 0.5
+    bm = b.copy()
+    bm[masked] = -np.inf
+    loss, dX, dW, db = O.lce_forward_backward(X, W, bm, t, reduction, -100, g)
+    keep = np.flatnonzero(~masked)
+    renum = np.full(19, -1)
+    renum[keep] = np.arange(keep.size)
+    tr = np.where(t >= 0, renum[np.maximum(t, 0)], -100)
+    rl, rX, rW, rb = O.lce_forward_backward(X, W[keep], b[keep], tr, reduction, -100, g)
+    np.testing.assert_allclose(loss, rl, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dX, rX, rtol=1e-11, atol=1e-14)
+    np.testing.assert_allclose(dW[keep], rW, rtol=1e-11, atol=1e-14)
+    np.testing.assert_allclose(db[keep], rb, rtol=1e-11, atol=1e-14)
+    assert (dW[masked] == 0).all() and (db[masked] == 0).all()
+    z = X @ W.T + bm
+    lz, gz = O.ce_from_logits(z, t, reduction, -100, g)
+    lr, gr = O.ce_from_logits(z[:, keep], tr, reduction, -100, g)
+    np.testing.assert_allclose(lz, lr, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(gz[:, keep], gr, rtol=1e-11, atol=1e-14)
+    assert (gz[:, masked] == 0).all()
