@@ -41,23 +41,24 @@ METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor
 MEASURED_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the full-size
     # step, per launch; see profiles/tc2_gemm_bf16_llm_head_traffic.md
-    ("bf16_llm_head", "gemm_logits_tc"): (1085808384 + 252943616 + 1376624896 + 714537728 + 1619247616
-                                          + 1047489280 + 1890603776 + 1382050304) / 4,  # mean of 4 slabs
-    ("bf16_llm_head", "gemm_dx_tc"): 17544397312 + 862763264,
-    ("bf16_llm_head", "gemm_dw_tc"): 11263625216 + 1043292160,
+    ("bf16_llm_head", "gemm_logits_tc"): (1081671424 + 253892608 + 1425042176 + 716508416 + 1808702976
+                                          + 1050503680 + 2234819584 + 1384733952) / 4,  # mean of 4 slabs
+    ("bf16_llm_head", "gemm_dx_tc"): 19847710976 + 863693568,
+    ("bf16_llm_head", "gemm_dw_tc"): 13010002944 + 1043941120,
     # see profiles/tc2_gemm_bf16_large_head.md: mean of the 5 logits launches of a step
-    ("bf16_large_head", "gemm_logits_tc"): (19411388160 + 70922496 + 1130574336 + 524168704 + 2069232128
-                                            + 1482686720 + 3842266624 + 2168438528 + 8193454848
-                                            + 2856722432) / 5,
-    ("bf16_large_head", "gemm_dx_tc"): 47722717696 + 1773781760,
-    ("bf16_large_head", "gemm_dw_tc"): 41360279808 + 1070604544,
-    # see profiles/ce_resident_ce_logits_fp32.md (full-size 1-pass capture)
-    ("ce_logits_fp32", "ce_resident"): 8590645760 + 8527984384,
+    ("bf16_large_head", "gemm_logits_tc"): (19786962688 + 70675712 + 1197277184 + 526145280 + 2738773504
+                                            + 1485039872 + 5055550464 + 2170395648 + 10151144448
+                                            + 2857333248) / 5,
+    ("bf16_large_head", "gemm_dx_tc"): 50299461888 + 1775522304,
+    ("bf16_large_head", "gemm_dw_tc"): 43473837056 + 1070721536,
+    # see profiles/ce_resident_ce_logits_fp32.md (full-size 1-pass capture, mean of 3 launches)
+    ("ce_logits_fp32", "ce_resident"): (8867879424 + 8882181632 + 8920732416
+                                        + 8539638016 + 8536874496 + 8537447936) / 3,
     # see profiles/tc2x3_gemm_fp32_mid.md
-    ("fp32_mid", "gemm_logits_3xtf32"): 42238208 + 10453504,
-    ("fp32_mid", "gemm_dx_3xtf32"): 176070656 + 531968,
-    ("fp32_mid", "gemm_dw_3xtf32"): 142706432 + 70656,
-    ("fp32_mid", "split_tf32"): (16799488 + 3676928 + 4215552 + 67134976 + 205030144) / 3,  # mean of 3
+    ("fp32_mid", "gemm_logits_3xtf32"): 42227456 + 10568960,
+    ("fp32_mid", "gemm_dx_3xtf32"): 177166080 + 1101312,
+    ("fp32_mid", "gemm_dw_3xtf32"): 142702848 + 47616,
+    ("fp32_mid", "split_tf32"): (16799232 + 3588864 + 4215296 + 67137024 + 205145344) / 3,  # mean of 3
 }
 
 
