@@ -145,6 +145,8 @@ LCE_API int lce_forward(const void* X, const void* W, const void* b, const int64
  *   compute_linear_bias_grad). db is only computed when b is given.
  *   mean with every row ignored gives NaN loss and NaN gradients
  *   (neg_weight_target divides by NaN when the valid count is 0).
+ *   A bias of -inf masks classes: they get probability 0, so dW rows and db
+ *   entries 0 (any block of them, including whole 256-class tiles).
  */
 LCE_API int lce_forward_backward(const void* X, const void* W, const void* b, const int64_t* target,
                          int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype,
@@ -153,11 +155,14 @@ LCE_API int lce_forward_backward(const void* X, const void* W, const void* b, co
                          void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * Cross entropy on given logits [N, V] (dtype LCE_F32 or LCE_BF16); the
- * gradient w_n (softmax - onehot) REPLACES the logits in place, in the
- * logits' own type (a PyTorch wrapper must declare the tensor dirty).
+ * Cross entropy on given logits [N, V] (dtype LCE_F32, LCE_BF16 or
+ * LCE_F16); the gradient w_n (softmax - onehot) REPLACES the logits in
+ * place, in the logits' own type (a PyTorch wrapper must declare the tensor
+ * dirty).
  *   grad_out: as lce_forward_backward (NULL = 1.0 for sum / mean: no extra
  *   scaling; required [N] for none). loss_out: [1] or [N].
+ *   Logits of -inf (a masked vocabulary) get probability 0 and gradient 0;
+ *   a row's target must then be a finite logit, else its loss is +inf.
  * Liger-Kernel issue #343: loss and gradient in one pass, gradient written
  * into the input buffer, so no separate gradient pass or accumulation runs.
  */
