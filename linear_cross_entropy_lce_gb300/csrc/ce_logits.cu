@@ -7,9 +7,11 @@
 //
 //  * resident kernel: a thread-block cluster of CS CTAs (CS = 1..16) owns a
 //    row; each CTA holds a 16384-element slice in registers (512 threads x
-//    32 elements, 16-byte vector loads), reduces its slice to (max, sum-exp),
-//    exchanges the pairs through distributed shared memory, and writes
-//    g * w_n * (softmax - onehot) back from registers. Clusters walk the
+//    32 elements, 16-byte vector loads), replaces each x_i by
+//    e_i = exp(x_i - m_thread) (one exponential per element), reduces its
+//    slice to (max, sum-exp), exchanges the pairs through distributed
+//    shared memory, and writes g * w_n * (softmax - onehot) back from
+//    registers as e_i * g * w_n * exp(m_thread - lse). Clusters walk the
 //    rows persistently, each CTA prefetching its slice of the next row into
 //    L2 with the copy engine. Needs V <= 16 * 16384 and 16-byte aligned rows.
 //  * streaming kernel (any V, any alignment; used when V > 262144, rows are
