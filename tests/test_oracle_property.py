@@ -96,3 +96,40 @@ def test_ce_from_logits_matches_torch_autograd(p):
     ref.backward(torch.tensor(g if g is not None else 1.0, dtype=torch.float64))
     np.testing.assert_allclose(loss, ref.detach().numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(grad, zt.grad.numpy(), rtol=1e-9, atol=1e-12)
+
+
+@hyp.settings(max_examples=100, deadline=None)
+@hyp.given(problems(), st.integers(0, 2**31 - 1))
+def test_masked_classes_equal_deleted_classes(p, seed):
+    """A bias of -inf on a random proper subset of the classes (none of them
+    a target) gives the same loss and dX as the problem with those classes
+    deleted and the targets renumbered, and zero dW rows and db entries for
+    them."""
+    X, W, b, t, reduction, ignore_index, g, cw = p
+    C = W.shape[0]
+    hyp.assume(C > 1)
+    rng = np.random.default_rng(seed)
+    valid = t != ignore_index
+    used = np.zeros(C, dtype=bool)
+    used[t[valid]] = True
+    free = np.flatnonzero(~used)
+    masked = np.zeros(C, dtype=bool)
+    masked[free[rng.random(free.size) < 0.5]] = True
+    hyp.assume(masked.any() and not masked.all())
+    hyp.assume(not (0 <= ignore_index < C and masked[ignore_index]))
+    keep = np.flatnonzero(~masked)
+    renum = np.full(C, -1)
+    renum[keep] = np.arange(keep.size)
+    ign_r = renum[ignore_index] if 0 <= ignore_index < C else ignore_index
+    tr = np.where(valid, renum[np.where(valid, t, 0)], ign_r)
+    b0 = np.zeros(C) if b is None else b
+    bm = b0.copy()
+    bm[masked] = -np.inf
+    cwr = None if cw is None else cw[keep]
+    loss, dX, dW, db = O.lce_forward_backward(X, W, bm, t, reduction, ignore_index, g, class_weight=cw)
+    rl, rX, rW, rb = O.lce_forward_backward(X, W[keep], b0[keep], tr, reduction, ign_r, g, class_weight=cwr)
+    np.testing.assert_allclose(loss, rl, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dX, rX, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(dW[keep], rW, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(db[keep], rb, rtol=1e-9, atol=1e-12)
+    assert (dW[masked] == 0).all() and (db[masked] == 0).all()
