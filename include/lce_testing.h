@@ -40,6 +40,25 @@
  *   receives the timeout bit (2); the context stays usable. For tests of
  *   the failure path only; out is left unspecified.
  * Return an lce_status_e code.
+ *
+ * Host-only planning entry points (no device needed; nothing is launched):
+ * lce_test_row_slabs: the row slabs a chunk of `rows` rows is cut into on
+ *   the CTA-pair backward path (used there when rows >= 1024): slab k is
+ *   [slab_off[k], slab_off[k + 1]). slab_off is a host array of 5; returns
+ *   the number of slabs (at most 4), or -1 on a NULL array or rows < 0.
+ * lce_test_plan: the workspace plan a loss call with these arguments makes
+ *   for a workspace of ws_bytes (the largest batch chunk that fits, as the
+ *   calls choose it). Writes LCE_TEST_PLAN_FIELDS int64 values to the host
+ *   array out: chunk rows, chunk count, total bytes, padded class count,
+ *   (max, sum-exp) segments per row, then the byte offsets of the regions
+ *   in workspace order: counters, row losses, target logits, target
+ *   columns, target gradients, (max, sum-exp) pairs, the [chunk, C_pad]
+ *   P~ / G buffer, fp32 dW accumulator, db accumulator, fp16 row weights,
+ *   fp16 weight sum, fp16 scaled X, then the TF32 parts W hi, W lo, W^T hi,
+ *   W^T lo, X hi, X lo, X^T hi, X^T lo, G lo, G^T hi, G^T lo. A region a
+ *   call does not use has the next region's offset (zero length). Returns
+ *   LCE_TEST_PLAN_FIELDS, 0 when no chunk fits ws_bytes, -1 on invalid
+ *   arguments.
  */
 #ifndef LCE_TESTING_H_
 #define LCE_TESTING_H_
@@ -69,6 +88,14 @@ LCE_API int lce_test_gemm_f32(const float* A, const float* B, float* out, int64_
 LCE_API int lce_test_gemm_bf16_unmet_dependency(const void* A, const void* B, float* out, int64_t M,
                                         int64_t N, int64_t K, int* counters, int* dev_status,
                                         void* stream);
+
+#define LCE_TEST_PLAN_FIELDS 28
+
+LCE_API int lce_test_row_slabs(int64_t rows, int64_t* slab_off);
+
+LCE_API int lce_test_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype,
+                          int want_dx, int want_dw, int want_db, size_t ws_bytes, int64_t* out,
+                          int n_out);
 
 LCE_API int lce_test_gemm_tf32x3(const float* A, const float* B, float* out, int64_t M, int64_t N,
                          int64_t K, int a_mn_major, int b_mn_major, int k_splits, void* workspace,

@@ -257,6 +257,30 @@ bool choose_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dt
   return false;
 }
 
+// Row slabs of a chunk of `rows` rows: slab k is [off[k], off[k+1]),
+// k < the returned count (1 when not slabbed). Slab k's G formation runs
+// beside slab k+1's logits GEMM, so the slabs grow, about 4 : 7 : 9 : 12 of
+// the rows: each side job forms fewer rows than the GEMM beside it
+// computes, and the largest, last slab goes to the long dX GEMM. The
+// boundaries are the cumulative shares 4, 11 and 20 of 32 rounded down to
+// the 256-row tile height, so every slab is within 256 rows of its share
+// and the last one never gets less than its share; a boundary that would
+// leave an empty slab is dropped.
+int row_slabs(int64_t rows, bool slabbed, int64_t off[5]) {
+  for (int k = 0; k < 5; ++k) off[k] = rows;
+  off[0] = 0;
+  if (!slabbed) return 1;
+  if (rows <= 0) return 0;
+  static const int64_t kCumShare[3] = {4, 11, 20};  // of 32
+  int n = 1;
+  for (int k = 0; k < 3; ++k) {
+    const int64_t b = rows * kCumShare[k] / 32 / 256 * 256;
+    if (b > off[n - 1] && b < rows) off[n++] = b;
+  }
+  off[n] = rows;
+  return n;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? LCE_OK : LCE_ERR_CUDA; }
@@ -394,24 +418,8 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       LCE_TRY(launch_split_tf32(sa, s));
     }
     const bool slabbed = p.tc && pair && backward && rows >= 1024;
-    // Slab k's G formation runs beside slab k+1's logits GEMM, so the slabs
-    // grow (about 4 : 7 : 9 : 12 of the rows, in multiples of 256): each side
-    // job forms fewer rows than the GEMM beside it computes, and the largest,
-    // last slab goes to the long dX GEMM.
-    int64_t slab_off[5] = {0, rows, rows, rows, rows};
-    int64_t nslab = 1;
-    if (slabbed) {
-      static const int64_t kSlabWeight[4] = {4, 7, 9, 12};  // of 32
-      int64_t off = 0;
-      nslab = 0;
-      for (int k = 0; k < 4 && off < rows; ++k) {
-        int64_t sz = k == 3 ? rows - off : ceil_div(ceil_div(rows * kSlabWeight[k], 32), 256) * 256;
-        if (sz > rows - off) sz = rows - off;
-        slab_off[nslab++] = off;
-        off += sz;
-      }
-      slab_off[nslab] = rows;
-    }
+    int64_t slab_off[5];
+    const int64_t nslab = row_slabs(rows, slabbed, slab_off);
     GradArgs ga_prev, ga_last;
     CombineArgs ca_prev, ca_last;  // merges deferred into the next GEMM's idle warps
     bool have_prev = false, have_last = false;
@@ -943,6 +951,34 @@ int lce_test_gemm_f32(const float* A, const float* B, float* out, int64_t M, int
   const int op = a_mn_major ? (b_mn_major ? TC_TEST_MM : TC_TEST_MK) : (b_mn_major ? TC_TEST_KM : TC_TEST_KK);
   return from_cuda(launch_simt_store(op, A, B, a_mn_major ? M : K, b_mn_major ? N : K, M, N, K, es,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+int lce_test_row_slabs(int64_t rows, int64_t* slab_off) {
+  if (slab_off == nullptr) return -1;
+  if (rows < 0) return -1;
+  return row_slabs(rows, true, slab_off);
+}
+
+int lce_test_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, int want_dx, int want_dw,
+                  int want_db, size_t ws_bytes, int64_t* out, int n_out) {
+  if (out == nullptr || n_out < LCE_TEST_PLAN_FIELDS) return -1;
+  if (op != LCE_OP_FORWARD && op != LCE_OP_FORWARD_BACKWARD) return -1;
+  if (check_common(N, D, C, dtype, LCE_F32, LCE_RED_MEAN) != LCE_OK) return -1;
+  Plan p;
+  if (!choose_plan(op, N, D, C, dtype, grad_dtype, want_dx != 0, want_dw != 0, want_db != 0, ws_bytes, &p))
+    return 0;
+  const int64_t v[LCE_TEST_PLAN_FIELDS] = {
+      p.Bc, p.nchunks, static_cast<int64_t>(p.total), p.C_pad, p.nseg,
+      static_cast<int64_t>(p.off_cnt), static_cast<int64_t>(p.off_loss), static_cast<int64_t>(p.off_zt),
+      static_cast<int64_t>(p.off_tcol), static_cast<int64_t>(p.off_gt), static_cast<int64_t>(p.off_partial),
+      static_cast<int64_t>(p.off_L), static_cast<int64_t>(p.off_dw), static_cast<int64_t>(p.off_db),
+      static_cast<int64_t>(p.off_wrow), static_cast<int64_t>(p.off_wbar), static_cast<int64_t>(p.off_xs),
+      static_cast<int64_t>(p.off_wh), static_cast<int64_t>(p.off_wl), static_cast<int64_t>(p.off_wth),
+      static_cast<int64_t>(p.off_wtl), static_cast<int64_t>(p.off_xh), static_cast<int64_t>(p.off_xl),
+      static_cast<int64_t>(p.off_xth), static_cast<int64_t>(p.off_xtl), static_cast<int64_t>(p.off_gl),
+      static_cast<int64_t>(p.off_gth), static_cast<int64_t>(p.off_gtl)};
+  for (int i = 0; i < LCE_TEST_PLAN_FIELDS; ++i) out[i] = v[i];
+  return LCE_TEST_PLAN_FIELDS;
 }
 
 }  // extern "C"
