@@ -35,31 +35,37 @@ from linear_cross_entropy_lce_gb300.workloads import WORKLOADS, make_workload  #
 METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor peak"
 
 
-# DRAM bytes (read + write) per launch of a kernel, from an ncu capture of
-# the same command: {(workload, kernel): bytes}. An entry is removed when the
-# kernel changes after its capture.
-MEASURED_TRAFFIC = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the full-size
-    # step, per launch; see profiles/tc2_gemm_bf16_llm_head_traffic.md
-    ("bf16_llm_head", "gemm_logits_tc"): (1081671424 + 253892608 + 1425042176 + 716508416 + 1808702976
-                                          + 1050503680 + 2234819584 + 1384733952) / 4,  # mean of 4 slabs
-    ("bf16_llm_head", "gemm_dx_tc"): 19847710976 + 863693568,
-    ("bf16_llm_head", "gemm_dw_tc"): 13010002944 + 1043941120,
-    # see profiles/tc2_gemm_bf16_large_head.md: mean of the 5 logits launches of a step
-    ("bf16_large_head", "gemm_logits_tc"): (19786962688 + 70675712 + 1197277184 + 526145280 + 2738773504
-                                            + 1485039872 + 5055550464 + 2170395648 + 10151144448
-                                            + 2857333248) / 5,
-    ("bf16_large_head", "gemm_dx_tc"): 50299461888 + 1775522304,
-    ("bf16_large_head", "gemm_dw_tc"): 43473837056 + 1070721536,
-    # see profiles/ce_resident_ce_logits_fp32.md (full-size 1-pass capture, mean of 3 launches)
-    ("ce_logits_fp32", "ce_resident"): (8867879424 + 8882181632 + 8920732416
-                                        + 8539638016 + 8536874496 + 8537447936) / 3,
-    # see profiles/tc2x3_gemm_fp32_mid.md
-    ("fp32_mid", "gemm_logits_3xtf32"): 42227456 + 10568960,
-    ("fp32_mid", "gemm_dx_3xtf32"): 177166080 + 1101312,
-    ("fp32_mid", "gemm_dw_3xtf32"): 142702848 + 47616,
-    ("fp32_mid", "split_tf32"): (16799232 + 3588864 + 4215296 + 67137024 + 205145344) / 3,  # mean of 3
-}
+# DRAM bytes (read + write) per launch of a kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum): {(workload, kernel):
+# (bytes, commit of the capture, hash of the kernel sources at the capture)}.
+# The bench reports an entry only while the kernel sources hash the same, so
+# a capture never outlives a change of the kernels it measured.
+MEASURED_TRAFFIC = {}
+
+CSRC = os.path.join(ROOT, "linear_cross_entropy_lce_gb300", "csrc")
+
+
+def kernel_sources_hash():
+    """sha256 (16 hex digits) over the CUDA sources of the library."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(CSRC)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, fn), "rb") as f:
+                h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload, kernel):
+    """(bytes per launch or None, note)."""
+    e = MEASURED_TRAFFIC.get((workload, kernel))
+    if e is None:
+        return None, "no ncu capture recorded for this kernel and workload"
+    nbytes, commit, src = e
+    if src != kernel_sources_hash():
+        return None, f"stale: captured at {commit}, kernel sources changed since"
+    return nbytes, f"ncu capture at {commit}"
 
 
 def _peaks():
@@ -256,9 +262,13 @@ def run_gpu(args):
         nbytes = lce.lce_workspace_size(lce.LCE_OP_CE_FROM_LOGITS, N, 1, V, lce.LCE_F32, lce.LCE_RED_MEAN,
                                         lce.LCE_F32, 0)
         wsbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        status_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+        status_word = wsbuf[:4].view(torch.int32)
 
         def step():
-            return lce.lce_cross_entropy_from_logits(logits, t, w.reduction, -100, workspace=wsbuf)
+            out = lce.lce_cross_entropy_from_logits(logits, t, w.reduction, -100, workspace=wsbuf)
+            status_acc.bitwise_or_(status_word)
+            return out
 
         flops = 0.0
     else:
@@ -269,6 +279,8 @@ def run_gpu(args):
         red = {"none": 0, "sum": 1, "mean": 2}[w.reduction]
         nbytes = lce.lce_workspace_size(lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, red, dt, 0)
         wsbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        status_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+        status_word = wsbuf[:4].view(torch.int32)
         dX = torch.empty_like(X)
         dW = torch.empty_like(W)
         db = torch.empty_like(b) if b is not None else None
@@ -282,11 +294,13 @@ def run_gpu(args):
             if red == 0:  # reduction none: forward, then forward+backward with the upstream vector
                 lce._check(lib.lce_forward(P(X), P(W), P(b), P(t), N, D, C, dt, 0, red, -100, P(loss), None,
                                            P(wsbuf), nbytes, ctypes.c_void_p(stream.cuda_stream)), "fwd")
+                status_acc.bitwise_or_(status_word)
                 if mark is not None:
                     mark()  # CUDA event between the two parts
             lce._check(lib.lce_forward_backward(P(X), P(W), P(b), P(t), N, D, C, dt, 0, red, -100, P(g), P(loss),
                                                 P(dX), P(dW), P(db), dt, P(wsbuf), nbytes,
                                                 ctypes.c_void_p(stream.cuda_stream)), "fwd+bwd")
+            status_acc.bitwise_or_(status_word)
             return loss
 
         flops = w.flops_fwd_bwd
@@ -296,9 +310,22 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    def check_status(where):
+        """Every kernel wait in the library is bounded; one that gave up sets a
+        bit in the workspace's status word, and a step whose pipeline gave up
+        did not do its work. Each call clears the word, so every step ORs it
+        into status_acc on the device right after its calls; any bit there
+        means the run is not a measurement."""
+        torch.cuda.synchronize()
+        st = int(status_acc.item())
+        status_acc.zero_()
+        if st != 0:
+            raise SystemExit(f"bench: device status bits {st} after the {where}; the run is not a measurement")
+
     for _ in range(args.warmup):
         step()
     barrier()
+    check_status("warm-up steps")
 
     # ---- device-timed region
     sampler = ClockSampler(local)
@@ -322,6 +349,7 @@ def run_gpu(args):
             step()
     e1.record(stream)
     barrier()
+    check_status("timed steps")
     launches = lce.launch_count() - launches0
     clocks = sampler.stop()
     ms = aggregate_ms(e0.elapsed_time(e1) / args.steps, dist, dev)
@@ -360,55 +388,78 @@ def run_gpu(args):
     for _ in range(prof_steps):
         step()
     barrier()
+    check_status("profiled steps")
     lce.profile_enable(False)
     prof = lce.profile_summary()
     lce.profile_reset()
 
     # ---- end to end through the public API with host buffers: every step
-    # copies its inputs from pinned host memory and reads its loss back. The
-    # inputs are double-buffered and copied on a second stream, so step k+1's
-    # copy overlaps step k's kernels, as an input pipeline would.
+    # copies its inputs from pinned host memory and copies its results (the
+    # loss and every gradient) back to pinned host memory. Inputs and outputs
+    # are double-buffered on the device; inputs go in on one copy stream and
+    # results come out on another, so step k+1's input copy and step k-1's
+    # result copy overlap step k's kernels, as a training input pipeline
+    # and an optimizer on the host would.
     if w.kind != "logits":
-        dev_sets = [[X, W, t, b, g]]
-        dev_sets.append([None if x is None else torch.empty_like(x) for x in dev_sets[0]])
-        host = [None if x is None else x.cpu().pin_memory() for x in dev_sets[0]]
-        out_loss = loss
+        in_sets = [[X, W, t, b, g]]
+        in_sets.append([None if x is None else torch.empty_like(x) for x in in_sets[0]])
+        out_sets = [[loss, dX, dW, db]]
+        out_sets.append([None if x is None else torch.empty_like(x) for x in out_sets[0]])
 
         def run_on(i):
-            Xi, Wi, ti, bi, gi = dev_sets[i]
+            Xi, Wi, ti, bi, gi = in_sets[i]
+            li, dXi, dWi, dbi = out_sets[i]
             if red == 0:
-                lce._check(lib.lce_forward(P(Xi), P(Wi), P(bi), P(ti), N, D, C, dt, 0, red, -100, P(loss), None,
+                lce._check(lib.lce_forward(P(Xi), P(Wi), P(bi), P(ti), N, D, C, dt, 0, red, -100, P(li), None,
                                            P(wsbuf), nbytes, ctypes.c_void_p(stream.cuda_stream)), "fwd")
+                status_acc.bitwise_or_(status_word)
             lce._check(lib.lce_forward_backward(P(Xi), P(Wi), P(bi), P(ti), N, D, C, dt, 0, red, -100, P(gi),
-                                                P(loss), P(dX), P(dW), P(db), dt, P(wsbuf), nbytes,
+                                                P(li), P(dXi), P(dWi), P(dbi), dt, P(wsbuf), nbytes,
                                                 ctypes.c_void_p(stream.cuda_stream)), "fwd+bwd")
+            status_acc.bitwise_or_(status_word)
     else:
-        dev_sets = [[logits, t], [torch.empty_like(logits), torch.empty_like(t)]]
-        host = [logits.cpu().pin_memory(), t.cpu().pin_memory()]
-        out_loss = torch.empty(1, dtype=torch.float32, device=dev)
+        # the gradient replaces the logits: the step's result is the loss and
+        # the whole logits buffer
+        e2e_loss = [torch.empty(1, dtype=torch.float32, device=dev) for _ in range(2)]
+        in_sets = [[logits, t], [torch.empty_like(logits), torch.empty_like(t)]]
+        out_sets = [[e2e_loss[0], in_sets[0][0]], [e2e_loss[1], in_sets[1][0]]]
 
         def run_on(i):
-            li, ti = dev_sets[i]
-            out_loss.copy_(lce.lce_cross_entropy_from_logits(li, ti, w.reduction, -100, workspace=wsbuf).reshape(1))
+            li, ti = in_sets[i]
+            e2e_loss[i].copy_(lce.lce_cross_entropy_from_logits(li, ti, w.reduction, -100,
+                                                                workspace=wsbuf).reshape(1))
+            status_acc.bitwise_or_(status_word)
 
-    h2d = sum(x.numel() * x.element_size() for x in host if x is not None)
-    hloss = torch.empty(out_loss.numel(), dtype=torch.float32).pin_memory()
-    d2h = hloss.numel() * 4
-    copy_stream = torch.cuda.Stream(device=dev)
-    ready = [torch.cuda.Event(), torch.cuda.Event()]
-    free = [torch.cuda.Event(), torch.cuda.Event()]
-    for e in free:
+    host_in = [None if x is None else x.cpu().pin_memory() for x in in_sets[0]]
+    host_out = [None if x is None else torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in out_sets[0]]
+    h2d = sum(x.numel() * x.element_size() for x in host_in if x is not None)
+    d2h = sum(x.numel() * x.element_size() for x in host_out if x is not None)
+    in_stream = torch.cuda.Stream(device=dev)
+    out_stream = torch.cuda.Stream(device=dev)
+    ready = [torch.cuda.Event(), torch.cuda.Event()]     # inputs of set i on the device
+    in_free = [torch.cuda.Event(), torch.cuda.Event()]   # kernels done reading input set i
+    done = [torch.cuda.Event(), torch.cuda.Event()]      # results of set i written
+    out_free = [torch.cuda.Event(), torch.cuda.Event()]  # results of set i copied to the host
+    for e in in_free + out_free:
         e.record(stream)
 
     def h2d_into(i, after=None):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(free[i])
+        with torch.cuda.stream(in_stream):
+            in_stream.wait_event(in_free[i])
             if after is not None:
-                copy_stream.wait_event(after)
-            for d, h in zip(dev_sets[i], host):
+                in_stream.wait_event(after)
+            for d, h in zip(in_sets[i], host_in):
                 if d is not None:
                     d.copy_(h, non_blocking=True)
-            ready[i].record(copy_stream)
+            ready[i].record(in_stream)
+
+    def d2h_from(i):
+        with torch.cuda.stream(out_stream):
+            out_stream.wait_event(done[i])
+            for d, h in zip(out_sets[i], host_out):
+                if d is not None:
+                    h.copy_(d, non_blocking=True)
+            out_free[i].record(out_stream)
 
     def e2e_steps(k_steps, start_ev):
         h2d_into(0, start_ev)
@@ -417,9 +468,13 @@ def run_gpu(args):
             if k + 1 < k_steps:
                 h2d_into(1 - i)
             stream.wait_event(ready[i])
+            stream.wait_event(out_free[i])  # results of step k - 2 have left this set
             run_on(i)
-            free[i].record(stream)
-            hloss.copy_(out_loss, non_blocking=True)
+            in_free[i].record(stream)
+            done[i].record(stream)
+            d2h_from(i)
+        stream.wait_event(out_free[(k_steps - 1) % 2])  # the last results are on the host
+        stream.wait_event(out_free[k_steps % 2])
 
     s0 = torch.cuda.Event()
     s0.record(stream)
@@ -431,10 +486,12 @@ def run_gpu(args):
     e2e_steps(args.steps, f0)
     f1.record(stream)
     barrier()
+    check_status("end-to-end steps")
     ems = aggregate_ms(f0.elapsed_time(f1) / args.steps, dist, dev)
     e2e = {"value": ws * N / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h), "ms_per_step": ems,
-           "pipelined": "inputs double-buffered, host-to-device copies on a second stream"}
+           "pipelined": "inputs and results double-buffered; host-to-device and device-to-host copies on "
+                        "two more streams, overlapping the neighbouring steps' kernels"}
 
     if rank != 0:
         if dist is not None:
@@ -448,42 +505,39 @@ def run_gpu(args):
         n_l, tot_ms, work = prof[dominant]
         avg_s = tot_ms / n_l / 1e3
         per_launch = work / n_l
-        traffic = MEASURED_TRAFFIC.get((name, dominant))
-        if dominant.startswith("gemm_") and dominant.endswith("_tc"):
+        traffic, traffic_note = measured_traffic(name, dominant)
+        common = {"traffic": traffic, "traffic_note": traffic_note, "kernel": dominant,
+                  "launches_per_step": n_l / prof_steps}
+        if dominant.startswith("gemm_") and (dominant.endswith("_tc") or dominant.endswith("_3xtf32")):
+            # bf16 / fp16 contractions against the measured cuBLAS bf16 peak;
+            # the fp32 product as three TF32 tensor-core products against the
+            # TF32 peak / 3, TF32 peak = measured bf16 x the nominal dense
+            # TF32 / bf16 ratio (1.1 / 2.25: no measured TF32 peak exists)
+            ratio = 1.0 if dominant.endswith("_tc") else (1.1 / 2.25) / 3.0
             achieved = per_launch / avg_s / 1e12
-            peak = peaks["bf16_tflops_sustained"]
+            peak = peaks["bf16_tflops"] * ratio
+            peak_s = peaks["bf16_tflops_sustained"] * ratio
+            how = "" if ratio == 1.0 else " x 1.1/2.25 (nominal TF32/bf16) / 3 (TF32 products per fp32 product)"
             roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                        "frac": achieved / peak, "traffic": traffic, "kernel": dominant,
-                        "peak_source": peaks["source"] + " bf16_tflops_sustained (the kernel runs inside a "
-                                                         "long sequence of back-to-back steps)",
-                        "algorithmic_flops_per_launch": per_launch}
-        elif dominant.startswith("gemm_") and dominant.endswith("_3xtf32"):
-            # fp32 product as three TF32 tensor-core products: the ceiling for
-            # its algorithmic flop is the TF32 peak / 3; TF32 peak = measured
-            # bf16 sustained x the nominal dense TF32 / bf16 ratio (1.1 / 2.25)
-            achieved = per_launch / avg_s / 1e12
-            peak = peaks["bf16_tflops_sustained"] * (1.1 / 2.25) / 3.0
-            roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                        "frac": achieved / peak, "traffic": traffic, "kernel": dominant,
-                        "peak_source": peaks["source"] + " bf16_tflops_sustained x 1.1/2.25 (nominal TF32/bf16) "
-                                                         "/ 3 (TF32 products per fp32 product)",
-                        "algorithmic_flops_per_launch": per_launch}
+                        "frac": achieved / peak, "peak_sustained": peak_s, "frac_sustained": achieved / peak_s,
+                        "peak_source": f"{peaks['source']} bf16_tflops (burst){how}; frac_sustained uses "
+                                       f"bf16_tflops_sustained{how}",
+                        "algorithmic_flops_per_launch": per_launch, **common}
         elif dominant.startswith("gemm_"):
             # exact fp32 FMA on the CUDA cores: SMs x 128 FP32 lanes x 2 flop x max SM clock
             sms = torch.cuda.get_device_properties(dev).multi_processor_count
             peak = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
             achieved = per_launch / avg_s / 1e12
             roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                        "frac": achieved / peak, "traffic": traffic, "kernel": dominant,
+                        "frac": achieved / peak,
                         "peak_source": f"derived: {sms} SMs x 128 FP32 FMA lanes x 2 flop x "
                                        f"{peaks['sm_max_mhz']:.0f} MHz",
-                        "algorithmic_flops_per_launch": per_launch}
+                        "algorithmic_flops_per_launch": per_launch, **common}
         else:
             achieved = per_launch / avg_s / 1e9
             roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": dominant,
-                        "peak_source": peaks["source"] + " hbm_gbs (copy)",
-                        "algorithmic_bytes_per_launch": per_launch}
+                        "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"] + " hbm_gbs (copy)",
+                        "algorithmic_bytes_per_launch": per_launch, **common}
 
     # ---- CPU baseline: the oracle on a bounded sample, rank 0, N=1 only
     cpu = None

@@ -46,8 +46,16 @@
  *    are fp32.
  *  - LCE_BF16 and LCE_F16 inputs run on the tcgen05 tensor cores and need
  *    D % 8 == 0 and 16-byte aligned X, W, dX, dW (else LCE_ERR_ALIGN).
- *    LCE_F32 inputs run exact fp32 FMA on the CUDA cores and accept any
- *    shape. With LCE_F16 the backward keeps the per-row weights w_n out of
+ *    LCE_F32 inputs accept any shape and also run on the tensor cores, as
+ *    three TF32 products per fp32 product (hi*hi + hi*lo + lo*hi with
+ *    hi = x rounded to TF32 and lo the rounded remainder; partial sums
+ *    folded in fp32 every 512 of K), which keeps the fp32 tolerances. Two
+ *    environment variables, each read once per process, select other
+ *    engines: LCE_F32_SIMT=1 runs LCE_F32 inputs with exact fp32 FMA on the
+ *    CUDA cores instead; LCE_TC_PAIR=0 runs LCE_BF16 inputs on the one-CTA
+ *    tcgen05 GEMM (128 x 256 tiles) instead of CTA pairs (256 x 256 tiles,
+ *    cta_group::2). Results agree within the tolerances either way.
+ *    With LCE_F16 the backward keeps the per-row weights w_n out of
  *    the 16-bit gradient tile (1/n_valid is below fp16's normal range for
  *    large batches; linear_cross_entropy.py keeps the per-row weight in
  *    fp32 for the same reason) and applies them in fp32 afterwards.
@@ -192,8 +200,14 @@ LCE_API int lce_cross_entropy_from_logits(void* logits_inout, const int64_t* tar
  *    overlap on the GPU, on different streams or from different threads,
  *    race and give wrong results. Serialise them on one stream.
  *  - the first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture on the device.
+ *    (cudaGetSymbolAddress) with that device current. CUDA loads device
+ *    code lazily by default, so that first call may also load the library's
+ *    module and reserve the array then. Make that first call before any
+ *    stream capture on the device and outside any region where memory must
+ *    not be reserved (e.g. at start-up).
+ *  - the address is cached per device until the process exits: resetting
+ *    the device (cudaDeviceReset or a primary-context reset) while the
+ *    library is loaded is not supported by this entry point.
  * The call allocates nothing (no cudaMalloc / cudaFree, no allocating
  * library routine).
  */
@@ -228,6 +242,20 @@ LCE_API int lce_cross_entropy_from_logits_ex(void* logits_inout, const int64_t* 
                                              int reduction, int64_t ignore_index, const float* grad_out,
                                              float* loss_out, void* workspace, size_t ws_bytes,
                                              void* stream);
+
+/*
+ * Gradients times a device scalar, in place: dX[:n_dx], dW[:n_dw] and
+ * db[:n_db] (elements of grad_dtype; a NULL pointer or a count of 0 skips
+ * that buffer) are multiplied by *grad_out (a device fp32 scalar). The
+ * kernel reads *grad_out first and touches nothing when it is exactly 1, so
+ * the caller needs no host-side test (and no synchronisation) to skip the
+ * pass. This is the backward of the scalar-reduction ops of
+ * linear_cross_entropy.py: their forward computes the gradients for an
+ * upstream gradient of 1 and their backward multiplies them by
+ * grad_output.
+ */
+LCE_API int lce_scale_gradients(void* dX, int64_t n_dx, void* dW, int64_t n_dw, void* db, int64_t n_db,
+                                int grad_dtype, const float* grad_out, void* stream);
 
 /* Human-readable text of a status code (static storage). */
 LCE_API const char* lce_status_string(int status);

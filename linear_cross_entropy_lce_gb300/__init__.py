@@ -64,6 +64,8 @@ _SIGNATURES = {
                                                  c_int64, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "lce_cross_entropy_from_logits_noalloc": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int,
                                                       c_int64, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "lce_scale_gradients": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64, c_int, c_void_p,
+                                    c_void_p]),
     "lce_status_string": (ctypes.c_char_p, [c_int]),
     "lce_read_device_status": (c_int, [c_void_p, c_void_p]),
     "lce_launch_count": (c_int64, []),
@@ -255,6 +257,23 @@ def lce_cross_entropy_from_logits(logits, target, reduction="mean", ignore_index
                                                 _ptr(g), _ptr(loss), _ptr(ws), ws.numel(), _stream(stream)),
            "lce_cross_entropy_from_logits")
     return loss if red == LCE_RED_NONE else loss[0]
+
+
+def lce_scale_gradients(dX, dW, db, grad_out, stream=None):
+    """dX, dW, db (any may be None; one dtype) *= grad_out (a device fp32
+    scalar tensor), in place; nothing is touched when grad_out == 1."""
+    lib = load_library()
+    ts = [t for t in (dX, dW, db) if t is not None]
+    if not ts:
+        return
+    gdt = _dtype_code(ts[0])
+    for t in ts:
+        if _dtype_code(t) != gdt or not t.is_contiguous():
+            raise ValueError("gradients must be contiguous and share one dtype")
+    g = grad_out.to(torch.float32).reshape(-1)[:1].contiguous()
+    n = lambda t: 0 if t is None else t.numel()
+    _check(lib.lce_scale_gradients(_ptr(dX), n(dX), _ptr(dW), n(dW), _ptr(db), n(db), gdt, _ptr(g), _stream(stream)),
+           "lce_scale_gradients")
 
 
 def lce_read_device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -8,8 +8,9 @@ split of the batch-chunked op in PyTorch's ``linear_cross_entropy.py``:
 
 * reduction "mean" / "sum": the forward computes the loss and, in the same
   library call, the gradients of every input that requires one (the scalar
-  ops of the page precompute the gradients); the backward scales them by
-  the upstream gradient (returned as they are when it is 1).
+  ops of the page precompute the gradients); the backward multiplies them
+  by the upstream gradient in place, in the library (a kernel that reads the
+  upstream gradient on the device and does nothing when it is 1).
 * reduction "none": the forward computes only the per-row losses and keeps
   the inputs; the backward recomputes the logits tile by tile and forms the
   vector-Jacobian product with the per-row upstream gradient in one call
@@ -25,12 +26,12 @@ from __future__ import annotations
 
 import torch
 
-from . import lce_forward, lce_forward_backward
+from . import lce_forward, lce_forward_backward, lce_scale_gradients
 
 
 class _ScalarReduction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, X, W, b, target, reduction, ignore_index, class_weight):
+    def forward(ctx, X, W, b, target, reduction, ignore_index, class_weight, allow_retain_graph):
         want_dx, want_dw, want_db = ctx.needs_input_grad[0], ctx.needs_input_grad[1], ctx.needs_input_grad[2]
         if want_dx or want_dw or want_db:
             loss, dX, dW, db = lce_forward_backward(X, W, b, target, reduction, ignore_index, None,
@@ -40,17 +41,24 @@ class _ScalarReduction(torch.autograd.Function):
             loss = lce_forward(X, W, b, target, reduction, ignore_index, class_weight=class_weight)
             dX = dW = db = None
         ctx.grads = (dX, dW, db)
+        ctx.allow_retain_graph = allow_retain_graph
         return loss
 
     @staticmethod
     def backward(ctx, grad_loss):
+        if ctx.grads is None:
+            raise RuntimeError("linear_cross_entropy: backward ran twice through a scalar-reduction loss whose "
+                               "gradients were already handed out; pass allow_retain_graph=True to keep them")
         dX, dW, db = ctx.grads
-        if not torch.equal(grad_loss, torch.ones_like(grad_loss)):
-            g = grad_loss.to(torch.float32)
-            dX = None if dX is None else (dX.float() * g).to(dX.dtype)
-            dW = None if dW is None else (dW.float() * g).to(dW.dtype)
-            db = None if db is None else (db.float() * g).to(db.dtype)
-        return dX, dW, db, None, None, None, None
+        if ctx.allow_retain_graph:
+            # keep the precomputed buffers for a later backward: scale copies
+            dX, dW, db = (None if x is None else x.clone() for x in (dX, dW, db))
+        else:
+            ctx.grads = None
+        # in place, in the library; its kernel leaves them untouched when the
+        # upstream gradient is 1 (decided on the device: no host sync)
+        lce_scale_gradients(dX, dW, db, grad_loss)
+        return dX, dW, db, None, None, None, None, None
 
 
 class _NoReduction(torch.autograd.Function):
@@ -73,14 +81,22 @@ class _NoReduction(torch.autograd.Function):
         return dX, dW, db, None, None, None
 
 
-def linear_cross_entropy(input, weight, target, bias=None, reduction="mean", ignore_index=-100, class_weight=None):
+def linear_cross_entropy(input, weight, target, bias=None, reduction="mean", ignore_index=-100, class_weight=None,
+                         allow_retain_graph=False):
     """Loss of cross_entropy(input @ weight.T + bias, target) without the
     [rows, classes] logits, differentiable in input, weight and bias.
 
-    input [..., D] (fp32 or bf16), weight [C, D], bias [C] or None (same
-    dtype), target [...] int64, class_weight [C] or None (per-class weights
-    of cross entropy, not differentiated). Returns a float32 scalar (mean,
-    sum) or a float32 tensor of target's shape (none).
+    input [..., D] (fp32, bf16 or fp16), weight [C, D], bias [C] or None
+    (same dtype), target [...] int64, class_weight [C] or None (per-class
+    weights of cross entropy, not differentiated). Returns a float32 scalar
+    (mean, sum) or a float32 tensor of target's shape (none).
+
+    allow_retain_graph (mean / sum only, as the page's option of that name):
+    False hands the precomputed gradient buffers to the backward, which
+    scales them in place, so a second backward through the same loss raises
+    RuntimeError; True keeps them and scales copies (one more gradient-sized
+    allocation per backward). reduction "none" recomputes in its backward and
+    supports retain_graph either way.
     """
     if reduction not in ("mean", "sum", "none"):
         raise ValueError(f"reduction must be mean, sum or none, got {reduction!r}")
@@ -93,4 +109,4 @@ def linear_cross_entropy(input, weight, target, bias=None, reduction="mean", ign
     b = None if bias is None else bias.contiguous()
     if reduction == "none":
         return _NoReduction.apply(X, W, b, t, ignore_index, class_weight).reshape(target.shape)
-    return _ScalarReduction.apply(X, W, b, t, reduction, ignore_index, class_weight)
+    return _ScalarReduction.apply(X, W, b, t, reduction, ignore_index, class_weight, allow_retain_graph)

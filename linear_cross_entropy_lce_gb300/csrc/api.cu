@@ -99,7 +99,7 @@ const char* kNames[K_NUM_IDS] = {
     "prep",          "gemm_logits_tc", "gemm_dx_tc",  "gemm_dw_tc",      "gemm_logits_simt",
     "gemm_dx_simt",  "gemm_dw_simt",   "lse_combine", "grad_logits",     "loss_finalize",
     "db_finalize",   "ce_resident",    "ce_stream",   "gemm_test",       "row_scale",
-    "gemm_logits_3xtf32", "gemm_dx_3xtf32", "gemm_dw_3xtf32", "split_tf32"};
+    "gemm_logits_3xtf32", "gemm_dx_3xtf32", "gemm_dw_3xtf32", "split_tf32", "scale_grads"};
 }  // namespace
 
 const char* kernel_id_name(int id) { return (id >= 0 && id < K_NUM_IDS) ? kNames[id] : "?"; }
@@ -260,25 +260,42 @@ bool choose_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dt
 // Row slabs of a chunk of `rows` rows: slab k is [off[k], off[k+1]),
 // k < the returned count (1 when not slabbed). Slab k's G formation runs
 // beside slab k+1's logits GEMM, so the slabs grow, about 4 : 7 : 9 : 12 of
-// the rows: each side job forms fewer rows than the GEMM beside it
+// the rows: each side job forms no more rows than the GEMM beside it
 // computes, and the largest, last slab goes to the long dX GEMM. The
-// boundaries are the cumulative shares 4, 11 and 20 of 32 rounded down to
-// the 256-row tile height, so every slab is within 256 rows of its share
-// and the last one never gets less than its share; a boundary that would
-// leave an empty slab is dropped.
+// boundaries are the cumulative shares rounded down to the 256-row tile
+// height, so every slab but the last is within 256 rows of its share and
+// the last one never gets less. Where four slabs would not come out
+// non-decreasing (fewer than 2048 rows), three slabs of shares 7 : 9 : 12
+// are tried, then two of 9 : 12, then one. Sizes are non-decreasing for
+// every row count and strictly growing from 8192 rows on.
 int row_slabs(int64_t rows, bool slabbed, int64_t off[5]) {
   for (int k = 0; k < 5; ++k) off[k] = rows;
   off[0] = 0;
   if (!slabbed) return 1;
   if (rows <= 0) return 0;
-  static const int64_t kCumShare[3] = {4, 11, 20};  // of 32
-  int n = 1;
-  for (int k = 0; k < 3; ++k) {
-    const int64_t b = rows * kCumShare[k] / 32 / 256 * 256;
-    if (b > off[n - 1] && b < rows) off[n++] = b;
+  static const int64_t kShares[3][4] = {{4, 7, 9, 12}, {7, 9, 12, 0}, {9, 12, 0, 0}};
+  for (int n = 4; n >= 2; --n) {
+    const int64_t* sh = kShares[4 - n];
+    int64_t total = 0;
+    for (int k = 0; k < n; ++k) total += sh[k];
+    int64_t cand[5];
+    cand[0] = 0;
+    int64_t cum = 0;
+    for (int k = 0; k + 1 < n; ++k) {
+      cum += sh[k];
+      cand[k + 1] = rows * cum / total / 256 * 256;
+    }
+    cand[n] = rows;
+    bool ok = true;
+    for (int k = 0; k < n && ok; ++k) {
+      const int64_t sz = cand[k + 1] - cand[k];
+      ok = sz > 0 && (k == 0 || sz >= cand[k] - cand[k - 1]);
+    }
+    if (!ok) continue;
+    for (int k = 0; k <= n; ++k) off[k] = cand[k];
+    return n;
   }
-  off[n] = rows;
-  return n;
+  return 1;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -747,18 +764,31 @@ int lce_cross_entropy_from_logits_ex(void* logits_inout, const int64_t* target, 
   return LCE_OK;
 }
 
+int lce_scale_gradients(void* dX, int64_t n_dx, void* dW, int64_t n_dw, void* db, int64_t n_db, int grad_dtype,
+                        const float* grad_out, void* stream) {
+  if (grad_dtype != LCE_F32 && grad_dtype != LCE_BF16 && grad_dtype != LCE_F16) return LCE_ERR_DTYPE;
+  if (grad_out == nullptr) return LCE_ERR_NULL;
+  if (n_dx < 0 || n_dw < 0 || n_db < 0) return LCE_ERR_SHAPE;
+  if ((n_dx > 0 && dX == nullptr) || (n_dw > 0 && dW == nullptr) || (n_db > 0 && db == nullptr)) return LCE_ERR_NULL;
+  const int st = check_device();
+  if (st != LCE_OK) return st;
+  return from_cuda(launch_scale_grads(dX, dX ? n_dx : 0, dW, dW ? n_dw : 0, db, db ? n_db : 0, grad_dtype, grad_out,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
 const char* lce_status_string(int status) {
   switch (status) {
     case LCE_OK: return "ok";
     case LCE_ERR_NULL: return "a required pointer is NULL";
     case LCE_ERR_SHAPE: return "invalid problem size";
-    case LCE_ERR_DTYPE: return "unsupported dtype (inputs fp32/bf16, accumulation fp32)";
+    case LCE_ERR_DTYPE: return "unsupported dtype (inputs and gradients fp32, bf16 or fp16; accumulation fp32)";
     case LCE_ERR_REDUCTION: return "reduction must be none, sum or mean";
     case LCE_ERR_GRAD_OUT: return "reduction none needs a per-row upstream gradient";
     case LCE_ERR_WORKSPACE: return "workspace missing or too small";
     case LCE_ERR_CUDA: return "CUDA runtime error or kernel launch failure";
     case LCE_ERR_TARGET_RANGE: return "a target is neither ignore_index nor a class index";
-    case LCE_ERR_ALIGN: return "bf16 path needs D % 8 == 0 and 16-byte aligned buffers";
+    case LCE_ERR_ALIGN:
+      return "bf16 / fp16 inputs need D % 8 == 0 and 16-byte aligned X, W, dX, dW; every workspace 16-byte aligned";
     case LCE_ERR_TIMEOUT: return "a device pipeline wait timed out";
     case LCE_ERR_DEVICE: return "device is not compute capability 10.3 (GB300)";
     default: return "unknown status";

@@ -34,6 +34,7 @@ enum KernelId {
   K_GEMM_DX_TX,
   K_GEMM_DW_TX,
   K_SPLIT_TF32,
+  K_SCALE_GRADS,
   K_NUM_IDS
 };
 const char* kernel_id_name(int id);
@@ -189,6 +190,10 @@ cudaError_t launch_row_scale(const void* X, const float* wrow, float* wbar, void
 cudaError_t launch_loss_finalize(const float* loss_rows, int64_t N, int reduction, const WsHeader* hdr,
                                  bool weighted, float* loss_out, cudaStream_t s);
 cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, int dt, cudaStream_t s);
+// a[:na], b[:nb], c[:nc] (type dt; NULL spans skipped) *= *g in place,
+// nothing touched when *g == 1 (decided on the device).
+cudaError_t launch_scale_grads(void* a, int64_t na, void* b, int64_t nb, void* c, int64_t nc, int dt,
+                               const float* g, cudaStream_t s);
 
 // ---- cross entropy on given logits (ce_logits.cu)
 struct CeArgs {

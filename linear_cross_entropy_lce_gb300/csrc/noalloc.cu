@@ -11,9 +11,15 @@
 // valid-target count and one fp32 loss per row) taken from a fixed array
 // that lives in this library's device image instead of a caller buffer.
 //
-// The array is reserved on every GPU that loads the library and stays
-// there until the process exits: 256 bytes plus 4 bytes per row for at
-// most LCE_NOALLOC_MAX_ROWS rows (4 MiB + 256 B).
+// The array is reserved on every GPU that loads the library's device code
+// and stays there until the process exits: 256 bytes plus 4 bytes per row
+// for at most LCE_NOALLOC_MAX_ROWS rows (4 MiB + 256 B). CUDA loads device
+// code lazily by default, so that reservation may happen at the first call
+// on a device (its address look-up below); a caller with a fixed memory
+// budget makes that first call outside its no-allocation region, e.g. at
+// start-up. The address is cached per device for the life of the process:
+// resetting a device (cudaDeviceReset, or a reset of the primary context)
+// while the library is loaded is not supported by this entry point.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -36,8 +42,9 @@ std::mutex g_mu;
 
 // Device address of the array on the current device, looked up once per
 // device (with that device current) and cached. The first call on a device
-// does this look-up, so that first call should come before any stream
-// capture on that device.
+// does this look-up, which may also load the module and reserve the array,
+// so that first call should come before any stream capture on that device
+// and before any region where the caller cannot let memory be reserved.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LCE_ERR_CUDA;

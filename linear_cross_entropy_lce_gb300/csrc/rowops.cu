@@ -257,4 +257,62 @@ cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, int dt,
   return e;
 }
 
+// Gradients times a device scalar g, in place, for the backward of the
+// scalar-reduction ops (linear_cross_entropy.py precomputes the gradients in
+// the forward and multiplies them by grad_output in the backward). Every
+// block reads g first and returns at once when g == 1, so a caller needs no
+// host-side test of g (no synchronisation) to skip the pass.
+template <class T>
+__device__ __forceinline__ void scale_span(T* p, int64_t n, float g, int64_t tid, int64_t nthreads) {
+  if (p == nullptr || n <= 0) return;
+  constexpr int VE = 16 / static_cast<int>(sizeof(T));
+  const bool vec = (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+  const int64_t nv = vec ? n / VE : 0;
+  for (int64_t i = tid; i < nv; i += nthreads) {
+    uint4 raw = reinterpret_cast<const uint4*>(p)[i];
+    T* e = reinterpret_cast<T*>(&raw);
+#pragma unroll
+    for (int k = 0; k < VE; ++k) e[k] = from_f32<T>(to_f32(e[k]) * g);
+    reinterpret_cast<uint4*>(p)[i] = raw;
+  }
+  for (int64_t i = nv * VE + tid; i < n; i += nthreads) p[i] = from_f32<T>(to_f32(p[i]) * g);
+}
+
+template <class T>
+__global__ void __launch_bounds__(256) scale_grads_kernel(T* a, int64_t na, T* b, int64_t nb, T* c, int64_t nc,
+                                                          const float* __restrict__ g) {
+  const float gv = *g;
+  if (gv == 1.0f) return;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  scale_span(a, na, gv, tid, nthreads);
+  scale_span(b, nb, gv, tid, nthreads);
+  scale_span(c, nc, gv, tid, nthreads);
+}
+
+cudaError_t launch_scale_grads(void* a, int64_t na, void* b, int64_t nb, void* c, int64_t nc, int dt,
+                               const float* g, cudaStream_t s) {
+  const int64_t total = na + nb + nc;
+  if (total == 0) return cudaSuccess;
+  const int esz = dt == LCE_F32 ? 4 : 2;
+  int64_t blocks = (total / (16 / esz) + 255) / 256;
+  if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
+  if (blocks < 1) blocks = 1;
+  prof_before(K_SCALE_GRADS, s, 2.0 * esz * total);
+  const unsigned nbk = static_cast<unsigned>(blocks);
+  if (dt == LCE_BF16)
+    scale_grads_kernel<__nv_bfloat16><<<nbk, 256, 0, s>>>(static_cast<__nv_bfloat16*>(a), na,
+                                                          static_cast<__nv_bfloat16*>(b), nb,
+                                                          static_cast<__nv_bfloat16*>(c), nc, g);
+  else if (dt == LCE_F16)
+    scale_grads_kernel<__half><<<nbk, 256, 0, s>>>(static_cast<__half*>(a), na, static_cast<__half*>(b), nb,
+                                                   static_cast<__half*>(c), nc, g);
+  else
+    scale_grads_kernel<float><<<nbk, 256, 0, s>>>(static_cast<float*>(a), na, static_cast<float*>(b), nb,
+                                                  static_cast<float*>(c), nc, g);
+  cudaError_t e = cudaGetLastError();
+  prof_after(K_SCALE_GRADS, s);
+  return e;
+}
+
 }  // namespace lce

@@ -49,10 +49,45 @@ def test_autograd_retain_graph_and_partial_grads(cuda_lib):
     inp = make_linear_inputs(128, 32, 300, torch.bfloat16, "cuda", seed=32, w_std=0.4)
     X = inp["X"].requires_grad_(True)
     W = inp["W"]  # no gradient wanted for the weight
-    loss = linear_cross_entropy(X, W, inp["target"], reduction="mean")
-    loss.backward(retain_graph=True)
+    # allow_retain_graph keeps the precomputed gradients: two backwards with
+    # an upstream gradient of 2 give the same (scaled once) gradient
+    loss = linear_cross_entropy(X, W, inp["target"], reduction="mean", allow_retain_graph=True)
+    (loss * 2.0).backward(retain_graph=True)
     g1 = X.grad.clone()
     X.grad = None
-    loss.backward()
+    (loss * 2.0).backward()
     assert torch.equal(g1, X.grad)
     assert W.grad is None
+    X.grad = None
+    ref = linear_cross_entropy(X, W, inp["target"], reduction="mean")
+    ref.backward()
+    assert rel_max(to64(g1), 2.0 * to64(X.grad)) < 1e-2
+    # without it the buffers are handed out and scaled in place: a second
+    # backward through the same loss raises, as the page's option says
+    loss = linear_cross_entropy(X, W, inp["target"], reduction="mean")
+    (loss * 3.0).backward(retain_graph=True)
+    with pytest.raises(RuntimeError):
+        loss.backward()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_scale_gradients_in_place(cuda_lib, dtype):
+    """lce_scale_gradients: buffers times a device scalar, untouched when it
+    is 1; ragged lengths and an unaligned start take the scalar tail path."""
+    g = torch.Generator(device="cuda").manual_seed(5)
+    dX = torch.randn(1001, generator=g, device="cuda").to(dtype)
+    dW = torch.randn(37, 129, generator=g, device="cuda").to(dtype)
+    base = torch.randn(301, generator=g, device="cuda").to(dtype)
+    db = base[1:]  # 2 or 4 bytes past a 16-byte boundary
+    first = base[0].clone()
+    keep = [x.clone() for x in (dX, dW, db)]
+    cuda_lib.lce_scale_gradients(dX, dW, db, torch.ones((), device="cuda"))
+    torch.cuda.synchronize()
+    for a, k in zip((dX, dW, db), keep):
+        assert torch.equal(a, k)
+    cuda_lib.lce_scale_gradients(dX, None, db, torch.tensor(-0.75, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(dW, keep[1])
+    for a, k in ((dX, keep[0]), (db, keep[2])):
+        assert torch.equal(a, (k.float() * -0.75).to(dtype))
+    assert torch.equal(base[0], first)  # the element before db is untouched

@@ -34,7 +34,8 @@ def _slabs(lib, rows):
     return n, list(off)
 
 
-@pytest.mark.parametrize("rows", [1024, 1025, 1100, 2048, 3000, 4096, 8192, 8193, 16384, 65536, 1 << 20])
+@pytest.mark.parametrize("rows", [1024, 1025, 1100, 1229, 1500, 1638, 2047, 2048, 3000, 4096, 8192, 8193, 16384,
+                                  65536, 1 << 20])
 def test_row_slabs_cover_the_chunk(lib, rows):
     n, off = _slabs(lib, rows)
     assert 1 <= n <= 4
@@ -44,12 +45,23 @@ def test_row_slabs_cover_the_chunk(lib, rows):
     # every slab but the last starts and ends on a 256-row boundary (the
     # CTA-pair tile height), so only the last one has a ragged tail
     assert all(off[k] % 256 == 0 for k in range(n))
+    assert sizes == sorted(sizes)
     if rows >= 8192:
-        # four growing slabs near 4 : 7 : 9 : 12 of the rows
+        # four strictly growing slabs near 4 : 7 : 9 : 12 of the rows
         assert n == 4
-        assert sizes == sorted(sizes)
+        assert all(a < b for a, b in zip(sizes, sizes[1:]))
         for s, wgt in zip(sizes, (4, 7, 9, 12)):
             assert abs(s / rows - wgt / 32) < 256 / rows + 1e-9
+
+
+def test_row_slabs_never_shrink(lib):
+    """Each slab's side job runs beside the next slab's GEMM, so no slab may
+    be larger than the one after it, at any row count the slabbed path takes
+    (every count from 1024 to 8192, then a stride beyond)."""
+    for rows in list(range(1024, 8193)) + list(range(8193, 70000, 97)):
+        n, off = _slabs(lib, rows)
+        sizes = [off[k + 1] - off[k] for k in range(n)]
+        assert n >= 2 and sizes == sorted(sizes) and off[n] == rows, (rows, sizes)
 
 
 def test_row_slabs_arguments(lib):

@@ -8,11 +8,13 @@ that a run stopping at its first failure has run every other test."""
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 import linear_cross_entropy_lce_gb300 as lce
 from linear_cross_entropy_lce_gb300.workloads import make_logits_inputs
+from oracle import lce_oracle as O
 from tests.util import TOL, rel_max, rel_scalar, to64
 
 pytestmark = pytest.mark.gpu
@@ -46,6 +48,7 @@ def test_noalloc_matches_workspace_entry_point(cuda_lib, dtype):
     tol = TOL[dtype]
     for inp, reduction, g in calls:
         a = inp["logits"]
+        snap = to64(a)  # the logits before either call overwrites its copy
         b = a.clone()
         t = inp["target"]
         ref_loss = lce.lce_cross_entropy_from_logits(a, t, reduction, -100, g)
@@ -57,6 +60,37 @@ def test_noalloc_matches_workspace_entry_point(cuda_lib, dtype):
         else:
             assert rel_scalar(loss.item(), ref_loss.item()) < tol["loss"]
         assert rel_max(to64(b), to64(a)) < tol["grad"]
+        # and against the float64 oracle directly
+        rl, rg = O.ce_from_logits(snap, t.cpu().numpy(), reduction, -100, None if g is None else to64(g))
+        if reduction == "none":
+            assert rel_max(to64(loss), rl) < tol["loss"]
+        else:
+            assert rel_scalar(loss.item(), rl) < tol["loss"]
+        assert rel_max(to64(b), rg) < tol["grad"]
+
+
+def test_noalloc_at_the_row_limit(cuda_lib):
+    """N == LCE_NOALLOC_MAX_ROWS fits the fixed scratch and matches the
+    workspace entry point and the oracle (a narrow vocabulary keeps the
+    logits at 32 MiB)."""
+    lib = lce.load_library()
+    N, V = lce.LCE_NOALLOC_MAX_ROWS, 8
+    inp = make_logits_inputs(N, V, torch.float32, "cuda", seed=24, std=1.0, n_ignored=11)
+    a = inp["logits"]
+    t = inp["target"]
+    snap = to64(a)
+    b = a.clone()
+    ref_loss = lce.lce_cross_entropy_from_logits(a, t, "mean", -100)
+    loss, status = _noalloc(lib, b, t, "mean", None)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    tol = TOL[torch.float32]
+    assert rel_scalar(loss.item(), ref_loss.item()) < tol["loss"]
+    assert rel_max(to64(b), to64(a)) < tol["grad"]
+    rl, rg = O.ce_from_logits(snap, t.cpu().numpy(), "mean", -100)
+    assert rel_scalar(loss.item(), rl) < tol["loss"]
+    assert np.isfinite(to64(b)).all()
+    assert rel_max(to64(b), rg) < tol["grad"]
 
 
 def test_noalloc_limits_and_status(cuda_lib):
