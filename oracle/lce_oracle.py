@@ -13,6 +13,8 @@ step in float64 with numpy (the matmul is the only library primitive used):
   lse_n     = m_n + log sum_j exp(z[n, j] - m_n),  m_n = max_j z[n, j]
   loss_n    = valid_n ? lse_n - z[n, target_n] : 0
   loss      = none: loss_n | sum: sum_n loss_n | mean: sum_n loss_n / n_valid
+              (or / d for a given denominator d: a data-parallel shard of a
+              batch divides by the whole batch's n_valid)
   w_n       = c_n * (mean: g / sum_n c_n | sum: g | none: g_n),
               c_n = valid_n * weight[target_n] (weight = 1 without class weights)
   (with class weights loss_n is c_n (lse_n - z[n, target_n]) and mean
@@ -110,7 +112,7 @@ def class_weight_of_rows(target, valid, class_weight):
 
 
 def row_weights(target, num_classes, reduction, ignore_index=DEFAULT_IGNORE_INDEX, grad_out=None,
-                class_weight=None):
+                class_weight=None, denominator=None):
     """Per-row loss weight w_n, with the upstream gradient folded in.
 
     linear_cross_entropy.py, ``_ChunkContext.neg_weight_target``: ignored
@@ -121,7 +123,10 @@ def row_weights(target, num_classes, reduction, ignore_index=DEFAULT_IGNORE_INDE
     upstream gradient multiplies the precomputed gradients
     (``_linear_cross_entropy_batch_chunked_backward``:
     ``grad.mul_(grad_output)``); it is folded into w_n here. grad_out=None
-    means 1.0 for mean/sum and is required for none.
+    means 1.0 for mean/sum and is required for none. denominator: None, or
+    the d that mean divides by instead of these rows' own (a shard of a
+    larger batch divides by the whole batch's d, so that the shards' results
+    add up to the whole batch's).
     """
     _check_reduction(reduction)
     valid = valid_mask(target, num_classes, ignore_index)
@@ -136,7 +141,7 @@ def row_weights(target, num_classes, reduction, ignore_index=DEFAULT_IGNORE_INDE
     g = 1.0 if grad_out is None else float(np.asarray(grad_out, dtype=np.float64).reshape(-1)[0])
     if reduction == "sum":
         return v * g
-    d = v.sum()
+    d = v.sum() if denominator is None else float(denominator)
     inv = math.nan if d == 0 else 1.0 / d
     return v * (inv * g)  # 0 * NaN = NaN: all rows NaN when n_valid == 0
 
@@ -158,15 +163,15 @@ def log_sum_exp(z: np.ndarray) -> np.ndarray:
         return m + np.log(np.exp(z - m[:, None]).sum(axis=1))
 
 
-def _reduce(loss_rows: np.ndarray, c: np.ndarray, reduction: str):
+def _reduce(loss_rows: np.ndarray, c: np.ndarray, reduction: str, denominator=None):
     """c: per-row class weights (0 on ignored rows; the valid mask without
-    class weights); mean divides by their sum."""
+    class weights); mean divides by their sum, or by the given denominator."""
     if reduction == "none":
         return loss_rows
     total = float(loss_rows.sum())
     if reduction == "sum":
         return total
-    d = float(np.asarray(c, dtype=np.float64).sum())
+    d = float(np.asarray(c, dtype=np.float64).sum()) if denominator is None else float(denominator)
     # mean over the valid rows; N == 0 or all rows ignored gives NaN
     # (linear_cross_entropy.py: the empty-batch mean and neg_weight_target's
     # d == 0 case).
@@ -174,7 +179,7 @@ def _reduce(loss_rows: np.ndarray, c: np.ndarray, reduction: str):
 
 
 def ce_from_logits(logits, target, reduction="mean", ignore_index=DEFAULT_IGNORE_INDEX,
-                   grad_out=None, want_grad=True, class_weight=None):
+                   grad_out=None, want_grad=True, class_weight=None, denominator=None):
     """Cross entropy on given logits [N, V], and the gradient that replaces them.
 
     Liger-Kernel issue #343: one pass gives the loss and writes
@@ -192,7 +197,7 @@ def ce_from_logits(logits, target, reduction="mean", ignore_index=DEFAULT_IGNORE
     grad = np.zeros_like(z) if want_grad else None
     w = None
     if want_grad:
-        w = row_weights(target, V, reduction, ignore_index, grad_out, class_weight)
+        w = row_weights(target, V, reduction, ignore_index, grad_out, class_weight, denominator)
     for r0 in range(0, N, ROW_BLOCK):
         r1 = min(N, r0 + ROW_BLOCK)
         zb = z[r0:r1]
@@ -205,10 +210,11 @@ def ce_from_logits(logits, target, reduction="mean", ignore_index=DEFAULT_IGNORE
             P = np.exp(zb - lse[:, None])
             P[rows, tc[r0:r1]] -= valid[r0:r1].astype(np.float64)
             grad[r0:r1] = w[r0:r1, None] * P
-    return _reduce(loss_rows, c, reduction), grad
+    return _reduce(loss_rows, c, reduction, denominator), grad
 
 
-def lce_forward(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE_INDEX, class_weight=None):
+def lce_forward(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE_INDEX, class_weight=None,
+                denominator=None):
     """Loss of the fused linear + cross-entropy, and lse per row.
 
     Returns (loss, lse[N]); loss is a float for sum/mean and loss_n [N] for
@@ -234,11 +240,11 @@ def lce_forward(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE_I
         zt = z[np.arange(r1 - r0), tc[r0:r1]]
         with np.errstate(invalid="ignore"):  # an ignored row's placeholder column may be -inf
             loss_rows[r0:r1] = np.where(valid[r0:r1], c[r0:r1] * (lse[r0:r1] - zt), 0.0)
-    return _reduce(loss_rows, c, reduction), lse
+    return _reduce(loss_rows, c, reduction, denominator), lse
 
 
 def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE_INDEX,
-                         grad_out=None, class_weight=None):
+                         grad_out=None, class_weight=None, denominator=None):
     """Loss and all gradients (dX, dW, db) of the fused linear + cross-entropy.
 
     Returns (loss, dX[N, D], dW[C, D], db[C] or None). For mean/sum the
@@ -259,7 +265,7 @@ def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=DEFAULT
     valid = valid_mask(target, C, ignore_index)
     tc = corrected_target(target, valid)
     c = class_weight_of_rows(target, valid, class_weight)
-    w = row_weights(target, C, reduction, ignore_index, grad_out, class_weight)
+    w = row_weights(target, C, reduction, ignore_index, grad_out, class_weight, denominator)
     loss_rows = np.zeros(N)
     dX = np.zeros((N, D))
     dW = np.zeros((C, D))
@@ -279,7 +285,7 @@ def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=DEFAULT
         dW += G.T @ X[r0:r1]
         if db is not None:
             db += G.sum(axis=0)
-    return _reduce(loss_rows, c, reduction), dX, dW, db
+    return _reduce(loss_rows, c, reduction, denominator), dX, dW, db
 
 
 # --------------------------------------------------------------------------

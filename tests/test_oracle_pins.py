@@ -293,7 +293,8 @@ def _mut_transposed_weight_grad(X, W, b, t, reduction, ignore_index, grad_out):
     return loss, dX, dW[::-1].copy(), db
 
 
-def _mut_mean_over_all_rows(target, num_classes, reduction, ignore_index=-100, grad_out=None, class_weight=None):
+def _mut_mean_over_all_rows(target, num_classes, reduction, ignore_index=-100, grad_out=None, class_weight=None,
+                            denominator=None):
     valid = O.valid_mask(target, num_classes, ignore_index).astype(np.float64)
     if reduction == "mean":
         return valid / len(valid)
@@ -386,3 +387,63 @@ def test_masked_classes_equal_deleted_classes(reduction):
     np.testing.assert_allclose(lz, lr, rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(gz[:, keep], gr, rtol=1e-11, atol=1e-14)
     assert (gz[:, masked] == 0).all()
+
+
+@pytest.mark.parametrize("class_weights", [False, True])
+@pytest.mark.parametrize("g", [None, 1.75])
+def test_given_denominator_shards_add_up_to_the_batch(class_weights, g):
+    """Data-parallel shards of one batch, each dividing by the WHOLE batch's
+    mean denominator: their losses, dW and db sum to the whole batch's and
+    their dX rows are the whole batch's rows (an empty shard and a shard of
+    ignored rows included)."""
+    X, W, b, t = _rand_case(N=23, D=6, C=9, n_ign=4, seed=77)
+    t[17:20] = -100  # the third shard below holds only ignored rows
+    cw = np.random.default_rng(5).uniform(0.2, 2.0, 9) if class_weights else None
+    whole = O.lce_forward_backward(X, W, b, t, "mean", -100, g, class_weight=cw)
+    valid = t != -100
+    d = float(valid.sum()) if cw is None else float(cw[t[valid]].sum())
+    cuts = [0, 9, 9, 17, 20, 23]  # shards [0,9), [9,9) (empty), [9,17), [17,20), [20,23)
+    loss = 0.0
+    dX = np.zeros_like(X)
+    dW = np.zeros_like(W)
+    db = np.zeros_like(b)
+    for a, e in zip(cuts[:-1], cuts[1:]):
+        sl, sX, sW, sb = O.lce_forward_backward(X[a:e], W, b, t[a:e], "mean", -100, g, class_weight=cw,
+                                                denominator=d)
+        if e > a:
+            loss += sl
+        dX[a:e] = sX
+        dW += sW
+        db += sb
+    assert math.isclose(loss, whole[0], rel_tol=1e-12)
+    for got, ref in ((dX, whole[1]), (dW, whole[2]), (db, whole[3])):
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_given_denominator_against_torch():
+    """A shard's mean with denominator d is torch's weighted sum of the shard's
+    row losses divided by d, gradients included (torch float64 autograd)."""
+    X, W, b, t = _rand_case(N=10, D=5, C=7, n_ign=2, seed=79)
+    cw = np.random.default_rng(6).uniform(0.5, 1.5, 7)
+    d = 37.5
+    loss, dX, dW, db = O.lce_forward_backward(X, W, b, t, "mean", -100, 0.5, class_weight=cw, denominator=d)
+    Xt = torch.tensor(X, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    bt = torch.tensor(b, requires_grad=True)
+    ref = F.cross_entropy(F.linear(Xt, Wt, bt), torch.tensor(t), weight=torch.tensor(cw), reduction="sum",
+                          ignore_index=-100) / d
+    (ref * 0.5).backward()
+    assert math.isclose(loss, ref.item(), rel_tol=1e-12)
+    for got, r in ((dX, Xt.grad), (dW, Wt.grad), (db, bt.grad)):
+        assert np.allclose(got, r.numpy(), rtol=1e-10, atol=1e-14)
+    # the same through cross entropy on given logits
+    z = O.logits_block(X, W, b)
+    l2, gz = O.ce_from_logits(z, t, "mean", -100, class_weight=cw, denominator=d)
+    zt = torch.tensor(z, requires_grad=True)
+    r2 = F.cross_entropy(zt, torch.tensor(t), weight=torch.tensor(cw), reduction="sum", ignore_index=-100) / d
+    r2.backward()
+    assert math.isclose(l2, r2.item(), rel_tol=1e-12)
+    assert np.allclose(gz, zt.grad.numpy(), rtol=1e-10, atol=1e-14)
+    # a zero denominator gives NaN, as the page's d == 0 does
+    l0, gX0, _, _ = O.lce_forward_backward(X, W, b, t, "mean", -100, denominator=0.0)
+    assert math.isnan(l0) and np.isnan(gX0).all()
