@@ -2,7 +2,8 @@
 
 Default: the bf16 LLM-head workload (N=8192 tokens, D=4096, C=128256, Zipf
 targets, 5% ignored, mean), one step = one lce_forward_backward call (loss,
-dX, dW) on inputs resident in HBM. Prints ONE JSON line.
+dX, dW) on inputs resident in HBM, with the library's default workspace
+plan (gradient buffer bounded by 1 GiB). Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl reference]
@@ -277,30 +278,47 @@ def run_gpu(args):
         C = W.shape[0]
         dt = lce.LCE_BF16 if X.dtype == torch.bfloat16 else lce.LCE_F32
         red = {"none": 0, "sum": 1, "mean": 2}[w.reduction]
-        nbytes = lce.lce_workspace_size(lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, red, dt, 0)
+        # reduction none: forward (loss, lse), then the backward from that lse
+        # (the page's none op); else one forward+backward call
+        bw_op = lce.LCE_OP_BACKWARD if red == 0 else lce.LCE_OP_FORWARD_BACKWARD
+        if args.buffer_mib is not None:
+            nbytes = lce.lce_workspace_size_for_buffer(bw_op, N, D, C, dt, red, dt, args.buffer_mib << 20)
+        else:
+            nbytes = lce.lce_workspace_size(bw_op, N, D, C, dt, red, dt, 0)
+        if red == 0:
+            nbytes = max(nbytes, lce.lce_workspace_size(lce.LCE_OP_FORWARD, N, D, C, dt, red, dt, 0))
         wsbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         status_acc = torch.zeros(1, dtype=torch.int32, device=dev)
         status_word = wsbuf[:4].view(torch.int32)
+        plan = lce.plan_of(bw_op, N, D, C, dt, dt, nbytes, want_db=b is not None)
         dX = torch.empty_like(X)
         dW = torch.empty_like(W)
         db = torch.empty_like(b) if b is not None else None
         loss = torch.empty(N if red == 0 else 1, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
         lib = lce.load_library()
         import ctypes
 
         P = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())
 
-        def step(mark=None):
-            if red == 0:  # reduction none: forward, then forward+backward with the upstream vector
-                lce._check(lib.lce_forward(P(X), P(W), P(b), P(t), N, D, C, dt, 0, red, -100, P(loss), None,
+        def calls(Xi, Wi, bi, ti, gi, li, dXi, dWi, dbi, mark=None):
+            if red == 0:
+                lce._check(lib.lce_forward(P(Xi), P(Wi), P(bi), P(ti), N, D, C, dt, 0, red, -100, P(li), P(lse),
                                            P(wsbuf), nbytes, ctypes.c_void_p(stream.cuda_stream)), "fwd")
                 status_acc.bitwise_or_(status_word)
                 if mark is not None:
                     mark()  # CUDA event between the two parts
-            lce._check(lib.lce_forward_backward(P(X), P(W), P(b), P(t), N, D, C, dt, 0, red, -100, P(g), P(loss),
-                                                P(dX), P(dW), P(db), dt, P(wsbuf), nbytes,
-                                                ctypes.c_void_p(stream.cuda_stream)), "fwd+bwd")
+                lce._check(lib.lce_backward(P(Xi), P(Wi), P(bi), P(ti), P(lse), N, D, C, dt, 0, red, -100, P(gi),
+                                            P(dXi), P(dWi), P(dbi), dt, P(wsbuf), nbytes,
+                                            ctypes.c_void_p(stream.cuda_stream)), "bwd")
+            else:
+                lce._check(lib.lce_forward_backward(P(Xi), P(Wi), P(bi), P(ti), N, D, C, dt, 0, red, -100, P(gi),
+                                                    P(li), P(dXi), P(dWi), P(dbi), dt, P(wsbuf), nbytes,
+                                                    ctypes.c_void_p(stream.cuda_stream)), "fwd+bwd")
             status_acc.bitwise_or_(status_word)
+
+        def step(mark=None):
+            calls(X, W, b, t, g, loss, dX, dW, db, mark)
             return loss
 
         flops = w.flops_fwd_bwd
@@ -353,6 +371,41 @@ def run_gpu(args):
     launches = lce.launch_count() - launches0
     clocks = sampler.stop()
     ms = aggregate_ms(e0.elapsed_time(e1) / args.steps, dist, dev)
+
+    # ---- context for the memory bound: the same step with the plan that
+    # keeps every class of every row in the gradient buffer (no
+    # recomputation), a few steps, outside the timed region
+    whole = None
+    if w.kind != "logits" and dist is None:
+        wbytes = lce.lce_workspace_size_for_buffer(bw_op, N, D, C, dt, red, dt, (1 << 63) - 1)
+        if red == 0:
+            wbytes = max(wbytes, lce.lce_workspace_size(lce.LCE_OP_FORWARD, N, D, C, dt, red, dt, 0))
+        wplan = lce.plan_of(bw_op, N, D, C, dt, dt, wbytes, want_db=b is not None)
+        free_b, _ = torch.cuda.mem_get_info(dev)
+        if (wplan["Cb"], wplan["Bc"]) != (plan["Cb"], plan["Bc"]) and wbytes + (1 << 30) < free_b:
+            main_ws, main_n = wsbuf, nbytes
+            wsbuf = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+            status_word = wsbuf[:4].view(torch.int32)
+            nbytes = wbytes
+            for _ in range(3):
+                step()
+            barrier()
+            k = min(args.steps, 10)
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(k):
+                step()
+            a1.record(stream)
+            barrier()
+            check_status("whole-buffer steps")
+            wms = a0.elapsed_time(a1) / k
+            whole = {"ms_per_step": wms, "tflops": flops / (wms / 1e3) / 1e12, "workspace_bytes": int(wbytes),
+                     "steps": k, "note": "every class of every row stored in the gradient buffer; not the "
+                                         "headline (timed after it, outside the timed region)"}
+            del wsbuf
+            wsbuf, nbytes = main_ws, main_n
+            status_word = wsbuf[:4].view(torch.int32)
 
     # ---- the same step captured once in a CUDA graph and replayed (the
     # library allocates and synchronizes nothing, so its calls capture):
@@ -409,14 +462,7 @@ def run_gpu(args):
         def run_on(i):
             Xi, Wi, ti, bi, gi = in_sets[i]
             li, dXi, dWi, dbi = out_sets[i]
-            if red == 0:
-                lce._check(lib.lce_forward(P(Xi), P(Wi), P(bi), P(ti), N, D, C, dt, 0, red, -100, P(li), None,
-                                           P(wsbuf), nbytes, ctypes.c_void_p(stream.cuda_stream)), "fwd")
-                status_acc.bitwise_or_(status_word)
-            lce._check(lib.lce_forward_backward(P(Xi), P(Wi), P(bi), P(ti), N, D, C, dt, 0, red, -100, P(gi),
-                                                P(li), P(dXi), P(dWi), P(dbi), dt, P(wsbuf), nbytes,
-                                                ctypes.c_void_p(stream.cuda_stream)), "fwd+bwd")
-            status_acc.bitwise_or_(status_word)
+            calls(Xi, Wi, bi, ti, gi, li, dXi, dWi, dbi)
     else:
         # the gradient replaces the logits: the step's result is the loss and
         # the whole logits buffer
@@ -549,6 +595,22 @@ def run_gpu(args):
                          f"float64 numpy, {sec:.1f} s"}
 
     tokens_per_s = ws * w.N / (ms / 1e3)
+    cfg = _config(w, ws)
+    cfg["workspace_bytes"] = int(nbytes)
+    executed = None
+    if w.kind != "logits":
+        esz = 2 if w.dtype == torch.bfloat16 else 4
+        cfg["gradient_buffer"] = {
+            "rows": plan["Bc"], "classes": plan["Cb"], "bytes": plan["Bc"] * plan["Cb"] * esz,
+            "stored_classes": min(plan["Cs"], w.C), "recomputed_class_chunks": plan["nvc"],
+            "batch_chunks": plan["nchunks"],
+            "whole_logits_bytes": w.N * w.C * esz,
+            "budget": f"{args.buffer_mib} MiB (--buffer-mib)" if args.buffer_mib is not None
+                      else "library default (1 GiB)"}
+        # tensor-core work actually run: the algorithmic 6NDC (8NDC for none),
+        # plus the logits of every class recomputed after the forward sweep
+        recomputed = max(0, w.C - min(plan["Cs"], w.C)) if red != 0 else 0
+        executed = flops + 2.0 * w.N * w.D * recomputed
     line = {
         "metric": METRIC,
         "value": tokens_per_s,
@@ -562,7 +624,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic",
-        "config": _config(w, ws),
+        "config": cfg,
         "gpu_launches": launches,
         "clocks": clocks,
         "roofline": roofline,
@@ -573,12 +635,16 @@ def run_gpu(args):
     }
     if graph_ms is not None:
         line["graph_replay_ms_per_step"] = graph_ms
+    if whole is not None:
+        line["whole_buffer_plan"] = whole
     if part_events:
         fwd_ms = sum(ev[0].elapsed_time(ev[1]) for ev in part_events) / len(part_events)
         fb_ms = sum(ev[1].elapsed_time(ev[2]) for ev in part_events) / len(part_events)
         ndc2 = 2.0 * w.N * w.D * w.C
         line["parts"] = {"forward_ms": fwd_ms, "forward_tflops": ndc2 / (fwd_ms / 1e3) / 1e12,
-                         "forward_backward_ms": fb_ms, "forward_backward_tflops": 3 * ndc2 / (fb_ms / 1e3) / 1e12}
+                         "backward_ms": fb_ms, "backward_tflops": 3 * ndc2 / (fb_ms / 1e3) / 1e12}
+    if executed is not None:
+        line["executed_tflops"] = executed * ws / (ms / 1e3) / 1e12
     if flops:
         line["tflops"] = flops * ws / (ms / 1e3) / 1e12
         line["pct_bf16_peak"] = 100.0 * line["tflops"] / ws / peaks["bf16_tflops"]
@@ -602,6 +668,8 @@ def main():
     ap.add_argument("--rows", type=int, default=0, help="override N (profiling a smaller case)")
     ap.add_argument("--dim", type=int, default=0, help="override D")
     ap.add_argument("--classes", type=int, default=0, help="override C (or V)")
+    ap.add_argument("--buffer-mib", type=int, default=None,
+                    help="gradient-buffer budget of the workspace plan (default: the library's 1 GiB)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -87,7 +87,7 @@ enum lce_dtype_e { LCE_F32 = 0, LCE_BF16 = 1, LCE_F16 = 2 };
 enum lce_reduction_e { LCE_RED_NONE = 0, LCE_RED_SUM = 1, LCE_RED_MEAN = 2 };
 
 /* Operations, for lce_workspace_size. */
-enum lce_op_e { LCE_OP_FORWARD = 0, LCE_OP_FORWARD_BACKWARD = 1, LCE_OP_CE_FROM_LOGITS = 2 };
+enum lce_op_e { LCE_OP_FORWARD = 0, LCE_OP_FORWARD_BACKWARD = 1, LCE_OP_CE_FROM_LOGITS = 2, LCE_OP_BACKWARD = 3 };
 
 /* Status codes. */
 enum lce_status_e {
@@ -107,22 +107,50 @@ enum lce_status_e {
 
 /*
  * Workspace bytes needed by one call.
- *   op          LCE_OP_FORWARD, LCE_OP_FORWARD_BACKWARD or LCE_OP_CE_FROM_LOGITS
+ *   op          LCE_OP_FORWARD, LCE_OP_FORWARD_BACKWARD, LCE_OP_BACKWARD or
+ *               LCE_OP_CE_FROM_LOGITS
  *   N, D, C     problem sizes (for CE_FROM_LOGITS pass D = 1 and C = V)
  *   dtype       input type; grad_dtype: gradient type (ignored for FORWARD)
- *   chunk_rows  rows per batch chunk of the backward; 0 picks the default:
- *               as many rows as keep the [chunk_rows, C] gradient buffer
- *               within 8 GiB. Fewer rows need less memory: the backward
- *               keeps one [chunk_rows, ceil(C/256)*256] buffer of the input
- *               type (the batch-chunked buffer of linear_cross_entropy.py)
- *               and, when there is more than one chunk and dW is bf16, an
- *               fp32 [C, D] accumulator for dW.
- * The size depends only on these arguments. A call given ws_bytes >= this
- * size uses the largest chunk (a multiple of 128 rows, or all rows) that
- * fits in ws_bytes. Returns 0 on invalid arguments.
+ *   chunk_rows  0: the default plan, whose gradient buffer is bounded by
+ *               1 GiB (below). > 0: batch chunks of that many rows (rounded
+ *               down to 128 * 2^k, or all N rows), each with one buffer for
+ *               every class: [rows, ceil(C/256)*256] of the input type, plus
+ *               an fp32 [C, D] accumulator for a bf16 / fp16 dW when there
+ *               is more than one chunk. chunk_rows >= N gives the plan with
+ *               the whole [N, C] buffer, which does no recomputation.
+ *
+ * The backward keeps the softmax of a [rows, classes] block of logits in a
+ * buffer of the input type (the batch-chunked buffer of
+ * linear_cross_entropy.py; the full [N, C] logits are never held unless
+ * they fit the budget). Under the default 1 GiB budget, on the bf16 / fp16
+ * path, the buffer keeps all N rows and as many classes Cb as fit (at
+ * least D rounded up to 256): the forward sweep stores its exp values for
+ * classes [0, Cb); classes [Cb, C) are recomputed in chunks of Cb (their
+ * logits computed a second time, 2 N D Cb flop each, formed straight into
+ * gradient tiles); dX is summed over the class chunks in an fp32 [N, D]
+ * accumulator and each chunk's rows of dW are complete when written (no
+ * [C, D] scratch). Only when even D classes of all rows exceed the budget
+ * does it also split the rows into batch chunks. fp32 inputs split rows only.
+ * E.g. N = 8192, C = 128256 (bf16): Cb = 65536, one recomputed chunk, total
+ * work 7 N D C instead of 6 N D C, buffer 1 GiB instead of 2.1 GB.
+ *
+ * The size depends only on these arguments. A call given any ws_bytes uses
+ * the fastest plan that fits: all rows and all classes; else all rows and
+ * the widest class chunk (a multiple of 256, at least D rounded up) that
+ * fits; else the same for the largest batch chunk of 128 * 2^k rows that
+ * fits. Returns 0 on invalid arguments.
  */
 LCE_API size_t lce_workspace_size(int op, int64_t N, int64_t D, int64_t C, int dtype,
                           int reduction, int grad_dtype, int64_t chunk_rows);
+
+/*
+ * Workspace bytes of the plan whose gradient buffer fits buffer_bytes (the
+ * rule of the default plan above with that budget; 0 means the default
+ * 1 GiB; (size_t)-1 gives the whole [N, C] buffer). Same arguments as
+ * lce_workspace_size otherwise; 0 on invalid arguments.
+ */
+LCE_API size_t lce_workspace_size_for_buffer(int op, int64_t N, int64_t D, int64_t C, int dtype,
+                                             int reduction, int grad_dtype, size_t buffer_bytes);
 
 /*
  * Loss only (linear_cross_entropy.py: the chunked forward and the
@@ -161,6 +189,26 @@ LCE_API int lce_forward_backward(const void* X, const void* W, const void* b, co
                          int reduction, int64_t ignore_index, const float* grad_out,
                          float* loss_out, void* dX, void* dW, void* db, int grad_dtype,
                          void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Gradients only, from the row log-sum-exp a forward call returned (its
+ * lse_out): the backward of reduction="none" in linear_cross_entropy.py,
+ * which saves the inputs and recomputes the logits chunk by chunk in its
+ * backward. Same arguments as lce_forward_backward, without loss_out and
+ * with lse [N] fp32 (device): it must be the lse of these X, W, b.
+ * On the bf16 / fp16 path every class is recomputed once (2 N D C flop)
+ * and formed straight into gradient tiles, so the call does 6 N D C flop
+ * where lce_forward_backward does the same plus nothing saved; a
+ * lce_forward + lce_backward pair is the 8 N D C of the page's none op.
+ * fp32 inputs do not use lse: the call computes the row statistics itself
+ * (its own forward sweep) and returns the same gradients.
+ * Workspace: lce_workspace_size(LCE_OP_BACKWARD, ...).
+ */
+LCE_API int lce_backward(const void* X, const void* W, const void* b, const int64_t* target,
+                         const float* lse, int64_t N, int64_t D, int64_t C, int dtype,
+                         int acc_dtype, int reduction, int64_t ignore_index, const float* grad_out,
+                         void* dX, void* dW, void* db, int grad_dtype, void* workspace,
+                         size_t ws_bytes, void* stream);
 
 /*
  * Cross entropy on given logits [N, V] (dtype LCE_F32, LCE_BF16 or
@@ -218,30 +266,60 @@ LCE_API int lce_cross_entropy_from_logits_noalloc(void* logits_inout, const int6
                                                   float* loss_out, int* device_status, void* stream);
 
 /*
- * Per-class weights (the page's `weight` argument of cross entropy).
- * Same as lce_forward / lce_forward_backward / lce_cross_entropy_from_logits
- * with one more input, class_weight: NULL (no class weights) or a device
- * fp32 [C] (or [V]) array. A valid row n then has loss weight
- * c_n = class_weight[target_n]: loss_n = c_n (lse_n - z[n, target_n]),
- * mean divides by the sum of c_n over the valid rows (NaN when that sum is
- * 0), and the gradients carry c_n in w_n (linear_cross_entropy.py,
- * neg_weight_target: the per-row weight is the class weight of the target,
- * divided by their sum for mean).
+ * Per-class weights and a given mean denominator. Same as lce_forward /
+ * lce_forward_backward / lce_backward / lce_cross_entropy_from_logits with
+ * two more inputs:
+ *  - class_weight: NULL (no class weights) or a device fp32 [C] (or [V])
+ *    array (the page's `weight` argument of cross entropy). A valid row n
+ *    then has loss weight c_n = class_weight[target_n]:
+ *    loss_n = c_n (lse_n - z[n, target_n]), and the gradients carry c_n in
+ *    w_n (linear_cross_entropy.py, neg_weight_target: the per-row weight is
+ *    the class weight of the target, divided by their sum for mean).
+ *  - denominator: NULL, or a device fp32 scalar d that replaces the mean's
+ *    denominator (otherwise the number of valid rows, or the sum of c_n over
+ *    them with class weights; the page's d). Only reduction mean reads it;
+ *    d == 0 gives NaN as usual. It is what a data-parallel shard of one
+ *    batch passes: with d the denominator of the WHOLE batch (the sum over
+ *    the shards of lce_mean_denominator), each shard's loss and gradients
+ *    are its exact share, so summing the shards' loss, dW and db (dX rows
+ *    are disjoint) gives the whole batch's mean loss and gradients.
  */
 LCE_API int lce_forward_ex(const void* X, const void* W, const void* b, const int64_t* target,
-                           const float* class_weight, int64_t N, int64_t D, int64_t C, int dtype,
-                           int acc_dtype, int reduction, int64_t ignore_index, float* loss_out,
-                           float* lse_out, void* workspace, size_t ws_bytes, void* stream);
+                           const float* class_weight, const float* denominator, int64_t N, int64_t D,
+                           int64_t C, int dtype, int acc_dtype, int reduction, int64_t ignore_index,
+                           float* loss_out, float* lse_out, void* workspace, size_t ws_bytes,
+                           void* stream);
 LCE_API int lce_forward_backward_ex(const void* X, const void* W, const void* b, const int64_t* target,
-                                    const float* class_weight, int64_t N, int64_t D, int64_t C,
-                                    int dtype, int acc_dtype, int reduction, int64_t ignore_index,
-                                    const float* grad_out, float* loss_out, void* dX, void* dW, void* db,
-                                    int grad_dtype, void* workspace, size_t ws_bytes, void* stream);
+                                    const float* class_weight, const float* denominator, int64_t N,
+                                    int64_t D, int64_t C, int dtype, int acc_dtype, int reduction,
+                                    int64_t ignore_index, const float* grad_out, float* loss_out,
+                                    void* dX, void* dW, void* db, int grad_dtype, void* workspace,
+                                    size_t ws_bytes, void* stream);
+LCE_API int lce_backward_ex(const void* X, const void* W, const void* b, const int64_t* target,
+                            const float* class_weight, const float* denominator, const float* lse,
+                            int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype, int reduction,
+                            int64_t ignore_index, const float* grad_out, void* dX, void* dW, void* db,
+                            int grad_dtype, void* workspace, size_t ws_bytes, void* stream);
 LCE_API int lce_cross_entropy_from_logits_ex(void* logits_inout, const int64_t* target,
-                                             const float* class_weight, int64_t N, int64_t V, int dtype,
-                                             int reduction, int64_t ignore_index, const float* grad_out,
+                                             const float* class_weight, const float* denominator,
+                                             int64_t N, int64_t V, int dtype, int reduction,
+                                             int64_t ignore_index, const float* grad_out,
                                              float* loss_out, void* workspace, size_t ws_bytes,
                                              void* stream);
+
+/*
+ * The mean's denominator of these rows, into the device fp32 scalar
+ * denominator_out: the number of rows whose target is neither ignore_index
+ * nor out of [0, C), or the sum of class_weight[target] over them when
+ * class_weight (device fp32 [C]) is given (linear_cross_entropy.py,
+ * neg_weight_target's d). A data-parallel shard sums this over the shards
+ * (an all-reduce) and passes the total as `denominator` above. workspace:
+ * device, 16-byte aligned, at least 256 bytes. Targets out of range set the
+ * device status (lce_read_device_status on this workspace).
+ */
+LCE_API int lce_mean_denominator(const int64_t* target, const float* class_weight, int64_t N,
+                                 int64_t C, int64_t ignore_index, float* denominator_out,
+                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Gradients times a device scalar, in place: dX[:n_dx], dW[:n_dw] and

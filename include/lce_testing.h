@@ -47,18 +47,21 @@
  *   [slab_off[k], slab_off[k + 1]). slab_off is a host array of 5; returns
  *   the number of slabs (at most 4), or -1 on a NULL array or rows < 0.
  * lce_test_plan: the workspace plan a loss call with these arguments makes
- *   for a workspace of ws_bytes (the largest batch chunk that fits, as the
- *   calls choose it). Writes LCE_TEST_PLAN_FIELDS int64 values to the host
- *   array out: chunk rows, chunk count, total bytes, padded class count,
- *   (max, sum-exp) segments per row, then the byte offsets of the regions
- *   in workspace order: counters, row losses, target logits, target
- *   columns, target gradients, (max, sum-exp) pairs, the [chunk, C_pad]
- *   P~ / G buffer, fp32 dW accumulator, db accumulator, fp16 row weights,
- *   fp16 weight sum, fp16 scaled X, then the TF32 parts W hi, W lo, W^T hi,
- *   W^T lo, X hi, X lo, X^T hi, X^T lo, G lo, G^T hi, G^T lo. A region a
- *   call does not use has the next region's offset (zero length). Returns
- *   LCE_TEST_PLAN_FIELDS, 0 when no chunk fits ws_bytes, -1 on invalid
- *   arguments.
+ *   for a workspace of ws_bytes (op LCE_OP_FORWARD, LCE_OP_FORWARD_BACKWARD
+ *   or LCE_OP_BACKWARD; the fastest plan that fits, as the calls choose it).
+ *   Writes LCE_TEST_PLAN_FIELDS int64 values to the host array out: chunk
+ *   rows, chunk count, total bytes, padded class count, (max, sum-exp)
+ *   segments per row, then the byte offsets of the regions in workspace
+ *   order: counters, row losses, target logits, target columns, target
+ *   gradients, (max, sum-exp) pairs, the [chunk rows, Cb] P~ / G buffer,
+ *   fp32 dW accumulator, db accumulator, fp16 row weights, fp16 weight sum,
+ *   fp16 scaled X, rows' lse and G weights of recomputed classes, fp32 dX
+ *   accumulator, then the TF32 parts W hi, W lo, W^T hi, W^T lo, X hi,
+ *   X lo, X^T hi, X^T lo, G lo, G^T hi, G^T lo; then Cb (buffer columns),
+ *   Cs (classes whose G the forward sweep stores) and the number of class
+ *   chunks recomputed after it. A region a call does not use has the next
+ *   region's offset (zero length). Returns LCE_TEST_PLAN_FIELDS, 0 when no
+ *   plan fits ws_bytes, -1 on invalid arguments.
  */
 #ifndef LCE_TESTING_H_
 #define LCE_TESTING_H_
@@ -89,7 +92,7 @@ LCE_API int lce_test_gemm_bf16_unmet_dependency(const void* A, const void* B, fl
                                         int64_t N, int64_t K, int* counters, int* dev_status,
                                         void* stream);
 
-#define LCE_TEST_PLAN_FIELDS 28
+#define LCE_TEST_PLAN_FIELDS 34
 
 LCE_API int lce_test_row_slabs(int64_t rows, int64_t* slab_off);
 

@@ -12,6 +12,8 @@ Functions (same names as the C ABI):
   lce_forward(X, W, b, target, reduction="mean", ignore_index=-100, ...)
   lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=-100,
                        grad_out=None, ...)
+  lce_backward(X, W, b, target, lse, reduction="mean", ...)
+  lce_workspace_size_for_buffer(op, N, D, C, dtype, reduction, grad_dtype, buffer_bytes)
   lce_cross_entropy_from_logits(logits, target, reduction="mean",
                                 ignore_index=-100, grad_out=None, ...)
   lce_status_string(code), lce_read_device_status(workspace)
@@ -30,8 +32,9 @@ LIB_PATH = os.path.join(_PKG, "liblce.so")
 
 LCE_F32, LCE_BF16, LCE_F16 = 0, 1, 2
 LCE_RED_NONE, LCE_RED_SUM, LCE_RED_MEAN = 0, 1, 2
-LCE_OP_FORWARD, LCE_OP_FORWARD_BACKWARD, LCE_OP_CE_FROM_LOGITS = 0, 1, 2
+LCE_OP_FORWARD, LCE_OP_FORWARD_BACKWARD, LCE_OP_CE_FROM_LOGITS, LCE_OP_BACKWARD = 0, 1, 2, 3
 LCE_NOALLOC_MAX_ROWS = 1 << 20
+LCE_ERR_WORKSPACE = 6
 STATUS = {
     0: "LCE_OK", 1: "LCE_ERR_NULL", 2: "LCE_ERR_SHAPE", 3: "LCE_ERR_DTYPE", 4: "LCE_ERR_REDUCTION",
     5: "LCE_ERR_GRAD_OUT", 6: "LCE_ERR_WORKSPACE", 7: "LCE_ERR_CUDA", 8: "LCE_ERR_TARGET_RANGE",
@@ -48,6 +51,13 @@ c_void_p, c_int, c_int64, c_size_t, c_double = (ctypes.c_void_p, ctypes.c_int, c
 
 _SIGNATURES = {
     "lce_workspace_size": (c_size_t, [c_int, c_int64, c_int64, c_int64, c_int, c_int, c_int, c_int64]),
+    "lce_workspace_size_for_buffer": (c_size_t, [c_int, c_int64, c_int64, c_int64, c_int, c_int, c_int, c_size_t]),
+    "lce_backward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int,
+                             c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
+                             c_size_t, c_void_p]),
+    "lce_backward_ex": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64,
+                                c_int64, c_int64, c_int, c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_int, c_void_p, c_size_t, c_void_p]),
     "lce_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int,
                             c_int, c_int64, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "lce_forward_backward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int,
@@ -55,13 +65,15 @@ _SIGNATURES = {
                                      c_int, c_void_p, c_size_t, c_void_p]),
     "lce_cross_entropy_from_logits": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_int64,
                                               c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
-    "lce_forward_ex": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int,
-                               c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
-    "lce_forward_backward_ex": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64,
-                                        c_int, c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
+    "lce_forward_ex": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64,
+                               c_int, c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "lce_forward_backward_ex": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64,
+                                        c_int64, c_int, c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
                                         c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
-    "lce_cross_entropy_from_logits_ex": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int, c_int,
-                                                 c_int64, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "lce_cross_entropy_from_logits_ex": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int,
+                                                 c_int, c_int64, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "lce_mean_denominator": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p, c_size_t,
+                                     c_void_p]),
     "lce_cross_entropy_from_logits_noalloc": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int,
                                                       c_int64, c_void_p, c_void_p, c_void_p, c_void_p]),
     "lce_scale_gradients": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64, c_int, c_void_p,
@@ -162,6 +174,28 @@ def _class_weight(cw, C, device):
     return cw
 
 
+def _denom(d, device):
+    """A given mean denominator as a device fp32 scalar tensor (or None)."""
+    if d is None:
+        return None
+    return torch.as_tensor(d, dtype=torch.float32, device=device).reshape(-1)[:1].contiguous()
+
+
+def lce_mean_denominator(target, C, ignore_index=-100, class_weight=None, stream=None):
+    """Device fp32 [1]: the mean's denominator of these rows (valid-row count,
+    or the sum of their class weights). Data-parallel shards sum it."""
+    lib = load_library()
+    if target.dtype != torch.int64 or not target.is_contiguous():
+        raise TypeError("target must be a contiguous int64 tensor")
+    dev = target.device
+    out = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    cw = _class_weight(class_weight, C, dev)
+    _check(lib.lce_mean_denominator(_ptr(target), _ptr(cw), target.numel(), C, ignore_index, _ptr(out), _ptr(ws), 256,
+                                    _stream(stream)), "lce_mean_denominator")
+    return out
+
+
 def _check_inputs(X, W, b, target):
     if X.dim() != 2 or W.dim() != 2 or X.shape[1] != W.shape[1]:
         raise ValueError("expected X [N, D] and W [C, D]")
@@ -177,9 +211,11 @@ def _check_inputs(X, W, b, target):
 
 
 def lce_forward(X, W, b, target, reduction="mean", ignore_index=-100, want_lse=False,
-                workspace=None, stream=None, class_weight=None):
+                workspace=None, stream=None, class_weight=None, denominator=None):
     """Loss (fp32 scalar, or [N] for 'none') and optionally lse [N].
-    class_weight: optional per-class weights [C] (fp32)."""
+    class_weight: optional per-class weights [C] (fp32). denominator:
+    optional device fp32 scalar replacing the mean's denominator (a
+    data-parallel shard passes the whole batch's; see lce.h)."""
     lib = load_library()
     _check_inputs(X, W, b, target)
     N, D = X.shape
@@ -192,20 +228,37 @@ def lce_forward(X, W, b, target, reduction="mean", ignore_index=-100, want_lse=F
     nbytes = lib.lce_workspace_size(LCE_OP_FORWARD, N, D, C, dt, red, LCE_F32, 0)
     ws = _workspace(nbytes, dev, workspace)
     cw = _class_weight(class_weight, C, dev)
-    _check(lib.lce_forward_ex(_ptr(X), _ptr(W), _ptr(b), _ptr(target), _ptr(cw), N, D, C, dt, LCE_F32, red,
+    _check(lib.lce_forward_ex(_ptr(X), _ptr(W), _ptr(b), _ptr(target), _ptr(cw), _ptr(_denom(denominator, dev)), N,
+                              D, C, dt, LCE_F32, red,
                               ignore_index, _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)),
            "lce_forward")
     loss = loss if red == LCE_RED_NONE else loss[0]
     return (loss, lse) if want_lse else loss
 
 
+def lce_workspace_size_for_buffer(op: int, N: int, D: int, C: int, dtype: int, reduction: int, grad_dtype: int,
+                                  buffer_bytes: int) -> int:
+    lib = load_library()
+    return int(lib.lce_workspace_size_for_buffer(op, N, D, C, dtype, reduction, grad_dtype, buffer_bytes))
+
+
+def _grad_ws_bytes(lib, op, N, D, C, dt, red, gdt, chunk_rows, buffer_bytes):
+    if buffer_bytes is not None:
+        if chunk_rows:
+            raise ValueError("give chunk_rows or buffer_bytes, not both")
+        return lib.lce_workspace_size_for_buffer(op, N, D, C, dt, red, gdt, buffer_bytes)
+    return lib.lce_workspace_size(op, N, D, C, dt, red, gdt, chunk_rows)
+
+
 def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=-100, grad_out=None,
                          want_dx=True, want_dw=True, want_db=True, grad_dtype=None, chunk_rows=0,
-                         workspace=None, stream=None, class_weight=None):
+                         workspace=None, stream=None, class_weight=None, buffer_bytes=None, denominator=None):
     """Loss and (dX, dW, db); a gradient not wanted (or db without bias) is None.
 
     grad_out: None (= 1) or a scalar / 1-element tensor for sum and mean; a
-    float32 [N] tensor for 'none'.
+    float32 [N] tensor for 'none'. The workspace (unless given) is sized for
+    the default plan, for batch chunks of chunk_rows rows, or for a gradient
+    buffer of at most buffer_bytes (see lce_workspace_size_for_buffer).
     """
     lib = load_library()
     _check_inputs(X, W, b, target)
@@ -225,17 +278,51 @@ def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=-100, g
     dX = torch.empty(N, D, dtype=gtype, device=dev) if want_dx else None
     dW = torch.empty(C, D, dtype=gtype, device=dev) if want_dw else None
     db = torch.empty(C, dtype=gtype, device=dev) if (want_db and b is not None) else None
-    nbytes = lib.lce_workspace_size(LCE_OP_FORWARD_BACKWARD, N, D, C, dt, red, gdt, chunk_rows)
+    nbytes = _grad_ws_bytes(lib, LCE_OP_FORWARD_BACKWARD, N, D, C, dt, red, gdt, chunk_rows, buffer_bytes)
     ws = _workspace(nbytes, dev, workspace)
     cw = _class_weight(class_weight, C, dev)
-    _check(lib.lce_forward_backward_ex(_ptr(X), _ptr(W), _ptr(b), _ptr(target), _ptr(cw), N, D, C, dt, LCE_F32,
+    _check(lib.lce_forward_backward_ex(_ptr(X), _ptr(W), _ptr(b), _ptr(target), _ptr(cw),
+                                       _ptr(_denom(denominator, dev)), N, D, C, dt, LCE_F32,
                                        red, ignore_index, _ptr(g), _ptr(loss), _ptr(dX), _ptr(dW), _ptr(db), gdt,
                                        _ptr(ws), ws.numel(), _stream(stream)), "lce_forward_backward")
     return (loss if red == LCE_RED_NONE else loss[0]), dX, dW, db
 
 
+def lce_backward(X, W, b, target, lse, reduction="mean", ignore_index=-100, grad_out=None,
+                 want_dx=True, want_dw=True, want_db=True, grad_dtype=None, chunk_rows=0,
+                 workspace=None, stream=None, class_weight=None, buffer_bytes=None, denominator=None):
+    """(dX, dW, db) from the row lse [N] (float32) of lce_forward(..., want_lse=True)."""
+    lib = load_library()
+    _check_inputs(X, W, b, target)
+    N, D = X.shape
+    C = W.shape[0]
+    red = _REDUCTION[reduction]
+    dt = _dtype_code(X)
+    gdt = dt if grad_dtype is None else _DTYPE[grad_dtype]
+    gtype = _TORCH_DTYPE[gdt]
+    dev = X.device
+    if lse.dtype != torch.float32 or lse.shape != (N,) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [N] tensor")
+    g = None
+    if grad_out is not None:
+        g = torch.as_tensor(grad_out, dtype=torch.float32, device=dev).reshape(-1).contiguous()
+        if red != LCE_RED_NONE and g.numel() != 1:
+            raise ValueError("grad_out must be a scalar for sum / mean")
+    dX = torch.empty(N, D, dtype=gtype, device=dev) if want_dx else None
+    dW = torch.empty(C, D, dtype=gtype, device=dev) if want_dw else None
+    db = torch.empty(C, dtype=gtype, device=dev) if (want_db and b is not None) else None
+    nbytes = _grad_ws_bytes(lib, LCE_OP_BACKWARD, N, D, C, dt, red, gdt, chunk_rows, buffer_bytes)
+    ws = _workspace(nbytes, dev, workspace)
+    cw = _class_weight(class_weight, C, dev)
+    _check(lib.lce_backward_ex(_ptr(X), _ptr(W), _ptr(b), _ptr(target), _ptr(cw), _ptr(_denom(denominator, dev)),
+                               _ptr(lse), N, D, C, dt, LCE_F32,
+                               red, ignore_index, _ptr(g), _ptr(dX), _ptr(dW), _ptr(db), gdt, _ptr(ws), ws.numel(),
+                               _stream(stream)), "lce_backward")
+    return dX, dW, db
+
+
 def lce_cross_entropy_from_logits(logits, target, reduction="mean", ignore_index=-100, grad_out=None,
-                                  workspace=None, stream=None, class_weight=None):
+                                  workspace=None, stream=None, class_weight=None, denominator=None):
     """Loss; the gradient overwrites ``logits`` in place."""
     lib = load_library()
     if logits.dim() != 2 or not logits.is_contiguous():
@@ -253,7 +340,8 @@ def lce_cross_entropy_from_logits(logits, target, reduction="mean", ignore_index
     nbytes = lib.lce_workspace_size(LCE_OP_CE_FROM_LOGITS, N, 1, V, dt, red, dt, 0)
     ws = _workspace(nbytes, dev, workspace)
     cw = _class_weight(class_weight, V, dev)
-    _check(lib.lce_cross_entropy_from_logits_ex(_ptr(logits), _ptr(target), _ptr(cw), N, V, dt, red, ignore_index,
+    _check(lib.lce_cross_entropy_from_logits_ex(_ptr(logits), _ptr(target), _ptr(cw), _ptr(_denom(denominator, dev)),
+                                                N, V, dt, red, ignore_index,
                                                 _ptr(g), _ptr(loss), _ptr(ws), ws.numel(), _stream(stream)),
            "lce_cross_entropy_from_logits")
     return loss if red == LCE_RED_NONE else loss[0]
@@ -274,6 +362,25 @@ def lce_scale_gradients(dX, dW, db, grad_out, stream=None):
     n = lambda t: 0 if t is None else t.numel()
     _check(lib.lce_scale_gradients(_ptr(dX), n(dX), _ptr(dW), n(dW), _ptr(db), n(db), gdt, _ptr(g), _stream(stream)),
            "lce_scale_gradients")
+
+
+def plan_of(op: int, N: int, D: int, C: int, dtype: int, grad_dtype: int, ws_bytes: int, want_dx=True, want_dw=True,
+            want_db=True) -> dict:
+    """The workspace plan a call makes for ws_bytes (host-only; see
+    lce_test_plan in lce_testing.h): rows per batch chunk Bc, chunk count,
+    total bytes, gradient-buffer columns Cb, classes stored by the forward
+    sweep Cs and recomputed class chunks nvc."""
+    lib = load_library()
+    fn = lib.lce_test_plan
+    fn.argtypes = [c_int, c_int64, c_int64, c_int64, c_int, c_int, c_int, c_int, c_int, c_size_t,
+                   ctypes.POINTER(c_int64), c_int]
+    fn.restype = c_int
+    out = (c_int64 * 34)()
+    r = fn(op, N, D, C, dtype, grad_dtype, int(want_dx), int(want_dw), int(want_db), ws_bytes, out, 34)
+    if r != 34:
+        raise LceError(LCE_ERR_WORKSPACE if r == 0 else 1, "plan_of")
+    v = list(out)
+    return {"Bc": v[0], "nchunks": v[1], "total": v[2], "C_pad": v[3], "Cb": v[31], "Cs": v[32], "nvc": v[33]}
 
 
 def lce_read_device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -11,11 +11,11 @@ split of the batch-chunked op in PyTorch's ``linear_cross_entropy.py``:
   ops of the page precompute the gradients); the backward multiplies them
   by the upstream gradient in place, in the library (a kernel that reads the
   upstream gradient on the device and does nothing when it is 1).
-* reduction "none": the forward computes only the per-row losses and keeps
-  the inputs; the backward recomputes the logits tile by tile and forms the
-  vector-Jacobian product with the per-row upstream gradient in one call
-  (the page's reduction="none" backward, which cannot keep the per-sample
-  softmax).
+* reduction "none": the forward computes the per-row losses and lse and
+  keeps the inputs; the backward recomputes the logits tile by tile from
+  them and forms the vector-Jacobian product with the per-row upstream
+  gradient in one call (the page's reduction="none" backward, which cannot
+  keep the per-sample softmax).
 
 Leading dimensions of ``input`` are flattened (``input.reshape(-1, D)``), as
 in PyTorch commit ddfa80bd "Fix NJT linear_backward() memory usage".
@@ -26,7 +26,7 @@ from __future__ import annotations
 
 import torch
 
-from . import lce_forward, lce_forward_backward, lce_scale_gradients
+from . import lce_backward, lce_forward, lce_forward_backward, lce_scale_gradients
 
 
 class _ScalarReduction(torch.autograd.Function):
@@ -64,20 +64,20 @@ class _ScalarReduction(torch.autograd.Function):
 class _NoReduction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, X, W, b, target, ignore_index, class_weight):
-        loss = lce_forward(X, W, b, target, "none", ignore_index, class_weight=class_weight)
-        ctx.save_for_backward(X, W, b, target)
+        loss, lse = lce_forward(X, W, b, target, "none", ignore_index, want_lse=True, class_weight=class_weight)
+        ctx.save_for_backward(X, W, b, target, lse)
         ctx.ignore_index = ignore_index
         ctx.class_weight = class_weight
         return loss
 
     @staticmethod
     def backward(ctx, grad_loss):
-        X, W, b, target = ctx.saved_tensors
+        X, W, b, target, lse = ctx.saved_tensors
         need = ctx.needs_input_grad
-        _, dX, dW, db = lce_forward_backward(X, W, b, target, "none", ctx.ignore_index,
-                                             grad_loss.to(torch.float32).contiguous(),
-                                             want_dx=need[0], want_dw=need[1],
-                                             want_db=need[2] and b is not None, class_weight=ctx.class_weight)
+        dX, dW, db = lce_backward(X, W, b, target, lse, "none", ctx.ignore_index,
+                                  grad_loss.to(torch.float32).reshape(-1).contiguous(),
+                                  want_dx=need[0], want_dw=need[1], want_db=need[2] and b is not None,
+                                  class_weight=ctx.class_weight)
         return dX, dW, db, None, None, None
 
 

@@ -99,7 +99,8 @@ const char* kNames[K_NUM_IDS] = {
     "prep",          "gemm_logits_tc", "gemm_dx_tc",  "gemm_dw_tc",      "gemm_logits_simt",
     "gemm_dx_simt",  "gemm_dw_simt",   "lse_combine", "grad_logits",     "loss_finalize",
     "db_finalize",   "ce_resident",    "ce_stream",   "gemm_test",       "row_scale",
-    "gemm_logits_3xtf32", "gemm_dx_3xtf32", "gemm_dw_3xtf32", "split_tf32", "scale_grads"};
+    "gemm_logits_3xtf32", "gemm_dx_3xtf32", "gemm_dw_3xtf32", "split_tf32", "scale_grads",
+    "gemm_recompute_tc", "backward_rows"};
 }  // namespace
 
 const char* kernel_id_name(int id) { return (id >= 0 && id < K_NUM_IDS) ? kNames[id] : "?"; }
@@ -122,7 +123,10 @@ void prof_after(int id, cudaStream_t s) {
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int64_t kDefaultChunkBytes = int64_t(8) << 30;  // chunk buffer budget of the default plan
+// Budget of the default plan for the backward's gradient buffer ([rows,
+// classes] of the input type): 1 GiB. The forward-only plan applies it to
+// its (max, sum-exp) pairs.
+constexpr int64_t kDefaultBufferBytes = int64_t(1) << 30;
 
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -135,16 +139,28 @@ constexpr int kCountersPerChunk = 16;
 struct Plan {
   bool tc;          // tensor-core (bf16 / fp16) path
   bool tf32;        // fp32 inputs on the tensor cores (3xTF32)
+  bool backward;    // a gradient call
+  bool given_lse;   // gradients from a given row lse (tensor-core path): no forward sweep
   int segw;         // columns per (max, sum-exp) segment
   int nseg;
-  int64_t C_pad;    // chunk buffer row pitch (elements)
-  int64_t Bc;       // rows per chunk
+  int64_t C_pad;    // classes padded to the tile width
+  int64_t Bc;       // rows per batch chunk
   int64_t nchunks;
-  bool dw_acc;      // fp32 dW accumulator in the workspace
+  // Classes of the backward. The gradient buffer has Cb columns. The forward
+  // sweep stores P~ for classes [0, Cs) in it; classes [Cs, C) are
+  // recomputed afterwards in nvc chunks of up to Cb classes, each formed
+  // into the same buffer (tensor-core path only). Without recomputation
+  // Cs = Cb = C_pad and nvc = 0; with a given lse, Cs = 0.
+  int64_t Cb, Cs, nvc;
+  bool dw_acc;      // fp32 dW accumulator in the workspace (bf16 / fp16 dW over several batch chunks)
+  bool dx_acc;      // fp32 dX accumulator (16-bit dX over several class chunks)
   size_t off_cnt, off_loss, off_zt, off_tcol, off_gt, off_partial, off_L, off_dw, off_db, total;
   // fp16 backward: per-row weights [Bc], their max |w| (one float), and the
   // rows of X scaled by w / max|w| for dW ([Bc, D] fp16)
   size_t off_wrow, off_wbar, off_xs;
+  // recomputed classes: the rows' lse and G weight [Bc], the fp32 dX
+  // accumulator [Bc, D]
+  size_t off_lse, off_wv, off_dx;
   // 3xTF32: TF32 hi / lo parts of W [C, ldD], W^T [D, ldC] (dX), the chunk's
   // X [Bc, ldD] and X^T [D, ldB] (dW), the lo part of G [Bc, C_pad] (its hi
   // part replaces G in the chunk buffer) and G^T [C, ldB] (dW)
@@ -152,25 +168,55 @@ struct Plan {
   size_t off_wh, off_wl, off_wth, off_wtl, off_xh, off_xl, off_xth, off_xtl, off_gl, off_gth, off_gtl;
 };
 
-// Bytes for chunk size Bc. backward: chunk buffer and gradient scratch;
-// need_dw_acc_if_multi: a bf16 dW needs an fp32 accumulator once Bc < N.
-bool make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, bool want_dx, bool want_dw,
-               bool want_db, int64_t Bc, Plan* p) {
-  const bool backward = op == LCE_OP_FORWARD_BACKWARD;
+inline bool is_backward_op(int op) { return op == LCE_OP_FORWARD_BACKWARD || op == LCE_OP_BACKWARD; }
+
+// Fewest classes a recomputed chunk of the tensor-core path takes: D
+// rounded up to the tile width (so the fp32 dX accumulator's traffic per
+// chunk, 8 bytes per row and feature, stays below the chunk's own G
+// traffic), at least one tile, at most all classes.
+int64_t min_class_chunk(int64_t D, int64_t C_pad) {
+  const int64_t c = std::max<int64_t>(256, ceil_div(D, 256) * 256);
+  return std::min(c, C_pad);
+}
+
+// The plan for batch chunks of Bc rows and a gradient buffer of Cb columns
+// (rounded down to the tile width and clamped to [256, C_pad] on the
+// tensor-core backward; C_pad elsewhere).
+void make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, bool want_dx, bool want_dw,
+               bool want_db, int64_t Bc, int64_t Cb, Plan* p) {
+  const bool backward = is_backward_op(op);
+  p->backward = backward;
   p->tc = dtype != LCE_F32;
   p->tf32 = dtype == LCE_F32 && f32_tensor_default();
+  // fp32 inputs have no recomputing GEMM: a given lse is not used there and
+  // the call runs its own forward sweep
+  p->given_lse = op == LCE_OP_BACKWARD && p->tc;
   p->segw = (p->tc || p->tf32) ? 256 : 64;
   p->nseg = static_cast<int>(ceil_div(C, p->segw));
   p->C_pad = (p->tc || p->tf32) ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
   if (N == 0) Bc = 0;
   p->Bc = Bc;
   p->nchunks = Bc > 0 ? ceil_div(N, Bc) : 0;
+  const bool vocab = backward && p->tc;
+  if (vocab) {
+    Cb = Cb / 256 * 256;
+    Cb = std::max<int64_t>(256, std::min(Cb, p->C_pad));
+  } else {
+    Cb = p->C_pad;
+  }
+  p->Cb = Cb;
+  p->Cs = p->given_lse ? 0 : Cb;
+  p->nvc = (vocab && C > p->Cs) ? ceil_div(C - p->Cs, Cb) : 0;
+  const int64_t dx_parts = (p->Cs > 0 ? 1 : 0) + p->nvc;
   p->dw_acc = backward && want_dw && p->nchunks > 1 && grad_dtype != LCE_F32;
+  p->dx_acc = backward && want_dx && dx_parts > 1 && grad_dtype != LCE_F32;
+  const bool recompute = p->nvc > 0;
+  const bool sweep = !p->given_lse;  // forward sweep with (max, sum-exp) pairs
   size_t off = align_up(sizeof(WsHeader));
   p->off_cnt = off;  // zeroed with the header at the start of every call
   off = align_up(off + static_cast<size_t>(p->nchunks) * kCountersPerChunk * sizeof(int));
   p->off_loss = off;
-  off = align_up(off + static_cast<size_t>(N) * 4);
+  if (sweep) off = align_up(off + static_cast<size_t>(N) * 4);
   p->off_zt = off;
   off = align_up(off + static_cast<size_t>(Bc) * 4);
   p->off_tcol = off;
@@ -178,9 +224,9 @@ bool make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtyp
   p->off_gt = off;
   off = align_up(off + static_cast<size_t>(Bc) * 4);
   p->off_partial = off;
-  off = align_up(off + static_cast<size_t>(p->nseg) * static_cast<size_t>(Bc) * 8);
+  if (sweep) off = align_up(off + static_cast<size_t>(p->nseg) * static_cast<size_t>(Bc) * 8);
   p->off_L = off;
-  if (backward) off = align_up(off + static_cast<size_t>(Bc) * static_cast<size_t>(p->C_pad) * esize(dtype));
+  if (backward) off = align_up(off + static_cast<size_t>(Bc) * static_cast<size_t>(Cb) * esize(dtype));
   p->off_dw = off;
   if (p->dw_acc) off = align_up(off + static_cast<size_t>(C) * static_cast<size_t>(D) * 4);
   p->off_db = off;
@@ -192,6 +238,12 @@ bool make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtyp
   if (f16bw) off = align_up(off + 4);
   p->off_xs = off;
   if (f16bw && want_dw) off = align_up(off + static_cast<size_t>(Bc) * static_cast<size_t>(D) * 2);
+  p->off_lse = off;
+  if (recompute) off = align_up(off + static_cast<size_t>(Bc) * 4);
+  p->off_wv = off;
+  if (recompute) off = align_up(off + static_cast<size_t>(Bc) * 4);
+  p->off_dx = off;
+  if (p->dx_acc) off = align_up(off + static_cast<size_t>(Bc) * static_cast<size_t>(D) * 4);
   p->ldD = ceil_div(D, 4) * 4;
   p->ldC = ceil_div(C, 4) * 4;
   p->ldB = ceil_div(Bc, 4) * 4;
@@ -221,38 +273,81 @@ bool make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtyp
   p->off_gth = take(tx_dw, gt_bytes);
   p->off_gtl = take(tx_dw, gt_bytes);
   p->total = off;
-  return true;
 }
 
-int64_t default_chunk(int op, int64_t N, int64_t D, int64_t C, int dtype) {
-  if (N == 0) return 0;
+// Rows per batch chunk and buffer columns of the plan whose gradient buffer
+// fits `budget` bytes: on the tensor-core backward all rows and as many
+// classes as fit (every class if they all do; at least min_class_chunk,
+// else fewer rows); elsewhere all rows if their per-row regions fit, else
+// the largest 128 * 2^k rows that do.
+void budget_dims(int op, int64_t N, int64_t D, int64_t C, int dtype, int64_t budget, int64_t* Bc, int64_t* Cb) {
   const bool tf32 = dtype == LCE_F32 && f32_tensor_default();
-  const bool bw = op == LCE_OP_FORWARD_BACKWARD;
-  const int64_t C_pad = (dtype != LCE_F32 || tf32) ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
+  const bool tc = dtype != LCE_F32;
+  const bool bw = is_backward_op(op);
+  const int64_t C_pad = (tc || tf32) ? ceil_div(C, 256) * 256 : ceil_div(C, 128) * 128;
+  *Cb = C_pad;
+  if (N == 0) {
+    *Bc = 0;
+    return;
+  }
+  if (bw && tc) {
+    const int64_t esz = esize(dtype);
+    const int64_t cmin = min_class_chunk(D, C_pad);
+    if (N * C_pad * esz <= budget) {
+      *Bc = N;
+    } else if (N * cmin * esz <= budget) {
+      *Bc = N;
+      *Cb = std::min(C_pad, budget / (N * esz) / 256 * 256);
+    } else {
+      int64_t bc = std::max<int64_t>(256, budget / (cmin * esz) / 256 * 256);
+      *Bc = std::min(bc, N);
+      *Cb = std::max(cmin, std::min(C_pad, budget / (*Bc * esz) / 256 * 256));
+    }
+    return;
+  }
   int64_t per_row = (bw ? C_pad * esize(dtype) : 0) + ceil_div(C, 64) * 8;
   if (tf32) per_row += 8 * D + (bw ? 4 * C_pad + 8 * C + 8 * D : 0);  // TF32 parts of X, G, X^T, G^T
-  if (N * per_row <= kDefaultChunkBytes) return N;
+  if (N * per_row <= budget) {
+    *Bc = N;
+    return;
+  }
   int64_t bc = 128;
-  while (bc * 2 * per_row <= kDefaultChunkBytes && bc * 2 < N) bc *= 2;
-  return bc;
+  while (bc * 2 * per_row <= budget && bc * 2 < N) bc *= 2;
+  *Bc = bc;
 }
 
-// Largest chunk (N itself, else 128 * 2^k < N) whose plan fits ws_bytes.
+// The fastest plan that fits ws_bytes: all rows and all classes; else all
+// rows and the widest class chunk (>= min_class_chunk) that fits; else the
+// same for the largest batch chunk of 128 * 2^k rows that fits.
 bool choose_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, bool want_dx, bool want_dw,
                  bool want_db, size_t ws_bytes, Plan* p) {
-  if (N == 0) {
-    make_plan(op, 0, D, C, dtype, grad_dtype, want_dx, want_dw, want_db, 0, p);
+  auto fits = [&](int64_t bc, int64_t cb) {
+    make_plan(op, N, D, C, dtype, grad_dtype, want_dx, want_dw, want_db, bc, cb, p);
     return p->total <= ws_bytes;
-  }
+  };
+  if (N == 0) return fits(0, 0);
   std::vector<int64_t> cands;
   cands.push_back(N);
   int64_t bc = 128;
   while (bc * 2 < N) bc *= 2;
   for (; bc >= 128; bc /= 2)
     if (bc < N) cands.push_back(bc);
-  for (int64_t c : cands) {
-    make_plan(op, N, D, C, dtype, grad_dtype, want_dx, want_dw, want_db, c, p);
-    if (p->total <= ws_bytes) return true;
+  make_plan(op, N, D, C, dtype, grad_dtype, want_dx, want_dw, want_db, N, 0, p);
+  const bool vocab = p->backward && p->tc;
+  const int64_t C_pad = p->C_pad;
+  const int64_t cmin = min_class_chunk(D, C_pad);
+  for (int64_t rows : cands) {
+    if (fits(rows, C_pad)) return true;
+    if (!vocab || cmin >= C_pad || !fits(rows, cmin)) continue;
+    int64_t lo = cmin / 256, hi = C_pad / 256;  // fits(lo * 256), !fits(hi * 256)
+    while (hi - lo > 1) {
+      const int64_t mid = (lo + hi) / 2;
+      if (fits(rows, mid * 256))
+        lo = mid;
+      else
+        hi = mid;
+    }
+    return fits(rows, lo * 256);
   }
   return false;
 }
@@ -317,17 +412,23 @@ int check_common(int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype, int 
     if (_e != cudaSuccess) return LCE_ERR_CUDA; \
   } while (0)
 
-// The shared body of lce_forward and lce_forward_backward.
-int run_lce(bool backward, const void* X, const void* W, const void* b, const int64_t* target,
-            const float* class_weight, int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype, int reduction,
+// The shared body of lce_forward, lce_forward_backward and lce_backward
+// (op: LCE_OP_FORWARD, LCE_OP_FORWARD_BACKWARD or LCE_OP_BACKWARD; lse_in
+// is the given row lse of LCE_OP_BACKWARD).
+int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* target, const float* class_weight,
+            const float* denominator, int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype, int reduction,
             int64_t ignore_index,
-            const float* grad_out, float* loss_out, float* lse_out, void* dX, void* dW, void* db, int grad_dtype,
-            void* workspace, size_t ws_bytes, void* stream) {
+            const float* lse_in, const float* grad_out, float* loss_out, float* lse_out, void* dX, void* dW,
+            void* db, int grad_dtype, void* workspace, size_t ws_bytes, void* stream) {
+  const bool backward = is_backward_op(op);
+  const bool given = op == LCE_OP_BACKWARD;
   int st = check_common(N, D, C, dtype, acc_dtype, reduction);
   if (st != LCE_OK) return st;
   if (backward && grad_dtype != LCE_F32 && grad_dtype != LCE_BF16 && grad_dtype != LCE_F16) return LCE_ERR_DTYPE;
-  if (N > 0 && (X == nullptr || W == nullptr || target == nullptr || loss_out == nullptr)) return LCE_ERR_NULL;
-  if (reduction != LCE_RED_NONE && loss_out == nullptr) return LCE_ERR_NULL;
+  if (N > 0 && (X == nullptr || W == nullptr || target == nullptr)) return LCE_ERR_NULL;
+  if (!given && N > 0 && loss_out == nullptr) return LCE_ERR_NULL;
+  if (!given && reduction != LCE_RED_NONE && loss_out == nullptr) return LCE_ERR_NULL;
+  if (given && N > 0 && lse_in == nullptr) return LCE_ERR_NULL;
   if (backward && reduction == LCE_RED_NONE && N > 0 && grad_out == nullptr) return LCE_ERR_GRAD_OUT;
   if (workspace == nullptr) return LCE_ERR_WORKSPACE;
   if (!aligned16(workspace)) return LCE_ERR_ALIGN;
@@ -340,9 +441,7 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
     if ((want_dx && !aligned16(dX)) || (want_dw && !aligned16(dW))) return LCE_ERR_ALIGN;
   }
   Plan p;
-  if (!choose_plan(backward ? LCE_OP_FORWARD_BACKWARD : LCE_OP_FORWARD, N, D, C, dtype, grad_dtype, want_dx,
-                   want_dw, want_db, ws_bytes, &p))
-    return LCE_ERR_WORKSPACE;
+  if (!choose_plan(op, N, D, C, dtype, grad_dtype, want_dx, want_dw, want_db, ws_bytes, &p)) return LCE_ERR_WORKSPACE;
   if (p.Bc > 2147483647LL) return LCE_ERR_SHAPE;
   st = check_device();
   if (st != LCE_OK) return st;
@@ -358,24 +457,38 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
   void* Lbuf = ws + p.off_L;
   float* dw_acc = reinterpret_cast<float*>(ws + p.off_dw);
   float* db_acc = reinterpret_cast<float*>(ws + p.off_db);
+  float* lse_ws = reinterpret_cast<float*>(ws + p.off_lse);
+  float* wv_ws = reinterpret_cast<float*>(ws + p.off_wv);
+  float* dx_acc = reinterpret_cast<float*>(ws + p.off_dx);
   const bool f16 = dtype == LCE_F16;
   float* wrow = f16 && backward ? reinterpret_cast<float*>(ws + p.off_wrow) : nullptr;
   float* wbar = reinterpret_cast<float*>(ws + p.off_wbar);
   void* Xs = ws + p.off_xs;
   const int gsz = esize(grad_dtype);
+  const int isz = esize(dtype);
+  const bool sweep = !p.given_lse;  // forward sweep (a given lse is only used on the tensor-core path)
+  const bool recompute = p.nvc > 0;
+  // classes whose G comes from the forward sweep's stored P~
+  const int64_t Cs_eff = std::min(p.Cs, C);
+  const int nseg_store = static_cast<int>(std::min<int64_t>(p.nseg, ceil_div(Cs_eff, p.segw)));
 
   LCE_TRY(cudaMemsetAsync(hdr, 0, p.off_cnt + static_cast<size_t>(p.nchunks) * kCountersPerChunk * sizeof(int), s));
   int* counters = reinterpret_cast<int*>(ws + p.off_cnt);
   if (N == 0) {
-    if (reduction != LCE_RED_NONE)
+    if (!given && reduction != LCE_RED_NONE) {
+      LCE_TRY(launch_prep(target, 0, C, ignore_index, class_weight, denominator, hdr, s));
       LCE_TRY(launch_loss_finalize(loss_rows, 0, reduction, hdr, class_weight != nullptr, loss_out, s));
+    }
     if (want_dw) LCE_TRY(cudaMemsetAsync(dW, 0, static_cast<size_t>(C) * D * gsz, s));
     if (want_db) LCE_TRY(cudaMemsetAsync(db, 0, static_cast<size_t>(C) * gsz, s));
     return LCE_OK;
   }
-  LCE_TRY(launch_prep(target, N, C, ignore_index, class_weight, hdr, s));
+  LCE_TRY(launch_prep(target, N, C, ignore_index, class_weight, denominator, hdr, s));
   if (want_db) LCE_TRY(cudaMemsetAsync(db_acc, 0, static_cast<size_t>(C) * 4, s));
-  float* rows_out = reduction == LCE_RED_NONE ? loss_out : loss_rows;
+  // per-row losses: the caller's vector for 'none', else the workspace (a
+  // given-lse call on the fp32 path runs a forward sweep whose losses are
+  // not returned)
+  float* rows_out = (reduction == LCE_RED_NONE && !given) ? loss_out : loss_rows;
 
   RowWeight rw;
   rw.grad_out = grad_out;
@@ -415,11 +528,6 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
   for (int64_t ci = 0; ci < p.nchunks; ++ci) {
     const int64_t row0 = ci * p.Bc;
     const int64_t rows = std::min(p.Bc, N - row0);
-    // ---- logits, row lse / loss, and G, over row slabs of the chunk. On the
-    // CTA-pair path with a backward (>= 1024 rows), the chunk is cut into up
-    // to 4 slabs; the idle warps of slab k's logits GEMM merge the rows of
-    // slab k-1 and form its G, and those of the dX GEMM do the same for the
-    // last slab.
     if (p.tf32) {  // TF32 parts of the chunk's rows of X (and of X^T for dW)
       SplitArgs sa;
       sa.src = static_cast<const float*>(X) + row0 * D;
@@ -434,108 +542,139 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       sa.ldt = p.ldB;
       LCE_TRY(launch_split_tf32(sa, s));
     }
-    const bool slabbed = p.tc && pair && backward && rows >= 1024;
-    int64_t slab_off[5];
-    const int64_t nslab = row_slabs(rows, slabbed, slab_off);
-    GradArgs ga_prev, ga_last;
-    CombineArgs ca_prev, ca_last;  // merges deferred into the next GEMM's idle warps
-    bool have_prev = false, have_last = false;
+    const bool slabbed = sweep && p.tc && pair && backward && rows >= 1024;
+    GradArgs ga_last;
+    CombineArgs ca_last;  // the last slab's merge, deferred into the dX GEMM's idle warps
+    bool have_last = false;
     int64_t last_row0 = 0, last_si = 0;
     int* cnt = counters + ci * kCountersPerChunk;
-    for (int64_t si = 0; si < nslab; ++si) {
-      const int64_t so = slab_off[si];                   // slab offset within the chunk
-      const int64_t sr = slab_off[si + 1] - so;          // rows in the slab
-      EpiLse::Params el;
-      el.bias = b;
-      el.bias_dt = dtype;
-      el.target = target + row0 + so;
-      el.C = C;
-      el.rows = static_cast<int>(sr);
-      el.partial = partial + so;
-      el.partial_ld = p.Bc;
-      el.zt = zt + so;
-      el.ptilde = backward ? static_cast<uint8_t*>(Lbuf) + static_cast<size_t>(so) * p.C_pad * esize(dtype)
-                           : nullptr;
-      el.ld_p = p.C_pad;
-      el.ptilde_dt = dtype;
-      if (p.tc) {
-        const void* Xc = static_cast<const uint16_t*>(X) + (row0 + so) * D;
-        CUtensorMap tmX_k, tmL;
-        if (!encode_tmap_bf16(&tmX_k, Xc, D, sr, D, TC_BM, dtype)) return LCE_ERR_CUDA;
-        const bool tma_out = pair && backward;
-        if (tma_out && !encode_tmap_bf16_store(&tmL, el.ptilde, p.C_pad, sr, p.C_pad, dtype)) return LCE_ERR_CUDA;
-        SideGrad side;
-        side.a = ga_prev;
-        side.enabled = have_prev ? 1 : 0;
-        side.claim = nullptr;
-        side.done = nullptr;
-        side.dep_row0 = 0;
-        side.ca = ca_prev;  // merge of slab si - 1, then its G formation
-        side.comb = have_prev ? 1 : 0;
-        side.cclaim = cnt + 2 * (si - 1);
-        side.cdone = cnt + 2 * (si - 1) + 1;
-        LCE_TRY(launch_tc_logits(tmX_k, tmW_k, tma_out ? &tmL : nullptr, static_cast<int>(sr), static_cast<int>(C),
-                                 static_cast<int>(D), &hdr->status, el, pair, s, have_prev ? &side : nullptr, f16));
-      } else if (p.tf32) {
-        const float* xh = wsf(p.off_xh) + so * p.ldD;
-        const float* xl = wsf(p.off_xl) + so * p.ldD;
-        if (!encode_tmap_f32(&tx_lg.ah, xh, D, sr, p.ldD, 128) || !encode_tmap_f32(&tx_lg.al, xl, D, sr, p.ldD, 128))
-          return LCE_ERR_CUDA;
-        LCE_TRY(launch_tx_logits(tx_lg, static_cast<int>(sr), static_cast<int>(C), static_cast<int>(D), &hdr->status,
-                                 el, s));
-      } else {
-        const float* Xc = static_cast<const float*>(X) + (row0 + so) * D;
-        LCE_TRY(launch_simt_logits(Xc, static_cast<const float*>(W), D, D, sr, C, D, el, s));
+    const float* lse_rows = nullptr;  // the chunk's row lse for recomputed classes
+    if (sweep) {
+      // ---- logits, row lse / loss, and G of the stored classes, over row
+      // slabs of the chunk. On the CTA-pair path with a backward (>= 1024
+      // rows), the chunk is cut into up to 4 slabs; the idle warps of slab
+      // k's logits GEMM merge the rows of slab k-1 and form its G, and those
+      // of the dX GEMM do the same for the last slab.
+      int64_t slab_off[5];
+      const int64_t nslab = row_slabs(rows, slabbed, slab_off);
+      GradArgs ga_prev;
+      CombineArgs ca_prev;
+      bool have_prev = false;
+      for (int64_t si = 0; si < nslab; ++si) {
+        const int64_t so = slab_off[si];           // slab offset within the chunk
+        const int64_t sr = slab_off[si + 1] - so;  // rows in the slab
+        EpiLse::Params el;
+        el.bias = b;
+        el.bias_dt = dtype;
+        el.target = target + row0 + so;
+        el.C = C;
+        el.rows = static_cast<int>(sr);
+        el.partial = partial + so;
+        el.partial_ld = p.Bc;
+        el.zt = zt + so;
+        el.ptilde =
+            backward ? static_cast<uint8_t*>(Lbuf) + static_cast<size_t>(so) * p.Cb * isz : nullptr;
+        el.ld_p = p.Cb;
+        el.ptilde_dt = dtype;
+        el.store_cols = p.Cs;
+        if (p.tc) {
+          const void* Xc = static_cast<const uint16_t*>(X) + (row0 + so) * D;
+          CUtensorMap tmX_k, tmL;
+          if (!encode_tmap_bf16(&tmX_k, Xc, D, sr, D, TC_BM, dtype)) return LCE_ERR_CUDA;
+          const bool tma_out = pair && backward;
+          if (tma_out && !encode_tmap_bf16_store(&tmL, el.ptilde, p.Cs, sr, p.Cb, dtype)) return LCE_ERR_CUDA;
+          SideGrad side;
+          side.a = ga_prev;
+          side.enabled = have_prev ? 1 : 0;
+          side.claim = nullptr;
+          side.done = nullptr;
+          side.dep_row0 = 0;
+          side.ca = ca_prev;  // merge of slab si - 1, then its G formation
+          side.comb = have_prev ? 1 : 0;
+          side.cclaim = cnt + 2 * (si - 1);
+          side.cdone = cnt + 2 * (si - 1) + 1;
+          LCE_TRY(launch_tc_logits(tmX_k, tmW_k, tma_out ? &tmL : nullptr, static_cast<int>(sr), static_cast<int>(C),
+                                   static_cast<int>(D), &hdr->status, el, pair, s, have_prev ? &side : nullptr, f16));
+        } else if (p.tf32) {
+          const float* xh = wsf(p.off_xh) + so * p.ldD;
+          const float* xl = wsf(p.off_xl) + so * p.ldD;
+          if (!encode_tmap_f32(&tx_lg.ah, xh, D, sr, p.ldD, 128) || !encode_tmap_f32(&tx_lg.al, xl, D, sr, p.ldD, 128))
+            return LCE_ERR_CUDA;
+          LCE_TRY(launch_tx_logits(tx_lg, static_cast<int>(sr), static_cast<int>(C), static_cast<int>(D),
+                                   &hdr->status, el, s));
+        } else {
+          const float* Xc = static_cast<const float*>(X) + (row0 + so) * D;
+          LCE_TRY(launch_simt_logits(Xc, static_cast<const float*>(W), D, D, sr, C, D, el, s));
+        }
+        CombineArgs ca;
+        ca.partial = partial + so;
+        ca.ld = p.Bc;
+        ca.nseg = p.nseg;
+        ca.rows = sr;
+        ca.row0 = row0 + so;
+        ca.zt = zt + so;
+        ca.tcol = tcol + so;
+        ca.gt = gt + so;
+        ca.target = target;
+        ca.ignore_index = ignore_index;
+        ca.C = C;
+        ca.rw = rw;
+        ca.hdr = hdr;
+        ca.loss_rows = rows_out;
+        ca.lse_out = lse_out;
+        ca.backward = backward ? 1 : 0;
+        ca.wrow = wrow != nullptr ? wrow + so : nullptr;
+        ca.nseg_store = nseg_store;
+        ca.lse_rows = recompute ? lse_ws + so : nullptr;
+        ca.w_rows = recompute ? wv_ws + so : nullptr;
+        // on the slabbed path the merge runs in the next GEMM's idle warps
+        const bool defer = slabbed && (si + 1 < nslab || want_dx);
+        if (!defer) LCE_TRY(launch_combine(ca, s));
+        if (!backward) continue;
+        GradArgs ga;
+        ga.L = el.ptilde;
+        ga.ld = p.Cb;
+        ga.rows = sr;
+        ga.C = Cs_eff;
+        ga.segw = p.segw;
+        ga.nseg = nseg_store;
+        ga.scale = partial + so;
+        ga.sld = p.Bc;
+        ga.tcol = tcol + so;
+        ga.gt = gt + so;
+        ga.db_acc = want_db ? db_acc : nullptr;
+        ga.wrow = wrow != nullptr ? wrow + so : nullptr;
+        if (slabbed && si + 1 < nslab) {
+          ga_prev = ga;  // merged and formed by the next slab's GEMM
+          ca_prev = ca;
+          have_prev = true;
+        } else if (slabbed && want_dx) {
+          ga_last = ga;  // merged and formed by the dX GEMM's idle warps before it reads these rows
+          ca_last = ca;
+          have_last = true;
+          last_row0 = so;
+          last_si = si;
+        } else {
+          if (nseg_store > 0) LCE_TRY(launch_grad_logits(ga, dtype, s));
+          have_prev = false;
+        }
       }
-      CombineArgs ca;
-      ca.partial = partial + so;
-      ca.ld = p.Bc;
-      ca.nseg = p.nseg;
-      ca.rows = sr;
-      ca.row0 = row0 + so;
-      ca.zt = zt + so;
-      ca.tcol = tcol + so;
-      ca.gt = gt + so;
-      ca.target = target;
-      ca.ignore_index = ignore_index;
-      ca.C = C;
-      ca.rw = rw;
-      ca.hdr = hdr;
-      ca.loss_rows = rows_out;
-      ca.lse_out = lse_out;
-      ca.backward = backward ? 1 : 0;
-      ca.wrow = wrow != nullptr ? wrow + so : nullptr;
-      // on the slabbed path the merge runs in the next GEMM's idle warps
-      const bool defer = slabbed && (si + 1 < nslab || want_dx);
-      if (!defer) LCE_TRY(launch_combine(ca, s));
-      if (!backward) continue;
-      GradArgs ga;
-      ga.L = el.ptilde;
-      ga.ld = p.C_pad;
-      ga.rows = sr;
-      ga.C = C;
-      ga.segw = p.segw;
-      ga.nseg = p.nseg;
-      ga.scale = partial + so;
-      ga.sld = p.Bc;
-      ga.tcol = tcol + so;
-      ga.gt = gt + so;
-      ga.db_acc = want_db ? db_acc : nullptr;
-      ga.wrow = wrow != nullptr ? wrow + so : nullptr;
-      if (slabbed && si + 1 < nslab) {
-        ga_prev = ga;  // merged and formed by the next slab's GEMM
-        ca_prev = ca;
-        have_prev = true;
-      } else if (slabbed && want_dx) {
-        ga_last = ga;  // merged and formed by the dX GEMM's idle warps before it reads these rows
-        ca_last = ca;
-        have_last = true;
-        last_row0 = so;
-        last_si = si;
-      } else {
-        LCE_TRY(launch_grad_logits(ga, dtype, s));
-        have_prev = false;
-      }
+      lse_rows = lse_ws;
+    } else {
+      // ---- given lse: the rows' weights and target columns
+      BackwardRowsArgs br;
+      br.target = target;
+      br.row0 = row0;
+      br.rows = rows;
+      br.C = C;
+      br.ignore_index = ignore_index;
+      br.rw = rw;
+      br.hdr = hdr;
+      br.tcol = tcol;
+      br.w_rows = wv_ws;
+      br.wrow = wrow;
+      LCE_TRY(launch_backward_rows(br, s));
+      lse_rows = lse_in + row0;
     }
     if (!backward) continue;
     if (p.tf32 && (want_dx || want_dw)) {  // TF32 parts of G (hi over G itself) and of G^T
@@ -552,57 +691,38 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
       sa.ldt = p.ldB;
       LCE_TRY(launch_split_tf32(sa, s));
     }
-    // ---- dX = G W
-    if (want_dx) {
+    // dX is the sum over the class parts (the stored classes, then each
+    // recomputed chunk); with several parts a 16-bit dX is summed in fp32
+    const int64_t nparts = (Cs_eff > 0 ? 1 : 0) + p.nvc;
+    auto dx_params = [&](int64_t part) {
       EpiStore::Params es;
       es.out = static_cast<uint8_t*>(dX) + static_cast<size_t>(row0) * D * gsz;
       es.out_dt = grad_dtype;
       es.ldo = D;
-      es.acc32 = nullptr;
-      es.mode = 0;
       es.rows = rows;
       es.cols = D;
       es.vec_ok = aligned16(dX) && ((D * gsz) % 16 == 0);
       es.row_scale = wrow;  // fp16: G without the row weights
       es.scalar_scale = nullptr;
-      if (p.tc) {
-        CUtensorMap tmG_k, tmdX;
-        if (!encode_tmap_bf16(&tmG_k, Lbuf, C, rows, p.C_pad, TC_BM, dtype)) return LCE_ERR_CUDA;
-        const bool tma_out = pair && es.out_dt != LCE_F32 && es.vec_ok;
-        if (tma_out && !encode_tmap_bf16_store(&tmdX, es.out, D, rows, D, grad_dtype)) return LCE_ERR_CUDA;
-        SideGrad side;
-        if (have_last) {
-          side.a = ga_last;
-          side.enabled = 1;
-          side.claim = cnt + 8;
-          side.done = cnt + 9;
-          side.dep_row0 = last_row0;
-          side.ca = ca_last;
-          side.comb = 1;
-          side.cclaim = cnt + 2 * last_si;
-          side.cdone = cnt + 2 * last_si + 1;
-        }
-        LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmW_n, tma_out ? &tmdX : nullptr, static_cast<int>(rows),
-                                static_cast<int>(D), static_cast<int>(C), &hdr->status, es, pair, s, f16,
-                                have_last ? &side : nullptr));
-      } else if (p.tf32) {
-        if (!encode_tmap_f32(&tx_dx.ah, Lbuf, C, rows, p.C_pad, 128) ||
-            !encode_tmap_f32(&tx_dx.al, wsf(p.off_gl), C, rows, p.C_pad, 128))
-          return LCE_ERR_CUDA;
-        LCE_TRY(launch_tx_store(TC_DX, tx_dx, static_cast<int>(rows), static_cast<int>(D), static_cast<int>(C),
-                                &hdr->status, es, s));
+      if (nparts == 1) {
+        es.mode = 0;
+        es.acc32 = nullptr;
+      } else if (grad_dtype == LCE_F32) {
+        es.mode = part == 0 ? 0 : 2;
+        es.acc32 = static_cast<float*>(es.out);
       } else {
-        LCE_TRY(launch_simt_store(TC_DX, static_cast<const float*>(Lbuf), static_cast<const float*>(W), p.C_pad, D,
-                                  rows, D, C, es, s));
+        es.mode = part == 0 ? 1 : (part == nparts - 1 ? 3 : 2);
+        es.acc32 = dx_acc;
       }
-    }
-    // ---- dW (+)= G^T X_c
-    if (want_dw) {
+      return es;
+    };
+    // dW rows [c0, c0 + cw): accumulated over the batch chunks
+    auto dw_params = [&](int64_t c0, int64_t cw) {
       EpiStore::Params es;
-      es.out = dW;
+      es.out = static_cast<uint8_t*>(dW) + static_cast<size_t>(c0) * D * gsz;
       es.out_dt = grad_dtype;
       es.ldo = D;
-      es.rows = C;
+      es.rows = cw;
       es.cols = D;
       es.vec_ok = aligned16(dW) && ((D * gsz) % 16 == 0);
       es.row_scale = nullptr;
@@ -612,39 +732,139 @@ int run_lce(bool backward, const void* X, const void* W, const void* b, const in
         es.acc32 = nullptr;
       } else if (grad_dtype == LCE_F32) {
         es.mode = ci == 0 ? 0 : 2;
-        es.acc32 = static_cast<float*>(dW);
+        es.acc32 = static_cast<float*>(es.out);
       } else {
         es.mode = ci == 0 ? 1 : (ci == p.nchunks - 1 ? 3 : 2);
-        es.acc32 = dw_acc;
+        es.acc32 = dw_acc + static_cast<size_t>(c0) * D;
       }
-      if (p.tc) {
-        const void* Xc = static_cast<const uint16_t*>(X) + row0 * D;
-        if (f16) {
-          LCE_TRY(launch_row_scale(Xc, wrow, wbar, Xs, rows, D, s));
-          Xc = Xs;
+      return es;
+    };
+    const void* Xc = p.tc ? static_cast<const void*>(static_cast<const uint16_t*>(X) + row0 * D) : nullptr;
+    const void* Xdw = Xc;  // the B operand of dW (fp16: X scaled per row)
+    bool xs_done = false;
+    auto prepare_dw = [&]() -> cudaError_t {
+      if (!f16 || xs_done) return cudaSuccess;
+      xs_done = true;
+      Xdw = Xs;
+      return launch_row_scale(Xc, wrow, wbar, Xs, rows, D, s);
+    };
+    int64_t part = 0;
+    if (Cs_eff > 0) {
+      // ---- dX = G W over the stored classes
+      if (want_dx) {
+        EpiStore::Params es = dx_params(part);
+        if (p.tc) {
+          CUtensorMap tmG_k, tmdX;
+          if (!encode_tmap_bf16(&tmG_k, Lbuf, Cs_eff, rows, p.Cb, TC_BM, dtype)) return LCE_ERR_CUDA;
+          const bool tma_out = pair && (es.mode == 0 || es.mode == 3) && es.out_dt != LCE_F32 && es.vec_ok;
+          if (tma_out && !encode_tmap_bf16_store(&tmdX, es.out, D, rows, D, grad_dtype)) return LCE_ERR_CUDA;
+          SideGrad side;
+          if (have_last) {
+            side.a = ga_last;
+            side.enabled = 1;
+            side.claim = cnt + 8;
+            side.done = cnt + 9;
+            side.dep_row0 = last_row0;
+            side.ca = ca_last;
+            side.comb = 1;
+            side.cclaim = cnt + 2 * last_si;
+            side.cdone = cnt + 2 * last_si + 1;
+          }
+          LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmW_n, tma_out ? &tmdX : nullptr, static_cast<int>(rows),
+                                  static_cast<int>(D), static_cast<int>(Cs_eff), &hdr->status, es, pair, s, f16,
+                                  have_last ? &side : nullptr));
+        } else if (p.tf32) {
+          if (!encode_tmap_f32(&tx_dx.ah, Lbuf, C, rows, p.C_pad, 128) ||
+              !encode_tmap_f32(&tx_dx.al, wsf(p.off_gl), C, rows, p.C_pad, 128))
+            return LCE_ERR_CUDA;
+          LCE_TRY(launch_tx_store(TC_DX, tx_dx, static_cast<int>(rows), static_cast<int>(D), static_cast<int>(C),
+                                  &hdr->status, es, s));
+        } else {
+          LCE_TRY(launch_simt_store(TC_DX, static_cast<const float*>(Lbuf), static_cast<const float*>(W), p.C_pad,
+                                    D, rows, D, C, es, s));
         }
-        CUtensorMap tmG_m, tmX_n, tmdW;
-        if (!encode_tmap_bf16(&tmG_m, Lbuf, C, rows, p.C_pad, 64, dtype)) return LCE_ERR_CUDA;
-        if (!encode_tmap_bf16(&tmX_n, Xc, D, rows, D, 64, dtype)) return LCE_ERR_CUDA;
-        const bool tma_out = pair && es.mode == 0 && es.out_dt != LCE_F32 && es.vec_ok;
-        if (tma_out && !encode_tmap_bf16_store(&tmdW, dW, D, C, D, grad_dtype)) return LCE_ERR_CUDA;
-        LCE_TRY(launch_tc_store(TC_DW, tmG_m, tmX_n, tma_out ? &tmdW : nullptr, static_cast<int>(C),
-                                static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s, f16));
-      } else if (p.tf32) {
-        bool ok = encode_tmap_f32(&tx_dw.ah, wsf(p.off_gth), rows, C, p.ldB, 128) &&
-                  encode_tmap_f32(&tx_dw.al, wsf(p.off_gtl), rows, C, p.ldB, 128) &&
-                  encode_tmap_f32(&tx_dw.bh, wsf(p.off_xth), rows, D, p.ldB, 128) &&
-                  encode_tmap_f32(&tx_dw.bl, wsf(p.off_xtl), rows, D, p.ldB, 128);
-        if (!ok) return LCE_ERR_CUDA;
-        LCE_TRY(launch_tx_store(TC_DW, tx_dw, static_cast<int>(C), static_cast<int>(D), static_cast<int>(rows),
-                                &hdr->status, es, s));
-      } else {
-        const float* Xc = static_cast<const float*>(X) + row0 * D;
-        LCE_TRY(launch_simt_store(TC_DW, static_cast<const float*>(Lbuf), Xc, p.C_pad, D, C, D, rows, es, s));
+      }
+      // ---- dW (+)= G^T X_c over the stored classes
+      if (want_dw) {
+        EpiStore::Params es = dw_params(0, Cs_eff);
+        if (p.tc) {
+          LCE_TRY(prepare_dw());
+          CUtensorMap tmG_m, tmX_n, tmdW;
+          if (!encode_tmap_bf16(&tmG_m, Lbuf, Cs_eff, rows, p.Cb, 64, dtype)) return LCE_ERR_CUDA;
+          if (!encode_tmap_bf16(&tmX_n, Xdw, D, rows, D, 64, dtype)) return LCE_ERR_CUDA;
+          const bool tma_out = pair && (es.mode == 0 || es.mode == 3) && es.out_dt != LCE_F32 && es.vec_ok;
+          if (tma_out && !encode_tmap_bf16_store(&tmdW, es.out, D, Cs_eff, D, grad_dtype)) return LCE_ERR_CUDA;
+          LCE_TRY(launch_tc_store(TC_DW, tmG_m, tmX_n, tma_out ? &tmdW : nullptr, static_cast<int>(Cs_eff),
+                                  static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s, f16));
+        } else if (p.tf32) {
+          bool ok = encode_tmap_f32(&tx_dw.ah, wsf(p.off_gth), rows, C, p.ldB, 128) &&
+                    encode_tmap_f32(&tx_dw.al, wsf(p.off_gtl), rows, C, p.ldB, 128) &&
+                    encode_tmap_f32(&tx_dw.bh, wsf(p.off_xth), rows, D, p.ldB, 128) &&
+                    encode_tmap_f32(&tx_dw.bl, wsf(p.off_xtl), rows, D, p.ldB, 128);
+          if (!ok) return LCE_ERR_CUDA;
+          LCE_TRY(launch_tx_store(TC_DW, tx_dw, static_cast<int>(C), static_cast<int>(D), static_cast<int>(rows),
+                                  &hdr->status, es, s));
+        } else {
+          const float* Xf = static_cast<const float*>(X) + row0 * D;
+          LCE_TRY(launch_simt_store(TC_DW, static_cast<const float*>(Lbuf), Xf, p.C_pad, D, C, D, rows, es, s));
+        }
+      }
+      ++part;
+    }
+    // ---- the recomputed classes, one chunk of up to Cb classes at a time:
+    // logits again with the gradient epilogue (G into the buffer), then the
+    // chunk's share of dX and its rows of dW
+    if (recompute) {
+      CUtensorMap tmXc_k;
+      if (!encode_tmap_bf16(&tmXc_k, Xc, D, rows, D, TC_BM, dtype)) return LCE_ERR_CUDA;
+      for (int64_t v = 0; v < p.nvc; ++v, ++part) {
+        const int64_t c0 = p.Cs + v * p.Cb;
+        const int64_t cw = std::min(p.Cb, C - c0);
+        const void* Wv = static_cast<const uint16_t*>(W) + c0 * D;
+        CUtensorMap tmWv_k, tmGv;
+        if (!encode_tmap_bf16(&tmWv_k, Wv, D, cw, D, pair ? 128 : TC_BN, dtype)) return LCE_ERR_CUDA;
+        if (pair && !encode_tmap_bf16_store(&tmGv, Lbuf, cw, rows, p.Cb, dtype)) return LCE_ERR_CUDA;
+        EpiGrad::Params eg;
+        eg.bias = b != nullptr ? static_cast<const void*>(static_cast<const uint16_t*>(b) + c0) : nullptr;
+        eg.bias_dt = dtype;
+        eg.tcol = tcol;
+        eg.col_base = c0;
+        eg.cols = cw;
+        eg.rows = static_cast<int>(rows);
+        eg.lse = lse_rows;
+        eg.wg = wv_ws;
+        eg.wdb = wrow;
+        eg.db_acc = want_db ? db_acc : nullptr;
+        eg.g = Lbuf;
+        eg.ld_g = p.Cb;
+        eg.g_dt = dtype;
+        LCE_TRY(launch_tc_grad(tmXc_k, tmWv_k, pair ? &tmGv : nullptr, static_cast<int>(rows), static_cast<int>(cw),
+                               static_cast<int>(D), &hdr->status, eg, pair, s, f16));
+        if (want_dx) {
+          EpiStore::Params es = dx_params(part);
+          CUtensorMap tmG_k, tmWv_n, tmdX;
+          if (!encode_tmap_bf16(&tmG_k, Lbuf, cw, rows, p.Cb, TC_BM, dtype)) return LCE_ERR_CUDA;
+          if (!encode_tmap_bf16(&tmWv_n, Wv, D, cw, D, 64, dtype)) return LCE_ERR_CUDA;
+          const bool tma_out = pair && (es.mode == 0 || es.mode == 3) && es.out_dt != LCE_F32 && es.vec_ok;
+          if (tma_out && !encode_tmap_bf16_store(&tmdX, es.out, D, rows, D, grad_dtype)) return LCE_ERR_CUDA;
+          LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmWv_n, tma_out ? &tmdX : nullptr, static_cast<int>(rows),
+                                  static_cast<int>(D), static_cast<int>(cw), &hdr->status, es, pair, s, f16));
+        }
+        if (want_dw) {
+          EpiStore::Params es = dw_params(c0, cw);
+          LCE_TRY(prepare_dw());
+          CUtensorMap tmG_m, tmX_n, tmdW;
+          if (!encode_tmap_bf16(&tmG_m, Lbuf, cw, rows, p.Cb, 64, dtype)) return LCE_ERR_CUDA;
+          if (!encode_tmap_bf16(&tmX_n, Xdw, D, rows, D, 64, dtype)) return LCE_ERR_CUDA;
+          const bool tma_out = pair && (es.mode == 0 || es.mode == 3) && es.out_dt != LCE_F32 && es.vec_ok;
+          if (tma_out && !encode_tmap_bf16_store(&tmdW, es.out, D, cw, D, grad_dtype)) return LCE_ERR_CUDA;
+          LCE_TRY(launch_tc_store(TC_DW, tmG_m, tmX_n, tma_out ? &tmdW : nullptr, static_cast<int>(cw),
+                                  static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s, f16));
+        }
       }
     }
   }
-  if (reduction != LCE_RED_NONE)
+  if (!given && reduction != LCE_RED_NONE)
     LCE_TRY(launch_loss_finalize(loss_rows, N, reduction, hdr, class_weight != nullptr, loss_out, s));
   if (want_db) LCE_TRY(launch_db_finalize(db_acc, db, C, grad_dtype, s));
   return LCE_OK;
@@ -663,68 +883,108 @@ size_t lce_workspace_size(int op, int64_t N, int64_t D, int64_t C, int dtype, in
     if (N < 0 || C < 1) return 0;
     return align_up(sizeof(WsHeader)) + align_up(static_cast<size_t>(N) * 4);
   }
-  if (op != LCE_OP_FORWARD && op != LCE_OP_FORWARD_BACKWARD) return 0;
+  if (op != LCE_OP_FORWARD && op != LCE_OP_FORWARD_BACKWARD && op != LCE_OP_BACKWARD) return 0;
   if (check_common(N, D, C, dtype, LCE_F32, reduction) != LCE_OK) return 0;
-  if (op == LCE_OP_FORWARD_BACKWARD && grad_dtype != LCE_F32 && grad_dtype != LCE_BF16 && grad_dtype != LCE_F16)
-    return 0;
+  if (is_backward_op(op) && grad_dtype != LCE_F32 && grad_dtype != LCE_BF16 && grad_dtype != LCE_F16) return 0;
   if (chunk_rows < 0) return 0;
-  int64_t bc;
+  int64_t bc, cb;
   if (chunk_rows == 0) {
-    bc = default_chunk(op, N, D, C, dtype);
-  } else if (chunk_rows >= N) {
-    bc = N;
+    budget_dims(op, N, D, C, dtype, kDefaultBufferBytes, &bc, &cb);
   } else {
-    // the calls use N or a power of two times 128 rows
-    bc = 128;
-    while (bc * 2 <= chunk_rows) bc *= 2;
-    if (bc >= N) bc = N;
+    // batch chunks of the given rows (the calls use N or a power of two
+    // times 128 rows), every class in one buffer
+    if (chunk_rows >= N) {
+      bc = N;
+    } else {
+      bc = 128;
+      while (bc * 2 <= chunk_rows) bc *= 2;
+      if (bc >= N) bc = N;
+    }
+    cb = int64_t(1) << 40;  // clamped to every class
   }
   Plan p;
-  make_plan(op, N, D, C, dtype, grad_dtype, true, true, true, bc, &p);
+  make_plan(op, N, D, C, dtype, grad_dtype, true, true, true, bc, cb, &p);
+  return p.total;
+}
+
+size_t lce_workspace_size_for_buffer(int op, int64_t N, int64_t D, int64_t C, int dtype, int reduction,
+                                     int grad_dtype, size_t buffer_bytes) {
+  if (op != LCE_OP_FORWARD && op != LCE_OP_FORWARD_BACKWARD && op != LCE_OP_BACKWARD) return 0;
+  if (check_common(N, D, C, dtype, LCE_F32, reduction) != LCE_OK) return 0;
+  if (is_backward_op(op) && grad_dtype != LCE_F32 && grad_dtype != LCE_BF16 && grad_dtype != LCE_F16) return 0;
+  const int64_t budget = buffer_bytes == 0 ? kDefaultBufferBytes
+                                           : static_cast<int64_t>(std::min<size_t>(buffer_bytes, size_t(1) << 62));
+  int64_t bc, cb;
+  budget_dims(op, N, D, C, dtype, budget, &bc, &cb);
+  Plan p;
+  make_plan(op, N, D, C, dtype, grad_dtype, true, true, true, bc, cb, &p);
   return p.total;
 }
 
 int lce_forward(const void* X, const void* W, const void* b, const int64_t* target, int64_t N, int64_t D, int64_t C,
                 int dtype, int acc_dtype, int reduction, int64_t ignore_index, float* loss_out, float* lse_out,
                 void* workspace, size_t ws_bytes, void* stream) {
-  return run_lce(false, X, W, b, target, nullptr, N, D, C, dtype, acc_dtype, reduction, ignore_index, nullptr,
-                 loss_out, lse_out, nullptr, nullptr, nullptr, LCE_F32, workspace, ws_bytes, stream);
+  return run_lce(LCE_OP_FORWARD, X, W, b, target, nullptr, nullptr, N, D, C, dtype, acc_dtype, reduction,
+                 ignore_index, nullptr, nullptr, loss_out, lse_out, nullptr, nullptr, nullptr, LCE_F32, workspace, ws_bytes,
+                 stream);
 }
 
 int lce_forward_ex(const void* X, const void* W, const void* b, const int64_t* target, const float* class_weight,
-                   int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype, int reduction, int64_t ignore_index,
-                   float* loss_out, float* lse_out, void* workspace, size_t ws_bytes, void* stream) {
-  return run_lce(false, X, W, b, target, class_weight, N, D, C, dtype, acc_dtype, reduction, ignore_index, nullptr,
-                 loss_out, lse_out, nullptr, nullptr, nullptr, LCE_F32, workspace, ws_bytes, stream);
+                   const float* denominator, int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype, int reduction,
+                   int64_t ignore_index, float* loss_out, float* lse_out, void* workspace, size_t ws_bytes,
+                   void* stream) {
+  return run_lce(LCE_OP_FORWARD, X, W, b, target, class_weight, denominator, N, D, C, dtype, acc_dtype, reduction,
+                 ignore_index, nullptr, nullptr, loss_out, lse_out, nullptr, nullptr, nullptr, LCE_F32, workspace, ws_bytes,
+                 stream);
 }
 
 int lce_forward_backward(const void* X, const void* W, const void* b, const int64_t* target, int64_t N, int64_t D,
                          int64_t C, int dtype, int acc_dtype, int reduction, int64_t ignore_index,
                          const float* grad_out, float* loss_out, void* dX, void* dW, void* db, int grad_dtype,
                          void* workspace, size_t ws_bytes, void* stream) {
-  return run_lce(true, X, W, b, target, nullptr, N, D, C, dtype, acc_dtype, reduction, ignore_index, grad_out,
-                 loss_out, nullptr, dX, dW, db, grad_dtype, workspace, ws_bytes, stream);
+  return run_lce(LCE_OP_FORWARD_BACKWARD, X, W, b, target, nullptr, nullptr, N, D, C, dtype, acc_dtype, reduction,
+                 ignore_index, nullptr, grad_out, loss_out, nullptr, dX, dW, db, grad_dtype, workspace, ws_bytes,
+                 stream);
 }
 
 int lce_forward_backward_ex(const void* X, const void* W, const void* b, const int64_t* target,
-                            const float* class_weight, int64_t N, int64_t D, int64_t C, int dtype, int acc_dtype,
-                            int reduction, int64_t ignore_index, const float* grad_out, float* loss_out, void* dX,
-                            void* dW, void* db, int grad_dtype, void* workspace, size_t ws_bytes, void* stream) {
-  return run_lce(true, X, W, b, target, class_weight, N, D, C, dtype, acc_dtype, reduction, ignore_index, grad_out,
-                 loss_out, nullptr, dX, dW, db, grad_dtype, workspace, ws_bytes, stream);
+                            const float* class_weight, const float* denominator, int64_t N, int64_t D, int64_t C,
+                            int dtype, int acc_dtype, int reduction, int64_t ignore_index, const float* grad_out,
+                            float* loss_out, void* dX, void* dW, void* db, int grad_dtype, void* workspace,
+                            size_t ws_bytes, void* stream) {
+  return run_lce(LCE_OP_FORWARD_BACKWARD, X, W, b, target, class_weight, denominator, N, D, C, dtype, acc_dtype,
+                 reduction, ignore_index, nullptr, grad_out, loss_out, nullptr, dX, dW, db, grad_dtype, workspace, ws_bytes,
+                 stream);
+}
+
+int lce_backward(const void* X, const void* W, const void* b, const int64_t* target, const float* lse, int64_t N,
+                 int64_t D, int64_t C, int dtype, int acc_dtype, int reduction, int64_t ignore_index,
+                 const float* grad_out, void* dX, void* dW, void* db, int grad_dtype, void* workspace,
+                 size_t ws_bytes, void* stream) {
+  return run_lce(LCE_OP_BACKWARD, X, W, b, target, nullptr, nullptr, N, D, C, dtype, acc_dtype, reduction,
+                 ignore_index, lse,
+                 grad_out, nullptr, nullptr, dX, dW, db, grad_dtype, workspace, ws_bytes, stream);
+}
+
+int lce_backward_ex(const void* X, const void* W, const void* b, const int64_t* target, const float* class_weight,
+                    const float* denominator, const float* lse, int64_t N, int64_t D, int64_t C, int dtype,
+                    int acc_dtype, int reduction, int64_t ignore_index, const float* grad_out, void* dX, void* dW,
+                    void* db, int grad_dtype, void* workspace, size_t ws_bytes, void* stream) {
+  return run_lce(LCE_OP_BACKWARD, X, W, b, target, class_weight, denominator, N, D, C, dtype, acc_dtype, reduction,
+                 ignore_index, lse, grad_out, nullptr, nullptr, dX, dW, db, grad_dtype, workspace, ws_bytes, stream);
 }
 
 int lce_cross_entropy_from_logits(void* logits_inout, const int64_t* target, int64_t N, int64_t V, int dtype,
                                   int reduction, int64_t ignore_index, const float* grad_out, float* loss_out,
                                   void* workspace, size_t ws_bytes, void* stream) {
-  return lce_cross_entropy_from_logits_ex(logits_inout, target, nullptr, N, V, dtype, reduction, ignore_index,
-                                          grad_out, loss_out, workspace, ws_bytes, stream);
+  return lce_cross_entropy_from_logits_ex(logits_inout, target, nullptr, nullptr, N, V, dtype, reduction,
+                                          ignore_index, grad_out, loss_out, workspace, ws_bytes, stream);
 }
 
 int lce_cross_entropy_from_logits_ex(void* logits_inout, const int64_t* target, const float* class_weight,
-                                     int64_t N, int64_t V, int dtype, int reduction, int64_t ignore_index,
-                                     const float* grad_out, float* loss_out, void* workspace, size_t ws_bytes,
-                                     void* stream) {
+                                     const float* denominator, int64_t N, int64_t V, int dtype, int reduction,
+                                     int64_t ignore_index, const float* grad_out, float* loss_out, void* workspace,
+                                     size_t ws_bytes, void* stream) {
   if (dtype != LCE_F32 && dtype != LCE_BF16 && dtype != LCE_F16) return LCE_ERR_DTYPE;
   if (reduction != LCE_RED_NONE && reduction != LCE_RED_SUM && reduction != LCE_RED_MEAN) return LCE_ERR_REDUCTION;
   if (N < 0 || V < 1 || N > (int64_t(1) << 40) || V > (int64_t(1) << 40)) return LCE_ERR_SHAPE;
@@ -742,8 +1002,8 @@ int lce_cross_entropy_from_logits_ex(void* logits_inout, const int64_t* target, 
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   float* loss_rows = reinterpret_cast<float*>(ws + align_up(sizeof(WsHeader)));
   LCE_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
+  LCE_TRY(launch_prep(target, N, V, ignore_index, class_weight, denominator, hdr, s));
   if (N > 0) {
-    LCE_TRY(launch_prep(target, N, V, ignore_index, class_weight, hdr, s));
     CeArgs a;
     a.logits = logits_inout;
     a.N = N;
@@ -774,6 +1034,23 @@ int lce_scale_gradients(void* dX, int64_t n_dx, void* dW, int64_t n_dw, void* db
   if (st != LCE_OK) return st;
   return from_cuda(launch_scale_grads(dX, dX ? n_dx : 0, dW, dW ? n_dw : 0, db, db ? n_db : 0, grad_dtype, grad_out,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+int lce_mean_denominator(const int64_t* target, const float* class_weight, int64_t N, int64_t C,
+                         int64_t ignore_index, float* denominator_out, void* workspace, size_t ws_bytes,
+                         void* stream) {
+  if (denominator_out == nullptr || workspace == nullptr) return LCE_ERR_NULL;
+  if (N > 0 && target == nullptr) return LCE_ERR_NULL;
+  if (N < 0 || C < 1 || N > (int64_t(1) << 40) || C > (int64_t(1) << 40)) return LCE_ERR_SHAPE;
+  if (ws_bytes < sizeof(WsHeader)) return LCE_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return LCE_ERR_ALIGN;
+  const int st = check_device();
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  LCE_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
+  LCE_TRY(launch_prep(target, N, C, ignore_index, class_weight, nullptr, hdr, s, denominator_out));
+  return LCE_OK;
 }
 
 const char* lce_status_string(int status) {
@@ -992,7 +1269,7 @@ int lce_test_row_slabs(int64_t rows, int64_t* slab_off) {
 int lce_test_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtype, int want_dx, int want_dw,
                   int want_db, size_t ws_bytes, int64_t* out, int n_out) {
   if (out == nullptr || n_out < LCE_TEST_PLAN_FIELDS) return -1;
-  if (op != LCE_OP_FORWARD && op != LCE_OP_FORWARD_BACKWARD) return -1;
+  if (op != LCE_OP_FORWARD && op != LCE_OP_FORWARD_BACKWARD && op != LCE_OP_BACKWARD) return -1;
   if (check_common(N, D, C, dtype, LCE_F32, LCE_RED_MEAN) != LCE_OK) return -1;
   Plan p;
   if (!choose_plan(op, N, D, C, dtype, grad_dtype, want_dx != 0, want_dw != 0, want_db != 0, ws_bytes, &p))
@@ -1003,10 +1280,12 @@ int lce_test_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_d
       static_cast<int64_t>(p.off_tcol), static_cast<int64_t>(p.off_gt), static_cast<int64_t>(p.off_partial),
       static_cast<int64_t>(p.off_L), static_cast<int64_t>(p.off_dw), static_cast<int64_t>(p.off_db),
       static_cast<int64_t>(p.off_wrow), static_cast<int64_t>(p.off_wbar), static_cast<int64_t>(p.off_xs),
+      static_cast<int64_t>(p.off_lse), static_cast<int64_t>(p.off_wv), static_cast<int64_t>(p.off_dx),
       static_cast<int64_t>(p.off_wh), static_cast<int64_t>(p.off_wl), static_cast<int64_t>(p.off_wth),
       static_cast<int64_t>(p.off_wtl), static_cast<int64_t>(p.off_xh), static_cast<int64_t>(p.off_xl),
       static_cast<int64_t>(p.off_xth), static_cast<int64_t>(p.off_xtl), static_cast<int64_t>(p.off_gl),
-      static_cast<int64_t>(p.off_gth), static_cast<int64_t>(p.off_gtl)};
+      static_cast<int64_t>(p.off_gth), static_cast<int64_t>(p.off_gtl),
+      p.Cb, p.Cs, p.nvc};
   for (int i = 0; i < LCE_TEST_PLAN_FIELDS; ++i) out[i] = v[i];
   return LCE_TEST_PLAN_FIELDS;
 }

@@ -2,8 +2,9 @@
 // its log-sum-exp, loss and gradient scales, for a block of 32 rows.
 //
 // lse = M + log sum_s s_s exp(m_s - M), loss_n = lse - z_t (0 on ignored
-// rows). For the backward each pair becomes the scale w_n exp(m_s - lse)
-// that maps the stored P~ to G, and G at the target column is
+// rows). For the backward each pair of a stored segment becomes the scale
+// w_n exp(m_s - lse) that maps the stored P~ to G (and the row's lse and
+// weight are kept for classes recomputed later), and G at the target column is
 // w_n (softmax_t - 1) from the fp32 target logit (expm1 keeps it accurate
 // when softmax_t ~ 1). Used by the stand-alone merge kernel and by the
 // otherwise idle warps of the next GEMM (64 threads).
@@ -73,6 +74,8 @@ __device__ __forceinline__ void combine_rows32(const CombineArgs& a, int64_t r0,
       a.tcol[r] = valid ? static_cast<int>(tg) : -1;
       a.gt[r] = valid ? ws * expm1f(zt - lse) : 0.0f;
       if (a.wrow != nullptr) a.wrow[r] = w;
+      if (a.lse_rows != nullptr) a.lse_rows[r] = lse;
+      if (a.w_rows != nullptr) a.w_rows[r] = ws;
       sLse[rl] = lse;
       sW[rl] = ws;
     }
@@ -82,17 +85,17 @@ __device__ __forceinline__ void combine_rows32(const CombineArgs& a, int64_t r0,
     if (in) {
       const float lse = sLse[rl];
       const float ws = sW[rl];
-      for (int s0 = sl; s0 < a.nseg; s0 += 8 * SL) {
+      for (int s0 = sl; s0 < a.nseg_store; s0 += 8 * SL) {
         float m[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int s = s0 + k * SL;
-          m[k] = s < a.nseg ? a.partial[s * a.ld + r].x : 0.0f;
+          m[k] = s < a.nseg_store ? a.partial[s * a.ld + r].x : 0.0f;
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int s = s0 + k * SL;
-          if (s < a.nseg) a.partial[s * a.ld + r].x = ws * expf(m[k] - lse);
+          if (s < a.nseg_store) a.partial[s * a.ld + r].x = ws * expf(m[k] - lse);
         }
       }
     }

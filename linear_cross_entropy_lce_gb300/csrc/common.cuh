@@ -24,14 +24,20 @@ struct WsHeader {
   int status;       // kStatus* bits, OR-ed by kernels
   int n_valid;      // rows whose target is a class index (not ignored, in range)
   double weight_sum;  // sum of class weights over valid rows (class-weighted calls)
-  int pad[60];
+  // the mean's denominator d: n_valid, or weight_sum with class weights, or
+  // the caller's given value; written once by the last block of the prep
+  // kernel, read by everything after it
+  double denom;
+  int prep_done;    // prep blocks finished
+  int pad[57];
 };
 static_assert(sizeof(WsHeader) <= 256, "header must fit 256 bytes");
 
 // Per-row weight parameters: w_n = valid ? c_n * base * (vec ? g[n] : g0) : 0,
 // with c_n = class_weight[target_n] (1 without class weights) and base = 1
-// (sum, none) or 1 / d (mean; d = n_valid, or the sum of c_n over valid rows
-// with class weights; NaN for every row when d == 0).
+// (sum, none) or 1 / d (mean; d = hdr->denom: n_valid, or the sum of c_n over
+// valid rows with class weights, or a denominator the caller gives; NaN for
+// every row when d == 0).
 struct RowWeight {
   const float* grad_out;      // device scalar (sum/mean) or [N] (none); may be NULL
   const float* class_weight;  // [C] or NULL
@@ -68,7 +74,7 @@ __device__ __forceinline__ float class_w(const RowWeight& rw, int64_t t, bool va
 __device__ __forceinline__ float row_weight(const RowWeight& rw, const WsHeader* hdr, int64_t n, int64_t t,
                                             bool valid) {
   const bool mean = rw.reduction == LCE_RED_MEAN;
-  const bool empty = rw.class_weight != nullptr ? hdr->weight_sum == 0.0 : hdr->n_valid == 0;
+  const bool empty = hdr->denom == 0.0;
   if (!valid) {
     // an ignored row still sees NaN under mean when the divisor is 0
     return (mean && empty) ? __int_as_float(0x7fc00000) : 0.0f;
@@ -78,8 +84,7 @@ __device__ __forceinline__ float row_weight(const RowWeight& rw, const WsHeader*
   const float c = rw.class_weight != nullptr ? rw.class_weight[t] : 1.0f;
   if (mean) {
     if (empty) return __int_as_float(0x7fc00000);
-    const float d = rw.class_weight != nullptr ? static_cast<float>(hdr->weight_sum)
-                                               : static_cast<float>(hdr->n_valid);
+    const float d = static_cast<float>(hdr->denom);
     return c * (1.0f / d) * g;
   }
   return c * g;

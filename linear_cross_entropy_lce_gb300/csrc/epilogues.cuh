@@ -125,6 +125,7 @@ struct EpiLse {
     void* ptilde;            // [rows][ld_p] of ptilde_dt, or NULL (forward only)
     int64_t ld_p;
     int ptilde_dt;
+    int64_t store_cols;      // P~ is stored for columns < store_cols only (a multiple of the tile width)
   };
 
   __device__ static __forceinline__ float bias_at(const Params& p, int64_t col) {
@@ -176,7 +177,8 @@ struct EpiLse {
         }
       }
     }
-    // pass 2: sum of exp(z - m), target logit, optional P~ store. A segment
+    // pass 2: sum of exp(z - m), target logit, optional P~ store (for the
+    // first store_cols columns; the others are recomputed later). A segment
     // whose logits are all -inf (a bias of -inf masks classes) is shifted
     // by 0, so that it stores P~ = exp(-inf) = 0 and sums to 0, not NaN.
     if (m == -INFINITY) m = 0.0f;
@@ -208,7 +210,7 @@ struct EpiLse {
           s += v[i];
         }
       }
-      if (p.ptilde == nullptr) continue;
+      if (p.ptilde == nullptr || col0 >= p.store_cols) continue;
 #pragma unroll
       for (int c = 0; c < GW; ++c) {
         float(&vc)[32] = *reinterpret_cast<float(*)[32]>(&v[32 * c]);
@@ -231,11 +233,148 @@ struct EpiLse {
   }
 };
 
+// Column sums of a warp's 32 rows: on entry x[i] is this lane's (row's)
+// value in column i < 32; on return lane L holds the sum over the 32 lanes
+// of column L. A transposing butterfly: at each step a lane keeps one half
+// of its columns, sends the other half to the lane `s` away and adds what it
+// receives, so 31 shuffles cover 32 columns. x is clobbered.
+__device__ __forceinline__ float warp_column_sum32(float (&x)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = up ? x[i] : x[i + s];
+      const float keep = up ? x[i + s] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return x[0];
+}
+
+// ---------------------------------------------------------------------------
+// Gradient epilogue of the recomputing GEMM: z = X W_v^T + b_v over one
+// chunk v of the classes, for rows whose log-sum-exp is already known.
+//
+// For its row the thread forms G[r, j] = wg_r (exp(z_j - lse_r) - [j == t_r])
+// over the chunk's classes j < cols (the target column from expm1, so that
+// softmax_t ~ 1 does not cancel; 0 in padding columns and on rows past the
+// chunk) and stores it in the buffer's type, through the output tensor map
+// when one is given. With db_acc it also adds the column sums of
+// wdb_r * G[r, j] into db_acc (global class col_base + j): each warp's 32
+// rows are summed per column with warp_column_sum32, then one lane per
+// column adds the sum. This is the second sweep of the page's chunked
+// backward (linear_cross_entropy.py: logits recomputed per chunk, scaled by
+// the row weight after the max shift, minus the one-hot), done on the tile
+// while it is in tensor memory.
+// ---------------------------------------------------------------------------
+struct EpiGrad {
+  struct Params {
+    const void* bias;   // [cols] of bias_dt (this chunk's slice), or NULL
+    int bias_dt;
+    const int* tcol;    // [rows] target class (global index) of a valid row, else -1
+    int64_t col_base;   // global class of the chunk's column 0
+    int64_t cols;       // classes in the chunk
+    int rows;           // rows in the batch chunk
+    const float* lse;   // [rows]
+    const float* wg;    // [rows] row weight folded into G
+    const float* wdb;   // [rows] weight of a row's G in the column sums, or NULL (1)
+    float* db_acc;      // [C] fp32, or NULL
+    void* g;            // [rows][ld_g] of g_dt: direct stores when no tensor map is given
+    int64_t ld_g;
+    int g_dt;
+  };
+
+  template <int NCHUNK, int GW, class Loader>
+  __device__ static __forceinline__ void run(const Params& p, int64_t row, int64_t col0, int64_t /*seg*/,
+                                             Loader&& load, EpiIO& io) {
+    static_assert(NCHUNK % GW == 0, "chunk groups");
+    constexpr int NG = NCHUNK / GW;
+    constexpr int W = GW * 32;
+    const bool row_ok = row < p.rows;
+    const float lse = row_ok ? p.lse[row] : 0.0f;
+    const float wg = row_ok ? p.wg[row] : 0.0f;
+    const float wdb = (row_ok && p.wdb != nullptr) ? p.wdb[row] : 1.0f;
+    const int64_t t = row_ok ? p.tcol[row] : -1;
+    const int64_t tloc = t - p.col_base - col0;
+    const int tl = (t >= 0 && tloc >= 0 && tloc < NCHUNK * 32) ? static_cast<int>(tloc) : -1;
+    const bool full = col0 + NCHUNK * 32 <= p.cols;
+    float* bs = (p.bias != nullptr && full) ? io.bias_s : nullptr;
+    if (bs != nullptr) {
+      __syncwarp();  // the previous tile's reads are done
+#pragma unroll
+      for (int k = 0; k < NCHUNK; ++k) bs[io.lane + 32 * k] = load_elem(p.bias, col0 + io.lane + 32 * k, p.bias_dt);
+      __syncwarp();
+    }
+    float v[W];
+#pragma unroll 1
+    for (int g = 0; g < NG; ++g) {
+      load(g, v);
+      if (bs != nullptr) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] += bs[W * g + i];
+      } else if (p.bias != nullptr) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+          const int64_t col = col0 + W * g + i;
+          v[i] += col < p.cols ? load_elem(p.bias, col, p.bias_dt) : 0.0f;
+        }
+      }
+      // the target column: wg (softmax_t - 1) from expm1, once per row
+      const bool t_here = tl >= W * g && tl < W * (g + 1);
+      float xt = 0.0f;
+      if (t_here) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) xt = (W * g + i == tl) ? v[i] : xt;
+      }
+      const float et = t_here ? wg * expm1f(xt - lse) : 0.0f;
+      if (full && row_ok) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] = wg * fast_exp2((v[i] - lse) * kLog2e);
+      } else {
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+          const float e = wg * fast_exp2((v[i] - lse) * kLog2e);
+          v[i] = (row_ok && col0 + W * g + i < p.cols) ? e : 0.0f;
+        }
+      }
+      if (t_here) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] = (W * g + i == tl) ? et : v[i];
+      }
+#pragma unroll
+      for (int c = 0; c < GW; ++c) {
+        float(&vc)[32] = *reinterpret_cast<float(*)[32]>(&v[32 * c]);
+        const int64_t cc = col0 + W * g + 32 * c;
+        if (io.tmap != nullptr) {
+          stage_store_16bit(io, vc, cc, p.g_dt);
+        } else if (row_ok) {
+          const int64_t off = row * p.ld_g + cc;
+          if (p.g_dt == LCE_F32)
+            store32_f32(static_cast<float*>(p.g) + off, vc);
+          else
+            store32_16bit(static_cast<uint16_t*>(p.g) + off, vc, p.g_dt);
+        }
+        if (p.db_acc != nullptr && cc < p.cols) {
+          // column sums of the fp32 values (before the 16-bit rounding of the store)
+          if (p.wdb != nullptr) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) vc[i] *= wdb;
+          }
+          const float sum = warp_column_sum32(vc, io.lane);
+          if (cc + io.lane < p.cols) atomicAdd(p.db_acc + p.col_base + cc + io.lane, sum);
+        }
+      }
+    }
+  }
+};
+
 // ---------------------------------------------------------------------------
 // Store epilogue for the dX = G W and dW = G^T X contractions (and the GEMM
-// tests). mode 0: out = acc; 1: acc32 = acc (first chunk of a dW
-// accumulated over chunks); 2: acc32 += acc; 3: out = acc32 + acc (last
-// chunk); 4: out += acc with fp32 atomics (one split of a split-K GEMM
+// tests). mode 0: out = acc; 1: acc32 = acc (first part of a gradient
+// accumulated over batch chunks (dW) or class chunks (dX)); 2: acc32 += acc;
+// 3: out = acc32 + acc (last part; like mode 0 it may store through the
+// output tensor map); 4: out += acc with fp32 atomics (one split of a split-K GEMM
 // into a zeroed fp32 out). out is fp32, bf16 or fp16 (out_dt); acc32 is
 // fp32 with the same leading dimension as out. Before any of this the
 // accumulator may be scaled per row (row_scale[row]) and by one device
@@ -255,20 +394,21 @@ struct EpiStore {
     const float* scalar_scale;  // device scalar or NULL
   };
 
-  __device__ static __forceinline__ void put(const Params& p, int64_t idx, float x) {
-    if (p.mode == 4) {  // split-K partial: add into the zeroed fp32 output
+  // mode: p.mode, except that mode 3 arrives here as 0 (its accumulator is
+  // already added)
+  __device__ static __forceinline__ void put(const Params& p, int mode, int64_t idx, float x) {
+    if (mode == 4) {  // split-K partial: add into the zeroed fp32 output
       atomicAdd(static_cast<float*>(p.out) + idx, x);
       return;
     }
-    if (p.mode == 1) {
+    if (mode == 1) {
       p.acc32[idx] = x;
       return;
     }
-    if (p.mode == 2) {
+    if (mode == 2) {
       p.acc32[idx] += x;
       return;
     }
-    if (p.mode == 3) x += p.acc32[idx];
     store_elem(p.out, idx, x, p.out_dt);
   }
 
@@ -294,41 +434,59 @@ struct EpiStore {
       for (int c = 0; c < GW; ++c) {
         float(&v)[32] = *reinterpret_cast<float(*)[32]>(&vg[32 * c]);
         const int64_t cb = col0 + W * g + 32 * c;
-        if (io.tmap != nullptr) {  // 16-bit, mode 0 (the host only sets tmap then)
+        const int64_t base = row * p.ldo + cb;
+        const bool vec = p.vec_ok && cb + 32 <= p.cols;
+        if (p.mode == 3 && row_ok) {  // last part of an accumulation: add the fp32 sum so far
+          if (vec) {
+            const float4* a = reinterpret_cast<const float4*>(p.acc32 + base);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 x = a[q];
+              v[4 * q] += x.x;
+              v[4 * q + 1] += x.y;
+              v[4 * q + 2] += x.z;
+              v[4 * q + 3] += x.w;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (cb + i < p.cols) v[i] += p.acc32[base + i];
+          }
+        }
+        const int mode = p.mode == 3 ? 0 : p.mode;
+        if (io.tmap != nullptr) {  // 16-bit, mode 0 or 3 (the host only sets tmap then)
           stage_store_16bit(io, v, cb, p.out_dt);
           continue;
         }
         if (!row_ok) continue;
-        const int64_t base = row * p.ldo + cb;
-        if (p.vec_ok && cb + 32 <= p.cols && p.mode == 4) {  // split-K partial: 8 vector reductions
+        if (vec && mode == 4) {  // split-K partial: 8 vector reductions
           float* o = static_cast<float*>(p.out) + base;
 #pragma unroll
           for (int q = 0; q < 8; ++q) red_add_v4(o + 4 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           continue;
         }
-        if (p.vec_ok && cb + 32 <= p.cols && p.mode != 4) {
-          if (p.mode == 0 && p.out_dt != LCE_F32) {
+        if (vec) {
+          if (mode == 0 && p.out_dt != LCE_F32) {
             store32_16bit(static_cast<uint16_t*>(p.out) + base, v, p.out_dt);
             continue;
           }
-          if (p.mode == 0 || p.mode == 1) {
-            store32_f32((p.mode == 1 ? p.acc32 : static_cast<float*>(p.out)) + base, v);
+          if (mode == 0 || mode == 1) {
+            store32_f32((mode == 1 ? p.acc32 : static_cast<float*>(p.out)) + base, v);
             continue;
           }
-          if (p.mode == 2 || (p.mode == 3 && p.out_dt == LCE_F32)) {
+          if (mode == 2) {
             float4* a = reinterpret_cast<float4*>(p.acc32 + base);
-            float4* o = reinterpret_cast<float4*>((p.mode == 2 ? p.acc32 : static_cast<float*>(p.out)) + base);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               float4 x = a[q];
-              o[q] = make_float4(x.x + v[4 * q], x.y + v[4 * q + 1], x.z + v[4 * q + 2], x.w + v[4 * q + 3]);
+              a[q] = make_float4(x.x + v[4 * q], x.y + v[4 * q + 1], x.z + v[4 * q + 2], x.w + v[4 * q + 3]);
             }
             continue;
           }
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          if (cb + i < p.cols) put(p, base + i, v[i]);
+          if (cb + i < p.cols) put(p, mode, base + i, v[i]);
         }
       }
     }

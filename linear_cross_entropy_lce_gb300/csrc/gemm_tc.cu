@@ -170,6 +170,17 @@ cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, con
   return launch_tc<false, false, EpiLse>(tmX, tmW, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s);
 }
 
+// recomputed logits of one class chunk with the gradient epilogue: the
+// same operands and tile order as the logits GEMM
+cudaError_t launch_tc_grad(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
+                           int K, int* status, const EpiGrad::Params& ep, bool pair, cudaStream_t s, bool f16) {
+  if (f16)
+    return launch_tc2<false, false, EpiGrad, true>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_RECOMPUTE_TC, s);
+  if (pair)
+    return launch_tc2<false, false, EpiGrad>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_RECOMPUTE_TC, s);
+  return launch_tc<false, false, EpiGrad>(tmX, tmW, M, N, K, 1, status, ep, K_GEMM_RECOMPUTE_TC, s);
+}
+
 cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M,
                             int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s,
                             bool f16, const SideGrad* side) {

@@ -35,6 +35,8 @@ enum KernelId {
   K_GEMM_DW_TX,
   K_SPLIT_TF32,
   K_SCALE_GRADS,
+  K_GEMM_RECOMPUTE_TC,
+  K_BACKWARD_ROWS,
   K_NUM_IDS
 };
 const char* kernel_id_name(int id);
@@ -68,6 +70,11 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
 cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
                              int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s,
                              const SideGrad* side = nullptr, bool f16 = false);
+// The logits GEMM of one class chunk again, with the gradient epilogue
+// (EpiGrad): tmW covers the chunk's rows of W; tmOut (pair kernel; NULL =
+// direct stores) is the store map of the chunk's G buffer.
+cudaError_t launch_tc_grad(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
+                           int K, int* status, const EpiGrad::Params& ep, bool pair, cudaStream_t s, bool f16);
 // side (TC_DX on the pair kernel only): G formation run in the GEMM's idle
 // warps, in the dynamic form of SideGrad.
 cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M,
@@ -123,8 +130,12 @@ cudaError_t launch_simt_store(int op, const float* A, const float* B, int64_t ld
                               int64_t N, int64_t K, const EpiStore::Params& ep, cudaStream_t s);
 
 // ---- row kernels (rowops.cu)
+// Valid-target count, class-weight sum, target-range check and the mean's
+// denominator (given_denom: NULL or a device fp32 scalar that replaces it);
+// out_denom (optional, device fp32) receives the denominator. The header
+// must be zeroed before.
 cudaError_t launch_prep(const int64_t* target, int64_t N, int64_t C, int64_t ignore_index, const float* cw,
-                        WsHeader* hdr, cudaStream_t s);
+                        const float* given_denom, WsHeader* hdr, cudaStream_t s, float* out_denom = nullptr);
 struct CombineArgs {
   float2* partial;  // [nseg][ld]; overwritten: .x = w_n exp(m - lse) when backward
   int64_t ld;
@@ -145,8 +156,29 @@ struct CombineArgs {
   // fp16 backward: scales and G at the target leave out w_n, which goes to
   // wrow[r] instead (NULL otherwise)
   float* wrow;
+  // backward: scales are written for segments < nseg_store only (the
+  // classes whose P~ the forward stored)
+  int nseg_store;
+  // backward with classes recomputed later (NULL otherwise): the row's lse
+  // and the weight folded into G (w_n, or 1 / 0 with wrow), [rows]
+  float* lse_rows;
+  float* w_rows;
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+// Per-row inputs of a backward whose row lse is given (no forward sweep):
+// tcol[r] = target (global class) of a valid row, else -1; w_rows[r] = the
+// weight folded into G (w_n, or with wrow: 1 on valid rows, 0 otherwise,
+// and wrow[r] = w_n), for chunk rows r < rows of global row row0 + r.
+struct BackwardRowsArgs {
+  const int64_t* target;  // global
+  int64_t row0, rows, C, ignore_index;
+  RowWeight rw;
+  const WsHeader* hdr;
+  int* tcol;
+  float* w_rows;
+  float* wrow;  // NULL unless fp16
+};
+cudaError_t launch_backward_rows(const BackwardRowsArgs& a, cudaStream_t s);
 struct GradArgs {
   void* L;  // [rows][ld] P~ in, G out
   int64_t ld;

@@ -13,9 +13,12 @@ namespace {
 // n_valid = #rows whose target is a class index; a target that is neither
 // ignore_index nor in [0, C) sets the target-range status bit
 // (linear_cross_entropy.py: the _mask / corrected_target / neg_weight_target
-// d = sum of unmasked weights).
+// d = sum of unmasked weights). The last block to finish sets the mean's
+// denominator: the caller's given value, else the class-weight sum or
+// n_valid. out_denom (optional) receives it as fp32.
 __global__ void prep_kernel(const int64_t* __restrict__ target, int64_t N, int64_t C, int64_t ign,
-                            const float* __restrict__ cw, WsHeader* hdr) {
+                            const float* __restrict__ cw, const float* __restrict__ given_denom, WsHeader* hdr,
+                            float* out_denom) {
   __shared__ int s_cnt[32];
   __shared__ int s_bad[32];
   __shared__ double s_ws[32];
@@ -61,6 +64,19 @@ __global__ void prep_kernel(const int64_t* __restrict__ target, int64_t N, int64
       if (cnt) atomicAdd(&hdr->n_valid, cnt);
       if (bad) atomicOr(&hdr->status, kStatusTargetRange);
       if (cw != nullptr && ws != 0.0) atomicAdd(&hdr->weight_sum, ws);
+      __threadfence();  // this block's sums are visible before it counts itself done
+      if (atomicAdd(&hdr->prep_done, 1) == static_cast<int>(gridDim.x) - 1) {
+        __threadfence();
+        double d;
+        if (given_denom != nullptr)
+          d = static_cast<double>(*given_denom);
+        else if (cw != nullptr)
+          d = atomicAdd(&hdr->weight_sum, 0.0);
+        else
+          d = static_cast<double>(atomicAdd(&hdr->n_valid, 0));
+        hdr->denom = d;
+        if (out_denom != nullptr) *out_denom = static_cast<float>(d);
+      }
     }
   }
 }
@@ -158,8 +174,8 @@ __global__ void loss_finalize_kernel(const float* __restrict__ loss_rows, int64_
       if (reduction == LCE_RED_SUM) {
         loss_out[0] = static_cast<float>(acc);
       } else {
-        // mean over the valid rows, or over their class weights
-        const double d = weighted ? hdr->weight_sum : static_cast<double>(hdr->n_valid);
+        // mean: over the valid rows, their class weights, or the given denominator
+        const double d = hdr->denom;
         loss_out[0] = d == 0.0 ? __int_as_float(0x7fc00000) : static_cast<float>(acc / d);
       }
     }
@@ -176,12 +192,13 @@ __global__ void db_finalize_kernel(const float* __restrict__ db_acc, T* db, int6
 }  // namespace
 
 cudaError_t launch_prep(const int64_t* target, int64_t N, int64_t C, int64_t ignore_index, const float* cw,
-                        WsHeader* hdr, cudaStream_t s) {
-  if (N == 0) return cudaSuccess;
+                        const float* given_denom, WsHeader* hdr, cudaStream_t s, float* out_denom) {
   int64_t blocks = (N + 1023) / 1024;
   if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
+  if (blocks < 1) blocks = 1;  // no rows: one block still sets the denominator
   prof_before(K_PREP, s, 8.0 * N);
-  prep_kernel<<<static_cast<unsigned>(blocks), 1024, 0, s>>>(target, N, C, ignore_index, cw, hdr);
+  prep_kernel<<<static_cast<unsigned>(blocks), 1024, 0, s>>>(target, N, C, ignore_index, cw, given_denom, hdr,
+                                                              out_denom);
   cudaError_t e = cudaGetLastError();
   prof_after(K_PREP, s);
   return e;
@@ -254,6 +271,31 @@ cudaError_t launch_db_finalize(const float* db_acc, void* db, int64_t C, int dt,
     db_finalize_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, s>>>(db_acc, static_cast<float*>(db), C);
   cudaError_t e = cudaGetLastError();
   prof_after(K_DB_FINALIZE, s);
+  return e;
+}
+
+// Per-row weights and target columns of a backward given the row lse.
+__global__ void backward_rows_kernel(const BackwardRowsArgs a) {
+  for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < a.rows;
+       r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t g = a.row0 + r;
+    const int64_t t = a.target[g];
+    const bool valid = target_valid(t, a.ignore_index, a.C);
+    const float w = row_weight(a.rw, a.hdr, g, t, valid);
+    a.tcol[r] = valid ? static_cast<int>(t) : -1;
+    a.w_rows[r] = a.wrow != nullptr ? (valid ? 1.0f : 0.0f) : w;
+    if (a.wrow != nullptr) a.wrow[r] = w;
+  }
+}
+
+cudaError_t launch_backward_rows(const BackwardRowsArgs& a, cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  int64_t blocks = (a.rows + 255) / 256;
+  if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
+  prof_before(K_BACKWARD_ROWS, s, 24.0 * a.rows);
+  backward_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  prof_after(K_BACKWARD_ROWS, s);
   return e;
 }
 

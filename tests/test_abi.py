@@ -45,14 +45,18 @@ def test_status_strings(lib):
 def test_workspace_size(lib):
     ws = lce.lce_workspace_size
     a = ws(lce.LCE_OP_FORWARD_BACKWARD, 8192, 4096, 128256, lce.LCE_BF16, lce.LCE_RED_MEAN, lce.LCE_BF16)
-    # one chunk: [8192, 128256] bf16 buffer plus small per-row arrays
-    assert 8192 * 128256 * 2 <= a < 8192 * 128256 * 2 * 1.05
-    # at this shape chunking does not pay: 8 chunks need the fp32 [C, D] dW accumulator
+    # the default plan: a 1 GiB gradient buffer (half the classes of all
+    # rows), the fp32 [N, D] dX accumulator and small per-row arrays
+    assert 1 << 30 <= a < (1 << 30) + 8192 * 4096 * 4 + (64 << 20)
+    # every class stored: the whole [8192, 128256] bf16 buffer
+    full = ws(lce.LCE_OP_FORWARD_BACKWARD, 8192, 4096, 128256, lce.LCE_BF16, lce.LCE_RED_MEAN, lce.LCE_BF16, 8192)
+    assert 8192 * 128256 * 2 <= full < 8192 * 128256 * 2 * 1.05
+    # batch chunks with every class: 8 chunks need the fp32 [C, D] dW accumulator
     eight = ws(lce.LCE_OP_FORWARD_BACKWARD, 8192, 4096, 128256, lce.LCE_BF16, lce.LCE_RED_MEAN,
                lce.LCE_BF16, 1024)
     assert eight > a and eight >= 128256 * 4096 * 4
     # many rows, narrow head: chunks bound the memory
-    big = ws(lce.LCE_OP_FORWARD_BACKWARD, 65536, 1024, 32000, lce.LCE_BF16, lce.LCE_RED_MEAN, lce.LCE_BF16, 0)
+    big = ws(lce.LCE_OP_FORWARD_BACKWARD, 65536, 1024, 32000, lce.LCE_BF16, lce.LCE_RED_MEAN, lce.LCE_BF16, 65536)
     small = ws(lce.LCE_OP_FORWARD_BACKWARD, 65536, 1024, 32000, lce.LCE_BF16, lce.LCE_RED_MEAN,
                lce.LCE_BF16, 1024)
     assert small < big / 10

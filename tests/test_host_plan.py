@@ -10,7 +10,7 @@ import pytest
 import linear_cross_entropy_lce_gb300 as lce
 from linear_cross_entropy_lce_gb300 import _build
 
-NF = 28  # LCE_TEST_PLAN_FIELDS
+NF = 34  # LCE_TEST_PLAN_FIELDS
 I64 = ctypes.c_int64
 
 
@@ -25,6 +25,9 @@ def lib():
     L.lce_test_plan.restype = ctypes.c_int
     L.lce_workspace_size.argtypes = [ctypes.c_int, I64, I64, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, I64]
     L.lce_workspace_size.restype = ctypes.c_size_t
+    L.lce_workspace_size_for_buffer.argtypes = [ctypes.c_int, I64, I64, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_size_t]
+    L.lce_workspace_size_for_buffer.restype = ctypes.c_size_t
     return L
 
 
@@ -94,8 +97,15 @@ SHAPES = [
 ]
 
 
+GIB = 1 << 30
+
+
+def _esz(dtype):
+    return 4 if dtype == lce.LCE_F32 else 2
+
+
 @pytest.mark.parametrize("N,D,C,dtype", SHAPES)
-@pytest.mark.parametrize("op", [lce.LCE_OP_FORWARD, lce.LCE_OP_FORWARD_BACKWARD])
+@pytest.mark.parametrize("op", [lce.LCE_OP_FORWARD, lce.LCE_OP_FORWARD_BACKWARD, lce.LCE_OP_BACKWARD])
 def test_plan_regions_fit_and_do_not_overlap(lib, op, N, D, C, dtype):
     for grad_dtype in (dtype, lce.LCE_F32):
         ws = _ws(lib, op, N, D, C, dtype, grad_dtype)
@@ -103,45 +113,82 @@ def test_plan_regions_fit_and_do_not_overlap(lib, op, N, D, C, dtype):
         r, v = _plan(lib, op, N, D, C, dtype, grad_dtype, ws)
         assert r == NF
         Bc, nchunks, total, C_pad, nseg = v[:5]
-        offs = v[5:]
-        # the plan the calls choose for the queried size is the one it was sized for
+        offs = v[5:31]
+        Cb, Cs, nvc = v[31:34]
+        # the plan the calls choose for the queried size is the one it was sized for (or a faster one)
         assert total <= ws
         assert 1 <= Bc <= N and nchunks == -(-N // Bc)
-        assert Bc == N or (Bc % 128 == 0 and Bc & (Bc - 1) == 0)
+        assert Bc == N or Bc % 128 == 0
         assert C_pad >= C and C_pad % 128 == 0 and nseg >= 1
         # regions in order, 256-byte aligned, inside the total
         assert all(o % 256 == 0 for o in offs)
         assert offs == sorted(offs) and offs[0] > 0 and offs[-1] <= total
-        # the regions the pages' method needs have room for their arrays
-        off_cnt, off_loss, off_zt, off_tcol, off_gt, off_partial, off_L, off_dw = offs[:8]
-        assert off_zt - off_loss >= 4 * N               # per-row losses, fp32
-        assert off_L - off_partial >= 8 * nseg * Bc     # (max, sum-exp) pairs of a chunk
-        if op == lce.LCE_OP_FORWARD_BACKWARD:
-            esz = 4 if dtype == lce.LCE_F32 else 2
-            assert off_dw - off_L >= Bc * C_pad * esz  # the chunk's P~ / G buffer
+        off_cnt, off_loss, off_zt, off_tcol, off_gt, off_partial, off_L, off_dw, off_db = offs[:9]
+        off_lse, off_wv, off_dx = offs[12:15]
+        backward = op != lce.LCE_OP_FORWARD
+        given_lse = op == lce.LCE_OP_BACKWARD and dtype != lce.LCE_F32
+        if not given_lse:
+            assert off_zt - off_loss >= 4 * N               # per-row losses, fp32
+            assert off_L - off_partial >= 8 * nseg * Bc     # (max, sum-exp) pairs of a chunk
+        if backward:
+            # the gradient buffer, within the default budget
+            assert off_dw - off_L >= Bc * Cb * _esz(dtype)
+            assert Bc * Cb * _esz(dtype) <= GIB or (dtype == lce.LCE_F32)
+            # every class is covered: stored [0, Cs), then nvc chunks of Cb
+            assert Cs + nvc * Cb >= C and (nvc == 0 or Cs + (nvc - 1) * Cb < C)
+            assert Cs == (0 if given_lse else Cb)
+            if nvc:  # recomputed classes keep the rows' lse and weights
+                assert off_wv - off_lse >= 4 * Bc and off_dx - off_wv >= 4 * Bc
         else:
             assert off_dw == off_L                      # no P~ buffer in the forward
 
 
-def test_plan_smaller_workspace_gives_smaller_chunks(lib):
+@pytest.mark.parametrize("N,D,C,Bc,Cb,nvc", [
+    (8192, 4096, 128256, 8192, 65536, 1),     # the LLM head: half the vocabulary stored, the rest recomputed
+    (16384, 4096, 131072, 16384, 32768, 3),   # the large head
+    (1 << 20, 1024, 32000, 524288, 1024, 31),  # so many rows that 1024 classes of all rows exceed 1 GiB
+    (2048, 512, 8192, 2048, 8192, 0),          # everything fits: nothing recomputed
+])
+def test_default_plan_bounds_the_gradient_buffer(lib, N, D, C, Bc, Cb, nvc):
+    dt = lce.LCE_BF16
+    ws = _ws(lib, lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, dt)
+    r, v = _plan(lib, lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, dt, ws)
+    assert r == NF
+    assert (v[0], v[31], v[33]) == (Bc, Cb, nvc)
+    assert v[0] * v[31] * 2 <= GIB
+    # no [C, D] fp32 scratch unless the rows are split into batch chunks
+    assert (v[13] - v[12] > 0) == (v[1] > 1)
+    # lce_workspace_size_for_buffer with 0 is the default; a huge budget stores every class
+    assert lib.lce_workspace_size_for_buffer(lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, lce.LCE_RED_MEAN, dt, 0) == ws
+    big = lib.lce_workspace_size_for_buffer(lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, lce.LCE_RED_MEAN, dt,
+                                            ctypes.c_size_t(-1).value)
+    r, v = _plan(lib, lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, dt, big)
+    assert v[33] == 0 and v[31] == v[3]
+
+
+def test_plan_smaller_workspace_recomputes_more(lib):
+    """Shrinking the workspace first narrows the stored classes (more of them
+    recomputed), then splits the rows; every plan fits what it was given."""
     op, N, D, C, dt = lce.LCE_OP_FORWARD_BACKWARD, 65536, 1024, 32000, lce.LCE_BF16
-    full = _ws(lib, op, N, D, C, dt, dt)
-    r, v = _plan(lib, op, N, D, C, dt, dt, full)
-    prev_bc = v[0]
-    for chunk in (8192, 2048, 512, 128):
-        ws = _ws(lib, op, N, D, C, dt, dt, chunk)
+    prev = None
+    for mib in (8192, 2048, 1024, 512, 256, 128, 64):
+        ws = lib.lce_workspace_size_for_buffer(op, N, D, C, dt, lce.LCE_RED_MEAN, dt, mib << 20)
         r, v = _plan(lib, op, N, D, C, dt, dt, ws)
-        assert r == NF and v[2] <= ws and v[0] <= min(prev_bc, chunk)
-        prev_bc = v[0]
-    # below the smallest chunk's plan nothing fits
+        assert r == NF and v[2] <= ws
+        Bc, Cb = v[0], v[31]
+        if prev is not None:
+            assert (Bc, Cb) <= prev or Bc < prev[0]
+        prev = (Bc, Cb)
+    # below the smallest plan nothing fits
     r, _ = _plan(lib, op, N, D, C, dt, dt, 4096)
     assert r == 0
 
 
-def test_plan_arguments(lib):
-    out = (I64 * NF)()
-    assert lib.lce_test_plan(7, 10, 8, 8, lce.LCE_BF16, lce.LCE_BF16, 1, 1, 1, 1 << 30, out, NF) == -1
-    assert lib.lce_test_plan(lce.LCE_OP_FORWARD, 10, 0, 8, lce.LCE_BF16, lce.LCE_BF16, 1, 1, 1, 1 << 30,
-                             out, NF) == -1
-    assert lib.lce_test_plan(lce.LCE_OP_FORWARD, 10, 8, 8, lce.LCE_BF16, lce.LCE_BF16, 1, 1, 1, 1 << 30,
-                             out, NF - 1) == -1
+def test_chunk_rows_plan(lib):
+    """chunk_rows sizes batch chunks with every class stored; chunk_rows >= N
+    stores the whole [N, C] buffer."""
+    op, N, D, C, dt = lce.LCE_OP_FORWARD_BACKWARD, 8192, 4096, 128256, lce.LCE_BF16
+    ws = _ws(lib, op, N, D, C, dt, dt, N)
+    r, v = _plan(lib, op, N, D, C, dt, dt, ws)
+    assert (v[0], v[31], v[33]) == (N, v[3], 0)
+    assert ws >= N * 128256 * 2  # the whole [N, C] buffer (2.1 GB)

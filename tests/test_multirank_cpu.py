@@ -31,7 +31,7 @@ def _worker(rank, world, port, out):
 def test_step_time_is_max_over_ranks():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     assert out[0] == out[1] == 15.0
