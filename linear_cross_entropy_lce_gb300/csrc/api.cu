@@ -16,8 +16,9 @@
 // runs over up to 4 row slabs of growing size, and combine + grad of slab k run in the idle warps
 // of the GEMM that follows it (slab k+1's logits GEMM, or the dX GEMM for
 // the last slab, whose producer waits for those rows), so no combine or
-// grad kernel is launched. fp32 inputs add the TF32 hi / lo splits of W,
-// X_c and G before the GEMMs that read them (3xTF32 engine).
+// grad kernel is launched. fp32 inputs add the TF32 hi / lo splits of W
+// and X_c before the GEMMs that read them, and form G together with its
+// split (3xTF32 engine).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -100,7 +101,7 @@ const char* kNames[K_NUM_IDS] = {
     "gemm_dx_simt",  "gemm_dw_simt",   "lse_combine", "grad_logits",     "loss_finalize",
     "db_finalize",   "ce_resident",    "ce_stream",   "gemm_test",       "row_scale",
     "gemm_logits_3xtf32", "gemm_dx_3xtf32", "gemm_dw_3xtf32", "split_tf32", "scale_grads",
-    "gemm_recompute_tc", "backward_rows"};
+    "gemm_recompute_tc", "backward_rows", "grad_split_tf32"};
 }  // namespace
 
 const char* kernel_id_name(int id) { return (id >= 0 && id < K_NUM_IDS) ? kNames[id] : "?"; }
@@ -543,7 +544,7 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
       LCE_TRY(launch_split_tf32(sa, s));
     }
     const bool slabbed = sweep && p.tc && pair && backward && rows >= 1024;
-    GradArgs ga_last;
+    GradArgs ga_last, ga_tx;
     CombineArgs ca_last;  // the last slab's merge, deferred into the dX GEMM's idle warps
     bool have_last = false;
     int64_t last_row0 = 0, last_si = 0;
@@ -654,6 +655,8 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
           have_last = true;
           last_row0 = so;
           last_si = si;
+        } else if (p.tf32 && (want_dx || want_dw)) {
+          ga_tx = ga;  // formed together with its TF32 split below
         } else {
           if (nseg_store > 0) LCE_TRY(launch_grad_logits(ga, dtype, s));
           have_prev = false;
@@ -677,7 +680,7 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
       lse_rows = lse_in + row0;
     }
     if (!backward) continue;
-    if (p.tf32 && (want_dx || want_dw)) {  // TF32 parts of G (hi over G itself) and of G^T
+    if (p.tf32 && (want_dx || want_dw)) {  // G formed from P~ and split: hi over P~ itself, lo, and G^T's parts
       SplitArgs sa;
       sa.src = static_cast<const float*>(Lbuf);
       sa.rows = rows;
@@ -689,7 +692,7 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
       sa.hiT = want_dw ? wsf(p.off_gth) : nullptr;
       sa.loT = want_dw ? wsf(p.off_gtl) : nullptr;
       sa.ldt = p.ldB;
-      LCE_TRY(launch_split_tf32(sa, s));
+      LCE_TRY(launch_grad_split_tf32(ga_tx, sa, s));
     }
     // dX is the sum over the class parts (the stored classes, then each
     // recomputed chunk); with several parts a 16-bit dX is summed in fp32

@@ -1,6 +1,7 @@
 // gemm_tf32.cu -- fp32 inputs on the tensor cores: the TF32 hi / lo split
 // and the host launchers of the 3xTF32 CTA-pair GEMM.
 #include <cstdlib>
+#include <cstring>
 
 #include "internal.h"
 #include "tc2x3_gemm.cuh"
@@ -28,10 +29,22 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
 // pitches and base pointers allow it; the transposed outputs go through
 // shared memory and are written as float4 runs along their rows, so every
 // global access is coalesced. Scalar code covers ragged tile edges.
+//
+// GRAD: src is the chunk buffer holding P~ of the fp32 path, and the value
+// split is G itself, formed on the way in: G[r, j] = P~[r, j] * scale of
+// (j's segment, r), or gt[r] at the row's target column (the same G as the
+// stand-alone G formation); with g.db_acc the tile's column sums of G are
+// added to it (one atomic per column per tile). G is never written in fp32:
+// its hi part goes over P~ in place (a.hi == a.src), its lo part and the
+// transposed parts to their buffers, so the G formation and the split read
+// the buffer once.
 constexpr int SP_T = 64;
-__global__ void __launch_bounds__(256) split_tf32_kernel(const SplitArgs a, int vec_in, int vec_t) {
+template <bool GRAD>
+__global__ void __launch_bounds__(256) split_tf32_kernel(const SplitArgs a, const GradArgs g, int vec_in,
+                                                         int vec_t) {
   __shared__ float th[SP_T][SP_T + 1];
   __shared__ float tl[SP_T][SP_T + 1];
+  __shared__ float cs[GRAD ? 16 : 1][SP_T];
   const int t = threadIdx.x;
   const int64_t tiles_c = (a.cols + SP_T - 1) / SP_T;
   const int64_t ntiles = ((a.rows + SP_T - 1) / SP_T) * tiles_c;
@@ -41,6 +54,8 @@ __global__ void __launch_bounds__(256) split_tf32_kernel(const SplitArgs a, int 
     const int64_t r0 = (tile / tiles_c) * SP_T;
     const int64_t c0 = (tile % tiles_c) * SP_T;
     const bool full_c = vec_in && c0 + cq + 4 <= a.cols;
+    const int seg = GRAD ? static_cast<int>((c0 + cq) / g.segw) : 0;  // the float4 lies in one segment
+    float colsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int lr = rq + 16 * k;
@@ -57,6 +72,16 @@ __global__ void __launch_bounds__(256) split_tf32_kernel(const SplitArgs a, int 
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             if (c0 + cq + e < a.cols) x[e] = a.src[r * a.lds + c0 + cq + e];
+        }
+        if (GRAD) {
+          const float sc = g.scale[seg * g.sld + r].x;
+          const int64_t tc = g.tcol[r];
+          const float gtv = g.gt[r];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[e] = (c0 + cq + e == tc) ? gtv : x[e] * sc;
+            colsum[e] += x[e];
+          }
         }
       }
       float h[4], l[4];
@@ -84,8 +109,18 @@ __global__ void __launch_bounds__(256) split_tf32_kernel(const SplitArgs a, int 
         }
       }
     }
+    if (GRAD && g.db_acc != nullptr) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cs[rq][cq + e] = colsum[e];
+    }
+    if (a.hiT != nullptr || (GRAD && g.db_acc != nullptr)) __syncthreads();
+    if (GRAD && g.db_acc != nullptr && t < SP_T) {
+      float sum = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) sum += cs[q][t];
+      if (c0 + t < g.C) atomicAdd(g.db_acc + c0 + t, sum);
+    }
     if (a.hiT != nullptr) {
-      __syncthreads();
       // transposed: output row cc (a column of src) holds the tile's 64 rows
       const int j = (t & 15) * 4;  // first src row of this thread's float4
 #pragma unroll
@@ -169,7 +204,9 @@ bool f32_tensor_default() {
   return v == 1;
 }
 
-cudaError_t launch_split_tf32(const SplitArgs& a, cudaStream_t s) {
+namespace {
+template <bool GRAD>
+cudaError_t launch_split(const SplitArgs& a, const GradArgs& g, int kid, double bytes, cudaStream_t s) {
   if (a.rows == 0 || a.cols == 0) return cudaSuccess;
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   const int vec_in = (a.lds % 4 == 0) && al16(a.src) &&
@@ -178,12 +215,25 @@ cudaError_t launch_split_tf32(const SplitArgs& a, cudaStream_t s) {
   const int64_t ntiles = ((a.rows + SP_T - 1) / SP_T) * ((a.cols + SP_T - 1) / SP_T);
   const int64_t cap = static_cast<int64_t>(num_sms()) * 6;
   const int grid = static_cast<int>(ntiles < cap ? ntiles : cap);
-  const double outs = (a.hi != nullptr ? 2.0 : 0.0) + (a.hiT != nullptr ? 2.0 : 0.0);
-  prof_before(K_SPLIT_TF32, s, 4.0 * (1.0 + outs) * a.rows * static_cast<double>(a.cols));
-  split_tf32_kernel<<<grid, 256, 0, s>>>(a, vec_in, vec_t);
+  prof_before(kid, s, bytes);
+  split_tf32_kernel<GRAD><<<grid, 256, 0, s>>>(a, g, vec_in, vec_t);
   cudaError_t e = cudaGetLastError();
-  prof_after(K_SPLIT_TF32, s);
+  prof_after(kid, s);
   return e;
+}
+}  // namespace
+
+cudaError_t launch_split_tf32(const SplitArgs& a, cudaStream_t s) {
+  const double outs = (a.hi != nullptr ? 2.0 : 0.0) + (a.hiT != nullptr ? 2.0 : 0.0);
+  GradArgs none;
+  memset(&none, 0, sizeof(none));
+  return launch_split<false>(a, none, K_SPLIT_TF32, 4.0 * (1.0 + outs) * a.rows * static_cast<double>(a.cols), s);
+}
+
+cudaError_t launch_grad_split_tf32(const GradArgs& g, const SplitArgs& a, cudaStream_t s) {
+  if (g.segw % SP_T != 0) return cudaErrorInvalidValue;  // a tile's float4 must lie in one segment
+  const double outs = (a.hi != nullptr ? 2.0 : 0.0) + (a.hiT != nullptr ? 2.0 : 0.0);
+  return launch_split<true>(a, g, K_GRAD_SPLIT_TF32, 4.0 * (1.0 + outs) * a.rows * static_cast<double>(a.cols), s);
 }
 
 cudaError_t launch_tx_logits(const TxOperands& o, int M, int N, int K, int* status, const EpiLse::Params& ep,

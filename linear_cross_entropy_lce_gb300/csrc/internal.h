@@ -37,6 +37,7 @@ enum KernelId {
   K_SCALE_GRADS,
   K_GEMM_RECOMPUTE_TC,
   K_BACKWARD_ROWS,
+  K_GRAD_SPLIT_TF32,
   K_NUM_IDS
 };
 const char* kernel_id_name(int id);
@@ -118,6 +119,11 @@ struct SplitArgs {
   int64_t ldt;
 };
 cudaError_t launch_split_tf32(const SplitArgs& a, cudaStream_t s);
+struct GradArgs;
+// The G formation of the fp32 tensor-core path fused with G's split: forms
+// G from P~ in a.src (= g.L) exactly as launch_grad_logits would (bias
+// gradient included) and writes only its TF32 parts (a.hi may be a.src).
+cudaError_t launch_grad_split_tf32(const GradArgs& g, const SplitArgs& a, cudaStream_t s);
 // Whether fp32 inputs take the 3xTF32 tensor-core path (default) or the
 // SIMT fp32 GEMM (LCE_F32_SIMT=1).
 bool f32_tensor_default();
