@@ -38,23 +38,53 @@ METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor
 
 # DRAM bytes (read + write) per launch of a kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum): {(workload, kernel):
-# (bytes, commit of the capture, hash of the kernel sources at the capture)}.
-# The bench reports an entry only while the kernel sources hash the same, so
-# a capture never outlives a change of the kernels it measured.
-MEASURED_TRAFFIC = {}
+# (bytes, commit of the capture, hash of the kernel's sources at the
+# capture)}. The bench reports an entry only while those sources hash the
+# same, so a capture never outlives a change of the kernel it measured.
+MEASURED_TRAFFIC = {
+    # full-size one-pass captures (gpu__time_duration.sum, dram__bytes_read.sum,
+    # dram__bytes_write.sum) of one step after one warm-up step
+    ("bf16_llm_head", "gemm_logits_tc"): (2225356928, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 4 launches
+    ("bf16_llm_head", "gemm_dx_tc"): (9608986240, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 2 launches
+    ("bf16_llm_head", "gemm_dw_tc"): (6947936512, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 2 launches
+    ("bf16_llm_head", "gemm_recompute_tc"): (4420268288, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 1 launches
+    ("bf16_large_head", "gemm_logits_tc"): (24091656448, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 1 launches
+    ("bf16_large_head", "gemm_recompute_tc"): (4909548480, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 4 launches
+    ("bf16_large_head", "gemm_dx_tc"): (9637890944, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 4 launches
+    ("bf16_large_head", "gemm_dw_tc"): (9054174976, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 4 launches
+    ("ce_logits_fp32", "ce_resident"): (17418256896, "0c74ba4", "7b5ff6e46f00e1da"),
+    ("fp32_mid", "gemm_logits_3xtf32"): (52743680, "0c74ba4", "20175e992ef81d97"),
+    ("fp32_mid", "gemm_dx_3xtf32"): (178551040, "0c74ba4", "20175e992ef81d97"),
+    ("fp32_mid", "gemm_dw_3xtf32"): (142775552, "0c74ba4", "20175e992ef81d97"),
+}
 
 CSRC = os.path.join(ROOT, "linear_cross_entropy_lce_gb300", "csrc")
+# the sources each kernel is built from
+_GEMM_SOURCES = ("common.cuh", "ptx.cuh", "epilogues.cuh", "tc2_gemm.cuh", "combine_unit.cuh", "grad_unit.cuh",
+                 "gemm_tc.cu", "internal.h")
+KERNEL_SOURCES = {
+    "gemm_logits_tc": _GEMM_SOURCES, "gemm_recompute_tc": _GEMM_SOURCES, "gemm_dx_tc": _GEMM_SOURCES,
+    "gemm_dw_tc": _GEMM_SOURCES,
+    "ce_resident": ("common.cuh", "ptx.cuh", "ce_logits.cu", "internal.h"),
+    "ce_stream": ("common.cuh", "ptx.cuh", "ce_logits.cu", "internal.h"),
+    "gemm_logits_3xtf32": ("common.cuh", "ptx.cuh", "epilogues.cuh", "tc2x3_gemm.cuh", "gemm_tf32.cu", "internal.h"),
+    "gemm_dx_3xtf32": ("common.cuh", "ptx.cuh", "epilogues.cuh", "tc2x3_gemm.cuh", "gemm_tf32.cu", "internal.h"),
+    "gemm_dw_3xtf32": ("common.cuh", "ptx.cuh", "epilogues.cuh", "tc2x3_gemm.cuh", "gemm_tf32.cu", "internal.h"),
+}
 
 
-def kernel_sources_hash():
-    """sha256 (16 hex digits) over the CUDA sources of the library."""
+def kernel_sources_hash(kernel):
+    """sha256 (16 hex digits) over the CUDA sources the kernel is built from
+    (every source file for a kernel not in KERNEL_SOURCES)."""
     import hashlib
 
+    files = KERNEL_SOURCES.get(kernel)
+    if files is None:
+        files = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h")))
     h = hashlib.sha256()
-    for fn in sorted(os.listdir(CSRC)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(CSRC, fn), "rb") as f:
-                h.update(fn.encode() + b"\0" + f.read())
+    for fn in sorted(files):
+        with open(os.path.join(CSRC, fn), "rb") as f:
+            h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -64,8 +94,8 @@ def measured_traffic(workload, kernel):
     if e is None:
         return None, "no ncu capture recorded for this kernel and workload"
     nbytes, commit, src = e
-    if src != kernel_sources_hash():
-        return None, f"stale: captured at {commit}, kernel sources changed since"
+    if src != kernel_sources_hash(kernel):
+        return None, f"stale: captured at {commit}, the kernel's sources changed since"
     return nbytes, f"ncu capture at {commit}"
 
 
@@ -668,9 +698,14 @@ def main():
     ap.add_argument("--rows", type=int, default=0, help="override N (profiling a smaller case)")
     ap.add_argument("--dim", type=int, default=0, help="override D")
     ap.add_argument("--classes", type=int, default=0, help="override C (or V)")
+    ap.add_argument("--print-source-hashes", action="store_true",
+                    help="print the source hash of every kernel in KERNEL_SOURCES and exit")
     ap.add_argument("--buffer-mib", type=int, default=None,
                     help="gradient-buffer budget of the workspace plan (default: the library's 1 GiB)")
     args = ap.parse_args()
+    if args.print_source_hashes:
+        print(json.dumps({k: kernel_sources_hash(k) for k in KERNEL_SOURCES}))
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -1,7 +1,10 @@
-"""Full-size bf16 heads, in the launch configuration the benchmark times,
-against the float64 oracle: a full blockwise pass gives every row's lse,
-the loss and db; dX is checked on sampled rows and dW on sampled classes
-(the most frequent targets, classes no row targets, and random ones)."""
+"""Full-size bf16 heads, in the launch configuration the benchmark times
+(the default workspace plan, whose gradient buffer is bounded by 1 GiB, so
+part or all of the classes are recomputed), against the float64 oracle: a
+full blockwise pass gives every row's lse, the loss and db; dX is checked
+on sampled rows and dW on sampled classes (the most frequent targets,
+classes no row targets, and random ones, in stored and recomputed class
+chunks alike)."""
 
 import numpy as np
 import pytest
@@ -31,8 +34,16 @@ def test_full_size_head(cuda_lib, name):
     inp = make_workload(name, "cuda")
     X, W, b, t = inp["X"], inp["W"], inp["b"], inp["target"]
     g = inp["grad_out"]
-    loss_f = cuda_lib.lce_forward(X, W, b, t, w.reduction, -100)
-    loss, dX, dW, db = cuda_lib.lce_forward_backward(X, W, b, t, w.reduction, -100, g)
+    if w.reduction == "none":
+        # the benchmark's launch configuration for reduction none: the
+        # forward (loss and lse), then the backward from that lse (every
+        # class recomputed under the default 1 GiB buffer)
+        loss_f, lse = cuda_lib.lce_forward(X, W, b, t, w.reduction, -100, want_lse=True)
+        dX, dW, db = cuda_lib.lce_backward(X, W, b, t, lse, w.reduction, -100, g)
+        loss = loss_f
+    else:
+        loss_f = cuda_lib.lce_forward(X, W, b, t, w.reduction, -100)
+        loss, dX, dW, db = cuda_lib.lce_forward_backward(X, W, b, t, w.reduction, -100, g)
     torch.cuda.synchronize()
     # exact host copies of the bf16 inputs (float32 holds every bf16 value)
     Xh = X.float().cpu().numpy()
@@ -58,3 +69,27 @@ def test_full_size_head(cuda_lib, name):
     if b is not None:
         assert rel_max(db.double().cpu().numpy(), st["db"]) < tol["grad"]
     assert torch.isfinite(dX).all() and torch.isfinite(dW).all()
+
+
+@pytest.mark.timeout(3600)
+def test_full_size_llm_head_whole_buffer(cuda_lib):
+    """The LLM head with every class stored (no recomputation): the plan
+    the benchmark reports beside the bounded one."""
+    w = WORKLOADS["bf16_llm_head"]
+    inp = make_workload("bf16_llm_head", "cuda")
+    X, W, t = inp["X"], inp["W"], inp["target"]
+    loss, dX, dW, _ = cuda_lib.lce_forward_backward(X, W, None, t, w.reduction, -100, chunk_rows=w.N)
+    torch.cuda.synchronize()
+    Xh = X.float().cpu().numpy()
+    Wh = W.float().cpu().numpy()
+    th = t.cpu().numpy()
+    st = O.forward_stats(Xh, Wh, None, th, w.reduction, row_block=512)
+    tol = TOL[torch.bfloat16]
+    assert rel_scalar(loss.item(), st["loss"]) < tol["loss"]
+    rng = np.random.default_rng(2)
+    rows = np.sort(rng.choice(w.N, 128, replace=False))
+    _, dXr = O.grad_rows(Xh, Wh, None, th, st["lse"], st["w"], rows)
+    assert rel_max(dX[torch.from_numpy(rows).cuda()].double().cpu().numpy(), dXr) < tol["grad"]
+    cls = _sample_classes(th, w.C, rng, k=128)
+    dWc, _ = O.dw_rows(Xh, Wh, None, th, st["lse"], st["w"], cls)
+    assert rel_max(dW[torch.from_numpy(cls).cuda()].double().cpu().numpy(), dWc) < tol["grad"]
