@@ -196,10 +196,10 @@ LCE_API int lce_forward_backward(const void* X, const void* W, const void* b, co
  * which saves the inputs and recomputes the logits chunk by chunk in its
  * backward. Same arguments as lce_forward_backward, without loss_out and
  * with lse [N] fp32 (device): it must be the lse of these X, W, b.
- * On the bf16 / fp16 path every class is recomputed once (2 N D C flop)
- * and formed straight into gradient tiles, so the call does 6 N D C flop
- * where lce_forward_backward does the same plus nothing saved; a
- * lce_forward + lce_backward pair is the 8 N D C of the page's none op.
+ * On the bf16 / fp16 path every class's logits are recomputed once
+ * (2 N D C flop) and formed straight into gradient tiles, so the call does
+ * 6 N D C flop and no forward sweep; an lce_forward + lce_backward pair is
+ * the 8 N D C of the page's none op.
  * fp32 inputs do not use lse: the call computes the row statistics itself
  * (its own forward sweep) and returns the same gradients.
  * Workspace: lce_workspace_size(LCE_OP_BACKWARD, ...).
