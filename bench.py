@@ -53,6 +53,9 @@ MEASURED_TRAFFIC = {
     ("bf16_large_head", "gemm_dx_tc"): (9637890944, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 4 launches
     ("bf16_large_head", "gemm_dw_tc"): (9054174976, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 4 launches
     ("ce_logits_fp32", "ce_resident"): (17418256896, "0c74ba4", "7b5ff6e46f00e1da"),
+    ("tiny_fp32", "gemm_logits_3xtf32"): (274944, "578c2cc", "20175e992ef81d97"),
+    ("tiny_fp32", "gemm_dx_3xtf32"): (487680, "578c2cc", "20175e992ef81d97"),
+    ("tiny_fp32", "gemm_dw_3xtf32"): (373760, "578c2cc", "20175e992ef81d97"),
     ("fp32_mid", "gemm_logits_3xtf32"): (52743680, "0c74ba4", "20175e992ef81d97"),
     ("fp32_mid", "gemm_dx_3xtf32"): (178551040, "0c74ba4", "20175e992ef81d97"),
     ("fp32_mid", "gemm_dw_3xtf32"): (142775552, "0c74ba4", "20175e992ef81d97"),
@@ -231,11 +234,34 @@ def _cores():
         return os.cpu_count()
 
 
-def _config(w, ws):
+L2_BYTES = 129 * 2 ** 20  # GB300 L2; the box's own figure is used when a device is present
+
+
+def input_bytes(w):
+    """Bytes of one step's inputs (X and W, or the logits)."""
+    esz = 2 if w.dtype in (torch.bfloat16, torch.float16) else 4
+    if w.kind == "logits":
+        return w.N * w.C * esz
+    return (w.N + w.C) * w.D * esz
+
+
+def flushes_l2(w, l2_bytes=L2_BYTES):
+    """Whether the bench flushes L2 between timed steps: when the step's
+    inputs are not well larger than L2, they would stay resident across
+    steps and time as cache hits."""
+    return input_bytes(w) < 2 * l2_bytes
+
+
+def _config(w, ws, l2_bytes=L2_BYTES):
     """The workload description both arms print."""
+    if flushes_l2(w, l2_bytes):
+        l2 = ("L2 flushed between timed steps (a %d MB write, outside each step's timing); inputs %.1f MB"
+              % (4 * l2_bytes // 2 ** 20, input_bytes(w) / 1e6))
+    else:
+        l2 = "inputs larger than L2, not flushed (%.2f GB of X and W, or logits)" % (input_bytes(w) / 1e9)
     return {"workload": w.name, "N": w.N, "D": w.D, "C": w.C, "reduction": w.reduction,
             "bias": w.bias, "targets": w.target_dist, "parallelism": "replicas" if ws > 1 else "single",
-            "l2": "inputs larger than L2 (W is %.2f GB)" % (w.C * max(w.D, 1) * 2 / 1e9)}
+            "l2": l2}
 
 
 def run_reference(args):
@@ -385,22 +411,43 @@ def run_gpu(args):
     e1 = torch.cuda.Event(enable_timing=True)
     part_events = []  # reduction none: (start, between, end) per step
     split_parts = w.kind == "linear" and w.reduction == "none"
-    e0.record(stream)
-    for _ in range(args.steps):
-        if split_parts:
+    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", L2_BYTES) or L2_BYTES
+    flush = flushes_l2(w, l2_bytes)
+    if flush:
+        # inputs that fit in L2: write a buffer of 4x L2 before every step and
+        # time each step on its own, so no step starts with its inputs cached
+        scrub = torch.empty(4 * l2_bytes, dtype=torch.uint8, device=dev)
+        step_events = []
+        for _ in range(args.steps):
+            scrub.fill_(1)
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
             ev[0].record(stream)
-            step(mark=lambda: ev[1].record(stream))
+            step(mark=lambda: ev[1].record(stream)) if split_parts else step()
             ev[2].record(stream)
-            part_events.append(ev)
-        else:
-            step()
-    e1.record(stream)
-    barrier()
+            step_events.append(ev)
+            if split_parts:
+                part_events.append(ev)
+        barrier()
+        per_step = sum(ev[0].elapsed_time(ev[2]) for ev in step_events) / args.steps
+        del scrub
+    else:
+        e0.record(stream)
+        for _ in range(args.steps):
+            if split_parts:
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                ev[0].record(stream)
+                step(mark=lambda: ev[1].record(stream))
+                ev[2].record(stream)
+                part_events.append(ev)
+            else:
+                step()
+        e1.record(stream)
+        barrier()
+        per_step = e0.elapsed_time(e1) / args.steps
     check_status("timed steps")
     launches = lce.launch_count() - launches0
     clocks = sampler.stop()
-    ms = aggregate_ms(e0.elapsed_time(e1) / args.steps, dist, dev)
+    ms = aggregate_ms(per_step, dist, dev)
 
     # ---- context for the memory bound: the same step with the plan that
     # keeps every class of every row in the gradient buffer (no
@@ -467,10 +514,15 @@ def run_gpu(args):
     # profiler (its events would add to the timed region on small steps)
     prof_steps = min(args.steps, 10)
     lce.profile_reset()
-    lce.profile_enable(True)
+    scrub = torch.empty(4 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
     for _ in range(prof_steps):
+        if scrub is not None:
+            scrub.fill_(1)  # outside the profiled launches, which are timed one by one
+        lce.profile_enable(True)
         step()
+        lce.profile_enable(False)
     barrier()
+    del scrub
     check_status("profiled steps")
     lce.profile_enable(False)
     prof = lce.profile_summary()
@@ -625,7 +677,7 @@ def run_gpu(args):
                          f"float64 numpy, {sec:.1f} s"}
 
     tokens_per_s = ws * w.N / (ms / 1e3)
-    cfg = _config(w, ws)
+    cfg = _config(w, ws, l2_bytes)
     cfg["workspace_bytes"] = int(nbytes)
     executed = None
     if w.kind != "logits":

@@ -2,23 +2,34 @@
 // launch sequence of the fused linear + cross-entropy loss.
 //
 // Launch sequence of lce_forward_backward for one call (all on `stream`):
-//   prep            valid-target count n_valid, target-range check
-//   per batch chunk of Bc rows (the page's batch chunking, with Bc chosen
-//   from the workspace so that a single chunk is the common case on GB300):
+//   prep            valid-target count n_valid, target-range check, the
+//                   mean's denominator
+//   per batch chunk of Bc rows (all rows unless the gradient buffer cannot
+//   hold D classes of them):
 //     logits GEMM   z = X_c W^T (+ b) with the per-segment (max, sum-exp)
-//                   epilogue; stores P~ = exp(z - m_seg) in the chunk buffer
-//     combine       row lse, loss_n, scales w_n exp(m_seg - lse), G at target
-//     grad          chunk buffer P~ -> G in place (+ bias-gradient column sums)
-//     dX GEMM       dX_c = G W
-//     dW GEMM       dW (+)= G^T X_c
+//                   epilogue; stores P~ = exp(z - m_seg) in the gradient
+//                   buffer for the classes [0, Cs) it holds
+//     combine       row lse, loss_n, scales w_n exp(m_seg - lse) of the
+//                   stored classes, G at target, the row's lse and weight
+//     grad          P~ -> G in place for the stored classes (+ bias-gradient
+//                   column sums)
+//     dX GEMM       dX_c (+)= G W over the stored classes
+//     dW GEMM       dW[0:Cs] (+)= G^T X_c
+//     per recomputed chunk of up to Cb classes [c0, c0 + cw):
+//       recompute   z again for those classes, G formed in the epilogue
+//                   (EpiGrad) into the buffer, bias-gradient column sums
+//       dX GEMM     dX_c += G W[c0 : c0 + cw] (fp32 accumulator, the last
+//                   part stored in grad_dtype)
+//       dW GEMM     dW[c0 : c0 + cw] (+)= G^T X_c
 //   loss finalize, bias-gradient finalize
-// On the bf16 / fp16 CTA-pair path with >= 1024 chunk rows the logits GEMM
-// runs over up to 4 row slabs of growing size, and combine + grad of slab k run in the idle warps
-// of the GEMM that follows it (slab k+1's logits GEMM, or the dX GEMM for
-// the last slab, whose producer waits for those rows), so no combine or
-// grad kernel is launched. fp32 inputs add the TF32 hi / lo splits of W
-// and X_c before the GEMMs that read them, and form G together with its
-// split (3xTF32 engine).
+// lce_backward (given lse) skips the logits sweep and the merge: every class
+// is a recomputed chunk. On the bf16 / fp16 CTA-pair path with >= 1024
+// chunk rows the logits GEMM runs over up to 4 row slabs of growing size,
+// and combine + grad of slab k run in the idle warps of the GEMM that
+// follows it (slab k+1's logits GEMM, or the dX GEMM for the last slab,
+// whose producer waits for those rows), so no combine or grad kernel is
+// launched. fp32 inputs add the TF32 hi / lo splits of W and X_c before the
+// GEMMs that read them, and form G together with its split (3xTF32 engine).
 #include <cuda.h>
 #include <cuda_runtime.h>
 

@@ -49,6 +49,42 @@ int main(void) {
                                               LCE_RED_MEAN, -100, NULL, loss, NULL, NULL) == LCE_ERR_SHAPE);
   CHECK(lce_test_gemm_bf16(NULL, fake, fake, 8, 8, 8, 0, 0, 0, NULL, NULL) == LCE_ERR_NULL);
 
+  /* the bounded backward's plan: the default budget is 1 GiB of gradient
+   * buffer; a larger budget stores more classes, a smaller one fewer */
+  {
+    const int64_t N = 8192, D = 4096, C = 128256;
+    size_t def = lce_workspace_size(LCE_OP_FORWARD_BACKWARD, N, D, C, LCE_BF16, LCE_RED_MEAN, LCE_BF16, 0);
+    size_t zero = lce_workspace_size_for_buffer(LCE_OP_FORWARD_BACKWARD, N, D, C, LCE_BF16, LCE_RED_MEAN, LCE_BF16, 0);
+    size_t big = lce_workspace_size_for_buffer(LCE_OP_FORWARD_BACKWARD, N, D, C, LCE_BF16, LCE_RED_MEAN, LCE_BF16,
+                                               (size_t)-1);
+    size_t small = lce_workspace_size_for_buffer(LCE_OP_FORWARD_BACKWARD, N, D, C, LCE_BF16, LCE_RED_MEAN,
+                                                 LCE_BF16, (size_t)256 << 20);
+    CHECK(def == zero && big > def && small < def);
+    CHECK(def < ((size_t)1 << 30) + ((size_t)256 << 20));
+    int64_t plan[LCE_TEST_PLAN_FIELDS];
+    CHECK(lce_test_plan(LCE_OP_FORWARD_BACKWARD, N, D, C, LCE_BF16, LCE_BF16, 1, 1, 0, def, plan,
+                        LCE_TEST_PLAN_FIELDS) == LCE_TEST_PLAN_FIELDS);
+    CHECK(plan[0] == N && plan[31] == 65536 && plan[32] == 65536 && plan[33] == 1); /* rows, Cb, Cs, chunks */
+    size_t bw = lce_workspace_size(LCE_OP_BACKWARD, N, D, C, LCE_BF16, LCE_RED_NONE, LCE_BF16, 0);
+    CHECK(lce_test_plan(LCE_OP_BACKWARD, N, D, C, LCE_BF16, LCE_BF16, 1, 1, 0, bw, plan,
+                        LCE_TEST_PLAN_FIELDS) == LCE_TEST_PLAN_FIELDS);
+    CHECK(plan[32] == 0 && plan[33] == 2); /* lse given: nothing stored, two recomputed chunks */
+  }
+
+  /* gradients from a given lse, a given denominator, scaling: host checks */
+  CHECK(lce_backward(fake, fake, NULL, target, NULL, 4, 8, 8, LCE_F32, LCE_F32, LCE_RED_MEAN, -100, NULL, fake,
+                     fake, NULL, LCE_F32, ws, sizeof ws, NULL) == LCE_ERR_NULL); /* no lse */
+  CHECK(lce_backward(fake, fake, NULL, target, (const float*)fake, 4, 8, 8, LCE_F32, LCE_F32, LCE_RED_NONE, -100,
+                     NULL, fake, fake, NULL, LCE_F32, ws, sizeof ws, NULL) == LCE_ERR_GRAD_OUT);
+  CHECK(lce_backward_ex(fake, fake, NULL, target, NULL, NULL, (const float*)fake, 4, 8, 8, LCE_F32, LCE_F32,
+                        LCE_RED_MEAN, -100, NULL, fake, fake, NULL, 9, ws, sizeof ws, NULL) == LCE_ERR_DTYPE);
+  CHECK(lce_forward_backward_ex(fake, fake, NULL, target, NULL, (const float*)fake, 4, 8, 8, LCE_F32, LCE_F32, 9,
+                                -100, NULL, loss, fake, fake, NULL, LCE_F32, ws, sizeof ws, NULL) == LCE_ERR_REDUCTION);
+  CHECK(lce_mean_denominator(target, NULL, 4, 8, -100, NULL, ws, sizeof ws, NULL) == LCE_ERR_NULL);
+  CHECK(lce_mean_denominator(target, NULL, 4, 8, -100, loss, ws, 16, NULL) == LCE_ERR_WORKSPACE);
+  CHECK(lce_scale_gradients(fake, 4, NULL, 0, NULL, 0, LCE_F32, NULL, NULL) == LCE_ERR_NULL);
+  CHECK(lce_scale_gradients(fake, 4, NULL, 0, NULL, 0, 7, loss, NULL) == LCE_ERR_DTYPE);
+
   /* status strings and kernel accounting */
   for (int s = LCE_OK; s <= LCE_ERR_DEVICE; ++s) CHECK(lce_status_string(s) != NULL && strlen(lce_status_string(s)) > 0);
   CHECK(lce_num_kernel_ids() >= 10);
