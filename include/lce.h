@@ -144,6 +144,17 @@ LCE_API size_t lce_workspace_size(int op, int64_t N, int64_t D, int64_t C, int d
                           int reduction, int grad_dtype, int64_t chunk_rows);
 
 /*
+ * The batch chunk size of linear_cross_entropy.py's "aspect_ratio" chunking
+ * method (LinearCrossEntropyOptions docs: each chunk's [rows, C] logits
+ * buffer about as large as the [N, D] input): next_pow2(ceil(N /
+ * ceil(C / D))), divided by divisor for "aspect_ratio:divisor", at least 1.
+ * Pass it as chunk_rows to lce_workspace_size to size a workspace with that
+ * page's policy (batch chunks, every class per chunk, an fp32 [C, D] dW
+ * accumulator across them). Returns 0 on invalid arguments.
+ */
+LCE_API int64_t lce_aspect_ratio_chunk_rows(int64_t N, int64_t D, int64_t C, int64_t divisor);
+
+/*
  * Workspace bytes of the plan whose gradient buffer fits buffer_bytes (the
  * rule of the default plan above with that budget; 0 means the default
  * 1 GiB; (size_t)-1 gives the whole [N, C] buffer). Same arguments as

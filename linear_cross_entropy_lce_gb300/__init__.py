@@ -52,6 +52,7 @@ c_void_p, c_int, c_int64, c_size_t, c_double = (ctypes.c_void_p, ctypes.c_int, c
 _SIGNATURES = {
     "lce_workspace_size": (c_size_t, [c_int, c_int64, c_int64, c_int64, c_int, c_int, c_int, c_int64]),
     "lce_workspace_size_for_buffer": (c_size_t, [c_int, c_int64, c_int64, c_int64, c_int, c_int, c_int, c_size_t]),
+    "lce_aspect_ratio_chunk_rows": (c_int64, [c_int64, c_int64, c_int64, c_int64]),
     "lce_backward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int,
                              c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
                              c_size_t, c_void_p]),
@@ -240,6 +241,11 @@ def lce_workspace_size_for_buffer(op: int, N: int, D: int, C: int, dtype: int, r
                                   buffer_bytes: int) -> int:
     lib = load_library()
     return int(lib.lce_workspace_size_for_buffer(op, N, D, C, dtype, reduction, grad_dtype, buffer_bytes))
+
+
+def lce_aspect_ratio_chunk_rows(N: int, D: int, C: int, divisor: int = 1) -> int:
+    """The page's "aspect_ratio[:divisor]" batch chunk size (see lce.h)."""
+    return int(load_library().lce_aspect_ratio_chunk_rows(N, D, C, divisor))
 
 
 def _grad_ws_bytes(lib, op, N, D, C, dt, red, gdt, chunk_rows, buffer_bytes):

@@ -31,12 +31,13 @@ from . import lce_backward, lce_forward, lce_forward_backward, lce_scale_gradien
 
 class _ScalarReduction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, X, W, b, target, reduction, ignore_index, class_weight, allow_retain_graph):
+    def forward(ctx, X, W, b, target, reduction, ignore_index, class_weight, allow_retain_graph, plan):
         want_dx, want_dw, want_db = ctx.needs_input_grad[0], ctx.needs_input_grad[1], ctx.needs_input_grad[2]
         if want_dx or want_dw or want_db:
             loss, dX, dW, db = lce_forward_backward(X, W, b, target, reduction, ignore_index, None,
                                                     want_dx=want_dx, want_dw=want_dw,
-                                                    want_db=want_db and b is not None, class_weight=class_weight)
+                                                    want_db=want_db and b is not None, class_weight=class_weight,
+                                                    **plan)
         else:
             loss = lce_forward(X, W, b, target, reduction, ignore_index, class_weight=class_weight)
             dX = dW = db = None
@@ -58,16 +59,17 @@ class _ScalarReduction(torch.autograd.Function):
         # in place, in the library; its kernel leaves them untouched when the
         # upstream gradient is 1 (decided on the device: no host sync)
         lce_scale_gradients(dX, dW, db, grad_loss)
-        return dX, dW, db, None, None, None, None, None
+        return dX, dW, db, None, None, None, None, None, None
 
 
 class _NoReduction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, X, W, b, target, ignore_index, class_weight):
+    def forward(ctx, X, W, b, target, ignore_index, class_weight, plan):
         loss, lse = lce_forward(X, W, b, target, "none", ignore_index, want_lse=True, class_weight=class_weight)
         ctx.save_for_backward(X, W, b, target, lse)
         ctx.ignore_index = ignore_index
         ctx.class_weight = class_weight
+        ctx.plan = plan
         return loss
 
     @staticmethod
@@ -77,12 +79,12 @@ class _NoReduction(torch.autograd.Function):
         dX, dW, db = lce_backward(X, W, b, target, lse, "none", ctx.ignore_index,
                                   grad_loss.to(torch.float32).reshape(-1).contiguous(),
                                   want_dx=need[0], want_dw=need[1], want_db=need[2] and b is not None,
-                                  class_weight=ctx.class_weight)
-        return dX, dW, db, None, None, None
+                                  class_weight=ctx.class_weight, **ctx.plan)
+        return dX, dW, db, None, None, None, None
 
 
 def linear_cross_entropy(input, weight, target, bias=None, reduction="mean", ignore_index=-100, class_weight=None,
-                         allow_retain_graph=False):
+                         allow_retain_graph=False, chunk_rows=0, buffer_bytes=None):
     """Loss of cross_entropy(input @ weight.T + bias, target) without the
     [rows, classes] logits, differentiable in input, weight and bias.
 
@@ -97,6 +99,13 @@ def linear_cross_entropy(input, weight, target, bias=None, reduction="mean", ign
     RuntimeError; True keeps them and scales copies (one more gradient-sized
     allocation per backward). reduction "none" recomputes in its backward and
     supports retain_graph either way.
+
+    chunk_rows / buffer_bytes choose the workspace plan of the gradient call
+    (the page's batch_chunk_size / chunking_method): 0 / None is the
+    library's default (a gradient buffer of at most 1 GiB); chunk_rows > 0
+    gives batch chunks of that many rows with every class (e.g.
+    lce_aspect_ratio_chunk_rows(N, D, C) for the page's "aspect_ratio");
+    buffer_bytes bounds the buffer at that many bytes instead.
     """
     if reduction not in ("mean", "sum", "none"):
         raise ValueError(f"reduction must be mean, sum or none, got {reduction!r}")
@@ -107,6 +116,7 @@ def linear_cross_entropy(input, weight, target, bias=None, reduction="mean", ign
         raise ValueError("target must have one entry per row of input")
     W = weight.contiguous()
     b = None if bias is None else bias.contiguous()
+    plan = {"chunk_rows": chunk_rows, "buffer_bytes": buffer_bytes}
     if reduction == "none":
-        return _NoReduction.apply(X, W, b, t, ignore_index, class_weight).reshape(target.shape)
-    return _ScalarReduction.apply(X, W, b, t, reduction, ignore_index, class_weight, allow_retain_graph)
+        return _NoReduction.apply(X, W, b, t, ignore_index, class_weight, plan).reshape(target.shape)
+    return _ScalarReduction.apply(X, W, b, t, reduction, ignore_index, class_weight, allow_retain_graph, plan)

@@ -921,6 +921,16 @@ size_t lce_workspace_size(int op, int64_t N, int64_t D, int64_t C, int dtype, in
   return p.total;
 }
 
+int64_t lce_aspect_ratio_chunk_rows(int64_t N, int64_t D, int64_t C, int64_t divisor) {
+  if (N < 1 || D < 1 || C < 1 || divisor < 1) return 0;
+  // next_pow2(ceil(N / ceil(C / D))), divided by the divisor, at least 1
+  const int64_t per = ceil_div(N, ceil_div(C, D));
+  int64_t p2 = 1;
+  while (p2 < per) p2 <<= 1;
+  const int64_t rows = p2 / divisor;
+  return rows < 1 ? 1 : rows;
+}
+
 size_t lce_workspace_size_for_buffer(int op, int64_t N, int64_t D, int64_t C, int dtype, int reduction,
                                      int grad_dtype, size_t buffer_bytes) {
   if (op != LCE_OP_FORWARD && op != LCE_OP_FORWARD_BACKWARD && op != LCE_OP_BACKWARD) return 0;

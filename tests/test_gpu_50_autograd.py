@@ -91,3 +91,30 @@ def test_scale_gradients_in_place(cuda_lib, dtype):
     for a, k in ((dX, keep[0]), (db, keep[2])):
         assert torch.equal(a, (k.float() * -0.75).to(dtype))
     assert torch.equal(base[0], first)  # the element before db is untouched
+
+
+@pytest.mark.parametrize("reduction", ["mean", "none"])
+def test_autograd_plan_options(cuda_lib, reduction):
+    """chunk_rows (the page's aspect_ratio chunk size: batch chunks) and
+    buffer_bytes (classes recomputed beyond a small buffer) give the same
+    gradients as the default plan, within the bf16 tolerance of the oracle."""
+    N, D, C = 1500, 64, 3000
+    inp = make_linear_inputs(N, D, C, torch.bfloat16, "cuda", seed=37, bias=True, w_std=0.4, b_std=0.2,
+                             n_ignored=40)
+    rows = cuda_lib.lce_aspect_ratio_chunk_rows(N, D, C)
+    g = torch.randn(N, device="cuda") if reduction == "none" else None
+    ref = O.lce_forward_backward(to64(inp["X"]), to64(inp["W"]), to64(inp["b"]), inp["target"].cpu().numpy(),
+                                 reduction, -100, None if g is None else to64(g))
+    for plan in ({"chunk_rows": rows}, {"buffer_bytes": N * 512 * 2}):
+        X = inp["X"].clone().requires_grad_(True)
+        W = inp["W"].clone().requires_grad_(True)
+        b = inp["b"].clone().requires_grad_(True)
+        loss = linear_cross_entropy(X, W, inp["target"], b, reduction, **plan)
+        if reduction == "none":
+            loss.backward(g)
+        else:
+            loss.backward()
+        tol = TOL[torch.bfloat16]
+        assert rel_max(to64(X.grad), ref[1]) < tol["grad"], plan
+        assert rel_max(to64(W.grad), ref[2]) < tol["grad"], plan
+        assert rel_max(to64(b.grad), ref[3]) < tol["grad"], plan

@@ -192,3 +192,23 @@ def test_chunk_rows_plan(lib):
     r, v = _plan(lib, op, N, D, C, dt, dt, ws)
     assert (v[0], v[31], v[33]) == (N, v[3], 0)
     assert ws >= N * 128256 * 2  # the whole [N, C] buffer (2.1 GB)
+
+
+def test_aspect_ratio_chunk_rows(lib):
+    """The page's "aspect_ratio[:k]" rule: next_pow2(ceil(N / ceil(C / D))) / k."""
+    f = lib.lce_aspect_ratio_chunk_rows
+    f.argtypes = [I64, I64, I64, I64]
+    f.restype = I64
+    assert f(8192, 4096, 128256, 1) == 256          # ceil(128256 / 4096) = 32 -> 8192 / 32 = 256
+    assert f(8192, 4096, 128256, 4) == 64
+    assert f(16384, 4096, 131072, 1) == 512
+    assert f(2048, 512, 8192, 1) == 128
+    assert f(1000, 64, 700, 1) == 128               # ceil(1000 / 11) = 91 -> 128
+    assert f(100, 4096, 1000, 1) == 128             # C <= D: one chunk covers all rows
+    assert f(8, 4096, 128256, 64) == 1              # never below one row
+    assert f(0, 8, 8, 1) == 0 and f(8, 8, 8, 0) == 0
+    # the plan for that chunk size: batch chunks with every class stored
+    op, dt = lce.LCE_OP_FORWARD_BACKWARD, lce.LCE_BF16
+    ws = _ws(lib, op, 8192, 4096, 128256, dt, dt, 256)
+    r, v = _plan(lib, op, 8192, 4096, 128256, dt, dt, ws)
+    assert r == NF and v[31] == v[3] and v[33] == 0
