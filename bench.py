@@ -44,14 +44,14 @@ METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor
 MEASURED_TRAFFIC = {
     # full-size one-pass captures (gpu__time_duration.sum, dram__bytes_read.sum,
     # dram__bytes_write.sum) of one step after one warm-up step
-    ("bf16_llm_head", "gemm_logits_tc"): (2225356928, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 4 launches
-    ("bf16_llm_head", "gemm_dx_tc"): (9608986240, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 2 launches
-    ("bf16_llm_head", "gemm_dw_tc"): (6947936512, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 2 launches
-    ("bf16_llm_head", "gemm_recompute_tc"): (4420268288, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 1 launches
-    ("bf16_large_head", "gemm_logits_tc"): (24091656448, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 1 launches
-    ("bf16_large_head", "gemm_recompute_tc"): (4909548480, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 4 launches
-    ("bf16_large_head", "gemm_dx_tc"): (9637890944, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 4 launches
-    ("bf16_large_head", "gemm_dw_tc"): (9054174976, "0c74ba4", "fb229e9e1aea03c9"),  # mean of 4 launches
+    ("bf16_llm_head", "gemm_logits_tc"): (1701708608, "dynamic-schedule build", "e83d01cb037b26be"),  # mean of 4 launches
+    ("bf16_llm_head", "gemm_dx_tc"): (9017741568, "dynamic-schedule build", "e83d01cb037b26be"),  # mean of 2 launches
+    ("bf16_llm_head", "gemm_dw_tc"): (4773951360, "dynamic-schedule build", "e83d01cb037b26be"),  # mean of 2 launches
+    ("bf16_llm_head", "gemm_recompute_tc"): (2337580032, "dynamic-schedule build", "e83d01cb037b26be"),  # mean of 1 launches
+    ("bf16_large_head", "gemm_logits_tc"): (4634980096, "dynamic-schedule build", "e83d01cb037b26be"),  # mean of 1 launches
+    ("bf16_large_head", "gemm_recompute_tc"): (2605425472, "dynamic-schedule build", "e83d01cb037b26be"),  # mean of 4 launches
+    ("bf16_large_head", "gemm_dx_tc"): (8640299776, "dynamic-schedule build", "e83d01cb037b26be"),  # mean of 4 launches
+    ("bf16_large_head", "gemm_dw_tc"): (8394217216, "dynamic-schedule build", "e83d01cb037b26be"),  # mean of 4 launches
     ("ce_logits_fp32", "ce_resident"): (17418256896, "0c74ba4", "7b5ff6e46f00e1da"),
     ("tiny_fp32", "gemm_logits_3xtf32"): (274944, "578c2cc", "20175e992ef81d97"),
     ("tiny_fp32", "gemm_dx_3xtf32"): (487680, "578c2cc", "20175e992ef81d97"),

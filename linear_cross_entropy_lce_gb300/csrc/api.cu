@@ -143,10 +143,16 @@ constexpr int64_t kDefaultBufferBytes = int64_t(1) << 30;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int esize(int dt) { return dt == LCE_F32 ? 4 : 2; }
-// Work counters of the idle-warp side jobs, per chunk: (claimed, done) for
-// the merge of slabs 0..3 at [2k, 2k + 1], for the last slab's G formation
-// in the dX GEMM at [8, 9].
-constexpr int kCountersPerChunk = 16;
+// Counters per batch chunk, zeroed at the start of every call. Work counters
+// of the idle-warp side jobs: (claimed, done) for the merge of slabs 0..3 at
+// [2k, 2k + 1], for the last slab's G formation in the dX GEMM at [8, 9].
+// Tile-schedule counters of the CTA-pair GEMMs (one per launch): logits slab
+// k at kSched + k, dX and dW of the stored classes at kSched + 4 and + 5,
+// and for recomputed chunk v the recompute, dX and dW at kSched + 6 + 3v,
+// + 7 + 3v and + 8 + 3v.
+constexpr int kSideCounters = 16;
+constexpr int kSched = kSideCounters;
+inline int64_t counters_per_chunk(int64_t nvc) { return kSched + 6 + 3 * nvc; }
 
 struct Plan {
   bool tc;          // tensor-core (bf16 / fp16) path
@@ -226,7 +232,7 @@ void make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtyp
   const bool sweep = !p->given_lse;  // forward sweep with (max, sum-exp) pairs
   size_t off = align_up(sizeof(WsHeader));
   p->off_cnt = off;  // zeroed with the header at the start of every call
-  off = align_up(off + static_cast<size_t>(p->nchunks) * kCountersPerChunk * sizeof(int));
+  off = align_up(off + static_cast<size_t>(p->nchunks) * counters_per_chunk(p->nvc) * sizeof(int));
   p->off_loss = off;
   if (sweep) off = align_up(off + static_cast<size_t>(N) * 4);
   p->off_zt = off;
@@ -484,7 +490,8 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
   const int64_t Cs_eff = std::min(p.Cs, C);
   const int nseg_store = static_cast<int>(std::min<int64_t>(p.nseg, ceil_div(Cs_eff, p.segw)));
 
-  LCE_TRY(cudaMemsetAsync(hdr, 0, p.off_cnt + static_cast<size_t>(p.nchunks) * kCountersPerChunk * sizeof(int), s));
+  const int64_t cstride = counters_per_chunk(p.nvc);
+  LCE_TRY(cudaMemsetAsync(hdr, 0, p.off_cnt + static_cast<size_t>(p.nchunks) * cstride * sizeof(int), s));
   int* counters = reinterpret_cast<int*>(ws + p.off_cnt);
   if (N == 0) {
     if (!given && reduction != LCE_RED_NONE) {
@@ -559,7 +566,8 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
     CombineArgs ca_last;  // the last slab's merge, deferred into the dX GEMM's idle warps
     bool have_last = false;
     int64_t last_row0 = 0, last_si = 0;
-    int* cnt = counters + ci * kCountersPerChunk;
+    int* cnt = counters + ci * cstride;
+    int* sched = cnt + kSched;  // tile-schedule counters of this chunk's pair GEMMs
     const float* lse_rows = nullptr;  // the chunk's row lse for recomputed classes
     if (sweep) {
       // ---- logits, row lse / loss, and G of the stored classes, over row
@@ -606,7 +614,8 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
           side.cclaim = cnt + 2 * (si - 1);
           side.cdone = cnt + 2 * (si - 1) + 1;
           LCE_TRY(launch_tc_logits(tmX_k, tmW_k, tma_out ? &tmL : nullptr, static_cast<int>(sr), static_cast<int>(C),
-                                   static_cast<int>(D), &hdr->status, el, pair, s, have_prev ? &side : nullptr, f16));
+                                   static_cast<int>(D), &hdr->status, el, pair, s, have_prev ? &side : nullptr, f16,
+                                   sched + si));
         } else if (p.tf32) {
           const float* xh = wsf(p.off_xh) + so * p.ldD;
           const float* xl = wsf(p.off_xl) + so * p.ldD;
@@ -786,7 +795,7 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
           }
           LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmW_n, tma_out ? &tmdX : nullptr, static_cast<int>(rows),
                                   static_cast<int>(D), static_cast<int>(Cs_eff), &hdr->status, es, pair, s, f16,
-                                  have_last ? &side : nullptr));
+                                  have_last ? &side : nullptr, sched + 4));
         } else if (p.tf32) {
           if (!encode_tmap_f32(&tx_dx.ah, Lbuf, C, rows, p.C_pad, 128) ||
               !encode_tmap_f32(&tx_dx.al, wsf(p.off_gl), C, rows, p.C_pad, 128))
@@ -809,7 +818,8 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
           const bool tma_out = pair && (es.mode == 0 || es.mode == 3) && es.out_dt != LCE_F32 && es.vec_ok;
           if (tma_out && !encode_tmap_bf16_store(&tmdW, es.out, D, Cs_eff, D, grad_dtype)) return LCE_ERR_CUDA;
           LCE_TRY(launch_tc_store(TC_DW, tmG_m, tmX_n, tma_out ? &tmdW : nullptr, static_cast<int>(Cs_eff),
-                                  static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s, f16));
+                                  static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s, f16,
+                                  nullptr, sched + 5));
         } else if (p.tf32) {
           bool ok = encode_tmap_f32(&tx_dw.ah, wsf(p.off_gth), rows, C, p.ldB, 128) &&
                     encode_tmap_f32(&tx_dw.al, wsf(p.off_gtl), rows, C, p.ldB, 128) &&
@@ -853,7 +863,7 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
         eg.ld_g = p.Cb;
         eg.g_dt = dtype;
         LCE_TRY(launch_tc_grad(tmXc_k, tmWv_k, pair ? &tmGv : nullptr, static_cast<int>(rows), static_cast<int>(cw),
-                               static_cast<int>(D), &hdr->status, eg, pair, s, f16));
+                               static_cast<int>(D), &hdr->status, eg, pair, s, f16, sched + 6 + 3 * v));
         if (want_dx) {
           EpiStore::Params es = dx_params(part);
           CUtensorMap tmG_k, tmWv_n, tmdX;
@@ -862,7 +872,8 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
           const bool tma_out = pair && (es.mode == 0 || es.mode == 3) && es.out_dt != LCE_F32 && es.vec_ok;
           if (tma_out && !encode_tmap_bf16_store(&tmdX, es.out, D, rows, D, grad_dtype)) return LCE_ERR_CUDA;
           LCE_TRY(launch_tc_store(TC_DX, tmG_k, tmWv_n, tma_out ? &tmdX : nullptr, static_cast<int>(rows),
-                                  static_cast<int>(D), static_cast<int>(cw), &hdr->status, es, pair, s, f16));
+                                  static_cast<int>(D), static_cast<int>(cw), &hdr->status, es, pair, s, f16, nullptr,
+                                  sched + 7 + 3 * v));
         }
         if (want_dw) {
           EpiStore::Params es = dw_params(c0, cw);
@@ -873,7 +884,8 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
           const bool tma_out = pair && (es.mode == 0 || es.mode == 3) && es.out_dt != LCE_F32 && es.vec_ok;
           if (tma_out && !encode_tmap_bf16_store(&tmdW, es.out, D, cw, D, grad_dtype)) return LCE_ERR_CUDA;
           LCE_TRY(launch_tc_store(TC_DW, tmG_m, tmX_n, tma_out ? &tmdW : nullptr, static_cast<int>(cw),
-                                  static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s, f16));
+                                  static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s, f16,
+                                  nullptr, sched + 8 + 3 * v));
         }
       }
     }

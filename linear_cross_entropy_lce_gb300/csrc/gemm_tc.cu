@@ -47,6 +47,7 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int
   g.m_inner = m_inner ? m_group_for(g.num_m_blocks, TC_BM, K, 2) : 0;
   g.status = status;
   g.use_tma_out = 0;
+  g.sched = nullptr;
   if (g.num_tiles == 0) return cudaSuccess;
   const int grid = g.num_tiles < num_sms() ? g.num_tiles : num_sms();
   prof_before(kid, s, 2.0 * M * N * static_cast<double>(K));
@@ -59,7 +60,7 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int
 template <bool A_MN, bool B_MN, class Epi, bool F16 = false>
 cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M, int N,
                        int K, int m_inner, int* status, const typename Epi::Params& ep, int kid, cudaStream_t s,
-                       const SideGrad* side = nullptr) {
+                       const SideGrad* side = nullptr, int* sched = nullptr) {
   auto kern = tc2_gemm_kernel<A_MN, B_MN, Epi, F16>;
   {
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), TC2_SMEM_BYTES);
@@ -75,6 +76,7 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   g.m_inner = m_inner ? m_group_for(g.num_m_blocks, TC2_TILE_M, K, 2) : 0;
   g.status = status;
   g.use_tma_out = tmOut != nullptr ? 1 : 0;
+  g.sched = sched;
   if (g.num_tiles == 0) return cudaSuccess;
   const int max_pairs = num_sms() / 2;
   const int pairs = g.num_tiles < max_pairs ? g.num_tiles : max_pairs;
@@ -161,37 +163,42 @@ bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64
 // tiles walk down the rows so the CTAs in flight share one W panel.
 cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
                              int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s,
-                             const SideGrad* side, bool f16) {
+                             const SideGrad* side, bool f16, int* sched) {
   if (f16)
     return launch_tc2<false, false, EpiLse, true>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s,
-                                                  side);
+                                                  side, sched);
   if (pair)
-    return launch_tc2<false, false, EpiLse>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s, side);
+    return launch_tc2<false, false, EpiLse>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s, side,
+                                            sched);
   return launch_tc<false, false, EpiLse>(tmX, tmW, M, N, K, 1, status, ep, K_GEMM_LOGITS_TC, s);
 }
 
 // recomputed logits of one class chunk with the gradient epilogue: the
 // same operands and tile order as the logits GEMM
 cudaError_t launch_tc_grad(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
-                           int K, int* status, const EpiGrad::Params& ep, bool pair, cudaStream_t s, bool f16) {
+                           int K, int* status, const EpiGrad::Params& ep, bool pair, cudaStream_t s, bool f16,
+                           int* sched) {
   if (f16)
-    return launch_tc2<false, false, EpiGrad, true>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_RECOMPUTE_TC, s);
+    return launch_tc2<false, false, EpiGrad, true>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_RECOMPUTE_TC, s,
+                                                   nullptr, sched);
   if (pair)
-    return launch_tc2<false, false, EpiGrad>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_RECOMPUTE_TC, s);
+    return launch_tc2<false, false, EpiGrad>(tmX, tmW, tmOut, M, N, K, 1, status, ep, K_GEMM_RECOMPUTE_TC, s,
+                                             nullptr, sched);
   return launch_tc<false, false, EpiGrad>(tmX, tmW, M, N, K, 1, status, ep, K_GEMM_RECOMPUTE_TC, s);
 }
 
 cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M,
                             int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s,
-                            bool f16, const SideGrad* side) {
+                            bool f16, const SideGrad* side, int* sched) {
   if (side != nullptr && !(op == TC_DX && (pair || f16))) return cudaErrorInvalidValue;
   if (f16) {  // fp16 operands: CTA-pair kernel only
     switch (op) {
       case TC_DX:
         return launch_tc2<false, true, EpiStore, true>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DX_TC, s,
-                                                       side);
+                                                       side, sched);
       case TC_DW:
-        return launch_tc2<true, true, EpiStore, true>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DW_TC, s);
+        return launch_tc2<true, true, EpiStore, true>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DW_TC, s,
+                                                      nullptr, sched);
       default:
         return cudaErrorInvalidValue;
     }
@@ -199,9 +206,11 @@ cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& t
   if (pair) {
     switch (op) {
       case TC_DX:
-        return launch_tc2<false, true, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DX_TC, s, side);
+        return launch_tc2<false, true, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DX_TC, s, side,
+                                                 sched);
       case TC_DW:
-        return launch_tc2<true, true, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DW_TC, s);
+        return launch_tc2<true, true, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_DW_TC, s, nullptr,
+                                                sched);
       case TC_TEST_KK:
         return launch_tc2<false, false, EpiStore>(tmA, tmB, tmOut, M, N, K, 0, status, ep, K_GEMM_TEST, s);
       case TC_TEST_KM:

@@ -68,19 +68,22 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
 // with 32 x 32 boxes and 64-byte swizzle (encode_tmap_bf16_store) through
 // which the epilogue writes P~ (logits) or the mode-0 bf16 result (store).
 // f16: fp16 operands (CTA-pair kernel); otherwise bf16.
+// sched (pair kernel; NULL = static tile order): a zeroed device counter
+// from which the CTA pairs claim tiles in order (one counter per launch).
 cudaError_t launch_tc_logits(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
                              int K, int* status, const EpiLse::Params& ep, bool pair, cudaStream_t s,
-                             const SideGrad* side = nullptr, bool f16 = false);
+                             const SideGrad* side = nullptr, bool f16 = false, int* sched = nullptr);
 // The logits GEMM of one class chunk again, with the gradient epilogue
 // (EpiGrad): tmW covers the chunk's rows of W; tmOut (pair kernel; NULL =
 // direct stores) is the store map of the chunk's G buffer.
 cudaError_t launch_tc_grad(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap* tmOut, int M, int N,
-                           int K, int* status, const EpiGrad::Params& ep, bool pair, cudaStream_t s, bool f16);
+                           int K, int* status, const EpiGrad::Params& ep, bool pair, cudaStream_t s, bool f16,
+                           int* sched = nullptr);
 // side (TC_DX on the pair kernel only): G formation run in the GEMM's idle
 // warps, in the dynamic form of SideGrad.
 cudaError_t launch_tc_store(int op, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmOut, int M,
                             int N, int K, int* status, const EpiStore::Params& ep, bool pair, cudaStream_t s,
-                            bool f16 = false, const SideGrad* side = nullptr);
+                            bool f16 = false, const SideGrad* side = nullptr, int* sched = nullptr);
 bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64_t rows, uint64_t ld,
                             int dt = LCE_BF16);
 // Whether the fused path uses the CTA-pair GEMM (default yes; LCE_TC_PAIR=0 selects the one-CTA kernel).

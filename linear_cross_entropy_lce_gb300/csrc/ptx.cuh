@@ -247,6 +247,11 @@ __device__ __forceinline__ bool mbar_wait_cluster_drain(uint64_t* bar, uint32_t 
   }
   return true;
 }
+// 32-bit store to shared memory given by its shared::cluster address (this
+// CTA's or a peer's).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
 // Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");

@@ -18,7 +18,10 @@
 // allocation, 2-3 an optional side job (the per-row merge and G formation
 // of another row slab, see SideGrad), 4-7 epilogue (128-column tensor-memory
 // loads, stores through TMA where an output map is given). Every wait is
-// bounded as in tc_gemm.cuh.
+// bounded as in tc_gemm.cuh. Tiles are taken in a static round-robin order,
+// or, with a schedule counter, claimed one at a time by the even CTA's
+// producer (TC2_SLOTS), so that the tiles in flight on all pairs stay
+// consecutive in the tile order however the pairs' speeds differ.
 #pragma once
 
 #include "common.cuh"
@@ -52,6 +55,25 @@ constexpr int TC2_THREADS = 256;
 constexpr int TC2_TMEM_COLS = 512;
 constexpr int TC2_TILE_M = 256;  // rows per pair tile (128 per CTA)
 constexpr int TC2_TILE_N = 256;
+// Dynamic schedule: the even CTA's producer claims tiles from a counter and
+// passes each tile index through a ring of slots in both CTAs' shared
+// memory. Every role of the pair reads every slot in order: the MMA warp,
+// the 4 epilogue warps of each CTA and the odd CTA's producer release a slot
+// on the even CTA's "slot empty" barrier.
+constexpr int TC2_SLOTS = 8;
+constexpr int TC2_SLOT_READERS = 10;
+
+// The tile of iteration `it` of the dynamic schedule: wait until the even
+// CTA has filled the slot, read it, release it. -1 when a wait gave up.
+__device__ __forceinline__ int take_slot(uint64_t* sfull, uint64_t* sempty, volatile int* stile, int it,
+                                         volatile int* abort_flag) {
+  const int s = it % TC2_SLOTS;
+  const uint32_t ph = static_cast<uint32_t>(it / TC2_SLOTS) & 1u;
+  if (!mbar_wait_cluster(&sfull[s], ph, abort_flag)) return -1;
+  const int t = stile[s];
+  mbar_arrive_cluster(mapa_u32(&sempty[s], 0));
+  return t;
+}
 
 // The side job of warps 2-3 (64 threads, named barrier 1): an optional
 // merge phase, then the G formation of side.a (see SideGrad).
@@ -172,7 +194,10 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
   uint64_t* empty = full + TC2_STAGES;
   uint64_t* tfull = empty + TC2_STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* sfull = tempty + 2;              // [TC2_SLOTS] dynamic schedule: slot filled
+  uint64_t* sempty = sfull + TC2_SLOTS;      // [TC2_SLOTS] slot read by every role (even CTA's are used)
+  volatile int* stile = reinterpret_cast<volatile int*>(sempty + TC2_SLOTS);  // [TC2_SLOTS]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + TC2_SLOTS) + TC2_SLOTS;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* unit_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);  // side job: claimed unit
 
@@ -191,6 +216,10 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 8);
     }
+    for (int q = 0; q < TC2_SLOTS; ++q) {
+      mbar_init(&sfull[q], 1);
+      mbar_init(&sempty[q], TC2_SLOT_READERS);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -208,6 +237,12 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nkb = (g.K + TC2_BK - 1) / TC2_BK;
+  const bool dyn = g.sched != nullptr;
+  // tile of iteration `it` for the roles that read slots (or the static order)
+  auto tile_of = [&](int it) -> int {
+    if (!dyn) return pair + it * npairs;
+    return take_slot(sfull, sempty, stile, it, abort_flag);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -218,7 +253,30 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
       bool ok = true;
       // rows of A formed by the side job of this launch: wait for all its units once
       bool dep_wait = side.enabled && side.claim != nullptr;
-      for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
+      for (int it = 0; ok; ++it) {
+        int tile;
+        if (dyn && rank == 0) {
+          // claim the next tile and hand it to both CTAs' roles
+          const int s = it % TC2_SLOTS;
+          const uint32_t ph = static_cast<uint32_t>(it / TC2_SLOTS) & 1u;
+          if (!mbar_wait_cluster(&sempty[s], ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tile = atomicAdd(g.sched, 1);
+          if (tile > g.num_tiles) tile = g.num_tiles;  // the end, for every reader
+          stile[s] = tile;
+          st_cluster_u32(mapa_u32(const_cast<int*>(&stile[s]), 1), static_cast<uint32_t>(tile));
+          mbar_arrive_cluster(mapa_u32(&sfull[s], 0));
+          mbar_arrive_cluster(mapa_u32(&sfull[s], 1));
+        } else {
+          tile = tile_of(it);
+          if (tile < 0) {
+            ok = false;
+            break;
+          }
+        }
+        if (tile >= g.num_tiles) break;
         int mb, nb;
         tc_tile_coords(g, tile, mb, nb);
         const int m0 = mb * TC2_TILE_M + static_cast<int>(rank) * 128;
@@ -271,9 +329,10 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
       constexpr uint32_t kIdesc = idesc_16_f32(TC2_TILE_M, TC2_TILE_N, A_MN, B_MN, F16);
       int stage = 0;
       uint32_t phase = 0;
-      int it = 0;
       bool ok = true;
-      for (int tile = pair; tile < g.num_tiles && ok; tile += npairs, ++it) {
+      for (int it = 0; ok; ++it) {
+        const int tile = tile_of(it);
+        if (tile < 0 || tile >= g.num_tiles) break;
         const int acc = it & 1;
         const uint32_t acc_par = (it >> 1) & 1;
         if (!mbar_wait_cluster(&tempty[acc], acc_par ^ 1u, abort_flag)) break;
@@ -311,8 +370,11 @@ __global__ void __launch_bounds__(TC2_THREADS, 1)
     // ---------------- epilogue (both CTAs): this CTA's 128 rows of the tile
     const int q = warp & 3;
     EpiIO io{g.use_tma_out ? &tmOut : nullptr, staging + q * 4096, 0, lane, 0, bias_s + q * 256};
-    int it = 0;
-    for (int tile = pair; tile < g.num_tiles; tile += npairs, ++it) {
+    for (int it = 0;; ++it) {
+      int tile = 0;
+      if (lane == 0) tile = tile_of(it);
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (tile < 0 || tile >= g.num_tiles) break;
       const int acc = it & 1;
       const uint32_t acc_par = (it >> 1) & 1;
       int ok = 1;

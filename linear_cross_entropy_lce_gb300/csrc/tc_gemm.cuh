@@ -51,6 +51,10 @@ struct TcGemmArgs {
   int m_inner;
   int* status;  // device status word or NULL
   int use_tma_out;  // CTA-pair kernel: epilogue stores bf16 results through the output tensor map
+  // CTA-pair kernel: NULL for the static schedule (pair p takes tiles p,
+  // p + pairs, ...), or a zeroed device counter from which the pairs claim
+  // tiles in order, one at a time (see tc2_gemm.cuh)
+  int* sched;
 };
 
 __device__ __forceinline__ void tc_tile_coords(const TcGemmArgs& g, int tile, int& mb, int& nb) {
