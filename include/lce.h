@@ -157,8 +157,10 @@ LCE_API int64_t lce_aspect_ratio_chunk_rows(int64_t N, int64_t D, int64_t C, int
 /*
  * Workspace bytes of the plan whose gradient buffer fits buffer_bytes (the
  * rule of the default plan above with that budget; 0 means the default
- * 1 GiB; (size_t)-1 gives the whole [N, C] buffer). Same arguments as
- * lce_workspace_size otherwise; 0 on invalid arguments.
+ * 1 GiB; (size_t)-1 gives the whole [N, C] buffer). The smallest plan keeps
+ * min(N, 256) rows and the minimum class chunk (D rounded up to 256, at
+ * most every class): a budget below that block's bytes gets that block.
+ * Same arguments as lce_workspace_size otherwise; 0 on invalid arguments.
  */
 LCE_API size_t lce_workspace_size_for_buffer(int op, int64_t N, int64_t D, int64_t C, int dtype,
                                              int reduction, int grad_dtype, size_t buffer_bytes);

@@ -212,3 +212,14 @@ def test_aspect_ratio_chunk_rows(lib):
     ws = _ws(lib, op, 8192, 4096, 128256, dt, dt, 256)
     r, v = _plan(lib, op, 8192, 4096, 128256, dt, dt, ws)
     assert r == NF and v[31] == v[3] and v[33] == 0
+
+
+def test_budget_below_the_smallest_block(lib):
+    """A budget below one block of 256 rows x the minimum class chunk gets
+    that block (the smallest plan), with batch chunks of 256 rows."""
+    f = lib.lce_workspace_size_for_buffer
+    op, N, D, C, dt = lce.LCE_OP_FORWARD_BACKWARD, 100000, 1024, 50000, lce.LCE_BF16
+    tiny = f(op, N, D, C, dt, lce.LCE_RED_MEAN, dt, 4096)
+    r, v = _plan(lib, op, N, D, C, dt, dt, tiny)
+    assert r == NF and v[0] == 256 and v[31] == 1024
+    assert v[2] <= tiny
