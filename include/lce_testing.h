@@ -25,11 +25,15 @@
  * lce_test_gemm_f32: fp32 A, B with fp32 FMA on the CUDA cores; any shape.
  * lce_test_gemm_tf32x3: fp32 A, B on the tensor cores as three TF32
  *   products (hi*hi + hi*lo + lo*hi, hi = x rounded to TF32, lo = the
- *   rounded remainder; Ootomo & Yokota 2022), accumulated in fp32. The
- *   operands are first split into K-major hi / lo copies in `workspace`
- *   (device, 16-byte aligned, at least 2 * (M + N) * ceil(K / 4) * 16 + 1024
- *   bytes); k_splits > 1 splits K over that many work items per tile which
- *   add into the zeroed output. Any shape up to 2^30 per dimension.
+ *   rounded remainder; Ootomo & Yokota 2022), accumulated in fp32. Each
+ *   operand is first split into hi / lo copies in its own layout in
+ *   `workspace` (device, 16-byte aligned); an operand stored [R, S] takes
+ *   two copies of R * ceil(S / 4) * 4 floats, each rounded up to 256 bytes
+ *   (2 * (M + N) * ceil(K / 4) * 16 + 1024 bytes always suffice when M, N
+ *   and K are multiples of 4); the tensor cores read them K-major or
+ *   MN-major as stored. k_splits > 1 splits K over that many work items per
+ *   tile which add into the zeroed output. Any shape up to 2^30 per
+ *   dimension.
  * lce_test_gemm_bf16_unmet_dependency: the CTA-pair GEMM in its dX form
  *   (A K-major [M, K], B MN-major [K, N]) with its side job's dependency
  *   made unsatisfiable: counters[0] (claimed work chunks, preset by the
@@ -56,12 +60,12 @@
  *   gradients, (max, sum-exp) pairs, the [chunk rows, Cb] P~ / G buffer,
  *   fp32 dW accumulator, db accumulator, fp16 row weights, fp16 weight sum,
  *   fp16 scaled X, rows' lse and G weights of recomputed classes, fp32 dX
- *   accumulator, then the TF32 parts W hi, W lo, W^T hi, W^T lo, X hi,
- *   X lo, X^T hi, X^T lo, G lo, G^T hi, G^T lo; then Cb (buffer columns),
- *   Cs (classes whose G the forward sweep stores) and the number of class
- *   chunks recomputed after it. A region a call does not use has the next
- *   region's offset (zero length). Returns LCE_TEST_PLAN_FIELDS, 0 when no
- *   plan fits ws_bytes, -1 on invalid arguments.
+ *   accumulator, then the TF32 parts W hi, W lo, X hi, X lo, G lo; then
+ *   Cb (buffer columns), Cs (classes whose G the forward sweep stores) and
+ *   the number of class chunks recomputed after it. A region a call does
+ *   not use has the next region's offset (zero length). Returns
+ *   LCE_TEST_PLAN_FIELDS, 0 when no plan fits ws_bytes, -1 on invalid
+ *   arguments.
  */
 #ifndef LCE_TESTING_H_
 #define LCE_TESTING_H_
@@ -92,7 +96,7 @@ LCE_API int lce_test_gemm_bf16_unmet_dependency(const void* A, const void* B, fl
                                         int64_t N, int64_t K, int* counters, int* dev_status,
                                         void* stream);
 
-#define LCE_TEST_PLAN_FIELDS 34
+#define LCE_TEST_PLAN_FIELDS 28
 
 LCE_API int lce_test_row_slabs(int64_t rows, int64_t* slab_off);
 

@@ -381,12 +381,14 @@ def plan_of(op: int, N: int, D: int, C: int, dtype: int, grad_dtype: int, ws_byt
     fn.argtypes = [c_int, c_int64, c_int64, c_int64, c_int, c_int, c_int, c_int, c_int, c_size_t,
                    ctypes.POINTER(c_int64), c_int]
     fn.restype = c_int
-    out = (c_int64 * 34)()
-    r = fn(op, N, D, C, dtype, grad_dtype, int(want_dx), int(want_dw), int(want_db), ws_bytes, out, 34)
-    if r != 34:
+    nf = 28  # LCE_TEST_PLAN_FIELDS
+    out = (c_int64 * nf)()
+    r = fn(op, N, D, C, dtype, grad_dtype, int(want_dx), int(want_dw), int(want_db), ws_bytes, out, nf)
+    if r != nf:
         raise LceError(LCE_ERR_WORKSPACE if r == 0 else 1, "plan_of")
     v = list(out)
-    return {"Bc": v[0], "nchunks": v[1], "total": v[2], "C_pad": v[3], "Cb": v[31], "Cs": v[32], "nvc": v[33]}
+    return {"Bc": v[0], "nchunks": v[1], "total": v[2], "C_pad": v[3], "Cb": v[nf - 3], "Cs": v[nf - 2],
+            "nvc": v[nf - 1]}
 
 
 def lce_read_device_status(workspace: torch.Tensor, stream=None) -> int:
@@ -449,8 +451,10 @@ def test_gemm_tf32x3(A, B, M, N, K, a_mn_major, b_mn_major, k_splits=1, status=N
     """lce_test_gemm_tf32x3: fp32 [M, N] = A B^T as three TF32 products on the tensor cores."""
     lib = load_library()
     out = torch.empty(M, N, dtype=torch.float32, device=A.device)
-    ldk = (K + 3) // 4 * 4
-    ws_bytes = 2 * (M + N) * ldk * 4 + 1024
+    def part(rows, cols):  # one hi or lo copy of an operand stored [rows, cols], 256-byte aligned
+        return ((rows * ((cols + 3) // 4 * 4) * 4) + 255) // 256 * 256
+
+    ws_bytes = 2 * (part(K, M) if a_mn_major else part(M, K)) + 2 * (part(K, N) if b_mn_major else part(N, K))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=A.device)
     _check(lib.lce_test_gemm_tf32x3(_ptr(A), _ptr(B), _ptr(out), M, N, K, int(a_mn_major), int(b_mn_major),
                                     int(k_splits), _ptr(ws), ws_bytes, _ptr(status), _stream(stream)),

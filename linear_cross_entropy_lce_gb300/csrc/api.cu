@@ -179,11 +179,11 @@ struct Plan {
   // recomputed classes: the rows' lse and G weight [Bc], the fp32 dX
   // accumulator [Bc, D]
   size_t off_lse, off_wv, off_dx;
-  // 3xTF32: TF32 hi / lo parts of W [C, ldD], W^T [D, ldC] (dX), the chunk's
-  // X [Bc, ldD] and X^T [D, ldB] (dW), the lo part of G [Bc, C_pad] (its hi
-  // part replaces G in the chunk buffer) and G^T [C, ldB] (dW)
-  int64_t ldD, ldC, ldB;
-  size_t off_wh, off_wl, off_wth, off_wtl, off_xh, off_xl, off_xth, off_xtl, off_gl, off_gth, off_gtl;
+  // 3xTF32: TF32 hi / lo parts of W [C, ldD] and of the chunk's X [Bc, ldD]
+  // (each read K-major by the logits, MN-major by dX / dW), and the lo part
+  // of G [Bc, C_pad] (its hi part replaces G in the chunk buffer)
+  int64_t ldD;
+  size_t off_wh, off_wl, off_xh, off_xl, off_gl;
 };
 
 inline bool is_backward_op(int op) { return op == LCE_OP_FORWARD_BACKWARD || op == LCE_OP_BACKWARD; }
@@ -263,33 +263,21 @@ void make_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_dtyp
   p->off_dx = off;
   if (p->dx_acc) off = align_up(off + static_cast<size_t>(Bc) * static_cast<size_t>(D) * 4);
   p->ldD = ceil_div(D, 4) * 4;
-  p->ldC = ceil_div(C, 4) * 4;
-  p->ldB = ceil_div(Bc, 4) * 4;
   const bool tx = p->tf32;
-  const bool tx_dx = tx && backward && want_dx;
-  const bool tx_dw = tx && backward && want_dw;
+  const bool tx_g = tx && backward && (want_dx || want_dw);
   auto take = [&off](bool on, size_t bytes) {
     const size_t at = off;
     if (on) off = align_up(off + bytes);
     return at;
   };
   const size_t w_bytes = static_cast<size_t>(C) * p->ldD * 4;
-  const size_t wt_bytes = static_cast<size_t>(D) * p->ldC * 4;
   const size_t x_bytes = static_cast<size_t>(Bc) * p->ldD * 4;
-  const size_t xt_bytes = static_cast<size_t>(D) * p->ldB * 4;
   const size_t gl_bytes = static_cast<size_t>(Bc) * p->C_pad * 4;
-  const size_t gt_bytes = static_cast<size_t>(C) * p->ldB * 4;
   p->off_wh = take(tx, w_bytes);
   p->off_wl = take(tx, w_bytes);
-  p->off_wth = take(tx_dx, wt_bytes);
-  p->off_wtl = take(tx_dx, wt_bytes);
   p->off_xh = take(tx, x_bytes);
   p->off_xl = take(tx, x_bytes);
-  p->off_xth = take(tx_dw, xt_bytes);
-  p->off_xtl = take(tx_dw, xt_bytes);
-  p->off_gl = take(tx_dx, gl_bytes);
-  p->off_gth = take(tx_dw, gt_bytes);
-  p->off_gtl = take(tx_dw, gt_bytes);
+  p->off_gl = take(tx_g, gl_bytes);
   p->total = off;
 }
 
@@ -324,7 +312,7 @@ void budget_dims(int op, int64_t N, int64_t D, int64_t C, int dtype, int64_t bud
     return;
   }
   int64_t per_row = (bw ? C_pad * esize(dtype) : 0) + ceil_div(C, 64) * 8;
-  if (tf32) per_row += 8 * D + (bw ? 4 * C_pad + 8 * C + 8 * D : 0);  // TF32 parts of X, G, X^T, G^T
+  if (tf32) per_row += 8 * D + (bw ? 4 * C_pad : 0);  // TF32 parts of X, lo part of G
   if (N * per_row <= budget) {
     *Bc = N;
     return;
@@ -521,33 +509,35 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
     if (!encode_tmap_bf16(&tmW_k, W, D, C, D, pair ? 128 : TC_BN, dtype)) return LCE_ERR_CUDA;
     if (want_dx && !encode_tmap_bf16(&tmW_n, W, D, C, D, 64, dtype)) return LCE_ERR_CUDA;
   }
-  // 3xTF32: every operand as K-major TF32 hi / lo parts in the workspace
+  // 3xTF32: TF32 hi / lo parts of W, X and G in their own row-major layouts;
+  // the logits read X and W K-major, dX reads G K-major and W MN-major (K =
+  // classes), dW reads G and X MN-major (K = rows), so nothing is transposed
   auto wsf = [ws](size_t off) { return reinterpret_cast<float*>(ws + off); };
-  TxOperands tx_lg, tx_dx, tx_dw;
+  TxOperands tx_lg{}, tx_dx{}, tx_dw{};
+  tx_dx.b_mn = 1;
+  tx_dw.a_mn = 1;
+  tx_dw.b_mn = 1;
+  SplitArgs split_w{};  // W's split, launched with the first chunk's X split
   if (p.tf32) {
-    SplitArgs sa;
-    sa.src = static_cast<const float*>(W);
-    sa.rows = C;
-    sa.cols = D;
-    sa.lds = D;
-    sa.hi = wsf(p.off_wh);
-    sa.lo = wsf(p.off_wl);
-    sa.ldo = p.ldD;
-    sa.hiT = want_dx ? wsf(p.off_wth) : nullptr;
-    sa.loT = want_dx ? wsf(p.off_wtl) : nullptr;
-    sa.ldt = p.ldC;
-    LCE_TRY(launch_split_tf32(sa, s));
-    bool ok = encode_tmap_f32(&tx_lg.bh, sa.hi, D, C, p.ldD, 128) && encode_tmap_f32(&tx_lg.bl, sa.lo, D, C, p.ldD, 128);
+    split_w.src = static_cast<const float*>(W);
+    split_w.rows = C;
+    split_w.cols = D;
+    split_w.lds = D;
+    split_w.hi = wsf(p.off_wh);
+    split_w.lo = wsf(p.off_wl);
+    split_w.ldo = p.ldD;
+    bool ok = encode_tmap_f32(&tx_lg.bh, split_w.hi, D, C, p.ldD, false) &&
+              encode_tmap_f32(&tx_lg.bl, split_w.lo, D, C, p.ldD, false);
     if (want_dx)
-      ok = ok && encode_tmap_f32(&tx_dx.bh, sa.hiT, C, D, p.ldC, 128) &&
-           encode_tmap_f32(&tx_dx.bl, sa.loT, C, D, p.ldC, 128);
+      ok = ok && encode_tmap_f32(&tx_dx.bh, split_w.hi, D, C, p.ldD, true) &&
+           encode_tmap_f32(&tx_dx.bl, split_w.lo, D, C, p.ldD, true);
     if (!ok) return LCE_ERR_CUDA;
   }
 
   for (int64_t ci = 0; ci < p.nchunks; ++ci) {
     const int64_t row0 = ci * p.Bc;
     const int64_t rows = std::min(p.Bc, N - row0);
-    if (p.tf32) {  // TF32 parts of the chunk's rows of X (and of X^T for dW)
+    if (p.tf32) {  // TF32 parts of the chunk's rows of X (and of W with the first chunk)
       SplitArgs sa;
       sa.src = static_cast<const float*>(X) + row0 * D;
       sa.rows = rows;
@@ -556,10 +546,7 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
       sa.hi = wsf(p.off_xh);
       sa.lo = wsf(p.off_xl);
       sa.ldo = p.ldD;
-      sa.hiT = want_dw ? wsf(p.off_xth) : nullptr;
-      sa.loT = want_dw ? wsf(p.off_xtl) : nullptr;
-      sa.ldt = p.ldB;
-      LCE_TRY(launch_split_tf32(sa, s));
+      LCE_TRY(launch_split_tf32(sa, s, ci == 0 ? &split_w : nullptr));
     }
     const bool slabbed = sweep && p.tc && pair && backward && rows >= 1024;
     GradArgs ga_last, ga_tx;
@@ -619,7 +606,8 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
         } else if (p.tf32) {
           const float* xh = wsf(p.off_xh) + so * p.ldD;
           const float* xl = wsf(p.off_xl) + so * p.ldD;
-          if (!encode_tmap_f32(&tx_lg.ah, xh, D, sr, p.ldD, 128) || !encode_tmap_f32(&tx_lg.al, xl, D, sr, p.ldD, 128))
+          if (!encode_tmap_f32(&tx_lg.ah, xh, D, sr, p.ldD, false) ||
+              !encode_tmap_f32(&tx_lg.al, xl, D, sr, p.ldD, false))
             return LCE_ERR_CUDA;
           LCE_TRY(launch_tx_logits(tx_lg, static_cast<int>(sr), static_cast<int>(C), static_cast<int>(D),
                                    &hdr->status, el, s));
@@ -700,18 +688,15 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
       lse_rows = lse_in + row0;
     }
     if (!backward) continue;
-    if (p.tf32 && (want_dx || want_dw)) {  // G formed from P~ and split: hi over P~ itself, lo, and G^T's parts
+    if (p.tf32 && (want_dx || want_dw)) {  // G formed from P~ and split: hi over P~ itself, lo beside it
       SplitArgs sa;
       sa.src = static_cast<const float*>(Lbuf);
       sa.rows = rows;
       sa.cols = C;
       sa.lds = p.C_pad;
-      sa.hi = want_dx ? static_cast<float*>(Lbuf) : nullptr;
-      sa.lo = want_dx ? wsf(p.off_gl) : nullptr;
+      sa.hi = static_cast<float*>(Lbuf);
+      sa.lo = wsf(p.off_gl);
       sa.ldo = p.C_pad;
-      sa.hiT = want_dw ? wsf(p.off_gth) : nullptr;
-      sa.loT = want_dw ? wsf(p.off_gtl) : nullptr;
-      sa.ldt = p.ldB;
       LCE_TRY(launch_grad_split_tf32(ga_tx, sa, s));
     }
     // dX is the sum over the class parts (the stored classes, then each
@@ -797,8 +782,8 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
                                   static_cast<int>(D), static_cast<int>(Cs_eff), &hdr->status, es, pair, s, f16,
                                   have_last ? &side : nullptr, sched + 4));
         } else if (p.tf32) {
-          if (!encode_tmap_f32(&tx_dx.ah, Lbuf, C, rows, p.C_pad, 128) ||
-              !encode_tmap_f32(&tx_dx.al, wsf(p.off_gl), C, rows, p.C_pad, 128))
+          if (!encode_tmap_f32(&tx_dx.ah, Lbuf, C, rows, p.C_pad, false) ||
+              !encode_tmap_f32(&tx_dx.al, wsf(p.off_gl), C, rows, p.C_pad, false))
             return LCE_ERR_CUDA;
           LCE_TRY(launch_tx_store(TC_DX, tx_dx, static_cast<int>(rows), static_cast<int>(D), static_cast<int>(C),
                                   &hdr->status, es, s));
@@ -821,10 +806,10 @@ int run_lce(int op, const void* X, const void* W, const void* b, const int64_t* 
                                   static_cast<int>(D), static_cast<int>(rows), &hdr->status, es, pair, s, f16,
                                   nullptr, sched + 5));
         } else if (p.tf32) {
-          bool ok = encode_tmap_f32(&tx_dw.ah, wsf(p.off_gth), rows, C, p.ldB, 128) &&
-                    encode_tmap_f32(&tx_dw.al, wsf(p.off_gtl), rows, C, p.ldB, 128) &&
-                    encode_tmap_f32(&tx_dw.bh, wsf(p.off_xth), rows, D, p.ldB, 128) &&
-                    encode_tmap_f32(&tx_dw.bl, wsf(p.off_xtl), rows, D, p.ldB, 128);
+          bool ok = encode_tmap_f32(&tx_dw.ah, Lbuf, C, rows, p.C_pad, true) &&
+                    encode_tmap_f32(&tx_dw.al, wsf(p.off_gl), C, rows, p.C_pad, true) &&
+                    encode_tmap_f32(&tx_dw.bh, wsf(p.off_xh), D, rows, p.ldD, true) &&
+                    encode_tmap_f32(&tx_dw.bl, wsf(p.off_xl), D, rows, p.ldD, true);
           if (!ok) return LCE_ERR_CUDA;
           LCE_TRY(launch_tx_store(TC_DW, tx_dw, static_cast<int>(C), static_cast<int>(D), static_cast<int>(rows),
                                   &hdr->status, es, s));
@@ -1228,36 +1213,44 @@ int lce_test_gemm_tf32x3(const float* A, const float* B, float* out, int64_t M, 
   if (A == nullptr || B == nullptr || out == nullptr || workspace == nullptr) return LCE_ERR_NULL;
   if (M < 1 || N < 1 || K < 1 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return LCE_ERR_SHAPE;
   if (!aligned16(workspace)) return LCE_ERR_ALIGN;
-  const int64_t ldk = ceil_div(K, 4) * 4;
-  const size_t a_bytes = align_up(static_cast<size_t>(M) * ldk * 4);
-  const size_t b_bytes = align_up(static_cast<size_t>(N) * ldk * 4);
-  if (ws_bytes < 2 * a_bytes + 2 * b_bytes) return LCE_ERR_WORKSPACE;
+  // each operand split into hi / lo parts in its own layout: [rows, K] when
+  // K-major, [K, rows] when MN-major, the contiguous dimension padded to 4
+  const bool mn[2] = {a_mn_major != 0, b_mn_major != 0};
+  const int64_t rows[2] = {M, N};
+  int64_t pr[2], pc[2], ld[2];
+  size_t bytes[2];
+  for (int op = 0; op < 2; ++op) {
+    pr[op] = mn[op] ? K : rows[op];
+    pc[op] = mn[op] ? rows[op] : K;
+    ld[op] = ceil_div(pc[op], 4) * 4;
+    bytes[op] = align_up(static_cast<size_t>(pr[op]) * ld[op] * 4);
+  }
+  if (ws_bytes < 2 * bytes[0] + 2 * bytes[1]) return LCE_ERR_WORKSPACE;
   int st = check_device();
   if (st != LCE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* parts[4] = {reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + a_bytes),
-                     reinterpret_cast<float*>(ws + 2 * a_bytes), reinterpret_cast<float*>(ws + 2 * a_bytes + b_bytes)};
-  // K-major parts: an MN-major operand ([K, rows] in memory) goes through the transposing split
+  float* parts[4] = {reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + bytes[0]),
+                     reinterpret_cast<float*>(ws + 2 * bytes[0]),
+                     reinterpret_cast<float*>(ws + 2 * bytes[0] + bytes[1])};
+  SplitArgs sa[2];
   for (int op = 0; op < 2; ++op) {
-    const bool mn = op == 0 ? a_mn_major != 0 : b_mn_major != 0;
-    const int64_t rows = op == 0 ? M : N;
-    SplitArgs sa;
-    sa.src = op == 0 ? A : B;
-    sa.rows = mn ? K : rows;
-    sa.cols = mn ? rows : K;
-    sa.lds = sa.cols;
-    sa.hi = mn ? nullptr : parts[2 * op];
-    sa.lo = mn ? nullptr : parts[2 * op + 1];
-    sa.ldo = ldk;
-    sa.hiT = mn ? parts[2 * op] : nullptr;
-    sa.loT = mn ? parts[2 * op + 1] : nullptr;
-    sa.ldt = ldk;
-    if (launch_split_tf32(sa, s) != cudaSuccess) return LCE_ERR_CUDA;
+    sa[op].src = op == 0 ? A : B;
+    sa[op].rows = pr[op];
+    sa[op].cols = pc[op];
+    sa[op].lds = pc[op];
+    sa[op].hi = parts[2 * op];
+    sa[op].lo = parts[2 * op + 1];
+    sa[op].ldo = ld[op];
   }
-  TxOperands o;
-  bool ok = encode_tmap_f32(&o.ah, parts[0], K, M, ldk, 128) && encode_tmap_f32(&o.al, parts[1], K, M, ldk, 128) &&
-            encode_tmap_f32(&o.bh, parts[2], K, N, ldk, 128) && encode_tmap_f32(&o.bl, parts[3], K, N, ldk, 128);
+  if (launch_split_tf32(sa[0], s, &sa[1]) != cudaSuccess) return LCE_ERR_CUDA;
+  TxOperands o{};
+  o.a_mn = mn[0] ? 1 : 0;
+  o.b_mn = mn[1] ? 1 : 0;
+  bool ok = encode_tmap_f32(&o.ah, parts[0], pc[0], pr[0], ld[0], mn[0]) &&
+            encode_tmap_f32(&o.al, parts[1], pc[0], pr[0], ld[0], mn[0]) &&
+            encode_tmap_f32(&o.bh, parts[2], pc[1], pr[1], ld[1], mn[1]) &&
+            encode_tmap_f32(&o.bl, parts[3], pc[1], pr[1], ld[1], mn[1]);
   if (!ok) return LCE_ERR_CUDA;
   EpiStore::Params es;
   es.out = out;
@@ -1317,10 +1310,8 @@ int lce_test_plan(int op, int64_t N, int64_t D, int64_t C, int dtype, int grad_d
       static_cast<int64_t>(p.off_L), static_cast<int64_t>(p.off_dw), static_cast<int64_t>(p.off_db),
       static_cast<int64_t>(p.off_wrow), static_cast<int64_t>(p.off_wbar), static_cast<int64_t>(p.off_xs),
       static_cast<int64_t>(p.off_lse), static_cast<int64_t>(p.off_wv), static_cast<int64_t>(p.off_dx),
-      static_cast<int64_t>(p.off_wh), static_cast<int64_t>(p.off_wl), static_cast<int64_t>(p.off_wth),
-      static_cast<int64_t>(p.off_wtl), static_cast<int64_t>(p.off_xh), static_cast<int64_t>(p.off_xl),
-      static_cast<int64_t>(p.off_xth), static_cast<int64_t>(p.off_xtl), static_cast<int64_t>(p.off_gl),
-      static_cast<int64_t>(p.off_gth), static_cast<int64_t>(p.off_gtl),
+      static_cast<int64_t>(p.off_wh), static_cast<int64_t>(p.off_wl), static_cast<int64_t>(p.off_xh),
+      static_cast<int64_t>(p.off_xl), static_cast<int64_t>(p.off_gl),
       p.Cb, p.Cs, p.nvc};
   for (int i = 0; i < LCE_TEST_PLAN_FIELDS; ++i) out[i] = v[i];
   return LCE_TEST_PLAN_FIELDS;

@@ -133,16 +133,16 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
   return r == CUDA_SUCCESS;
 }
 
-bool encode_tmap_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
-                     uint32_t box_rows) {
+bool encode_tmap_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld, bool mn_major) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {ld * 4};
-  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t box[2] = {32, mn_major ? TX_MN_ROWS : 128u};
   cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = mn_major ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -8,6 +8,8 @@
 
 namespace lce {
 
+static_assert(TX_MN_ROWS == TX_BK, "an MN-major box holds one K block");
+
 namespace {
 
 // hi = x rounded to TF32; lo = (x - hi) rounded to TF32. x - hi is exact in
@@ -24,135 +26,106 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
   }
 }
 
-// One 64 x 64 tile of src per iteration, 256 threads. Reads and row-major
-// writes move float4s (16 threads per 64-float row segment) when the row
-// pitches and base pointers allow it; the transposed outputs go through
-// shared memory and are written as float4 runs along their rows, so every
-// global access is coalesced. Scalar code covers ragged tile edges.
+// One 64 x 64 tile per iteration, 256 threads, over the tiles of a and then
+// of b (b.rows == 0: none); reads and writes move float4s (16 threads per
+// 64-float row segment) when the matrix's pitches and base pointers allow it
+// (vec_a, vec_b), scalar code covers ragged tile edges.
 //
-// GRAD: src is the chunk buffer holding P~ of the fp32 path, and the value
-// split is G itself, formed on the way in: G[r, j] = P~[r, j] * scale of
-// (j's segment, r), or gt[r] at the row's target column (the same G as the
-// stand-alone G formation); with g.db_acc the tile's column sums of G are
-// added to it (one atomic per column per tile). G is never written in fp32:
-// its hi part goes over P~ in place (a.hi == a.src), its lo part and the
-// transposed parts to their buffers, so the G formation and the split read
-// the buffer once.
+// GRAD (a only): a.src is the chunk buffer holding P~ of the fp32 path, and
+// the value split is G itself, formed on the way in: G[r, j] = P~[r, j] *
+// scale of (j's segment, r), or gt[r] at the row's target column (the same G
+// as the stand-alone G formation); with g.db_acc the tile's column sums of G
+// are added to it (one atomic per column per tile). G is never written in
+// fp32: its hi part goes over P~ in place (a.hi == a.src) and its lo part to
+// its buffer, so the G formation and the split read the buffer once.
 constexpr int SP_T = 64;
+__host__ __device__ inline int64_t split_tiles(const SplitArgs& m) {
+  return ((m.rows + SP_T - 1) / SP_T) * ((m.cols + SP_T - 1) / SP_T);
+}
 template <bool GRAD>
-__global__ void __launch_bounds__(256) split_tf32_kernel(const SplitArgs a, const GradArgs g, int vec_in,
-                                                         int vec_t) {
-  __shared__ float th[SP_T][SP_T + 1];
-  __shared__ float tl[SP_T][SP_T + 1];
+__global__ void __launch_bounds__(256) split_tf32_kernel(const SplitArgs a, const SplitArgs b, const GradArgs g,
+                                                         int vec_a, int vec_b) {
   __shared__ float cs[GRAD ? 16 : 1][SP_T];
   const int t = threadIdx.x;
-  const int64_t tiles_c = (a.cols + SP_T - 1) / SP_T;
-  const int64_t ntiles = ((a.rows + SP_T - 1) / SP_T) * tiles_c;
+  const int64_t na = split_tiles(a);
+  const int64_t ntiles = na + split_tiles(b);
   const int cq = (t & 15) * 4;  // column of this thread's float4 within the tile
   const int rq = t >> 4;        // first row (of 16) within the tile
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int64_t r0 = (tile / tiles_c) * SP_T;
-    const int64_t c0 = (tile % tiles_c) * SP_T;
-    const bool full_c = vec_in && c0 + cq + 4 <= a.cols;
+    const bool in_a = tile < na;
+    const float* src = in_a ? a.src : b.src;
+    float* hi = in_a ? a.hi : b.hi;
+    float* lo = in_a ? a.lo : b.lo;
+    const int64_t rows = in_a ? a.rows : b.rows, cols = in_a ? a.cols : b.cols;
+    const int64_t lds = in_a ? a.lds : b.lds, ldo = in_a ? a.ldo : b.ldo;
+    const int64_t lt = in_a ? tile : tile - na;
+    const int64_t tiles_c = (cols + SP_T - 1) / SP_T;
+    const int64_t r0 = (lt / tiles_c) * SP_T;
+    const int64_t c0 = (lt % tiles_c) * SP_T;
+    const bool full_c = (in_a ? vec_a : vec_b) && c0 + cq + 4 <= cols;
     const int seg = GRAD ? static_cast<int>((c0 + cq) / g.segw) : 0;  // the float4 lies in one segment
     float colsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int lr = rq + 16 * k;
-      const int64_t r = r0 + lr;
+      const int64_t r = r0 + rq + 16 * k;
+      if (r >= rows) continue;
       float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (r < a.rows) {
-        if (full_c) {
-          const float4 v = *reinterpret_cast<const float4*>(a.src + r * a.lds + c0 + cq);
-          x[0] = v.x;
-          x[1] = v.y;
-          x[2] = v.z;
-          x[3] = v.w;
-        } else {
+      if (full_c) {
+        const float4 v = *reinterpret_cast<const float4*>(src + r * lds + c0 + cq);
+        x[0] = v.x;
+        x[1] = v.y;
+        x[2] = v.z;
+        x[3] = v.w;
+      } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (c0 + cq + e < a.cols) x[e] = a.src[r * a.lds + c0 + cq + e];
-        }
-        if (GRAD) {
-          const float sc = g.scale[seg * g.sld + r].x;
-          const int64_t tc = g.tcol[r];
-          const float gtv = g.gt[r];
+        for (int e = 0; e < 4; ++e)
+          if (c0 + cq + e < cols) x[e] = src[r * lds + c0 + cq + e];
+      }
+      if (GRAD) {
+        const float sc = g.scale[seg * g.sld + r].x;
+        const int64_t tc = g.tcol[r];
+        const float gtv = g.gt[r];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[e] = (c0 + cq + e == tc) ? gtv : x[e] * sc;
-            colsum[e] += x[e];
-          }
+        for (int e = 0; e < 4; ++e) {
+          x[e] = (c0 + cq + e == tc) ? gtv : x[e] * sc;
+          colsum[e] += x[e];
         }
       }
       float h[4], l[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) split_tf32(x[e], h[e], l[e]);
-      if (a.hi != nullptr && r < a.rows) {
-        if (full_c) {
-          *reinterpret_cast<float4*>(a.hi + r * a.ldo + c0 + cq) = make_float4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<float4*>(a.lo + r * a.ldo + c0 + cq) = make_float4(l[0], l[1], l[2], l[3]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (c0 + cq + e < a.cols) {
-              a.hi[r * a.ldo + c0 + cq + e] = h[e];
-              a.lo[r * a.ldo + c0 + cq + e] = l[e];
-            }
-          }
-        }
-      }
-      if (a.hiT != nullptr) {
+      if (full_c) {
+        *reinterpret_cast<float4*>(hi + r * ldo + c0 + cq) = make_float4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<float4*>(lo + r * ldo + c0 + cq) = make_float4(l[0], l[1], l[2], l[3]);
+      } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          th[lr][cq + e] = h[e];
-          tl[lr][cq + e] = l[e];
+          if (c0 + cq + e < cols) {
+            hi[r * ldo + c0 + cq + e] = h[e];
+            lo[r * ldo + c0 + cq + e] = l[e];
+          }
         }
       }
     }
     if (GRAD && g.db_acc != nullptr) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) cs[rq][cq + e] = colsum[e];
-    }
-    if (a.hiT != nullptr || (GRAD && g.db_acc != nullptr)) __syncthreads();
-    if (GRAD && g.db_acc != nullptr && t < SP_T) {
-      float sum = 0.0f;
+      __syncthreads();
+      if (t < SP_T) {
+        float sum = 0.0f;
 #pragma unroll
-      for (int q = 0; q < 16; ++q) sum += cs[q][t];
-      if (c0 + t < g.C) atomicAdd(g.db_acc + c0 + t, sum);
-    }
-    if (a.hiT != nullptr) {
-      // transposed: output row cc (a column of src) holds the tile's 64 rows
-      const int j = (t & 15) * 4;  // first src row of this thread's float4
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int lc = (t >> 4) + 16 * p;
-        const int64_t cc = c0 + lc;
-        if (cc >= a.cols) continue;
-        const int64_t rr = r0 + j;
-        float* dh = a.hiT + cc * a.ldt + rr;
-        float* dl = a.loT + cc * a.ldt + rr;
-        if (vec_t && rr + 4 <= a.rows) {
-          *reinterpret_cast<float4*>(dh) = make_float4(th[j][lc], th[j + 1][lc], th[j + 2][lc], th[j + 3][lc]);
-          *reinterpret_cast<float4*>(dl) = make_float4(tl[j][lc], tl[j + 1][lc], tl[j + 2][lc], tl[j + 3][lc]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (rr + e < a.rows) {
-              dh[e] = th[j + e][lc];
-              dl[e] = tl[j + e][lc];
-            }
-          }
-        }
+        for (int q = 0; q < 16; ++q) sum += cs[q][t];
+        if (c0 + t < g.C) atomicAdd(g.db_acc + c0 + t, sum);
       }
+      __syncthreads();
     }
-    __syncthreads();
   }
 }
 
-template <class Epi>
+template <bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_tx(const TxOperands& o, int M, int N, int K, int m_inner, int splits, int* status,
                       const typename Epi::Params& ep, int kid, cudaStream_t s) {
-  auto kern = tc2x3_gemm_kernel<Epi>;
+  auto kern = tc2x3_gemm_kernel<A_MN, B_MN, Epi>;
   {
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), TX_SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -193,6 +166,17 @@ cudaError_t launch_tx(const TxOperands& o, int M, int N, int K, int m_inner, int
   return e;
 }
 
+// The kernel for the operands' layouts.
+cudaError_t launch_tx_store_any(const TxOperands& o, int M, int N, int K, int splits, int* status,
+                                const EpiStore::Params& ep, int kid, cudaStream_t s) {
+  if (o.a_mn) {
+    return o.b_mn ? launch_tx<true, true, EpiStore>(o, M, N, K, 0, splits, status, ep, kid, s)
+                  : launch_tx<true, false, EpiStore>(o, M, N, K, 0, splits, status, ep, kid, s);
+  }
+  return o.b_mn ? launch_tx<false, true, EpiStore>(o, M, N, K, 0, splits, status, ep, kid, s)
+                : launch_tx<false, false, EpiStore>(o, M, N, K, 0, splits, status, ep, kid, s);
+}
+
 }  // namespace
 
 bool f32_tensor_default() {
@@ -206,39 +190,47 @@ bool f32_tensor_default() {
 
 namespace {
 template <bool GRAD>
-cudaError_t launch_split(const SplitArgs& a, const GradArgs& g, int kid, double bytes, cudaStream_t s) {
-  if (a.rows == 0 || a.cols == 0) return cudaSuccess;
+cudaError_t launch_split(const SplitArgs& a, const SplitArgs& b, const GradArgs& g, int kid, cudaStream_t s) {
+  const int64_t ntiles = split_tiles(a) + split_tiles(b);
+  if (ntiles == 0) return cudaSuccess;
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-  const int vec_in = (a.lds % 4 == 0) && al16(a.src) &&
-                     (a.hi == nullptr || ((a.ldo % 4 == 0) && al16(a.hi) && al16(a.lo)));
-  const int vec_t = a.hiT != nullptr && (a.ldt % 4 == 0) && al16(a.hiT) && al16(a.loT);
-  const int64_t ntiles = ((a.rows + SP_T - 1) / SP_T) * ((a.cols + SP_T - 1) / SP_T);
-  const int64_t cap = static_cast<int64_t>(num_sms()) * 6;
+  auto vec = [&](const SplitArgs& m) {
+    return (m.lds % 4 == 0) && (m.ldo % 4 == 0) && al16(m.src) && al16(m.hi) && al16(m.lo) ? 1 : 0;
+  };
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   const int grid = static_cast<int>(ntiles < cap ? ntiles : cap);
-  prof_before(kid, s, bytes);
-  split_tf32_kernel<GRAD><<<grid, 256, 0, s>>>(a, g, vec_in, vec_t);
+  // algorithmic bytes: each source read once, its hi and lo parts written
+  prof_before(kid, s, 12.0 * (a.rows * static_cast<double>(a.cols) + b.rows * static_cast<double>(b.cols)));
+  split_tf32_kernel<GRAD><<<grid, 256, 0, s>>>(a, b, g, vec(a), vec(b));
   cudaError_t e = cudaGetLastError();
   prof_after(kid, s);
   return e;
 }
 }  // namespace
 
-cudaError_t launch_split_tf32(const SplitArgs& a, cudaStream_t s) {
-  const double outs = (a.hi != nullptr ? 2.0 : 0.0) + (a.hiT != nullptr ? 2.0 : 0.0);
-  GradArgs none;
+cudaError_t launch_split_tf32(const SplitArgs& a, cudaStream_t s, const SplitArgs* b) {
+  SplitArgs none;
   memset(&none, 0, sizeof(none));
-  return launch_split<false>(a, none, K_SPLIT_TF32, 4.0 * (1.0 + outs) * a.rows * static_cast<double>(a.cols), s);
+  if (a.rows > 0 && a.cols > 0 && (a.hi == nullptr || a.lo == nullptr)) return cudaErrorInvalidValue;
+  if (b != nullptr && b->rows > 0 && b->cols > 0 && (b->hi == nullptr || b->lo == nullptr))
+    return cudaErrorInvalidValue;
+  GradArgs ng;
+  memset(&ng, 0, sizeof(ng));
+  return launch_split<false>(a, b != nullptr && b->cols > 0 ? *b : none, ng, K_SPLIT_TF32, s);
 }
 
 cudaError_t launch_grad_split_tf32(const GradArgs& g, const SplitArgs& a, cudaStream_t s) {
   if (g.segw % SP_T != 0) return cudaErrorInvalidValue;  // a tile's float4 must lie in one segment
-  const double outs = (a.hi != nullptr ? 2.0 : 0.0) + (a.hiT != nullptr ? 2.0 : 0.0);
-  return launch_split<true>(a, g, K_GRAD_SPLIT_TF32, 4.0 * (1.0 + outs) * a.rows * static_cast<double>(a.cols), s);
+  if (a.hi == nullptr || a.lo == nullptr) return cudaErrorInvalidValue;
+  SplitArgs none;
+  memset(&none, 0, sizeof(none));
+  return launch_split<true>(a, none, g, K_GRAD_SPLIT_TF32, s);
 }
 
 cudaError_t launch_tx_logits(const TxOperands& o, int M, int N, int K, int* status, const EpiLse::Params& ep,
                              cudaStream_t s) {
-  return launch_tx<EpiLse>(o, M, N, K, 1, 1, status, ep, K_GEMM_LOGITS_TX, s);
+  if (o.a_mn || o.b_mn) return cudaErrorInvalidValue;
+  return launch_tx<false, false, EpiLse>(o, M, N, K, 1, 1, status, ep, K_GEMM_LOGITS_TX, s);
 }
 
 cudaError_t launch_tx_store(int op, const TxOperands& o, int M, int N, int K, int* status,
@@ -264,21 +256,21 @@ cudaError_t launch_tx_store(int op, const TxOperands& o, int M, int N, int K, in
         e2.mode = 4;
         cudaError_t e = cudaMemsetAsync(ep.out, 0, static_cast<size_t>(M) * ep.ldo * sizeof(float), s);
         if (e != cudaSuccess) return e;
-        return launch_tx<EpiStore>(o, M, N, K, 0, static_cast<int>(splits), status, e2, K_GEMM_DX_TX, s);
+        return launch_tx_store_any(o, M, N, K, static_cast<int>(splits), status, e2, K_GEMM_DX_TX, s);
       }
     }
-    return launch_tx<EpiStore>(o, M, N, K, 0, 1, status, ep, K_GEMM_DX_TX, s);
+    return launch_tx_store_any(o, M, N, K, 1, status, ep, K_GEMM_DX_TX, s);
   }
-  if (op == TC_DW) return launch_tx<EpiStore>(o, M, N, K, 0, 1, status, ep, K_GEMM_DW_TX, s);
+  if (op == TC_DW) return launch_tx_store_any(o, M, N, K, 1, status, ep, K_GEMM_DW_TX, s);
   if (op == TC_TEST_KK) {
     if (test_splits > 1) {
       EpiStore::Params e2 = ep;
       e2.mode = 4;
       cudaError_t e = cudaMemsetAsync(ep.out, 0, static_cast<size_t>(M) * ep.ldo * sizeof(float), s);
       if (e != cudaSuccess) return e;
-      return launch_tx<EpiStore>(o, M, N, K, 0, test_splits, status, e2, K_GEMM_TEST, s);
+      return launch_tx_store_any(o, M, N, K, test_splits, status, e2, K_GEMM_TEST, s);
     }
-    return launch_tx<EpiStore>(o, M, N, K, 0, 1, status, ep, K_GEMM_TEST, s);
+    return launch_tx_store_any(o, M, N, K, 1, status, ep, K_GEMM_TEST, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -90,18 +90,25 @@ bool encode_tmap_bf16_store(CUtensorMap* map, void* base, uint64_t inner, uint64
 bool tc_pair_default();
 
 // ---- fp32 GEMM on the tensor cores by three TF32 products (gemm_tf32.cu)
+constexpr uint32_t TX_MN_ROWS = 32;  // box rows of an MN-major operand map: one K block
 // Encodes a 2-D fp32 tensor map over a row-major matrix (rows x inner, row
-// pitch ld elements, ld * 4 a multiple of 16 bytes), box {32, box_rows},
-// 128B swizzle.
-bool encode_tmap_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
-                     uint32_t box_rows);
-// Operands as hi / lo pairs of tensor maps (box rows 128), all K-major:
-// A [M, K], B [N, K]. op: TC_LOGITS (EpiLse), TC_DX or TC_DW (EpiStore);
-// TC_DX with an fp32 mode-0 output and few tiles splits K over work items
-// that add into the output after zeroing it; TC_TEST_KK does the same with
-// test_splits work items per tile when test_splits > 1 (fp32 mode-0 output).
+// pitch ld elements, ld * 4 a multiple of 16 bytes) for a 3xTF32 operand:
+// K-major (inner = K) box {32, 128} with the 128-byte swizzle, or MN-major
+// (inner = M or N) box {32, TX_MN_ROWS} with the 128-byte swizzle of
+// 32-byte atoms.
+bool encode_tmap_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld, bool mn_major);
+// Operands as hi / lo pairs of tensor maps; a_mn / b_mn = 1: that operand
+// is MN-major (A stored [K, M], B [K, N]; maps with 32-row boxes), else
+// K-major (A [M, K], B [N, K]; 128-row boxes). The logits take both K-major
+// (launch_tx_logits, EpiLse); launch_tx_store (EpiStore) takes any layout:
+// op TC_DX (A K-major G, B MN-major W), TC_DW (both MN-major) or
+// TC_TEST_KK. TC_DX with an fp32 mode-0 output and few tiles splits K over
+// work items that add into the output after zeroing it; TC_TEST_KK does the
+// same with test_splits work items per tile when test_splits > 1 (fp32
+// mode-0 output).
 struct TxOperands {
   CUtensorMap ah, al, bh, bl;
+  int a_mn, b_mn;
 };
 cudaError_t launch_tx_logits(const TxOperands& o, int M, int N, int K, int* status, const EpiLse::Params& ep,
                              cudaStream_t s);
@@ -109,19 +116,16 @@ cudaError_t launch_tx_store(int op, const TxOperands& o, int M, int N, int K, in
                             const EpiStore::Params& ep, cudaStream_t s, int test_splits = 0);
 // Splits an fp32 matrix src [rows, cols] (pitch lds) into TF32 hi / lo parts:
 // hi[r, c] = x rounded to TF32, lo[r, c] = (x - hi) rounded to TF32, written
-// row-major (hi / lo, pitch ldo; hi may be src itself with ldo == lds) and /
-// or transposed (hiT / loT [cols, rows], pitch ldt). A NULL pair is skipped.
+// in the layout of src (pitch ldo; hi may be src itself with ldo == lds).
 struct SplitArgs {
   const float* src;
   int64_t rows, cols, lds;
   float* hi;
   float* lo;
   int64_t ldo;
-  float* hiT;
-  float* loT;
-  int64_t ldt;
 };
-cudaError_t launch_split_tf32(const SplitArgs& a, cudaStream_t s);
+// b (optional): a second matrix split in the same launch.
+cudaError_t launch_split_tf32(const SplitArgs& a, cudaStream_t s, const SplitArgs* b = nullptr);
 struct GradArgs;
 // The G formation of the fp32 tensor-core path fused with G's split: forms
 // G from P~ in a.src (= g.L) exactly as launch_grad_logits would (bias

@@ -114,6 +114,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same with swizzle mode 1: 128 bytes with 32-byte atoms (32-byte
+// chunks of each 128-byte row XOR-ed with the row index mod 4), the layout
+// tcgen05 reads 32-bit MN-major operands from.
+__device__ __forceinline__ uint64_t sdesc_sw128_atom32(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (sdesc_sw128(saddr, lbo, sbo) & ~(static_cast<uint64_t>(7) << 61)) | (static_cast<uint64_t>(1) << 61);
+}
+
 // Instruction descriptor for kind::f16 with 16-bit A and B and an fp32
 // accumulator: D format F32 (bits 4-5 = 1), A and B format (bits 7-9,
 // 10-12: 0 = F16, 1 = BF16), A / B major-ness (bit 15 / 16: 1 = MN-major),

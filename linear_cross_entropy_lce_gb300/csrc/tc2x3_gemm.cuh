@@ -4,12 +4,18 @@
 // (hi = x rounded to TF32, lo = x - hi, exact in fp32): the accumulator
 // receives Ahi*Bhi + Ahi*Blo + Alo*Bhi in fp32 (the dropped Alo*Blo is
 // below 2^-21 of |A||B|), so products carry about fp32 accuracy while the
-// multiply runs at the TF32 tensor rate (Ootomo & Yokota, 2022). All four
-// operands are K-major.
+// multiply runs at the TF32 tensor rate (Ootomo & Yokota, 2022).
+//
+// Each operand is K-major (stored [rows, K]: the logits' X and W, dX's G) or
+// MN-major (stored [K, rows]: dX's W, dW's G and X); kind::tf32 takes both,
+// as the 16-bit kinds do, so no operand is ever transposed in memory.
 //
 // The loads and MMAs follow tc2_gemm.cuh (CTA pairs, cta_group::2, 256 x 256
 // tiles, bounded waits): per stage each CTA loads 128 rows x 32 fp32 of Ahi,
-// Alo, Bhi, Blo (64 KB), 3 stages.
+// Alo, Bhi, Blo (64 KB), 3 stages. A K-major part is one 128-row box of 128
+// bytes of K per row, 128-byte swizzle; an MN-major part is four boxes of
+// 32 K rows x 32 fp32 (128 bytes) of MN, 4 KB apart, in the 128-byte
+// swizzle with 32-byte atoms that tcgen05 takes 32-bit MN-major operands in.
 //
 // Accumulation. The tensor cores add each MMA's products into the fp32
 // accumulator with an error that does not average out over a long K (on
@@ -69,8 +75,36 @@ constexpr int TX_STAGE_BYTES = 4 * TX_OP_BYTES;
 constexpr int TX_SMEM_BYTES = TX_STAGES * TX_STAGE_BYTES + 1024 + 512;
 constexpr int TX_THREADS = 256;
 constexpr int TX_KB_CHUNK = 16;  // K blocks of 32 accumulated in tensor memory before a fold
+constexpr int TX_MN_BOX_BYTES = TX_BK * 32 * 4;  // MN-major box: 32 K rows x 32 fp32
 
-template <class Epi>
+// kind::tf32 instruction descriptor with the operands' major-ness: bit 15
+// (A) / bit 16 (B) set = MN-major.
+__host__ __device__ constexpr uint32_t idesc_tf32_major(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_tf32_f32(M, N) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
+}
+
+// Shared-memory descriptor of K step kk (8 fp32 of K) of one 128-row part.
+// K-major: rows of 128 bytes of K, 8-row groups 1024 bytes apart, K step
+// 32 bytes into the swizzled row. MN-major: rows of 128 bytes of MN (one K
+// value each, consecutive), the four 32-wide MN boxes TX_MN_BOX_BYTES apart
+// (leading offset), 4-row K groups (the 32-byte-atom swizzle's period)
+// 512 bytes apart; a K step of 8 rows is 1024 bytes.
+template <bool MN>
+__device__ __forceinline__ uint64_t tx_sdesc(uint32_t part, int kk) {
+  return MN ? sdesc_sw128_atom32(part + kk * 1024, TX_MN_BOX_BYTES, 512) : sdesc_sw128(part + kk * 32, 16, 1024);
+}
+
+template <bool MN>
+__device__ __forceinline__ void tx_load_part(uint8_t* dst, const CUtensorMap* map, uint32_t bar, int k0, int r0) {
+  if (!MN) {
+    tma_load_2d_pair(dst, map, bar, k0, r0);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d_pair(dst + j * TX_MN_BOX_BYTES, map, bar, r0 + 32 * j, k0);
+  }
+}
+
+template <bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(TX_THREADS, 1)
     tc2x3_gemm_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
                       const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
@@ -137,10 +171,10 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
           if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * TX_STAGE_BYTES);
           const uint32_t bar = mapa_u32(&full[stage], 0);
           const int k0 = kb * TX_BK;
-          tma_load_2d_pair(st, &tmAh, bar, k0, m0);
-          tma_load_2d_pair(st + TX_OP_BYTES, &tmAl, bar, k0, m0);
-          tma_load_2d_pair(st + 2 * TX_OP_BYTES, &tmBh, bar, k0, n0);
-          tma_load_2d_pair(st + 3 * TX_OP_BYTES, &tmBl, bar, k0, n0);
+          tx_load_part<A_MN>(st, &tmAh, bar, k0, m0);
+          tx_load_part<A_MN>(st + TX_OP_BYTES, &tmAl, bar, k0, m0);
+          tx_load_part<B_MN>(st + 2 * TX_OP_BYTES, &tmBh, bar, k0, n0);
+          tx_load_part<B_MN>(st + 3 * TX_OP_BYTES, &tmBl, bar, k0, n0);
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == TX_STAGES) {
@@ -156,7 +190,7 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (even CTA only): 3 TF32 products per K
       // step into the partial P, one chunk of TX_KB_CHUNK K blocks at a time
-      constexpr uint32_t kIdesc = idesc_tf32_f32(256, 256);
+      constexpr uint32_t kIdesc = idesc_tf32_major(256, 256, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t q = 0;  // chunks issued so far (pfull / pempty phase)
@@ -180,11 +214,10 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
             const uint32_t base = smem_u32(smem + stage * TX_STAGE_BYTES);
 #pragma unroll
             for (int kk = 0; kk < TX_BK / 8; ++kk) {
-              // K-major, 128-byte swizzle: a K step of 8 fp32 is 32 bytes
-              const uint64_t ah = sdesc_sw128(base + kk * 32, 16, 1024);
-              const uint64_t al = sdesc_sw128(base + TX_OP_BYTES + kk * 32, 16, 1024);
-              const uint64_t bh = sdesc_sw128(base + 2 * TX_OP_BYTES + kk * 32, 16, 1024);
-              const uint64_t bl = sdesc_sw128(base + 3 * TX_OP_BYTES + kk * 32, 16, 1024);
+              const uint64_t ah = tx_sdesc<A_MN>(base, kk);
+              const uint64_t al = tx_sdesc<A_MN>(base + TX_OP_BYTES, kk);
+              const uint64_t bh = tx_sdesc<B_MN>(base + 2 * TX_OP_BYTES, kk);
+              const uint64_t bl = tx_sdesc<B_MN>(base + 3 * TX_OP_BYTES, kk);
               const uint32_t acc = (kb == c0 && kk == 0) ? 0u : 1u;
               tc_mma_tf32_pair(tmem_base, ah, bh, kIdesc, acc);
               tc_mma_tf32_pair(tmem_base, ah, bl, kIdesc, 1u);

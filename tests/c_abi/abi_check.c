@@ -64,11 +64,12 @@ int main(void) {
     int64_t plan[LCE_TEST_PLAN_FIELDS];
     CHECK(lce_test_plan(LCE_OP_FORWARD_BACKWARD, N, D, C, LCE_BF16, LCE_BF16, 1, 1, 0, def, plan,
                         LCE_TEST_PLAN_FIELDS) == LCE_TEST_PLAN_FIELDS);
-    CHECK(plan[0] == N && plan[31] == 65536 && plan[32] == 65536 && plan[33] == 1); /* rows, Cb, Cs, chunks */
+    const int cb = LCE_TEST_PLAN_FIELDS - 3, cs = cb + 1, nvc = cb + 2; /* the last three fields */
+    CHECK(plan[0] == N && plan[cb] == 65536 && plan[cs] == 65536 && plan[nvc] == 1); /* rows, Cb, Cs, chunks */
     size_t bw = lce_workspace_size(LCE_OP_BACKWARD, N, D, C, LCE_BF16, LCE_RED_NONE, LCE_BF16, 0);
     CHECK(lce_test_plan(LCE_OP_BACKWARD, N, D, C, LCE_BF16, LCE_BF16, 1, 1, 0, bw, plan,
                         LCE_TEST_PLAN_FIELDS) == LCE_TEST_PLAN_FIELDS);
-    CHECK(plan[32] == 0 && plan[33] == 2); /* lse given: nothing stored, two recomputed chunks */
+    CHECK(plan[cs] == 0 && plan[nvc] == 2); /* lse given: nothing stored, two recomputed chunks */
   }
 
   /* gradients from a given lse, a given denominator, scaling: host checks */

@@ -22,19 +22,10 @@ from tests.util import TOL, rel_max, rel_scalar, to64
 
 pytestmark = pytest.mark.gpu
 
-NF = 34  # LCE_TEST_PLAN_FIELDS
 
-
-def _plan(lib, op, N, D, C, dt, gdt, ws, want=(1, 1, 1)):
-    fn = lib.lce_test_plan
-    fn.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
-                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int64),
-                   ctypes.c_int]
-    fn.restype = ctypes.c_int
-    out = (ctypes.c_int64 * NF)()
-    assert fn(op, N, D, C, dt, gdt, *want, ws, out, NF) == NF
-    v = list(out)
-    return {"Bc": v[0], "nchunks": v[1], "total": v[2], "Cb": v[31], "Cs": v[32], "nvc": v[33]}
+def _plan(op, N, D, C, dt, gdt, ws):
+    """The plan a call makes for ws bytes (lce_test_plan through the binding)."""
+    return lce_mod.plan_of(op, N, D, C, dt, gdt, ws)
 
 
 def _tol(dtype, grad_dtype):
@@ -96,7 +87,7 @@ def test_recomputed_classes_match_oracle(cuda_lib, N, D, C, dtype, reduction, bi
     gd = lce_mod._DTYPE[gdt or dtype]
     red = lce_mod._REDUCTION[reduction]
     ws = lce_mod.lce_workspace_size_for_buffer(lce_mod.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, red, gd, budget)
-    plan = _plan(lce_mod.load_library(), lce_mod.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, gd, ws)
+    plan = _plan(lce_mod.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, gd, ws)
     assert plan["Cb"] == cols and plan["nvc"] >= 1 and plan["nchunks"] == 1, plan
     workspace = torch.empty(ws, dtype=torch.uint8, device="cuda")
     loss, dX, dW, db = cuda_lib.lce_forward_backward(X, W, b, t, reduction, -100, g, grad_dtype=gdt,
@@ -114,13 +105,12 @@ def test_recomputed_and_batch_chunks_together(cuda_lib):
     N, D, C, dtype = 1500, 64, 2000, torch.bfloat16
     inp = make_linear_inputs(N, D, C, dtype, "cuda", seed=41, bias=True, w_std=0.5, b_std=0.3, n_ignored=30)
     X, W, b, t = inp["X"], inp["W"], inp["b"], inp["target"]
-    lib = cuda_lib.load_library()
     dt = lce_mod.LCE_BF16
     ws = None
     for budget in range(N * 256 * 2 - 1, 2 * 256 * 256, -4096):
         cand = cuda_lib.lce_workspace_size_for_buffer(lce_mod.LCE_OP_FORWARD_BACKWARD, N, D, C, dt,
                                                       lce_mod.LCE_RED_MEAN, dt, budget)
-        p = _plan(lib, lce_mod.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, dt, cand)
+        p = _plan(lce_mod.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, dt, cand)
         if p["nchunks"] > 1 and p["nvc"] > 0:
             ws = cand
             break

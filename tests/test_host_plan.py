@@ -4,13 +4,14 @@ the workspace plan (batch chunk, region offsets) at sizes far beyond what
 the GPU tests run. Nothing here touches a GPU."""
 
 import ctypes
+import os
 
 import pytest
 
 import linear_cross_entropy_lce_gb300 as lce
 from linear_cross_entropy_lce_gb300 import _build
 
-NF = 34  # LCE_TEST_PLAN_FIELDS
+NF = 28  # LCE_TEST_PLAN_FIELDS
 I64 = ctypes.c_int64
 
 
@@ -113,8 +114,8 @@ def test_plan_regions_fit_and_do_not_overlap(lib, op, N, D, C, dtype):
         r, v = _plan(lib, op, N, D, C, dtype, grad_dtype, ws)
         assert r == NF
         Bc, nchunks, total, C_pad, nseg = v[:5]
-        offs = v[5:31]
-        Cb, Cs, nvc = v[31:34]
+        offs = v[5:25]
+        Cb, Cs, nvc = v[25:28]
         # the plan the calls choose for the queried size is the one it was sized for (or a faster one)
         assert total <= ws
         assert 1 <= Bc <= N and nchunks == -(-N // Bc)
@@ -141,6 +142,15 @@ def test_plan_regions_fit_and_do_not_overlap(lib, op, N, D, C, dtype):
                 assert off_wv - off_lse >= 4 * Bc and off_dx - off_wv >= 4 * Bc
         else:
             assert off_dw == off_L                      # no P~ buffer in the forward
+        if dtype == lce.LCE_F32 and os.environ.get("LCE_F32_SIMT") != "1":
+            # 3xTF32: hi / lo of W and of the chunk's X in their own layout,
+            # and G's lo part beside the buffer; no transposed copies
+            off_wh, off_wl, off_xh, off_xl, off_gl = offs[15:20]
+            ldD = -(-D // 4) * 4
+            assert off_wl - off_wh >= C * ldD * 4 and off_xh - off_wl >= C * ldD * 4
+            assert off_xl - off_xh >= Bc * ldD * 4 and off_gl - off_xl >= Bc * ldD * 4
+            if backward:
+                assert total - off_gl >= Bc * C_pad * 4
 
 
 @pytest.mark.parametrize("N,D,C,Bc,Cb,nvc", [
@@ -154,8 +164,8 @@ def test_default_plan_bounds_the_gradient_buffer(lib, N, D, C, Bc, Cb, nvc):
     ws = _ws(lib, lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, dt)
     r, v = _plan(lib, lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, dt, ws)
     assert r == NF
-    assert (v[0], v[31], v[33]) == (Bc, Cb, nvc)
-    assert v[0] * v[31] * 2 <= GIB
+    assert (v[0], v[25], v[27]) == (Bc, Cb, nvc)
+    assert v[0] * v[25] * 2 <= GIB
     # no [C, D] fp32 scratch unless the rows are split into batch chunks
     assert (v[13] - v[12] > 0) == (v[1] > 1)
     # lce_workspace_size_for_buffer with 0 is the default; a huge budget stores every class
@@ -163,7 +173,7 @@ def test_default_plan_bounds_the_gradient_buffer(lib, N, D, C, Bc, Cb, nvc):
     big = lib.lce_workspace_size_for_buffer(lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, lce.LCE_RED_MEAN, dt,
                                             ctypes.c_size_t(-1).value)
     r, v = _plan(lib, lce.LCE_OP_FORWARD_BACKWARD, N, D, C, dt, dt, big)
-    assert v[33] == 0 and v[31] == v[3]
+    assert v[27] == 0 and v[25] == v[3]
 
 
 def test_plan_smaller_workspace_recomputes_more(lib):
@@ -175,7 +185,7 @@ def test_plan_smaller_workspace_recomputes_more(lib):
         ws = lib.lce_workspace_size_for_buffer(op, N, D, C, dt, lce.LCE_RED_MEAN, dt, mib << 20)
         r, v = _plan(lib, op, N, D, C, dt, dt, ws)
         assert r == NF and v[2] <= ws
-        Bc, Cb = v[0], v[31]
+        Bc, Cb = v[0], v[25]
         if prev is not None:
             assert (Bc, Cb) <= prev or Bc < prev[0]
         prev = (Bc, Cb)
@@ -190,7 +200,7 @@ def test_chunk_rows_plan(lib):
     op, N, D, C, dt = lce.LCE_OP_FORWARD_BACKWARD, 8192, 4096, 128256, lce.LCE_BF16
     ws = _ws(lib, op, N, D, C, dt, dt, N)
     r, v = _plan(lib, op, N, D, C, dt, dt, ws)
-    assert (v[0], v[31], v[33]) == (N, v[3], 0)
+    assert (v[0], v[25], v[27]) == (N, v[3], 0)
     assert ws >= N * 128256 * 2  # the whole [N, C] buffer (2.1 GB)
 
 
@@ -211,7 +221,7 @@ def test_aspect_ratio_chunk_rows(lib):
     op, dt = lce.LCE_OP_FORWARD_BACKWARD, lce.LCE_BF16
     ws = _ws(lib, op, 8192, 4096, 128256, dt, dt, 256)
     r, v = _plan(lib, op, 8192, 4096, 128256, dt, dt, ws)
-    assert r == NF and v[31] == v[3] and v[33] == 0
+    assert r == NF and v[25] == v[3] and v[27] == 0
 
 
 def test_budget_below_the_smallest_block(lib):
@@ -221,5 +231,5 @@ def test_budget_below_the_smallest_block(lib):
     op, N, D, C, dt = lce.LCE_OP_FORWARD_BACKWARD, 100000, 1024, 50000, lce.LCE_BF16
     tiny = f(op, N, D, C, dt, lce.LCE_RED_MEAN, dt, 4096)
     r, v = _plan(lib, op, N, D, C, dt, dt, tiny)
-    assert r == NF and v[0] == 256 and v[31] == 1024
+    assert r == NF and v[0] == 256 and v[25] == 1024
     assert v[2] <= tiny
