@@ -44,21 +44,21 @@ METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor
 MEASURED_TRAFFIC = {
     # full-size one-pass captures (gpu__time_duration.sum, dram__bytes_read.sum,
     # dram__bytes_write.sum) of one step after one warm-up step
-    ("bf16_llm_head", "gemm_logits_tc"): (1701708608, "4ef7923", "e83d01cb037b26be"),  # mean of 4 launches
-    ("bf16_llm_head", "gemm_dx_tc"): (9017741568, "4ef7923", "e83d01cb037b26be"),  # mean of 2 launches
-    ("bf16_llm_head", "gemm_dw_tc"): (4773951360, "4ef7923", "e83d01cb037b26be"),  # mean of 2 launches
-    ("bf16_llm_head", "gemm_recompute_tc"): (2337580032, "4ef7923", "e83d01cb037b26be"),  # mean of 1 launches
-    ("bf16_large_head", "gemm_logits_tc"): (4634980096, "4ef7923", "e83d01cb037b26be"),  # mean of 1 launches
-    ("bf16_large_head", "gemm_recompute_tc"): (2605425472, "4ef7923", "e83d01cb037b26be"),  # mean of 4 launches
-    ("bf16_large_head", "gemm_dx_tc"): (8640299776, "4ef7923", "e83d01cb037b26be"),  # mean of 4 launches
-    ("bf16_large_head", "gemm_dw_tc"): (8394217216, "4ef7923", "e83d01cb037b26be"),  # mean of 4 launches
-    ("ce_logits_fp32", "ce_resident"): (17380607744, "4ef7923", "e672dda6789166aa"),
-    ("tiny_fp32", "gemm_logits_3xtf32"): (275200, "4ef7923", "fdfbb03045cc9877"),
-    ("tiny_fp32", "gemm_dx_3xtf32"): (488448, "4ef7923", "fdfbb03045cc9877"),
-    ("tiny_fp32", "gemm_dw_3xtf32"): (373248, "4ef7923", "fdfbb03045cc9877"),
-    ("fp32_mid", "gemm_logits_3xtf32"): (52793344, "4ef7923", "fdfbb03045cc9877"),
-    ("fp32_mid", "gemm_dx_3xtf32"): (176351488, "4ef7923", "fdfbb03045cc9877"),
-    ("fp32_mid", "gemm_dw_3xtf32"): (142777600, "4ef7923", "fdfbb03045cc9877"),
+    ("bf16_llm_head", "gemm_logits_tc"): (1707260288, "3a95670", "161db653d4f29df5"),  # mean of 4 launches
+    ("bf16_llm_head", "gemm_dx_tc"): (7157857024, "3a95670", "161db653d4f29df5"),  # mean of 2 launches
+    ("bf16_llm_head", "gemm_dw_tc"): (5025593600, "3a95670", "161db653d4f29df5"),  # mean of 2 launches
+    ("bf16_llm_head", "gemm_recompute_tc"): (2370174464, "3a95670", "161db653d4f29df5"),  # mean of 1 launches
+    ("bf16_large_head", "gemm_logits_tc"): (4621625344, "3a95670", "161db653d4f29df5"),  # mean of 1 launches
+    ("bf16_large_head", "gemm_recompute_tc"): (2669385216, "3a95670", "161db653d4f29df5"),  # mean of 4 launches
+    ("bf16_large_head", "gemm_dx_tc"): (7491472512, "3a95670", "161db653d4f29df5"),  # mean of 4 launches
+    ("bf16_large_head", "gemm_dw_tc"): (6940999488, "3a95670", "161db653d4f29df5"),  # mean of 4 launches
+    ("ce_logits_fp32", "ce_resident"): (17415280640, "3a95670", "cbc8eadfcfbde878"),
+    ("tiny_fp32", "gemm_logits_3xtf32"): (274688, "3a95670", "874a1b0a4e9d30f9"),
+    ("tiny_fp32", "gemm_dx_3xtf32"): (486400, "3a95670", "874a1b0a4e9d30f9"),
+    ("tiny_fp32", "gemm_dw_3xtf32"): (371456, "3a95670", "874a1b0a4e9d30f9"),
+    ("fp32_mid", "gemm_logits_3xtf32"): (52609792, "3a95670", "874a1b0a4e9d30f9"),
+    ("fp32_mid", "gemm_dx_3xtf32"): (179825408, "3a95670", "874a1b0a4e9d30f9"),
+    ("fp32_mid", "gemm_dw_3xtf32"): (142753280, "3a95670", "874a1b0a4e9d30f9"),
 }
 
 CSRC = os.path.join(ROOT, "linear_cross_entropy_lce_gb300", "csrc")
