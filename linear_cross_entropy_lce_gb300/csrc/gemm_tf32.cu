@@ -142,6 +142,7 @@ cudaError_t launch_tx(const TxOperands& o, int M, int N, int K, int m_inner, int
   if (splits > nkb) splits = nkb;
   g.kb_per_split = (nkb + splits - 1) / splits;
   splits = (nkb + g.kb_per_split - 1) / g.kb_per_split;  // no empty work item
+  g.single = g.kb_per_split <= TX_KB_CHUNK ? 1 : 0;
   g.num_tiles = g.mn_tiles * splits;
   g.m_inner = m_inner ? m_group_for(g.num_m_blocks, 256, K, 8) : 0;  // hi + lo fp32 parts of A
   g.status = status;

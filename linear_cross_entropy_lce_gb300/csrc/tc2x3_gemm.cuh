@@ -28,6 +28,11 @@
 // chunk; the tile's epilogue then reads R. The error stays that of a
 // 512-long chain whatever K is (about 4e-6 of the largest entry).
 //
+// When every work item's K range fits in one chunk (g.single), no partial
+// ever needs folding: the two halves of tensor memory are then two
+// accumulators used in turn, the epilogue reads each directly, and the MMAs
+// of the next item run while the epilogue drains the previous one.
+//
 // The K range may be split over k_splits work items per output tile, whose
 // epilogues then add into a zeroed fp32 output (EpiStore mode 4).
 #pragma once
@@ -45,6 +50,7 @@ struct TxArgs {
   int num_tiles;                   // mn_tiles * k_splits
   int kb_per_split;                // 32-wide K blocks per work item
   int m_inner;                     // as TcGemmArgs::m_inner (0, or row blocks per group)
+  int single;                      // every work item has at most TX_KB_CHUNK K blocks
   int* status;
 };
 
@@ -113,9 +119,11 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + TX_STAGES * TX_STAGE_BYTES);
   uint64_t* empty = full + TX_STAGES;
-  uint64_t* pfull = empty + TX_STAGES;  // partial P complete (MMA -> fold)
-  uint64_t* pempty = pfull + 1;         // P folded into R (fold -> MMA), 8 arrivals
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + 1);
+  // [2]: partial P complete (MMA -> fold), or with g.single accumulator b complete
+  uint64_t* pfull = empty + TX_STAGES;
+  // [2]: P folded into R (fold -> MMA), or accumulator b drained; 8 arrivals
+  uint64_t* pempty = pfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -129,8 +137,10 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(pfull, 1);
-    mbar_init(pempty, 8);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&pfull[b], 1);
+      mbar_init(&pempty[b], 8);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -194,13 +204,18 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t q = 0;  // chunks issued so far (pfull / pempty phase)
+      const bool single = g.single != 0;
       bool ok = true;
       for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
         int mb, nb, kb0, kb1;
         tx_tile(g, tile, mb, nb, kb0, kb1);
         for (int c0 = kb0; c0 < kb1 && ok; c0 += TX_KB_CHUNK, ++q) {
           const int c1 = c0 + TX_KB_CHUNK < kb1 ? c0 + TX_KB_CHUNK : kb1;
-          if (!mbar_wait_cluster(pempty, (q & 1u) ^ 1u, abort_flag)) {
+          // accumulator of this chunk: P (columns 0-255), or with single
+          // work items the two halves in turn
+          const uint32_t buf = single ? (q & 1u) : 0u;
+          const uint32_t par = single ? ((q >> 1) & 1u) : (q & 1u);
+          if (!mbar_wait_cluster(&pempty[buf], par ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -219,9 +234,10 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
               const uint64_t bh = tx_sdesc<B_MN>(base + 2 * TX_OP_BYTES, kk);
               const uint64_t bl = tx_sdesc<B_MN>(base + 3 * TX_OP_BYTES, kk);
               const uint32_t acc = (kb == c0 && kk == 0) ? 0u : 1u;
-              tc_mma_tf32_pair(tmem_base, ah, bh, kIdesc, acc);
-              tc_mma_tf32_pair(tmem_base, ah, bl, kIdesc, 1u);
-              tc_mma_tf32_pair(tmem_base, al, bh, kIdesc, 1u);
+              const uint32_t d = tmem_base + buf * 256;
+              tc_mma_tf32_pair(d, ah, bh, kIdesc, acc);
+              tc_mma_tf32_pair(d, ah, bl, kIdesc, 1u);
+              tc_mma_tf32_pair(d, al, bh, kIdesc, 1u);
             }
             tc_commit_pair_mc(&empty[stage], 0x3);
             if (++stage == TX_STAGES) {
@@ -229,7 +245,7 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
               phase ^= 1u;
             }
           }
-          if (ok) tc_commit_pair_mc(pfull, 0x3);
+          if (ok) tc_commit_pair_mc(&pfull[buf], 0x3);
         }
       }
     }
@@ -244,9 +260,28 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
     for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
       int mb, nb, kb0, kb1;
       tx_tile(g, tile, mb, nb, kb0, kb1);
+      const int64_t row = static_cast<int64_t>(mb) * 256 + rank * 128 + qw * 32 + lane;
+      const int64_t col0 = static_cast<int64_t>(nb) * 256;
+      if (g.single) {
+        // one chunk: the epilogue reads the accumulator itself, then frees it
+        const uint32_t buf = q & 1u;
+        int okw = 1;
+        if (lane == 0) okw = mbar_wait_cluster(&pfull[buf], (q >> 1) & 1u, abort_flag) ? 1 : 0;
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) break;
+        tc_fence_after();
+        const uint32_t tA = tP + buf * 256;
+        Epi::template run<8, 4>(
+            ep, row, col0, nb, [&](int g, float (&v)[128]) { tmem_ld128(tA + g * 128, v); }, io);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_u32(&pempty[buf], 0));
+        ++q;
+        continue;
+      }
       for (int c0 = kb0; c0 < kb1; c0 += TX_KB_CHUNK, ++q) {
         int okw = 1;
-        if (lane == 0) okw = mbar_wait_cluster(pfull, q & 1u, abort_flag) ? 1 : 0;
+        if (lane == 0) okw = mbar_wait_cluster(&pfull[0], q & 1u, abort_flag) ? 1 : 0;
         okw = __shfl_sync(0xffffffffu, okw, 0);
         if (!okw) {
           ok = false;
@@ -272,11 +307,9 @@ __global__ void __launch_bounds__(TX_THREADS, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_u32(pempty, 0));
+        if (lane == 0) mbar_arrive_cluster(mapa_u32(&pempty[0], 0));
       }
       if (!ok) break;
-      const int64_t row = static_cast<int64_t>(mb) * 256 + rank * 128 + qw * 32 + lane;
-      const int64_t col0 = static_cast<int64_t>(nb) * 256;
       Epi::template run<8, 4>(
           ep, row, col0, nb, [&](int g, float (&v)[128]) { tmem_ld128(tR + g * 128, v); }, io);
     }
