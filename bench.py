@@ -44,14 +44,14 @@ METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s at 1 GB300; % bf16 tensor
 MEASURED_TRAFFIC = {
     # full-size one-pass captures (gpu__time_duration.sum, dram__bytes_read.sum,
     # dram__bytes_write.sum) of one step after one warm-up step
-    ("bf16_llm_head", "gemm_logits_tc"): (1707260288, "3a95670", "161db653d4f29df5"),  # mean of 4 launches
-    ("bf16_llm_head", "gemm_dx_tc"): (7157857024, "3a95670", "161db653d4f29df5"),  # mean of 2 launches
-    ("bf16_llm_head", "gemm_dw_tc"): (5025593600, "3a95670", "161db653d4f29df5"),  # mean of 2 launches
-    ("bf16_llm_head", "gemm_recompute_tc"): (2370174464, "3a95670", "161db653d4f29df5"),  # mean of 1 launches
-    ("bf16_large_head", "gemm_logits_tc"): (4621625344, "3a95670", "161db653d4f29df5"),  # mean of 1 launches
-    ("bf16_large_head", "gemm_recompute_tc"): (2669385216, "3a95670", "161db653d4f29df5"),  # mean of 4 launches
-    ("bf16_large_head", "gemm_dx_tc"): (7491472512, "3a95670", "161db653d4f29df5"),  # mean of 4 launches
-    ("bf16_large_head", "gemm_dw_tc"): (6940999488, "3a95670", "161db653d4f29df5"),  # mean of 4 launches
+    ("bf16_llm_head", "gemm_logits_tc"): (1710572416, "f97684c", "08ce547b25b2a1b7"),  # mean of 4 launches
+    ("bf16_llm_head", "gemm_dx_tc"): (5836620416, "f97684c", "08ce547b25b2a1b7"),  # mean of 2 launches
+    ("bf16_llm_head", "gemm_dw_tc"): (4515026816, "f97684c", "08ce547b25b2a1b7"),  # mean of 2 launches
+    ("bf16_llm_head", "gemm_recompute_tc"): (2388614144, "f97684c", "08ce547b25b2a1b7"),  # mean of 1 launches
+    ("bf16_large_head", "gemm_logits_tc"): (4606856448, "f97684c", "08ce547b25b2a1b7"),  # mean of 1 launches
+    ("bf16_large_head", "gemm_recompute_tc"): (2726271488, "f97684c", "08ce547b25b2a1b7"),  # mean of 4 launches
+    ("bf16_large_head", "gemm_dx_tc"): (6234672448, "f97684c", "08ce547b25b2a1b7"),  # mean of 4 launches
+    ("bf16_large_head", "gemm_dw_tc"): (5786866944, "f97684c", "08ce547b25b2a1b7"),  # mean of 4 launches
     ("ce_logits_fp32", "ce_resident"): (17415280640, "3a95670", "cbc8eadfcfbde878"),
     ("tiny_fp32", "gemm_logits_3xtf32"): (301312, "acaef4c", "f5ad3eb2b57b7737"),
     ("tiny_fp32", "gemm_dx_3xtf32"): (507392, "acaef4c", "f5ad3eb2b57b7737"),
