@@ -6,7 +6,13 @@ dX, dW) on inputs resident in HBM, with the library's default workspace
 plan (gradient buffer bounded by 1 GiB). Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl reference]
+                  [--impl reference] [--dtype f16] [--class-weights]
+                  [--api autograd]
+
+--dtype f16 runs a bf16 workload's inputs in fp16, --class-weights adds
+per-class cross-entropy weights (the _ex entry points), --api autograd
+times the step through linear_cross_entropy(...).backward(); each prints
+the same JSON line for that variant of the workload.
 
 --impl reference times the float64 CPU oracle on the host cores on a
 bounded sample of the same workload (the method has no other reference
@@ -172,7 +178,7 @@ def _dist():
     return ws, rank
 
 
-def _oracle_sample_seconds(name, rows, device_inputs=None, seed=0):
+def _oracle_sample_seconds(name, rows, device_inputs=None, seed=0, class_weight=None):
     """Time the float64 oracle on `rows` rows of the workload (host cores)."""
     from oracle import lce_oracle as O
 
@@ -189,8 +195,9 @@ def _oracle_sample_seconds(name, rows, device_inputs=None, seed=0):
     b = None if inp["b"] is None else inp["b"].double().cpu().numpy()
     t = inp["target"][:rows].cpu().numpy()
     g = None if inp["grad_out"] is None else inp["grad_out"][:rows].double().cpu().numpy()
+    cw = None if class_weight is None else class_weight.double().cpu().numpy()
     t0 = time.perf_counter()
-    O.lce_forward_backward(X, W, b, t, w.reduction, -100, g)
+    O.lce_forward_backward(X, W, b, t, w.reduction, -100, g, class_weight=cw)
     return time.perf_counter() - t0
 
 
@@ -312,6 +319,12 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     peaks = _peaks()
+    variant = []  # departures from the named workload (--dtype, --class-weights, --api)
+    cw = None
+    if args.api == "autograd":
+        if w.kind == "logits":
+            raise SystemExit("bench: --api autograd applies to the linear workloads")
+        variant.append("autograd")
 
     if w.kind == "logits":
         logits, t = inp["logits"], inp["target"]
@@ -327,12 +340,24 @@ def run_gpu(args):
             status_acc.bitwise_or_(status_word)
             return out
 
+        dt = lce.LCE_F32
         flops = 0.0
     else:
         X, W, b, t, g = inp["X"], inp["W"], inp["b"], inp["target"], inp["grad_out"]
         N, D = X.shape
         C = W.shape[0]
-        dt = lce.LCE_BF16 if X.dtype == torch.bfloat16 else lce.LCE_F32
+        if args.dtype == "f16":
+            if X.dtype != torch.bfloat16:
+                raise SystemExit("bench: --dtype f16 applies to the bf16 workloads")
+            X, W = X.half(), W.half()
+            b = None if b is None else b.half()
+            inp = dict(inp, X=X, W=W, b=b)
+            variant.append("f16")
+        if args.class_weights:
+            gen = torch.Generator(device=dev).manual_seed(7)
+            cw = torch.rand(C, generator=gen, device=dev) + 0.5
+            variant.append("class_weights")
+        dt = {torch.bfloat16: lce.LCE_BF16, torch.float16: lce.LCE_F16}.get(X.dtype, lce.LCE_F32)
         red = {"none": 0, "sum": 1, "mean": 2}[w.reduction]
         # reduction none: forward (loss, lse), then the backward from that lse
         # (the page's none op); else one forward+backward call
@@ -358,24 +383,58 @@ def run_gpu(args):
         P = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())
 
         def calls(Xi, Wi, bi, ti, gi, li, dXi, dWi, dbi, mark=None):
+            st = ctypes.c_void_p(stream.cuda_stream)
             if red == 0:
-                lce._check(lib.lce_forward(P(Xi), P(Wi), P(bi), P(ti), N, D, C, dt, 0, red, -100, P(li), P(lse),
-                                           P(wsbuf), nbytes, ctypes.c_void_p(stream.cuda_stream)), "fwd")
+                if cw is None:
+                    e = lib.lce_forward(P(Xi), P(Wi), P(bi), P(ti), N, D, C, dt, 0, red, -100, P(li), P(lse),
+                                        P(wsbuf), nbytes, st)
+                else:
+                    e = lib.lce_forward_ex(P(Xi), P(Wi), P(bi), P(ti), P(cw), None, N, D, C, dt, 0, red, -100,
+                                           P(li), P(lse), P(wsbuf), nbytes, st)
+                lce._check(e, "fwd")
                 status_acc.bitwise_or_(status_word)
                 if mark is not None:
                     mark()  # CUDA event between the two parts
-                lce._check(lib.lce_backward(P(Xi), P(Wi), P(bi), P(ti), P(lse), N, D, C, dt, 0, red, -100, P(gi),
-                                            P(dXi), P(dWi), P(dbi), dt, P(wsbuf), nbytes,
-                                            ctypes.c_void_p(stream.cuda_stream)), "bwd")
-            else:
+                if cw is None:
+                    e = lib.lce_backward(P(Xi), P(Wi), P(bi), P(ti), P(lse), N, D, C, dt, 0, red, -100, P(gi),
+                                         P(dXi), P(dWi), P(dbi), dt, P(wsbuf), nbytes, st)
+                else:
+                    e = lib.lce_backward_ex(P(Xi), P(Wi), P(bi), P(ti), P(cw), None, P(lse), N, D, C, dt, 0, red,
+                                            -100, P(gi), P(dXi), P(dWi), P(dbi), dt, P(wsbuf), nbytes, st)
+                lce._check(e, "bwd")
+            elif cw is None:
                 lce._check(lib.lce_forward_backward(P(Xi), P(Wi), P(bi), P(ti), N, D, C, dt, 0, red, -100, P(gi),
-                                                    P(li), P(dXi), P(dWi), P(dbi), dt, P(wsbuf), nbytes,
-                                                    ctypes.c_void_p(stream.cuda_stream)), "fwd+bwd")
+                                                    P(li), P(dXi), P(dWi), P(dbi), dt, P(wsbuf), nbytes, st),
+                           "fwd+bwd")
+            else:
+                lce._check(lib.lce_forward_backward_ex(P(Xi), P(Wi), P(bi), P(ti), P(cw), None, N, D, C, dt, 0,
+                                                       red, -100, P(gi), P(li), P(dXi), P(dWi), P(dbi), dt,
+                                                       P(wsbuf), nbytes, st), "fwd+bwd")
             status_acc.bitwise_or_(status_word)
 
-        def step(mark=None):
-            calls(X, W, b, t, g, loss, dX, dW, db, mark)
-            return loss
+        if args.api == "autograd":
+            # the public autograd function: its own workspace (the library's
+            # default plan) and gradient buffers from torch's caching
+            # allocator; after the timed steps its gradients are compared
+            # with the C-ABI call's (a pipeline that gave up would not match)
+            from linear_cross_entropy_lce_gb300.autograd import linear_cross_entropy
+
+            leaves = [x.detach().requires_grad_() if x is not None else None for x in (X, W, b)]
+
+            def step(mark=None):
+                for p in leaves:
+                    if p is not None:
+                        p.grad = None
+                out = linear_cross_entropy(leaves[0], leaves[1], t, bias=leaves[2], reduction=w.reduction,
+                                           ignore_index=-100, class_weight=cw)
+                if mark is not None:
+                    mark()
+                out.backward(None if g is None else g.reshape(out.shape))
+                return out
+        else:
+            def step(mark=None):
+                calls(X, W, b, t, g, loss, dX, dW, db, mark)
+                return loss
 
         flops = w.flops_fwd_bwd
 
@@ -448,12 +507,23 @@ def run_gpu(args):
     launches = lce.launch_count() - launches0
     clocks = sampler.stop()
     ms = aggregate_ms(per_step, dist, dev)
+    if args.api == "autograd":
+        # the autograd function's workspace is its own, so its status word is
+        # not visible here: check its gradients against the C-ABI call instead
+        step()
+        calls(X, W, b, t, g, loss, dX, dW, db)
+        barrier()
+        check_status("C-ABI comparison call")
+        for got, ref, what in ((leaves[0].grad, dX, "dX"), (leaves[1].grad, dW, "dW")):
+            err = float((got.float() - ref.float()).abs().max() / ref.float().abs().max().clamp_min(1e-30))
+            if not err <= 1e-3:
+                raise SystemExit(f"bench: autograd {what} differs from the C-ABI call ({err:.2e}); not a measurement")
 
     # ---- context for the memory bound: the same step with the plan that
     # keeps every class of every row in the gradient buffer (no
     # recomputation), a few steps, outside the timed region
     whole = None
-    if w.kind != "logits" and dist is None:
+    if w.kind != "logits" and dist is None and args.api == "abi":
         wbytes = lce.lce_workspace_size_for_buffer(bw_op, N, D, C, dt, red, dt, (1 << 63) - 1)
         if red == 0:
             wbytes = max(wbytes, lce.lce_workspace_size(lce.LCE_OP_FORWARD, N, D, C, dt, red, dt, 0))
@@ -488,7 +558,7 @@ def run_gpu(args):
     # library allocates and synchronizes nothing, so its calls capture):
     # reported for short steps, where launch overhead is visible
     graph_ms = None
-    if ms < 5.0 and dist is None:
+    if ms < 5.0 and dist is None and args.api == "abi":
         cap_stream = torch.cuda.Stream()
         cap_stream.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
@@ -543,6 +613,19 @@ def run_gpu(args):
 
         def run_on(i):
             Xi, Wi, ti, bi, gi = in_sets[i]
+            if args.api == "autograd":
+                # fresh gradient tensors each step: they are handed to the
+                # result copy's stream so their memory is not reused early
+                lv = [x.detach().requires_grad_() if x is not None else None for x in (Xi, Wi, bi)]
+                out = linear_cross_entropy(lv[0], lv[1], ti, bias=lv[2], reduction=w.reduction, ignore_index=-100,
+                                           class_weight=cw)
+                out.backward(None if gi is None else gi.reshape(out.shape))
+                res = [out.detach(), lv[0].grad, lv[1].grad, None if lv[2] is None else lv[2].grad]
+                for r in res:
+                    if r is not None:
+                        r.record_stream(out_stream)
+                out_sets[i] = res
+                return
             li, dXi, dWi, dbi = out_sets[i]
             calls(Xi, Wi, bi, ti, gi, li, dXi, dWi, dbi)
     else:
@@ -633,7 +716,8 @@ def run_gpu(args):
         n_l, tot_ms, work = prof[dominant]
         avg_s = tot_ms / n_l / 1e3
         per_launch = work / n_l
-        traffic, traffic_note = measured_traffic(name, dominant)
+        # captures are of the named workloads as given: a variant has none
+        traffic, traffic_note = measured_traffic("+".join([name] + variant), dominant)
         common = {"traffic": traffic, "traffic_note": traffic_note, "kernel": dominant,
                   "launches_per_step": n_l / prof_steps}
         if dominant.startswith("gemm_") and (dominant.endswith("_tc") or dominant.endswith("_3xtf32")):
@@ -671,7 +755,7 @@ def run_gpu(args):
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
         rows = args.cpu_rows
-        sec = _oracle_sample_seconds(args.workload, rows, inp)
+        sec = _oracle_sample_seconds(args.workload, rows, inp, class_weight=cw)
         cpu = {"value": rows / sec, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
                "sample": f"{rows} of {w.N} rows, full method (loss and all gradients for those rows) in "
                          f"float64 numpy, {sec:.1f} s"}
@@ -679,9 +763,14 @@ def run_gpu(args):
     tokens_per_s = ws * w.N / (ms / 1e3)
     cfg = _config(w, ws, l2_bytes)
     cfg["workspace_bytes"] = int(nbytes)
+    if variant:
+        cfg["variant"] = {"input_dtype": "f16" if "f16" in variant else None,
+                          "class_weights": "uniform [0.5, 1.5), seed 7" if cw is not None else None,
+                          "api": "autograd: linear_cross_entropy(...).backward()" if args.api == "autograd"
+                                 else "C ABI"}
     executed = None
     if w.kind != "logits":
-        esz = 2 if w.dtype == torch.bfloat16 else 4
+        esz = X.element_size()
         cfg["gradient_buffer"] = {
             "rows": plan["Bc"], "classes": plan["Cb"], "bytes": plan["Bc"] * plan["Cb"] * esz,
             "stored_classes": min(plan["Cs"], w.C), "recomputed_class_chunks": plan["nvc"],
@@ -704,7 +793,7 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "dtype": {lce.LCE_BF16: "bf16", lce.LCE_F16: "f16"}.get(dt, "f32"),
         "data": "synthetic",
         "config": cfg,
         "gpu_launches": launches,
@@ -754,6 +843,12 @@ def main():
                     help="print the source hash of every kernel in KERNEL_SOURCES and exit")
     ap.add_argument("--buffer-mib", type=int, default=None,
                     help="gradient-buffer budget of the workspace plan (default: the library's 1 GiB)")
+    ap.add_argument("--dtype", default="input", choices=["input", "f16"],
+                    help="f16: a bf16 workload's X, W and bias in fp16 instead")
+    ap.add_argument("--class-weights", action="store_true",
+                    help="per-class cross-entropy weights, uniform in [0.5, 1.5) (seed 7)")
+    ap.add_argument("--api", default="abi", choices=["abi", "autograd"],
+                    help="autograd: the step is linear_cross_entropy(...).backward() on the same inputs")
     args = ap.parse_args()
     if args.print_source_hashes:
         print(json.dumps({k: kernel_sources_hash(k) for k in KERNEL_SOURCES}))
