@@ -297,18 +297,23 @@ def lce_forward_backward(X, W, b, target, reduction="mean", ignore_index=DEFAULT
 
 
 def forward_stats(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE_INDEX,
-                  grad_out=None, want_db=False, row_block=ROW_BLOCK):
+                  grad_out=None, want_db=False, row_block=ROW_BLOCK, class_weight=None):
     """One full blockwise pass: lse[N], loss_n[N], the reduced loss, w[N]
     and (optionally) db[C] = sum_n G[n, :]. X and W may be float32/bfloat16
-    values held in float32 arrays; each block is upcast to float64."""
+    values held in float32 arrays; each block is upcast to float64. With
+    class weights (the page's weight option), a valid row's loss is
+    weight[t_n] (lse_n - z_t) and mean divides by the sum of those weights,
+    as in lce_forward."""
     _check_reduction(reduction)
     N = X.shape[0]
     C = W.shape[0]
     target = np.asarray(target, dtype=np.int64).reshape(-1)
     valid = valid_mask(target, C, ignore_index)
     tc = corrected_target(target, valid)
+    c = class_weight_of_rows(target, valid, class_weight)
     w = row_weights(target, C, reduction, ignore_index,
-                    grad_out if (grad_out is not None or reduction != "none") else np.ones(N))
+                    grad_out if (grad_out is not None or reduction != "none") else np.ones(N),
+                    class_weight=class_weight)
     W64 = _f64(W)
     lse = np.zeros(N)
     loss_rows = np.zeros(N)
@@ -319,7 +324,7 @@ def forward_stats(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE
         z = logits_block(X[r0:r1], W64, b)
         l = log_sum_exp(z)
         lse[r0:r1] = l
-        loss_rows[r0:r1] = np.where(valid[r0:r1], l - z[rows, tc[r0:r1]], 0.0)
+        loss_rows[r0:r1] = np.where(valid[r0:r1], c[r0:r1] * (l - z[rows, tc[r0:r1]]), 0.0)
         if db is not None:
             G = np.exp(z - l[:, None])
             G[rows, tc[r0:r1]] -= valid[r0:r1].astype(np.float64)
@@ -327,7 +332,7 @@ def forward_stats(X, W, b, target, reduction="mean", ignore_index=DEFAULT_IGNORE
     return {
         "lse": lse,
         "loss_rows": loss_rows,
-        "loss": _reduce(loss_rows, valid.astype(np.float64), reduction),
+        "loss": _reduce(loss_rows, c, reduction),
         "w": w,
         "valid": valid,
         "db": db,

@@ -258,9 +258,12 @@ def test_ce_from_logits_against_torch(reduction, g):
 
 def test_sampled_paths_match_full():
     X, W, b, t = _rand_case(N=300, D=8, C=40, n_ign=20, seed=9)
-    for reduction, g in (("mean", 1.7), ("none", RNG.standard_normal(300))):
-        loss, dX, dW, db = O.lce_forward_backward(X, W, b, t, reduction, grad_out=g)
-        st = O.forward_stats(X, W, b, t, reduction, grad_out=g, want_db=True, row_block=64)
+    cw = RNG.uniform(0.3, 2.0, 40)
+    cases = [("mean", 1.7, None), ("none", RNG.standard_normal(300), None), ("mean", 1.7, cw), ("sum", None, cw),
+             ("none", RNG.standard_normal(300), cw)]
+    for reduction, g, c in cases:
+        loss, dX, dW, db = O.lce_forward_backward(X, W, b, t, reduction, grad_out=g, class_weight=c)
+        st = O.forward_stats(X, W, b, t, reduction, grad_out=g, want_db=True, row_block=64, class_weight=c)
         np.testing.assert_allclose(st["loss"], loss, rtol=1e-12)
         np.testing.assert_allclose(st["db"], db, rtol=1e-10, atol=1e-13)
         rows = np.array([0, 5, 77, 299])
