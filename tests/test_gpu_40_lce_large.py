@@ -93,3 +93,33 @@ def test_full_size_llm_head_whole_buffer(cuda_lib):
     cls = _sample_classes(th, w.C, rng, k=128)
     dWc, _ = O.dw_rows(Xh, Wh, None, th, st["lse"], st["w"], cls)
     assert rel_max(dW[torch.from_numpy(cls).cuda()].double().cpu().numpy(), dWc) < tol["grad"]
+
+
+@pytest.mark.timeout(3600)
+def test_full_size_llm_head_f16_class_weights(cuda_lib):
+    """The widened rows at full size, as the bench's variants run them: the
+    LLM head's inputs in fp16 with per-class weights (uniform in [0.5, 1.5),
+    seed 7), default plan (classes beyond the 1 GiB buffer recomputed),
+    against the float64 oracle on the exact fp16 values."""
+    w = WORKLOADS["bf16_llm_head"]
+    inp = make_workload("bf16_llm_head", "cuda")
+    X, W, t = inp["X"].half(), inp["W"].half(), inp["target"]
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    cw = torch.rand(w.C, generator=gen, device="cuda") + 0.5
+    loss, dX, dW, db = cuda_lib.lce_forward_backward(X, W, None, t, "mean", -100, class_weight=cw)
+    torch.cuda.synchronize()
+    Xh = X.float().cpu().numpy()
+    Wh = W.float().cpu().numpy()
+    th = t.cpu().numpy()
+    cwh = cw.double().cpu().numpy()
+    st = O.forward_stats(Xh, Wh, None, th, "mean", row_block=512, class_weight=cwh)
+    tol = TOL[torch.float16]
+    assert rel_scalar(loss.item(), st["loss"]) < tol["loss"]
+    rng = np.random.default_rng(2)
+    rows = np.sort(rng.choice(w.N, 256, replace=False))
+    _, dXr = O.grad_rows(Xh, Wh, None, th, st["lse"], st["w"], rows)
+    assert rel_max(dX[torch.from_numpy(rows).cuda()].double().cpu().numpy(), dXr) < tol["grad"]
+    cls = _sample_classes(th, w.C, rng)
+    dWc, _ = O.dw_rows(Xh, Wh, None, th, st["lse"], st["w"], cls)
+    assert rel_max(dW[torch.from_numpy(cls).cuda()].double().cpu().numpy(), dWc) < tol["grad"]
+    assert torch.isfinite(dX).all() and torch.isfinite(dW).all()
