@@ -93,7 +93,7 @@ enum lce_op_e { LCE_OP_FORWARD = 0, LCE_OP_FORWARD_BACKWARD = 1, LCE_OP_CE_FROM_
 enum lce_status_e {
   LCE_OK = 0,
   LCE_ERR_NULL = 1,         /* a required pointer is NULL */
-  LCE_ERR_SHAPE = 2,        /* N < 0, D < 1, C < 1 or V < 1, or a size too large */
+  LCE_ERR_SHAPE = 2,        /* N < 0, D < 1, C < 1 or V < 1, or N or V > 2^40, D or C > 2^30 */
   LCE_ERR_DTYPE = 3,        /* unknown dtype, or acc_dtype != LCE_F32 */
   LCE_ERR_REDUCTION = 4,    /* reduction not one of none / sum / mean */
   LCE_ERR_GRAD_OUT = 5,     /* reduction none without a per-row upstream gradient */
