@@ -70,3 +70,11 @@ def test_reference_arm_prints_one_json_line():
     assert d["config"]["workload"] == "tiny_fp32"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_committed_traffic_was_captured_from_the_committed_kernels():
+    """Every entry's source hash is the current one: the table in the tree
+    describes the kernels in the tree (a change to a kernel's sources needs
+    a new capture, or the entry removed)."""
+    stale = [(w, k) for (w, k), (_, _, src) in bench.MEASURED_TRAFFIC.items() if src != bench.kernel_sources_hash(k)]
+    assert not stale, stale
