@@ -22,7 +22,7 @@ from tests.util import TOL, rel_max, rel_scalar, to64
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 40
+N_CASES = 80
 
 
 def _case(i):
@@ -95,7 +95,7 @@ def test_random_case(cuda_lib, i):
             assert got is None, (name, what)
 
 
-N_BOUNDED = 30
+N_BOUNDED = 60
 
 
 def _bounded_case(i):
@@ -184,7 +184,7 @@ def _ce_case(i):
                 std=r.choice([0.5, 2.0, 8.0]), seed=r.randrange(1 << 30))
 
 
-@pytest.mark.parametrize("i", range(24))
+@pytest.mark.parametrize("i", range(48))
 def test_random_ce_case(cuda_lib, i):
     c = _ce_case(i)
     inp = make_logits_inputs(c["N"], c["V"], c["dtype"], "cuda", seed=c["seed"], std=c["std"],
