@@ -100,7 +100,7 @@ enum lce_status_e {
   LCE_ERR_WORKSPACE = 6,    /* workspace NULL or smaller than needed for 128-row chunks */
   LCE_ERR_CUDA = 7,         /* a CUDA runtime call or kernel launch failed */
   LCE_ERR_TARGET_RANGE = 8, /* device: a target neither ignore_index nor in [0, C) */
-  LCE_ERR_ALIGN = 9,        /* bf16 path: D % 8 != 0 or a pointer not 16-byte aligned */
+  LCE_ERR_ALIGN = 9,        /* bf16 / fp16: D % 8 != 0 or a pointer not 16-byte aligned */
   LCE_ERR_TIMEOUT = 10,     /* device: an internal pipeline wait gave up */
   LCE_ERR_DEVICE = 11       /* current device is not compute capability 10.3 */
 };
